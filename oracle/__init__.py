@@ -1,0 +1,283 @@
+"""fp64 CPU oracle for tree verification -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg import this package.  The CUDA library never calls it and it never calls
+the CUDA library; the two share only the seeded input generators
+(``workloads``).
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision): the naive
+serial tree walk that materialises one state matrix per draft node (Bole
+summary page, "Core techniques" §1-§2 and the naive baseline it compares
+against), the greedy acceptance walk (LLM Primer VI ch. 9, §9.1) and the
+commit of the accepted path's state (Bole §2).  This file only builds the C
+source, marshals arrays and splits work over threads.
+
+Parity pins for each function are in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_I32P = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_F32P = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_F64P = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".%d.tmp" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
+                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def load(path: str):
+    """Load a compiled oracle library (the default build, or a test's variant)."""
+    L = ctypes.CDLL(path)
+    i = ctypes.c_int
+    L.orc_check_tree.argtypes = [i, _I32P]
+    L.orc_verify_unit.argtypes = [i, _I32P, i, i, i, _F64P, _F64P, _F64P, _F64P, _F64P,
+                                  _F64P, ctypes.c_void_p]
+    L.orc_accept.argtypes = [i, _I32P, _I32P, _I32P, ctypes.c_int32, i, _I32P, _I32P,
+                             _I32P]
+    L.orc_commit_unit.argtypes = [i, _I32P, i, i, i, _F64P, _F64P, _F64P, _F64P, _F64P]
+    L.orc_verify_batch.argtypes = [i, i, i, i, i, _I32P, _I32P, _F32P, _F32P, _F32P,
+                                   _F32P, _F32P, i, _I32P, _F64P]
+    L.orc_accept_batch.argtypes = [i, _I32P, _I32P, _I32P, _I32P, _I32P, i, _I32P, _I32P,
+                                   _I32P]
+    L.orc_commit_batch.argtypes = [i, i, i, i, i, _I32P, _F32P, _F32P, _F32P, _F32P,
+                                   _I32P, _I32P, i, i, _I32P, _F64P]
+    for f in (L.orc_check_tree, L.orc_verify_unit, L.orc_accept, L.orc_commit_unit,
+              L.orc_verify_batch, L.orc_accept_batch, L.orc_commit_batch):
+        f.restype = ctypes.c_int
+    return L
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load(build())
+    return _lib
+
+
+_override = threading.local()
+
+
+def _L():
+    return getattr(_override, "lib", None) or lib()
+
+
+class using:
+    """Context manager: route this thread's oracle calls to another build."""
+
+    def __init__(self, L):
+        self.L = L
+
+    def __enter__(self):
+        self.prev = getattr(_override, "lib", None)
+        _override.lib = self.L
+
+    def __exit__(self, *a):
+        _override.lib = self.prev
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _rc(rc: int, what: str):
+    if rc != 0:
+        raise OracleError("%s failed with code %d" % (what, rc))
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+# ------------------------------------------------------------------ unit level
+
+
+def verify_unit(parent, q, k, v, g, H0, *, diag: bool, return_states: bool = False):
+    """Naive serial walk for one (request, head).  q,k: [n,dk]; v: [n,dv];
+    g: [n] or [n,dk]; H0: [dk,dv].  Returns out [n,dv] (and states [n,dk,dv])."""
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    n = len(parent)
+    q, k, v, g, H0 = _f64(q), _f64(k), _f64(v), _f64(g), _f64(H0)
+    dk, dv = H0.shape
+    out = np.zeros((n, dv), dtype=np.float64)
+    states = np.zeros((max(n, 1), dk, dv), dtype=np.float64)
+    _rc(_L().orc_verify_unit(n, parent, dk, dv, int(diag), g.reshape(-1) if n else np.zeros(1),
+                              q.reshape(-1) if n else np.zeros(1),
+                              k.reshape(-1) if n else np.zeros(1),
+                              v.reshape(-1) if n else np.zeros(1), H0.reshape(-1),
+                              out.reshape(-1) if n else np.zeros(1),
+                              states.ctypes.data_as(ctypes.c_void_p)), "verify_unit")
+    return (out, states[:n]) if return_states else out
+
+
+def accept(parent, draft, target, root_tok: int, max_depth: int):
+    """Greedy walk for one request: returns (len, path[max_depth], bonus)."""
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    ln = np.zeros(1, np.int32)
+    bonus = np.zeros(1, np.int32)
+    path = np.zeros(max(max_depth, 1), np.int32)
+    _rc(_L().orc_accept(len(parent), parent, np.ascontiguousarray(draft, np.int32),
+                         np.ascontiguousarray(target, np.int32), int(root_tok), max_depth, ln,
+                         path, bonus), "accept")
+    return int(ln[0]), path[:max_depth], int(bonus[0])
+
+
+def commit_unit(path, L: int, k, v, g, H0, *, diag: bool):
+    """Replay the recurrence from H0 along path[:L]; returns H_new [dk,dv]."""
+    H0 = _f64(H0)
+    dk, dv = H0.shape
+    out = np.zeros((dk, dv), np.float64)
+    k, v, g = _f64(k), _f64(v), _f64(g)
+    _rc(_L().orc_commit_unit(L, np.ascontiguousarray(path, np.int32), dk, dv, int(diag),
+                              g.reshape(-1) if g.size else np.zeros(1),
+                              k.reshape(-1) if k.size else np.zeros(1),
+                              v.reshape(-1) if v.size else np.zeros(1), H0.reshape(-1),
+                              out.reshape(-1)), "commit_unit")
+    return out
+
+
+# ------------------------------------------------------------------ batch level
+
+
+class _Packed:
+    """float32 views of a workloads.Batch, as the C batch drivers read them."""
+
+    def __init__(self, batch):
+        self.b = batch
+        self.q = np.ascontiguousarray(batch.qkv_f32(batch.q)).reshape(-1)
+        self.k = np.ascontiguousarray(batch.qkv_f32(batch.k)).reshape(-1)
+        self.v = np.ascontiguousarray(batch.qkv_f32(batch.v)).reshape(-1)
+        self.g = np.ascontiguousarray(batch.g, dtype=np.float32).reshape(-1)
+        self.H0 = np.ascontiguousarray(batch.H0, dtype=np.float32).reshape(-1)
+        self.offs = np.ascontiguousarray(batch.node_offsets, np.int32)
+        self.parent = np.ascontiguousarray(batch.parent, np.int32)
+        for name in ("q", "k", "v", "g", "parent"):
+            a = getattr(self, name)
+            if a.size == 0:
+                setattr(self, name, np.zeros(1, a.dtype))
+
+
+def _split(seq: np.ndarray, parts: int):
+    parts = max(1, min(parts, len(seq)))
+    return [s for s in np.array_split(seq, parts) if len(s)]
+
+
+def verify(batch, units: Optional[Sequence[int]] = None, threads: int = 1, packed=None):
+    """Outputs of the listed units (u = b*H + h; default all).
+
+    Returns a dict u -> out [N_b, dv] (float64)."""
+    b = batch
+    P = packed or _Packed(b)
+    if units is None:
+        units = np.arange(b.B * b.H, dtype=np.int32)
+    units = np.ascontiguousarray(units, dtype=np.int32)
+    sizes = np.diff(b.node_offsets)
+    res = {}
+
+    def run(chunk):
+        rows = int(sum(sizes[u // b.H] for u in chunk))
+        out = np.zeros((max(rows, 1), b.dv), np.float64)
+        _rc(_L().orc_verify_batch(b.B, b.H, b.dk, b.dv, int(b.decay == "diag"), P.offs,
+                                   P.parent, P.g, P.q, P.k, P.v, P.H0, len(chunk),
+                                   np.ascontiguousarray(chunk, np.int32), out.reshape(-1)),
+            "verify_batch")
+        r = 0
+        part = {}
+        for u in chunk:
+            n = int(sizes[u // b.H])
+            part[int(u)] = out[r:r + n]
+            r += n
+        return part
+
+    chunks = _split(units, threads * 4)
+    if threads <= 1:
+        for c in chunks:
+            res.update(run(c))
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            for part in ex.map(run, chunks):
+                res.update(part)
+    return res
+
+
+def verify_dense(batch, threads: int = 1) -> np.ndarray:
+    """All outputs as a packed [T,H,dv] float64 array."""
+    res = verify(batch, threads=threads)
+    out = np.zeros((batch.T, batch.H, batch.dv), np.float64)
+    for u, o in res.items():
+        bb, h = divmod(u, batch.H)
+        s, e = batch.node_offsets[bb], batch.node_offsets[bb + 1]
+        out[s:e, h, :] = o
+    return out
+
+
+def accept_batch(batch, max_depth: Optional[int] = None, root_argmax=None, target=None):
+    """Greedy walk for every request: (len[B], path[B,max_depth], bonus[B])."""
+    b = batch
+    md = b.max_depth if max_depth is None else max_depth
+    ln = np.zeros(max(b.B, 1), np.int32)
+    bonus = np.zeros(max(b.B, 1), np.int32)
+    path = np.zeros(max(b.B * md, 1), np.int32)
+    root = np.ascontiguousarray(b.root_argmax if root_argmax is None else root_argmax, np.int32)
+    tgt = np.ascontiguousarray(b.target if target is None else target, np.int32)
+    par = np.ascontiguousarray(b.parent, np.int32)
+    drf = np.ascontiguousarray(b.draft, np.int32)
+    if par.size == 0:
+        par, drf, tgt = np.zeros(1, np.int32), np.zeros(1, np.int32), np.zeros(1, np.int32)
+    _rc(_L().orc_accept_batch(b.B, np.ascontiguousarray(b.node_offsets, np.int32), par, drf, tgt,
+                               root if root.size else np.zeros(1, np.int32), md, ln, path, bonus),
+        "accept_batch")
+    return ln[:b.B], path[:b.B * md].reshape(b.B, md), bonus[:b.B]
+
+
+def commit(batch, accept_len, path, units: Optional[Sequence[int]] = None, threads: int = 1,
+           packed=None):
+    """H_new of the listed units: dict u -> [dk, dv] float64."""
+    b = batch
+    P = packed or _Packed(b)
+    if units is None:
+        units = np.arange(b.B * b.H, dtype=np.int32)
+    units = np.ascontiguousarray(units, dtype=np.int32)
+    path = np.ascontiguousarray(path, np.int32)
+    md = path.shape[1] if path.ndim == 2 else b.max_depth
+    ln = np.ascontiguousarray(accept_len, np.int32)
+    res = {}
+
+    def run(chunk):
+        out = np.zeros((len(chunk), b.dk, b.dv), np.float64)
+        _rc(_L().orc_commit_batch(b.B, b.H, b.dk, b.dv, int(b.decay == "diag"), P.offs, P.g,
+                                   P.k, P.v, P.H0, ln, path.reshape(-1), md, len(chunk),
+                                   np.ascontiguousarray(chunk, np.int32), out.reshape(-1)),
+            "commit_batch")
+        return {int(u): out[i] for i, u in enumerate(chunk)}
+
+    chunks = _split(units, threads * 4)
+    if threads <= 1:
+        for c in chunks:
+            res.update(run(c))
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            for part in ex.map(run, chunks):
+                res.update(part)
+    return res
