@@ -1,0 +1,518 @@
+"""Benchmark of the tree-verification hot path on GB300: one step = tv_verify +
+tv_accept_greedy + tv_commit over one batch of the Mamba-2-like workload
+(B=16 requests, H=24 heads, dk=128, dv=64, 16-node top-4 draft trees, bf16
+q/k/v, fp32 states, scalar decay).
+
+Prints one JSON line (rank 0).  Metric: tree-verify node-head updates per
+second (node-heads = nodes x heads per batch), whole job.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: inputs resident in HBM; R distinct input sets (> 4x L2 in total) are
+used in rotation so every step reads cold data; the K timed steps run as CUDA
+graph replays bracketed by CUDA events on the launching stream, with a barrier
+and synchronize on both sides, max over ranks.  `e2e` repeats the step through
+the Python binding with pinned host buffers and the host<->device copies inside
+the timed region.  `--impl reference` times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify node-head updates/s"
+UNIT = "node-head/s"
+WORKLOAD = ("Mamba-2-like layer: B=16 requests, H=24 heads, dk=128, dv=64, 16-node top-4 "
+            "draft tree (4 chains of depth 4), bf16 q/k/v, fp32 H0, scalar decay")
+KERNEL_SOURCES = ["tree_speculative_verify_tv_gb300/csrc/verify_tc.cu",
+                  "tree_speculative_verify_tv_gb300/csrc/verify_simt.cu",
+                  "tree_speculative_verify_tv_gb300/csrc/tv_internal.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sets", type=int, default=0, help="rotated input sets (0 = auto, >4x L2)")
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--variant", type=int, default=0, help="tv_verify variant (0 auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- byte accounting
+
+
+def verify_bytes(b) -> int:
+    """Algorithmic HBM bytes of one tv_verify launch: H0 read once, every factor
+    row read once, every output row written once, tree metadata read once."""
+    qk = 2 if b.qkv_dtype == "bf16" else 4
+    g = 4 if b.decay == "scalar" else 4 * b.dk
+    per_node_head = 2 * b.dk * qk + b.dv * qk + g + 4 * b.dv
+    return (b.B * b.H * 4 * b.dk * b.dv + b.T * b.H * per_node_head + 8 * b.T
+            + 4 * (b.B + 1))
+
+
+def commit_bytes(b, lens) -> int:
+    """H0 read + H_new written, plus the accepted path's factor rows."""
+    qk = 2 if b.qkv_dtype == "bf16" else 4
+    g = 4 if b.decay == "scalar" else 4 * b.dk
+    L = int(np.sum(lens))
+    return b.B * b.H * 8 * b.dk * b.dv + L * b.H * (b.dk * qk + b.dv * qk + g)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        fp = os.path.join(ROOT, p)
+        if os.path.exists(fp):
+            h.update(open(fp, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the verify kernel from the committed ncu summary,
+    valid only while the kernel sources are unchanged since the capture."""
+    fp = os.path.join(ROOT, "profiles", "verify_c2_dram_traffic.txt")
+    if not os.path.exists(fp):
+        return None
+    vals = {}
+    for line in open(fp):
+        if "=" in line and not line.startswith("#"):
+            k, _, v = line.partition("=")
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    fp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(fp):
+        try:
+            return json.load(open(fp)), "measured"
+        except ValueError:
+            pass
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_start: float, t_end: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t_start - 0.06 <= r[0] <= t_end + 0.06]
+        window = "timed"
+        if not inside and rows:
+            mid = 0.5 * (t_start + t_end)
+            inside = sorted(rows, key=lambda r: abs(r[0] - mid))[:3]
+            window = "nearest"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for nm, val in zip(names, r[3][5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median([r[1] for r in inside])),
+                "sm_max_mhz": float(max(r[2] for r in inside)), "reasons": sorted(reasons),
+                "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------- distributed
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_step(batch, units, threads, packed):
+    """One bounded sample of the workload on the CPU oracle: verify of the listed
+    (request, head) units, the greedy walk of every request, commit of the units."""
+    import oracle
+    oracle.verify(batch, units=units, threads=threads, packed=packed)
+    ln, path, _ = oracle.accept_batch(batch)
+    oracle.commit(batch, ln, path, units=units, threads=threads, packed=packed)
+
+
+def time_oracle(batch, total_steps: int, budget_s: float, threads: int):
+    """Pick a sample size (units per step) so total_steps steps take about budget_s;
+    returns (node_heads_per_s, units_per_step, steps_run, seconds, threads_used)."""
+    import oracle
+    packed = oracle._Packed(batch)
+    n_units = batch.B * batch.H
+    sizes = np.diff(batch.node_offsets)
+    probe = np.arange(min(n_units, max(threads * 2, 8)), dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle_step(batch, probe, threads, packed)
+    per_unit = (time.perf_counter() - t0) / len(probe)
+    want = budget_s / max(total_steps, 1) / max(per_unit, 1e-9)
+    upl = int(min(n_units, max(1, want)))
+    units_all = np.arange(n_units, dtype=np.int32)
+    t0 = time.perf_counter()
+    nh = 0
+    for s in range(total_steps):
+        start = (s * upl) % n_units
+        units = np.take(units_all, np.arange(start, start + upl), mode="wrap")
+        oracle_step(batch, units, threads, packed)
+        nh += int(sum(sizes[u // batch.H] for u in units))
+    dt = time.perf_counter() - t0
+    used = min(threads, upl)
+    return nh / dt, upl, total_steps, dt, used
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import workloads
+    b = workloads.config2()
+    threads = cpu_cores()
+    steps = args.steps + args.warmup
+    value, upl, n, dt, threads = time_oracle(b, steps, 60.0, threads)
+    ms = dt / n * 1e3
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "B": b.B, "H": b.H, "dk": b.dk, "dv": b.dv,
+                       "nodes_per_request": 16},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "%d steps, each the fp64 oracle on %d of the %d "
+                                       "(request, head) units (verify + greedy walk of all "
+                                       "requests + commit)" % (n, upl, b.B * b.H)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    import workloads
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    tv.build()
+    tv.load()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
+
+    base = workloads.config2(seed=1002 + 7919 * rank)
+    per_set = verify_bytes(base) + base.B * base.H * base.dk * base.dv * 4 * 2
+    R = args.sets or max(4, int(np.ceil(4.0 * l2 / per_set)) + 1)
+    sets = [workloads.config2(seed=1002 + 7919 * rank + 101 * r) for r in range(R)]
+    dbs = [tv.DeviceBatch(s, device=dev) for s in sets]
+    stream = torch.cuda.Stream(device=dev)
+    node_heads = base.T * base.H
+
+    def step(d):
+        d.verify(stream=stream, variant=args.variant)
+        d.accept(stream=stream)
+        d.commit(stream=stream)
+
+    with torch.cuda.stream(stream):
+        for d in dbs:
+            d.status.zero_()
+        for w in range(args.warmup):
+            step(dbs[w % R])
+    stream.synchronize()
+    for d, s in zip(dbs, sets):
+        st = int(d.status[0].item())
+        if st != 0:
+            raise SystemExit("device status %d (%s) during warm-up" % (st, tv.status_string(st)))
+
+    def capture(fn_list):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for fn in fn_list:
+                fn()
+        return g
+
+    def graphs_for(kind, K):
+        """Graphs whose replays launch exactly K units of `kind` cycling through the sets."""
+        def one(i):
+            d = dbs[i % R]
+            if kind == "step":
+                return lambda d=d: step(d)
+            if kind == "verify":
+                return lambda d=d: d.verify(stream=stream, variant=args.variant)
+            if kind == "accept":
+                return lambda d=d: d.accept(stream=stream)
+            return lambda d=d: d.commit(stream=stream)
+        full = capture([one(i) for i in range(R)])
+        rem = K % R
+        remg = capture([one(i) for i in range(rem)]) if rem else None
+        return full, K // R, remg
+
+    def timed(kind, K, sampler=None):
+        full, reps, remg = graphs_for(kind, K)
+        full.replay()  # upload / warm
+        if remg is not None:
+            remg.replay()
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        t_host0 = time.time()
+        e0.record(stream)
+        for _ in range(reps):
+            full.replay()
+        if remg is not None:
+            remg.replay()
+        e1.record(stream)
+        e1.synchronize()
+        t_host1 = time.time()
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) * 1e-3, t_host0, t_host1
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    K = args.steps
+    t_step, th0, th1 = timed("step", K)
+    clocks = sampler.summary(th0, th1)
+    t_verify, _, _ = timed("verify", K)
+    t_accept, _, _ = timed("accept", K)
+    t_commit, _, _ = timed("commit", K)
+    sampler.stop()
+    for d in dbs:
+        st = int(d.status[0].item())
+        if st != 0:
+            raise SystemExit("device status %d (%s)" % (st, tv.status_string(st)))
+
+    t_step_max = max_over_ranks(t_step, world)
+    total_nh = sum_over_ranks(node_heads * K, world)
+    value = total_nh / t_step_max
+    ms_per_step = t_step_max / K * 1e3
+
+    # ---------------- end to end through the binding with pinned host buffers
+    e2e = run_e2e(args, sets[0], dev, stream, tv, world)
+
+    # ---------------- roofline of the dominant kernel (verify)
+    peaks, peak_kind = measured_peaks()
+    vb = verify_bytes(base)
+    v_launch = t_verify / K
+    achieved = vb / v_launch / 1e9
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    lens = [int(x) for x in dbs[0].accept_len[:base.B].cpu().numpy()]
+    cb = commit_bytes(base, lens)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(),
+                "kernel": "tv_verify", "bytes_per_launch": vb,
+                "launch_us": v_launch * 1e6, "peak_kind": "%s (hbm_gbs burst copy)" % peak_kind}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = cpu_cores()
+        v, upl, n, dt, threads = time_oracle(base, 40, 15.0, threads)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "%d steps of the fp64 oracle, each on %d of the %d (request, head) "
+                         "units (verify + greedy walk + commit), %.1f s" % (n, upl,
+                                                                              base.B * base.H,
+                                                                              dt)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": base.B, "H": base.H, "dk": base.dk,
+                       "dv": base.dv, "nodes_per_request": 16, "node_heads_per_step": node_heads,
+                       "inputs": "bf16 q/k/v, fp32 g/H0/out/H_new",
+                       "l2": "inputs larger than L2: %d input sets rotated, %.0f MB touched per "
+                             "cycle vs %.0f MB L2" % (R, R * per_set / 1e6, l2 / 1e6),
+                       "timing": "CUDA graph replays of the K steps, CUDA events on the "
+                                 "launching stream"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+            "kernels_us": {"verify": t_verify / K * 1e6, "accept": t_accept / K * 1e6,
+                           "commit": t_commit / K * 1e6},
+            "verify_only": {"value": node_heads / v_launch, "unit": UNIT,
+                            "gbs": achieved},
+            "commit_gbs": cb / (t_commit / K) / 1e9,
+            "transient_bytes": {"library_workspace": 0,
+                                "factors": int(base.T * base.H * (2 * base.dk * 2 + base.dv * 2
+                                                                 + 4)),
+                                "naive_per_node_states": int(base.T * base.H * base.dk * base.dv
+                                                             * 4)},
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, host_batch, dev, stream, tv, world):
+    """The step through the binding with host buffers: pinned host -> device copies
+    of the step's inputs, the three calls, device -> pinned host copies of its results."""
+    import torch
+    hb = tv.DeviceBatch(host_batch, pin=True)
+    db = tv.DeviceBatch(host_batch, device=dev)
+    ins = ["node_offsets", "parent", "depth", "q", "k", "v", "g", "H0", "draft", "target",
+           "root_argmax"]
+    outs = ["out", "H_new", "accept_len", "path", "bonus", "status"]
+    h2d = sum(getattr(hb, n).numel() * getattr(hb, n).element_size() for n in ins)
+    d2h = sum(getattr(db, n).numel() * getattr(db, n).element_size() for n in outs)
+    K = max(1, args.e2e_steps)
+
+    def one():
+        for n in ins:
+            getattr(db, n).copy_(getattr(hb, n), non_blocking=True)
+        db.status.zero_()
+        db.verify(stream=stream, variant=args.variant)
+        db.accept(stream=stream)
+        db.commit(stream=stream)
+        for n in outs:
+            getattr(hb, n).copy_(getattr(db, n), non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            one()
+        stream.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            one()
+        e1.record(stream)
+        e1.synchronize()
+    dt = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world)
+    if int(hb.status[0]) != 0:
+        raise SystemExit("device status %d in e2e" % int(hb.status[0]))
+    nh = sum_over_ranks(host_batch.T * host_batch.H * K, world)
+    return {"value": nh / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": dt / K * 1e3}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * treeverify.h -- C ABI of libtreeverify: verification of a whole draft tree
+ * through a gated linear-recurrence layer, greedy acceptance, and commit of the
+ * accepted path's state, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (Bole summary page, "Core techniques" §1):
+ *   the layer's recurrence h_{t+1} = S_t h_t + u_t, specialised to
+ *   S_i = diag(exp g_i) and u_i = k_i v_i^T, with read-out o_i = H_i^T q_i.
+ *   On a draft tree every node continues its parent's state:
+ *     H_i = diag(exp g_i) H_parent(i) + k_i v_i^T,    H_parent = H0 at the context.
+ *   The library never forms H_i.  It evaluates the tree closed form
+ *     o_i = H0^T (e^{G_i} * q_i) + sum_{j in anc*(i)} (sum_c q_ic k_jc e^{G_ic - G_jc}) v_j
+ *   with anc*(i) the root path of node i including i and G_i = sum_{j in anc*(i)} g_j,
+ *   so all nodes are verified in parallel and only the per-token factors
+ *   (g_i, k_i, v_i) are kept (§2, "token-level factor encoding").
+ *
+ * Conventions shared by every call
+ *   - All array pointers are DEVICE memory owned by the caller.  The library
+ *     allocates nothing, keeps no state between calls and is thread-safe.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *     legacy default stream) and returns after the launch.
+ *   - Array pointers must be 16-byte aligned (TV_ERR_ALIGN otherwise).
+ *   - Host-checkable errors are returned synchronously and launch nothing.
+ *   - Errors only the device can see (a malformed tree, offsets or path) are
+ *     written into *dev_status (int32, device memory, zeroed by the caller) with
+ *     an atomic compare-and-swap, so the first error wins; the kernels never
+ *     trap.  The affected request's outputs are then defined per call below.
+ *   - Packed ragged layout: the B requests' trees are concatenated, T nodes in
+ *     all; node_offsets[b] .. node_offsets[b+1]-1 are request b's nodes.  Per
+ *     node t and head h, rows are contiguous:
+ *       q, k  [T][H][dk]   (bf16 or fp32, per tv_problem.qkv_dtype)
+ *       v     [T][H][dv]
+ *       g     [T][H]       (scalar decay)  or  [T][H][dk]  (per-channel decay), fp32,
+ *                          natural-log decay: the state is scaled by exp(g) (g <= 0
+ *                          gives a contraction; any finite g is accepted)
+ *       out   [T][H][dv]   fp32
+ *       H0, H_new [B][H][dk][dv] fp32 (row = key channel, dv contiguous)
+ *     Several layers of one request fold into H (they share the request's tree).
+ */
+#ifndef TREEVERIFY_H
+#define TREEVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TV_VERSION 1
+
+/* Limits of this build. */
+#define TV_MAX_NODES 256  /* nodes per request tree */
+#define TV_MAX_DEPTH 32   /* depth of any node (1 = child of the context) */
+#define TV_MAX_DIM   256  /* dk and dv */
+
+typedef enum tv_status {
+    TV_OK = 0,
+    TV_ERR_NULL = 1,        /* a required pointer is NULL */
+    TV_ERR_SHAPE = 2,       /* B, H, dk, dv, T, max_nodes or max_depth out of range */
+    TV_ERR_DTYPE = 3,       /* unknown decay kind or element type */
+    TV_ERR_ALIGN = 4,       /* an array pointer is not 16-byte aligned */
+    TV_ERR_UNSUPPORTED = 5, /* a limit of this build is exceeded, or a forced variant
+                               cannot run this shape */
+    TV_ERR_TREE = 6,        /* device-detected: bad node_offsets, parent, depth or path */
+    TV_ERR_CUDA = 7,        /* a CUDA runtime call failed (launch error) */
+    TV_ERR_TIMEOUT = 8      /* device-detected: a bounded wait inside a kernel expired */
+} tv_status;
+
+typedef enum tv_decay {
+    TV_DECAY_SCALAR = 0,    /* g[T][H]: one decay per node and head */
+    TV_DECAY_DIAG = 1       /* g[T][H][dk]: one decay per node, head and key channel */
+} tv_decay;
+
+typedef enum tv_dtype {
+    TV_BF16 = 0,            /* q, k, v are bfloat16 */
+    TV_F32 = 1              /* q, k, v are float32 */
+} tv_dtype;
+
+/* Kernel choice for tv_verify_ex (tv_verify uses TV_VARIANT_AUTO). */
+typedef enum tv_variant {
+    TV_VARIANT_AUTO = 0,    /* tensor-core kernel where it applies, else SIMT */
+    TV_VARIANT_SIMT = 1,    /* CUDA-core kernel, every supported shape */
+    TV_VARIANT_TC = 2       /* tcgen05 tensor-core kernel: bf16 q/k/v, dk in {64,128},
+                               dv in {64,128}; TV_ERR_UNSUPPORTED otherwise */
+} tv_variant;
+
+/*
+ * Shape and tree of one batch.  The three tree arrays are device memory.
+ *   B            number of requests (>= 0)
+ *   H            heads per request, layers folded in (>= 1)
+ *   dk, dv       key and value widths: multiples of 8 in [8, 256]
+ *   total_nodes  T = node_offsets[B] (host copy, used for bounds)
+ *   max_nodes    bound on any request's node count, 1..256
+ *   max_depth    bound on any node's depth, 1..32; also the row length of `path`
+ *   decay        tv_decay
+ *   qkv_dtype    tv_dtype
+ *   node_offsets [B+1] int32, non-decreasing, node_offsets[0] = 0, node_offsets[B] = T
+ *   parent       [T] int32, local index within the request: -1 (child of the
+ *                committed context) or an earlier node of the same request
+ *   depth        [T] int32: 1 for a child of the context, else depth(parent)+1;
+ *                redundant with parent and validated, never trusted
+ */
+typedef struct tv_problem {
+    int32_t B, H, dk, dv;
+    int32_t total_nodes;
+    int32_t max_nodes;
+    int32_t max_depth;
+    int32_t decay;
+    int32_t qkv_dtype;
+    const int32_t *node_offsets;
+    const int32_t *parent;
+    const int32_t *depth;
+} tv_problem;
+
+/*
+ * tv_verify -- outputs of every draft node through the recurrence layer.
+ * Bole summary page, "Core techniques" §1 (tree closed form, all nodes in
+ * parallel) and §2 (per-token factors instead of per-node states).
+ *
+ *   H0    [B][H][dk][dv] fp32   state of the committed context (read only)
+ *   q, k  [T][H][dk]            bf16 or fp32
+ *   v     [T][H][dv]            bf16 or fp32
+ *   g     [T][H] or [T][H][dk]  fp32 log-decay
+ *   out   [T][H][dv] fp32       o_i = H_i^T q_i for every node i and head
+ *   dev_status  int32 (device)  see conventions
+ * Device-detected errors: a request whose offsets, parent or depth entries are
+ * malformed gets status TV_ERR_TREE and its out rows are written as zeros
+ * (rows of requests whose offsets themselves are unusable are left untouched).
+ * Transient memory: shared memory only; nothing is allocated.
+ */
+tv_status tv_verify(const tv_problem *p, const float *H0, const void *q, const void *k,
+                    const void *v, const float *g, float *out, int32_t *dev_status,
+                    void *stream);
+
+/* tv_verify with an explicit kernel choice (tv_variant). */
+tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, const void *k,
+                       const void *v, const float *g, float *out, int32_t *dev_status,
+                       void *stream, int32_t variant);
+
+/*
+ * tv_accept_greedy -- greedy acceptance walk of every request's tree.
+ * LLM Primer VI ch. 9 §9.1: the longest draft prefix that matches the target is
+ * accepted, and at the first mismatch the target's own token is kept.  On a tree:
+ * start at the context with t = root_argmax[b]; repeatedly move to the
+ * lowest-index child whose draft token equals t and set t = target_argmax of
+ * that child; stop when no child matches.  bonus[b] = t.
+ *
+ *   node_offsets [B+1], parent [T]       as in tv_problem (total_nodes = T)
+ *   draft_tokens [T]   token each node proposes
+ *   target_argmax[T]   the target model's argmax after each node
+ *   root_argmax  [B]   the target model's argmax at the committed context
+ *   accept_len   [B]   out: accepted node count L (0..max_depth)
+ *   path         [B][max_depth]  out: accepted local node indices, root first,
+ *                      -1 after the first L entries
+ *   bonus        [B]   out: the target's token after the accepted prefix
+ * Device-detected errors (bad offsets, a parent outside [-1, i), or an accepted
+ * path longer than max_depth): TV_ERR_TREE, accept_len = 0, path = -1, bonus = -1
+ * for that request.  Integer-only; results are exact.
+ */
+tv_status tv_accept_greedy(int32_t B, int32_t total_nodes, int32_t max_nodes, int32_t max_depth,
+                           const int32_t *node_offsets, const int32_t *parent,
+                           const int32_t *draft_tokens, const int32_t *target_argmax,
+                           const int32_t *root_argmax, int32_t *accept_len, int32_t *path,
+                           int32_t *bonus, int32_t *dev_status, void *stream);
+
+/*
+ * tv_commit -- state after the accepted path, rebuilt from the factors.
+ * Bole summary page, "Core techniques" §2: only the accepted path's state is
+ * restored, h_k = Chain(S_k..S_1) h_0 + accumulated updates; here
+ *   H_new = diag(e^{G_L}) H0 + sum_{m=1..L} diag(e^{G_L - G_{p_m}}) k_{p_m} v_{p_m}^T
+ * with p_1..p_L = path[b][0..L), L = accept_len[b] and G the running sum of g
+ * along the path.  L = 0 gives H_new = H0.
+ *
+ *   p          shape and tree (tv_problem; node_offsets and parent are read)
+ *   H0         [B][H][dk][dv] fp32
+ *   g, k, v    as in tv_verify
+ *   path, accept_len   as written by tv_accept_greedy (path rows of max_depth)
+ *   H_new      [B][H][dk][dv] fp32; may equal H0 (in place), must not overlap it
+ *              otherwise
+ * Device-detected errors (L outside [0, max_depth], a path entry outside the
+ * request, or a path that is not a root path of the tree): TV_ERR_TREE and that
+ * request's H_new is left untouched.
+ */
+tv_status tv_commit(const tv_problem *p, const float *H0, const float *g, const void *k,
+                    const void *v, const int32_t *path, const int32_t *accept_len,
+                    float *H_new, int32_t *dev_status, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *tv_status_string(int32_t status);
+
+/* TV_VERSION of the loaded library. */
+int32_t tv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREEVERIFY_H */

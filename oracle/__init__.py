@@ -211,7 +211,7 @@ def verify(batch, units: Optional[Sequence[int]] = None, threads: int = 1, packe
         return part
 
     chunks = _split(units, threads * 4)
-    if threads <= 1:
+    if threads <= 1 or len(chunks) == 1:
         for c in chunks:
             res.update(run(c))
     else:
@@ -273,7 +273,7 @@ def commit(batch, accept_len, path, units: Optional[Sequence[int]] = None, threa
         return {int(u): out[i] for i, u in enumerate(chunk)}
 
     chunks = _split(units, threads * 4)
-    if threads <= 1:
+    if threads <= 1 or len(chunks) == 1:
         for c in chunks:
             res.update(run(c))
     else:

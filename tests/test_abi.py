@@ -1,0 +1,148 @@
+"""C ABI checks that need no GPU: the library builds, loads, exports every
+function include/treeverify.h declares, and rejects bad arguments on the host
+(before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tree_speculative_verify_tv_gb300 as tv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "treeverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tv.build()
+    return tv.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(tv_[a-z_]+)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert {"tv_verify", "tv_verify_ex", "tv_accept_greedy", "tv_commit", "tv_status_string",
+            "tv_version"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(tv.EXPORTED)
+
+
+def test_version_and_status_strings(lib):
+    assert tv.tv_version() == 1
+    for code in range(9):
+        s = tv.status_string(code)
+        assert s.startswith("TV_"), s
+    assert "unknown" in tv.status_string(99)
+
+
+def test_header_constants_match_binding():
+    src = open(HEADER).read()
+    for name, val in (("TV_MAX_NODES", 256), ("TV_MAX_DEPTH", 32), ("TV_MAX_DIM", 256)):
+        assert re.search(r"#define %s\s+%d" % (name, val), src)
+    for name in ("TV_OK", "TV_ERR_NULL", "TV_ERR_SHAPE", "TV_ERR_DTYPE", "TV_ERR_ALIGN",
+                 "TV_ERR_UNSUPPORTED", "TV_ERR_TREE", "TV_ERR_CUDA", "TV_ERR_TIMEOUT"):
+        m = re.search(r"%s\s*=\s*(\d+)" % name, src)
+        assert m and int(m.group(1)) == getattr(tv, name), name
+
+
+# fake, aligned "device" addresses: every call below must fail before touching them
+A = 0x10000
+P = [A + 0x1000 * i for i in range(16)]
+
+
+def prob(**kw):
+    d = dict(B=2, H=3, dk=16, dv=16, total_nodes=5, max_nodes=4, max_depth=3,
+             decay=tv.TV_DECAY_SCALAR, qkv_dtype=tv.TV_BF16, node_offsets=P[0], parent=P[1],
+             depth=P[2])
+    d.update(kw)
+    return tv.make_problem(**d)
+
+
+def verify_rc(p, **kw):
+    args = dict(H0=P[3], q=P[4], k=P[5], v=P[6], g=P[7], out=P[8], dev_status=P[9])
+    args.update(kw)
+    return tv.tv_verify(p, args["H0"], args["q"], args["k"], args["v"], args["g"], args["out"],
+                        args["dev_status"], stream=0, variant=kw.get("variant", 0), check=False)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), tv.TV_ERR_SHAPE), (dict(H=0), tv.TV_ERR_SHAPE), (dict(dk=12), tv.TV_ERR_SHAPE),
+    (dict(dv=0), tv.TV_ERR_SHAPE), (dict(dk=264), tv.TV_ERR_UNSUPPORTED),
+    (dict(max_nodes=257), tv.TV_ERR_UNSUPPORTED), (dict(max_depth=33), tv.TV_ERR_UNSUPPORTED),
+    (dict(max_nodes=0), tv.TV_ERR_SHAPE), (dict(decay=2), tv.TV_ERR_DTYPE),
+    (dict(qkv_dtype=7), tv.TV_ERR_DTYPE), (dict(total_nodes=9), tv.TV_ERR_SHAPE),
+    (dict(total_nodes=-1), tv.TV_ERR_SHAPE), (dict(node_offsets=None), tv.TV_ERR_NULL),
+    (dict(parent=None), tv.TV_ERR_NULL), (dict(depth=None), tv.TV_ERR_NULL),
+    (dict(node_offsets=A + 4), tv.TV_ERR_ALIGN),
+])
+def test_verify_rejects_bad_problem(lib, kw, code):
+    assert verify_rc(prob(**kw)) == code
+
+
+@pytest.mark.parametrize("field", ["H0", "q", "k", "v", "g", "out", "dev_status"])
+def test_verify_rejects_null_and_misaligned_arrays(lib, field):
+    assert verify_rc(prob(), **{field: None}) == tv.TV_ERR_NULL
+    if field != "dev_status":
+        assert verify_rc(prob(), **{field: P[10] + 8}) == tv.TV_ERR_ALIGN
+
+
+def test_verify_forced_tc_on_unsupported_shape(lib):
+    # fp32 q/k/v and dk=16 are outside the tensor-core kernel
+    assert verify_rc(prob(qkv_dtype=tv.TV_F32), variant=tv.TV_VARIANT_TC) == tv.TV_ERR_UNSUPPORTED
+    assert verify_rc(prob(), variant=9) == tv.TV_ERR_DTYPE
+
+
+def test_empty_batches_are_no_ops(lib):
+    assert verify_rc(prob(B=0, total_nodes=0)) == tv.TV_OK
+    assert verify_rc(prob(total_nodes=0)) == tv.TV_OK
+    rc = tv.tv_accept_greedy(0, 0, 4, 3, P[0], P[1], P[2], P[3], P[4], P[5], P[6], P[7], P[8],
+                             stream=0, check=False)
+    assert rc == tv.TV_OK
+
+
+def test_accept_rejects_bad_arguments(lib):
+    def rc(**kw):
+        a = dict(B=2, T=5, mn=4, md=3, offs=P[0], par=P[1], dr=P[2], tg=P[3], root=P[4],
+                 ln=P[5], path=P[6], bonus=P[7], st=P[8])
+        a.update(kw)
+        return tv.tv_accept_greedy(a["B"], a["T"], a["mn"], a["md"], a["offs"], a["par"],
+                                   a["dr"], a["tg"], a["root"], a["ln"], a["path"], a["bonus"],
+                                   a["st"], stream=0, check=False)
+    assert rc(B=-1) == tv.TV_ERR_SHAPE
+    assert rc(md=0) == tv.TV_ERR_SHAPE
+    assert rc(md=40) == tv.TV_ERR_UNSUPPORTED
+    assert rc(T=100) == tv.TV_ERR_SHAPE
+    assert rc(root=None) == tv.TV_ERR_NULL
+    assert rc(dr=None) == tv.TV_ERR_NULL
+    assert rc(st=None) == tv.TV_ERR_NULL
+    assert rc(path=P[6] + 4) == tv.TV_ERR_ALIGN
+
+
+def test_commit_rejects_bad_arguments(lib):
+    def rc(p=None, **kw):
+        a = dict(H0=P[3], g=P[7], k=P[5], v=P[6], path=P[10], ln=P[11], Hn=P[12], st=P[9])
+        a.update(kw)
+        return tv.tv_commit(p or prob(), a["H0"], a["g"], a["k"], a["v"], a["path"], a["ln"],
+                            a["Hn"], a["st"], stream=0, check=False)
+    assert rc(prob(dv=7)) == tv.TV_ERR_SHAPE
+    assert rc(path=None) == tv.TV_ERR_NULL
+    assert rc(Hn=None) == tv.TV_ERR_NULL
+    assert rc(Hn=P[3] + 16) == tv.TV_ERR_SHAPE      # overlaps H0 without being H0
+    assert rc(Hn=P[12] + 4) == tv.TV_ERR_ALIGN
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        tv.load(str(tmp_path / "missing.so"))

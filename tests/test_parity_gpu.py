@@ -1,0 +1,241 @@
+"""GPU parity: the CUDA library against the fp64 oracle, called through the C ABI.
+
+Outputs and committed states within 2e-3 normwise relative error (per node row,
+per (request, head) matrix); acceptance length, path and bonus bit-exact.
+"""
+import numpy as np
+import pytest
+
+import workloads
+from gpu_util import (TOL, check_accept, check_commit, check_verify, mat_rel_err, row_rel_err,
+                      run_library)
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = {"auto": 0, "simt": 1, "tc": 2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import tree_speculative_verify_tv_gb300 as tv
+    tv.build()
+    tv.load()
+
+
+def _tc_supported(batch):
+    return (batch.qkv_dtype == "bf16" and batch.dk in (64, 128) and batch.dv in (64, 128))
+
+
+def _full_check(batch, variant="auto", units=None):
+    if variant == "tc" and not _tc_supported(batch):
+        pytest.skip("shape outside the tensor-core kernel")
+    res = run_library(batch, variant=VARIANTS[variant])
+    assert res["status"] == 0, res["status"]
+    ev = check_verify(batch, res["out"], units=units)
+    ln, path = check_accept(batch, res)
+    ec = check_commit(batch, res["H_new"], ln, path, units=units)
+    return ev, ec
+
+
+@pytest.mark.parametrize("variant", ["simt", "auto"])
+@pytest.mark.parametrize("c", [1, 2, 3, 4])
+def test_config_full_size(c, variant):
+    _full_check(workloads.make_config(c), variant)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_config1_seeds(seed):
+    _full_check(workloads.config1(seed=seed), "simt")
+
+
+@pytest.mark.parametrize("seed", range(3))
+@pytest.mark.parametrize("variant", ["simt", "auto"])
+def test_config2_seeds(seed, variant):
+    _full_check(workloads.config2(seed=seed), variant)
+
+
+@pytest.mark.parametrize("variant", ["simt", "auto"])
+def test_config5_reduced(variant):
+    _full_check(workloads.config5(B=2, layers=2, heads=4, seed=11), variant)
+
+
+def test_config5_full_size_sampled():
+    """B=8, 36 layers x 32 heads, 256-node trees: every output compared on a sample of
+    (request, head) units the oracle evaluates one by one."""
+    b = workloads.config5()
+    rng = np.random.default_rng(5)
+    units = np.sort(rng.choice(b.B * b.H, 48, replace=False)).astype(np.int32)
+    _full_check(b, "auto", units=units)
+
+
+SHAPES = [  # (dk, dv, decay, dtype)
+    (8, 8, "scalar", "f32"), (16, 24, "diag", "f32"), (32, 16, "scalar", "bf16"),
+    (64, 64, "diag", "bf16"), (64, 128, "scalar", "bf16"), (128, 64, "diag", "bf16"),
+    (96, 40, "scalar", "bf16"), (128, 128, "diag", "f32"), (256, 256, "scalar", "bf16"),
+    (256, 32, "diag", "bf16"),
+]
+
+
+@pytest.mark.parametrize("variant", ["simt", "auto"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "%dx%d-%s-%s" % s)
+def test_random_shapes_ragged(shape, variant):
+    dk, dv, decay, dt = shape
+    rng = np.random.default_rng(dk * 1000 + dv)
+    sizes = [0, 1, 37, 5, 256, 64, 0, 33, 100, 2]
+    b = workloads.random_batch(rng, sizes, 3, dk, dv, decay=decay, qkv_dtype=dt, depth_cap=32,
+                               max_depth=32, max_nodes=256)
+    _full_check(b, variant)
+
+
+@pytest.mark.parametrize("variant", ["simt", "auto"])
+def test_deepest_chain_and_widest_star(variant):
+    rng = np.random.default_rng(3)
+    chain = np.arange(-1, 31, dtype=np.int32)          # depth 32
+    star = np.full(256, -1, dtype=np.int32)            # 256 children of the context
+    parents = [chain, star]
+    b = workloads.assemble(rng, parents, 4, 128, 64, decay="diag", qkv_dtype="bf16",
+                           g_kind="logsig16", h0_std=0.05, vocab=2, max_depth=32, max_nodes=256)
+    # plant a full-depth acceptance along the chain
+    b.draft[:32] = 1
+    b.target[:32] = 1
+    b.root_argmax[0] = 1
+    _full_check(b, variant)
+    res = run_library(b, variant=VARIANTS[variant])
+    assert res["len"][0] == 32
+
+
+def test_strong_decay_and_zero_decay():
+    rng = np.random.default_rng(9)
+    for g_kind, scale in (("zero", 0.0), ("softplus01", 30.0)):
+        b = workloads.random_batch(rng, [17, 40], 2, 64, 64, decay="diag", qkv_dtype="bf16",
+                                   g_kind="softplus01", depth_cap=12, max_depth=12)
+        b.g = (b.g * scale).astype(np.float32)
+        _full_check(b, "simt")
+        _full_check(b, "auto")
+
+
+def test_commit_in_place():
+    b = workloads.config2(seed=4)
+    res = run_library(b, commit_in_place=True)
+    assert res["status"] == 0
+    ln, path = check_accept(b, res)
+    check_commit(b, res["H_new"], ln, path)
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Canary check: verify and commit write exactly their own rows."""
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    b = workloads.random_batch(np.random.default_rng(1), [3, 9, 1], 2, 64, 64, decay="scalar")
+    d = tv.DeviceBatch(b)
+    canary = 12345.0
+    out = torch.full((b.T + 8, b.H, b.dv), canary, device="cuda")
+    Hn = torch.full((b.B + 2, b.H, b.dk, b.dv), canary, device="cuda")
+    d.status.zero_()
+    tv.tv_verify(d.problem(), d.H0, d.q, d.k, d.v, d.g, out, d.status)
+    d.accept()
+    tv.tv_commit(d.problem(), d.H0, d.g, d.k, d.v, d.path, d.accept_len, Hn, d.status)
+    torch.cuda.synchronize()
+    assert int(d.status[0]) == 0
+    assert torch.all(out[b.T:] == canary) and torch.all(Hn[b.B:] == canary)
+    assert not torch.any(out[:b.T] == canary)
+
+
+# ------------------------------------------------------------------ device-detected errors
+
+
+def _bad_tree_batch():
+    rng = np.random.default_rng(2)
+    return workloads.random_batch(rng, [6, 5, 7], 2, 32, 32, decay="scalar", qkv_dtype="bf16",
+                                  depth_cap=6, max_depth=6)
+
+
+@pytest.mark.parametrize("variant", ["simt", "auto"])
+@pytest.mark.parametrize("defect", ["parent_forward", "parent_self", "depth_mismatch",
+                                    "too_deep"])
+def test_malformed_tree_sets_status_and_zero_rows(defect, variant):
+    b = _bad_tree_batch()
+    s = b.node_offsets[1]                      # corrupt request 1 only
+    if defect == "parent_forward":
+        b.parent[s + 2] = 4
+    elif defect == "parent_self":
+        b.parent[s + 3] = 3
+    elif defect == "depth_mismatch":
+        b.depth[s + 4] += 1
+    else:
+        b.max_depth = int(b.depth[s:b.node_offsets[2]].max()) - 1
+        if b.max_depth < 1:
+            pytest.skip("tree too shallow")
+    res = run_library(b, variant=VARIANTS[variant], steps=("verify",))
+    assert res["status"] == 6  # TV_ERR_TREE
+    e = b.node_offsets[2]
+    assert np.all(res["out"][s:e] == 0.0)
+    # the other requests are still correct
+    import oracle
+    units = [u for u in range(b.B * b.H) if u // b.H != 1]
+    if defect == "too_deep":
+        return
+    ref = oracle.verify(b, units=units)
+    for u, o in ref.items():
+        bb, h = divmod(u, b.H)
+        ss, ee = b.node_offsets[bb], b.node_offsets[bb + 1]
+        assert row_rel_err(res["out"][ss:ee, h], o) <= TOL
+
+
+def test_bad_offsets_set_status():
+    b = _bad_tree_batch()
+    b.node_offsets = b.node_offsets.copy()
+    b.node_offsets[2] = b.node_offsets[1] - 1   # negative length for request 1
+    res = run_library(b, steps=("verify",))
+    assert res["status"] == 6
+
+
+def test_accept_path_longer_than_bound_sets_status():
+    n = 6
+    chain = np.arange(-1, n - 1, dtype=np.int32)
+    rng = np.random.default_rng(0)
+    b = workloads.assemble(rng, [chain, chain], 1, 16, 16, decay="scalar", qkv_dtype="f32",
+                           g_kind="softplus01", h0_std=0.1, vocab=2, max_depth=n)
+    b.draft[:] = 1
+    b.target[:] = 1
+    b.root_argmax[:] = [1, 0]
+    b.max_depth = 4                              # walk of request 0 would reach depth 6
+    res = run_library(b, steps=("accept",))
+    assert res["status"] == 6
+    assert res["len"][0] == 0 and res["bonus"][0] == -1 and np.all(res["path"][0] == -1)
+    assert res["len"][1] == 0 and res["bonus"][1] == 0  # request 1: nothing matches
+
+
+def test_commit_rejects_path_that_is_not_a_root_path():
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    b = workloads.config2(seed=1, B=2, H=2)
+    d = tv.DeviceBatch(b)
+    d.status.zero_()
+    d.accept_len.copy_(torch.tensor([2, 1], dtype=torch.int32))
+    d.path.copy_(torch.tensor([[0, 5, -1, -1], [3, -1, -1, -1]], dtype=torch.int32))  # 5 is not a child of 0
+    d.H_new.fill_(7.0)
+    d.commit()
+    torch.cuda.synchronize()
+    assert int(d.status[0]) == 6
+    Hn = d.H_new.cpu().numpy()
+    assert np.all(Hn[0] == 7.0)                  # request 0 untouched
+    import oracle
+    r = oracle.commit(b, np.array([0, 1], np.int32), np.array([[0, -1, -1, -1], [3, -1, -1, -1]],
+                                                              np.int32), units=[2, 3])
+    assert mat_rel_err(Hn[1, 0], r[2]) <= TOL and mat_rel_err(Hn[1, 1], r[3]) <= TOL
+
+
+def test_empty_requests_and_empty_batch():
+    b = workloads.random_batch(np.random.default_rng(4), [0, 0, 3, 0], 2, 16, 16,
+                               decay="scalar", qkv_dtype="f32")
+    _full_check(b, "simt")
+    b0 = workloads.random_batch(np.random.default_rng(4), [0, 0], 2, 16, 16, decay="scalar",
+                                qkv_dtype="f32")
+    res = run_library(b0)
+    assert res["status"] == 0 and np.all(res["len"] == 0)
+    assert np.array_equal(res["bonus"], b0.root_argmax)
+    assert mat_rel_err(res["H_new"], b0.H0.astype(np.float64)) == 0.0

@@ -1,0 +1,139 @@
+// tv_api.cu -- the C ABI of libtreeverify: argument checks, kernel choice, launch.
+//
+// Host-checkable errors return before any CUDA call, so they can be exercised
+// without a GPU.  Nothing here allocates device memory or synchronises.
+#include <stdint.h>
+
+#include <initializer_list>
+
+#include "tv_internal.cuh"
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tv_status check_dims(const tv_problem *p) {
+    if (!p) return TV_ERR_NULL;
+    if (p->B < 0 || p->H < 1 || p->total_nodes < 0) return TV_ERR_SHAPE;
+    if (p->dk < 8 || p->dv < 8 || (p->dk % 8) || (p->dv % 8)) return TV_ERR_SHAPE;
+    if (p->max_nodes < 1 || p->max_depth < 1) return TV_ERR_SHAPE;
+    if (p->dk > TV_MAX_DIM || p->dv > TV_MAX_DIM) return TV_ERR_UNSUPPORTED;
+    if (p->max_nodes > TV_MAX_NODES || p->max_depth > TV_MAX_DEPTH) return TV_ERR_UNSUPPORTED;
+    if (p->decay != TV_DECAY_SCALAR && p->decay != TV_DECAY_DIAG) return TV_ERR_DTYPE;
+    if (p->qkv_dtype != TV_BF16 && p->qkv_dtype != TV_F32) return TV_ERR_DTYPE;
+    if ((int64_t)p->total_nodes > (int64_t)p->B * p->max_nodes) return TV_ERR_SHAPE;
+    if ((int64_t)p->B * p->H > 0x7fffffffLL) return TV_ERR_UNSUPPORTED;
+    if (!p->node_offsets) return TV_ERR_NULL;
+    if (p->total_nodes > 0 && !p->parent) return TV_ERR_NULL;
+    return TV_OK;
+}
+
+tv_status check_ptrs(std::initializer_list<const void *> ptrs) {
+    for (const void *q : ptrs)
+        if (!q) return TV_ERR_NULL;
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return TV_ERR_ALIGN;
+    return TV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *tv_status_string(int32_t s) {
+    switch (s) {
+        case TV_OK: return "TV_OK";
+        case TV_ERR_NULL: return "TV_ERR_NULL: a required pointer is NULL";
+        case TV_ERR_SHAPE: return "TV_ERR_SHAPE: a size argument is out of range";
+        case TV_ERR_DTYPE: return "TV_ERR_DTYPE: unknown decay kind or element type";
+        case TV_ERR_ALIGN: return "TV_ERR_ALIGN: an array pointer is not 16-byte aligned";
+        case TV_ERR_UNSUPPORTED: return "TV_ERR_UNSUPPORTED: a limit of this build is exceeded";
+        case TV_ERR_TREE: return "TV_ERR_TREE: malformed tree, offsets or path";
+        case TV_ERR_CUDA: return "TV_ERR_CUDA: a CUDA runtime call failed";
+        case TV_ERR_TIMEOUT: return "TV_ERR_TIMEOUT: a bounded device wait expired";
+        default: return "unknown tv_status";
+    }
+}
+
+int32_t tv_version(void) { return TV_VERSION; }
+
+tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, const void *k,
+                       const void *v, const float *g, float *out, int32_t *dev_status,
+                       void *stream, int32_t variant) {
+    tv_status st = check_dims(p);
+    if (st != TV_OK) return st;
+    if (!p->depth && p->total_nodes > 0) return TV_ERR_NULL;
+    if (variant < TV_VARIANT_AUTO || variant > TV_VARIANT_TC) return TV_ERR_DTYPE;
+    if (!dev_status) return TV_ERR_NULL;
+    if (p->B == 0 || p->total_nodes == 0) return TV_OK;
+    st = check_ptrs({H0, q, k, v, g, out, p->node_offsets, p->parent, p->depth, dev_status});
+    if (st != TV_OK) return st;
+
+    tv::VerifyArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
+                     p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
+                     H0, q, k, v, g, out, dev_status};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool tc_ok = tv::verify_tc_supported(a);
+    if (variant == TV_VARIANT_TC && !tc_ok) return TV_ERR_UNSUPPORTED;
+    const bool use_tc = variant == TV_VARIANT_TC || (variant == TV_VARIANT_AUTO && tc_ok);
+    cudaError_t e = use_tc ? tv::launch_verify_tc(a, s) : tv::launch_verify_simt(a, s);
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+tv_status tv_verify(const tv_problem *p, const float *H0, const void *q, const void *k,
+                    const void *v, const float *g, float *out, int32_t *dev_status,
+                    void *stream) {
+    return tv_verify_ex(p, H0, q, k, v, g, out, dev_status, stream, TV_VARIANT_AUTO);
+}
+
+tv_status tv_accept_greedy(int32_t B, int32_t total_nodes, int32_t max_nodes, int32_t max_depth,
+                           const int32_t *node_offsets, const int32_t *parent,
+                           const int32_t *draft_tokens, const int32_t *target_argmax,
+                           const int32_t *root_argmax, int32_t *accept_len, int32_t *path,
+                           int32_t *bonus, int32_t *dev_status, void *stream) {
+    if (B < 0 || total_nodes < 0 || max_nodes < 1 || max_depth < 1) return TV_ERR_SHAPE;
+    if (max_nodes > TV_MAX_NODES || max_depth > TV_MAX_DEPTH) return TV_ERR_UNSUPPORTED;
+    if ((int64_t)total_nodes > (int64_t)B * max_nodes) return TV_ERR_SHAPE;
+    if (!node_offsets || !root_argmax || !accept_len || !path || !bonus || !dev_status)
+        return TV_ERR_NULL;
+    if (total_nodes > 0 && (!parent || !draft_tokens || !target_argmax)) return TV_ERR_NULL;
+    if (B == 0) return TV_OK;
+    tv_status st = check_ptrs({node_offsets, root_argmax, accept_len, path, bonus, dev_status});
+    if (st != TV_OK) return st;
+    if (total_nodes > 0) {
+        st = check_ptrs({parent, draft_tokens, target_argmax});
+        if (st != TV_OK) return st;
+    }
+    tv::AcceptArgs a{B, total_nodes, max_nodes, max_depth, node_offsets, parent, draft_tokens,
+                     target_argmax, root_argmax, accept_len, path, bonus, dev_status};
+    cudaError_t e = tv::launch_accept(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+tv_status tv_commit(const tv_problem *p, const float *H0, const float *g, const void *k,
+                    const void *v, const int32_t *path, const int32_t *accept_len,
+                    float *H_new, int32_t *dev_status, void *stream) {
+    tv_status st = check_dims(p);
+    if (st != TV_OK) return st;
+    if (!dev_status || !H0 || !H_new || !path || !accept_len) return TV_ERR_NULL;
+    if (p->total_nodes > 0 && (!g || !k || !v)) return TV_ERR_NULL;
+    if (p->B == 0) return TV_OK;
+    // H_new is H0 or disjoint from it
+    const size_t bytes = (size_t)p->B * p->H * p->dk * p->dv * sizeof(float);
+    const char *h0 = reinterpret_cast<const char *>(H0);
+    const char *hn = reinterpret_cast<const char *>(H_new);
+    if (hn != h0 && hn < h0 + bytes && h0 < hn + bytes) return TV_ERR_SHAPE;
+    st = check_ptrs({H0, H_new, path, accept_len, p->node_offsets, dev_status});
+    if (st != TV_OK) return st;
+    if (p->total_nodes > 0) {
+        st = check_ptrs({g, k, v, p->parent});
+        if (st != TV_OK) return st;
+    }
+    tv::CommitArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
+                     p->decay, p->qkv_dtype, p->node_offsets, p->parent, H0, g, k, v, path,
+                     accept_len, H_new, dev_status};
+    cudaError_t e = tv::launch_commit(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+}  // extern "C"

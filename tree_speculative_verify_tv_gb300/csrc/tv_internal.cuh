@@ -1,0 +1,112 @@
+// tv_internal.cuh -- shared declarations of libtreeverify's kernels and launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "treeverify.h"
+
+namespace tv {
+
+constexpr int kMaxNodes = TV_MAX_NODES;
+constexpr int kMaxDepth = TV_MAX_DEPTH;
+constexpr int kMaxDim = TV_MAX_DIM;
+
+// Everything a verify launch needs, passed by value to the kernels.
+struct VerifyArgs {
+    int32_t B, H, dk, dv, T, max_nodes, max_depth, decay, qkv_dtype;
+    const int32_t *node_offsets, *parent, *depth;
+    const float *H0;
+    const void *q, *k, *v;
+    const float *g;
+    float *out;
+    int32_t *status;
+};
+
+struct AcceptArgs {
+    int32_t B, T, max_nodes, max_depth;
+    const int32_t *node_offsets, *parent, *draft, *target, *root;
+    int32_t *len, *path, *bonus, *status;
+};
+
+struct CommitArgs {
+    int32_t B, H, dk, dv, T, max_nodes, max_depth, decay, qkv_dtype;
+    const int32_t *node_offsets, *parent;
+    const float *H0, *g;
+    const void *k, *v;
+    const int32_t *path, *len;
+    float *H_new;
+    int32_t *status;
+};
+
+cudaError_t launch_verify_simt(const VerifyArgs &a, cudaStream_t s);
+// Returns cudaErrorNotSupported when the shape is outside the tensor-core kernel.
+cudaError_t launch_verify_tc(const VerifyArgs &a, cudaStream_t s);
+bool verify_tc_supported(const VerifyArgs &a);
+cudaError_t launch_accept(const AcceptArgs &a, cudaStream_t s);
+cudaError_t launch_commit(const CommitArgs &a, cudaStream_t s);
+
+// ---------------------------------------------------------------- device helpers
+
+// First error wins; later errors leave the code unchanged.
+__device__ __forceinline__ void report(int32_t *status, int32_t code) {
+    atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename E>
+__device__ __forceinline__ float ldg_f(const E *p, size_t i) {
+    return to_f32(p[i]);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Request b's node range; false when node_offsets are unusable.
+__device__ __forceinline__ bool request_range(const int32_t *offs, int b, int T, int max_nodes,
+                                              int &off, int &n) {
+    off = offs[b];
+    int end = offs[b + 1];
+    n = end - off;
+    return off >= 0 && end >= off && end <= T && n <= max_nodes;
+}
+
+}  // namespace tv
+
+namespace tv {
+
+// Loads one request's parent[] (and depth[] when s_dep != nullptr) into shared
+// memory and checks the tree: parent[i] in [-1, i) (parents precede children,
+// so every root path ends at the context) and depth[i] = depth[parent]+1 (1 for
+// a child of the context) with depth <= max_depth.  Every thread of the block
+// must call it; returns the same verdict in all threads.
+__device__ __forceinline__ bool load_check_tree(const int32_t *parent, const int32_t *depth,
+                                                int off, int n, int max_depth, int *s_par,
+                                                int *s_dep, int *s_flag) {
+    if (threadIdx.x == 0) *s_flag = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        int p = parent[off + i];
+        s_par[i] = p;
+        if (s_dep) s_dep[i] = depth[off + i];
+        if (p < -1 || p >= i) *s_flag = 1;
+    }
+    __syncthreads();
+    if (s_dep && *s_flag == 0) {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            int p = s_par[i];
+            int want = p < 0 ? 1 : s_dep[p] + 1;
+            if (s_dep[i] != want || s_dep[i] > max_depth) *s_flag = 1;
+        }
+    }
+    __syncthreads();
+    return *s_flag == 0;
+}
+
+}  // namespace tv
