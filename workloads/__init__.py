@@ -232,7 +232,7 @@ def assemble(rng, parents: List[np.ndarray], H: int, dk: int, dv: int, *, decay:
                  node_offsets=offs, parent=parent, depth=depth, q=q, k=k, v=v, g=g,
                  H0=H0, draft=np.asarray(draft, np.int32), target=np.asarray(target, np.int32),
                  root_argmax=np.asarray(root_argmax, np.int32),
-                 max_nodes=int(max_nodes if max_nodes is not None else (sizes.max() if B else 1)),
+                 max_nodes=int(max_nodes if max_nodes is not None else max(1, int(sizes.max()) if B else 1)),
                  max_depth=int(max_depth if max_depth is not None else md), name=name)
 
 
