@@ -26,7 +26,9 @@ def _lib():
 
 
 def _tc_supported(batch):
-    return (batch.qkv_dtype == "bf16" and batch.dk in (64, 128) and batch.dv in (64, 128))
+    """Shapes the tcgen05 kernel takes (it reports TV_ERR_UNSUPPORTED otherwise)."""
+    return (batch.qkv_dtype == "bf16" and batch.decay == "scalar" and batch.dk in (64, 128)
+            and batch.dv in (64, 128))
 
 
 def _full_check(batch, variant="auto", units=None):
@@ -44,6 +46,36 @@ def _full_check(batch, variant="auto", units=None):
 @pytest.mark.parametrize("c", [1, 2, 3, 4])
 def test_config_full_size(c, variant):
     _full_check(workloads.make_config(c), variant)
+
+
+@pytest.mark.parametrize("c", [2, 4])
+def test_config_full_size_tensor_core(c):
+    _full_check(workloads.make_config(c), "tc")
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64), (128, 128)])
+def test_tensor_core_ragged_scalar(dk, dv):
+    rng = np.random.default_rng(dk + 7 * dv)
+    sizes = [1, 16, 17, 0, 200, 64, 31, 256, 5]
+    b = workloads.random_batch(rng, sizes, 3, dk, dv, decay="scalar", qkv_dtype="bf16",
+                               depth_cap=32, max_depth=32, max_nodes=256)
+    _full_check(b, "tc")
+
+
+def test_tensor_core_agrees_with_simt():
+    b = workloads.config2(seed=3)
+    r_tc = run_library(b, variant=2, steps=("verify",))
+    r_simt = run_library(b, variant=1, steps=("verify",))
+    assert r_tc["status"] == 0 and r_simt["status"] == 0
+    assert row_rel_err(r_tc["out"], r_simt["out"]) <= 1e-4
+
+
+def test_tensor_core_rejects_unsupported_shapes():
+    import tree_speculative_verify_tv_gb300 as tv
+    b = workloads.config3(B=2, H=2)   # diagonal decay
+    with pytest.raises(tv.TVError) as ei:
+        run_library(b, variant=2, steps=("verify",))
+    assert ei.value.code == tv.TV_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("seed", range(10))
@@ -149,11 +181,11 @@ def test_outputs_stay_inside_their_buffers():
 
 def _bad_tree_batch():
     rng = np.random.default_rng(2)
-    return workloads.random_batch(rng, [6, 5, 7], 2, 32, 32, decay="scalar", qkv_dtype="bf16",
+    return workloads.random_batch(rng, [6, 5, 7], 2, 64, 64, decay="scalar", qkv_dtype="bf16",
                                   depth_cap=6, max_depth=6)
 
 
-@pytest.mark.parametrize("variant", ["simt", "auto"])
+@pytest.mark.parametrize("variant", ["simt", "auto", "tc"])
 @pytest.mark.parametrize("defect", ["parent_forward", "parent_self", "depth_mismatch",
                                     "too_deep"])
 def test_malformed_tree_sets_status_and_zero_rows(defect, variant):
