@@ -184,6 +184,14 @@ class ClockSampler:
 # ---------------------------------------------------------------- distributed
 
 
+def shard_requests(B: int, world: int, rank: int):
+    """Contiguous request range [lo, hi) of `rank` when one batch is split across
+    ranks (requests are independent: no collective is needed on the data path)."""
+    base, extra = divmod(B, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

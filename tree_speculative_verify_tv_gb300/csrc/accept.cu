@@ -5,9 +5,11 @@
 // On a tree: t = root_argmax[b]; move to the lowest-index child whose draft token
 // equals t, set t = target_argmax[child]; stop when no child matches; bonus = t.
 //
-// One warp per request.  Children of node c all have larger indices than c, so
-// each step scans the nodes after the current one 32 at a time; a ballot finds
-// the lowest matching index.  Integer-only, exact.
+// One warp per request.  The request's parent/draft/target arrays are first
+// copied to shared memory with independent coalesced loads (one round trip to
+// memory), then the walk runs on shared memory: children of node c all have
+// larger indices than c, so each step scans the nodes after the current one 32
+// at a time and a ballot finds the lowest matching index.  Integer-only, exact.
 #include "tv_internal.cuh"
 
 namespace tv {
@@ -16,34 +18,43 @@ namespace {
 constexpr int kWarps = 8;
 
 __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    __shared__ int s_par[kWarps][kMaxNodes];
+    __shared__ int s_drf[kWarps][kMaxNodes];
+    __shared__ int s_tgt[kWarps][kMaxNodes];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int b = blockIdx.x * kWarps + w;
     if (b >= a.B) return;
     const int md = a.max_depth;
     int32_t *path = a.path + (size_t)b * md;
+    int *par = s_par[w], *drf = s_drf[w], *tgt = s_tgt[w];
 
     int off, n;
     bool ok = request_range(a.node_offsets, b, a.T, a.max_nodes, off, n);
+    const int32_t root = a.root[b];
     if (ok) {
         // parents precede children: parent[i] in [-1, i)
         bool bad = false;
         for (int i = lane; i < n; i += 32) {
-            int p = a.parent[off + i];
+            const int p = a.parent[off + i];
+            par[i] = p;
+            drf[i] = a.draft[off + i];
+            tgt[i] = a.target[off + i];
             bad |= (p < -1 || p >= i);
         }
         ok = !__any_sync(0xffffffffu, bad);
     }
+    __syncwarp();
 
     int L = 0;
-    int32_t t = a.root[b];
+    int32_t t = root;
     if (ok) {
         int cur = -1;
         for (;;) {
             int found = -1;
             for (int base = cur + 1; base < n; base += 32) {
                 const int i = base + lane;
-                bool hit = i < n && a.parent[off + i] == cur && a.draft[off + i] == t;
-                unsigned m = __ballot_sync(0xffffffffu, hit);
+                const bool hit = i < n && par[i] == cur && drf[i] == t;
+                const unsigned m = __ballot_sync(0xffffffffu, hit);
                 if (m) {
                     found = base + __ffs(m) - 1;
                     break;
@@ -56,7 +67,7 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
             }
             if (lane == 0) path[L] = found;
             ++L;
-            t = a.target[off + found];
+            t = tgt[found];
             cur = found;
         }
     }

@@ -7,11 +7,13 @@
 //   alpha_r  = exp(sum_{l=1..L} g_{p_l, r})
 //   a_{m,r}  = exp(sum_{l=m+1..L} g_{p_l, r}) k_{p_m, r}
 // (for a scalar decay g_{p,r} = g_p).  A streaming rank-L update of H0: each
-// thread reads a float4 of H0, applies the update and writes the float4 of
+// thread reads float4s of H0, applies the update and writes the float4s of
 // H_new, so H_new may be H0 itself.
 //
 // Launch: grid (B*H, ceil(dk/32)), 256 threads; one CTA = 32 key rows of one
-// (request, head).
+// (request, head).  Each thread issues its H0 loads first, so their latency
+// overlaps the path checks and the factor gathers, which are all independent
+// loads issued in parallel.
 #include "tv_internal.cuh"
 
 namespace tv {
@@ -19,11 +21,14 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kRows = 32;
+constexpr int kMaxItems = kRows * (kMaxDim / 4) / kThreads;  // float4s per thread
 
 template <typename E, bool DIAG>
 __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
     __shared__ int s_path[kMaxDepth];
-    __shared__ int s_L, s_flag;
+    __shared__ int s_flag;
+    __shared__ float s_k[kMaxDepth][kRows];
+    __shared__ float s_g[kMaxDepth][kRows];
     __shared__ float s_a[kMaxDepth][kRows];
     __shared__ float s_alpha[kRows];
     extern __shared__ float s_v[];  // [L][dv] value rows of the path
@@ -32,66 +37,84 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
     const int b = unit / a.H, h = unit % a.H;
     const int r0 = blockIdx.y * kRows;
     const int rows = min(kRows, a.dk - r0);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int dk = a.dk, dv = a.dv, H = a.H;
     const E *k = static_cast<const E *>(a.k);
     const E *v = static_cast<const E *>(a.v);
+
+    // this thread's H0 float4s, loaded before anything else
+    const int c4n = dv / 4;
+    const int items = rows * c4n;
+    const float4 *src = reinterpret_cast<const float4 *>(a.H0 + ((size_t)unit * dk + r0) * dv);
+    float4 x[kMaxItems];
+#pragma unroll
+    for (int t = 0; t < kMaxItems; ++t)
+        if (tid + t * kThreads < items) x[t] = src[tid + t * kThreads];
 
     int off, n;
     if (!request_range(a.node_offsets, b, a.T, a.max_nodes, off, n)) {
         if (tid == 0 && h == 0 && blockIdx.y == 0) report(a.status, TV_ERR_TREE);
         return;
     }
-    if (tid == 0) {
+    const int L = a.len[b];
+    if (tid < 32) {
         // the path must be a root path of request b's tree, at most max_depth long
-        int L = a.len[b], bad = (L < 0 || L > a.max_depth);
-        int prev = -1;
-        for (int m = 0; !bad && m < L; ++m) {
-            int p = a.path[(size_t)b * a.max_depth + m];
-            if (p < 0 || p >= n || a.parent[off + p] != prev) bad = 1;
-            else s_path[m] = p;
-            prev = p;
+        bool bad = (L < 0 || L > a.max_depth);
+        int p = -1, par = -2;
+        if (!bad && lane < L) {
+            p = a.path[(size_t)b * a.max_depth + lane];
+            if (p < 0 || p >= n) bad = true;
+            else par = a.parent[off + p];
         }
-        s_L = bad ? 0 : L;
-        s_flag = bad;
+        const int prev = __shfl_up_sync(0xffffffffu, p, 1);
+        if (!bad && lane < L && par != (lane == 0 ? -1 : prev)) bad = true;
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane < L && !bad) s_path[lane] = p;
+        if (lane == 0) s_flag = bad;
     }
     __syncthreads();
     if (s_flag) {
         if (tid == 0 && h == 0 && blockIdx.y == 0) report(a.status, TV_ERR_TREE);
         return;
     }
-    const int L = s_L;
 
+    // gather the path's factor rows (independent loads, all threads)
     for (int e = tid; e < L * dv; e += kThreads) {
-        int m = e / dv, c = e % dv;
+        const int m = e / dv, c = e % dv;
         s_v[e] = ldg_f(v, ((size_t)(off + s_path[m]) * H + h) * dv + c);
     }
+    for (int e = tid; e < L * rows; e += kThreads) {
+        const int m = e / rows, r = e % rows;
+        const size_t row = (size_t)(off + s_path[m]) * H + h;
+        s_k[m][r] = ldg_f(k, row * dk + r0 + r);
+        s_g[m][r] = DIAG ? a.g[row * dk + r0 + r] : a.g[row];
+    }
+    __syncthreads();
     if (tid < rows) {
-        const int r = r0 + tid;
         float s = 0.f;  // sum of g over the path nodes after m
         for (int m = L - 1; m >= 0; --m) {
-            const size_t row = (size_t)(off + s_path[m]) * H + h;
-            s_a[m][tid] = expf(s) * ldg_f(k, row * dk + r);
-            s += DIAG ? a.g[row * dk + r] : a.g[row];
+            s_a[m][tid] = expf(s) * s_k[m][tid];
+            s += s_g[m][tid];
         }
         s_alpha[tid] = expf(s);
     }
     __syncthreads();
 
-    const int c4n = dv / 4;
-    const float4 *src = reinterpret_cast<const float4 *>(a.H0 + ((size_t)unit * dk + r0) * dv);
     float4 *dst = reinterpret_cast<float4 *>(a.H_new + ((size_t)unit * dk + r0) * dv);
-    for (int item = tid; item < rows * c4n; item += kThreads) {
+#pragma unroll
+    for (int t = 0; t < kMaxItems; ++t) {
+        const int item = tid + t * kThreads;
+        if (item >= items) break;
         const int r = item / c4n, c = (item % c4n) * 4;
-        float4 x = src[item];
+        float4 y = x[t];
         const float al = s_alpha[r];
-        x.x *= al; x.y *= al; x.z *= al; x.w *= al;
+        y.x *= al; y.y *= al; y.z *= al; y.w *= al;
         for (int m = 0; m < L; ++m) {
             const float am = s_a[m][r];
-            const float *vm = s_v + m * dv + c;
-            x.x += am * vm[0]; x.y += am * vm[1]; x.z += am * vm[2]; x.w += am * vm[3];
+            const float4 vm = *reinterpret_cast<const float4 *>(s_v + m * dv + c);
+            y.x += am * vm.x; y.y += am * vm.y; y.z += am * vm.z; y.w += am * vm.w;
         }
-        dst[item] = x;
+        dst[item] = y;
     }
 }
 

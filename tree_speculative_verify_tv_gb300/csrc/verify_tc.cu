@@ -39,19 +39,24 @@ __host__ __device__ constexpr uint32_t align_up(uint32_t x, uint32_t a) {
     return (x + a - 1) / a * a;
 }
 
-// Shared-memory plan, identical on host and device.
+// Shared-memory plan, identical on host and device.  TMA destinations are
+// 1024-byte aligned.
 struct TcLayout {
-    uint32_t a_off, b_off, x_off, w_off, eg_off, par_off, dep_off, bar_off, misc_off, total;
+    uint32_t a_off, q_off, k_off, v_off, x_off, w_off, eg_off, g_off, par_off, dep_off, bar_off,
+        misc_off, total;
     __host__ __device__ TcLayout(int dk, int dv, int npad_max, int max_depth) {
-        a_off = 0;                                                    // H0 fp32 / A bf16 hi,lo
-        b_off = align_up(a_off + dk * dv * 4, 1024);                  // q tiles, SW128
-        x_off = align_up(b_off + (dk / 64) * npad_max * 128, 16);     // lo-part exchange
+        a_off = 0;                                               // H0 fp32 -> A bf16 hi,lo
+        q_off = align_up(a_off + dk * dv * 4, 1024);             // q tiles, 128B-swizzled
+        k_off = align_up(q_off + (dk / 64) * npad_max * 128, 1024);  // k rows [n][dk]
+        v_off = align_up(k_off + npad_max * dk * 2, 1024);       // v rows [n][dv]
+        x_off = align_up(v_off + npad_max * dv * 2, 16);         // lo-part exchange (dv = 64)
         w_off = align_up(x_off + (dv == 64 ? npad_max * 64 * 4 : 0), 16);
         eg_off = align_up(w_off + npad_max * max_depth * 4, 16);
-        par_off = align_up(eg_off + npad_max * 4, 16);
+        g_off = align_up(eg_off + npad_max * 4, 16);
+        par_off = align_up(g_off + npad_max * 4, 16);
         dep_off = align_up(par_off + npad_max * 4, 16);
         bar_off = align_up(dep_off + npad_max * 4, 16);
-        misc_off = bar_off + 16;
+        misc_off = bar_off + 32;
         total = align_up(misc_off + 16, 16) + 1024;  // + slack for 1024-byte base alignment
     }
 };
@@ -64,7 +69,9 @@ struct TcParams {
 
 template <int DV>
 __global__ void __launch_bounds__(kThreads, 1)
-    verify_tc_scalar_kernel(const __grid_constant__ CUtensorMap tm_q, const TcParams P) {
+    verify_tc_scalar_kernel(const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const TcParams P) {
     const VerifyArgs &a = P.a;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -73,10 +80,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const TcLayout L(dk, DV, P.npad_max, md);
     float *sH0 = reinterpret_cast<float *>(smem + L.a_off);
     uint8_t *sA = smem + L.a_off;
-    uint8_t *sB = smem + L.b_off;
+    uint8_t *sQ = smem + L.q_off;
+    const __nv_bfloat16 *sK = reinterpret_cast<const __nv_bfloat16 *>(smem + L.k_off);
+    const __nv_bfloat16 *sV = reinterpret_cast<const __nv_bfloat16 *>(smem + L.v_off);
     float *sX = reinterpret_cast<float *>(smem + L.x_off);
     float *sW = reinterpret_cast<float *>(smem + L.w_off);
     float *sEG = reinterpret_cast<float *>(smem + L.eg_off);
+    float *sG = reinterpret_cast<float *>(smem + L.g_off);
     int *sPar = reinterpret_cast<int *>(smem + L.par_off);
     int *sDep = reinterpret_cast<int *>(smem + L.dep_off);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -85,26 +95,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x, b = unit / H, h = unit % H;
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
+    const uint32_t bar_h0 = ptx::smem_addr(&bars[0]);
+    const uint32_t bar_qkv = ptx::smem_addr(&bars[1]);
+    const uint32_t bar_mma = ptx::smem_addr(&bars[2]);
 
-    ptx::grid_dependency_wait();  // inputs may come from the previous kernel in the stream
-
-    int off, n;
-    if (!request_range(a.node_offsets, b, a.T, a.max_nodes, off, n)) {
-        if (tid == 0 && h == 0) report(a.status, TV_ERR_TREE);
-        return;
-    }
-    if (n == 0) return;
-    const int npad = (n + 15) & ~15;
-    const uint32_t bar_load = ptx::smem_addr(&bars[0]);
-    const uint32_t bar_mma = ptx::smem_addr(&bars[1]);
-
-    // ---- barriers, tensor memory, and the unit's loads
+    // ---- prologue that touches no input: barriers, tensor memory
     if (tid == 0) {
         ptx::prefetch_tensormap(&tm_q);
-        ptx::mbar_init(bar_load, 1);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+        ptx::mbar_init(bar_h0, 1);
+        ptx::mbar_init(bar_qkv, 1);
         ptx::mbar_init(bar_mma, 1);
         ptx::fence_mbar_init();
     }
@@ -117,61 +118,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *sTmem;
 
-    const int slabs = dk / 64;
+    // inputs may be written by the previous kernel in the stream
+    ptx::grid_dependency_wait();
     if (tid == 0) {
-        const uint32_t bytes = dk * DV * 4 + slabs * npad * 128;
-        ptx::mbar_arrive_expect_tx(bar_load, bytes);
-        ptx::bulk_g2s(ptx::smem_addr(sH0), a.H0 + (size_t)unit * dk * DV, dk * DV * 4, bar_load);
-        for (int s = 0; s < slabs; ++s)
-            for (int r = 0; r < npad; r += 16)
-                ptx::tma_load_3d(ptx::smem_addr(sB + s * P.npad_max * 128 + r * 128), &tm_q,
-                                 s * 64, h, off + r, bar_load);
+        ptx::mbar_arrive_expect_tx(bar_h0, dk * DV * 4);
+        ptx::bulk_g2s(ptx::smem_addr(sH0), a.H0 + (size_t)unit * dk * DV, dk * DV * 4, bar_h0);
     }
 
-    // ---- tree checks and ancestor scores (overlap the copies)
-    bool ok = load_check_tree(a.parent, a.depth, off, n, md, sPar, sDep, sFlag);
-    if (ok) {
-        const int per_lane = dk / 32;  // 2 or 4 channels per lane
+    int off = 0, n = 0;
+    const bool range_ok = request_range(a.node_offsets, b, a.T, a.max_nodes, off, n);
+    if (!range_ok && tid == 0 && h == 0) report(a.status, TV_ERR_TREE);
+    const int npad = (n + 15) & ~15;
+    const int slabs = dk / 64;
+    const bool have_nodes = range_ok && n > 0;
+    if (have_nodes && tid == 0) {
+        const uint32_t tile = slabs * npad * 128;  // q or k bytes; v: npad * DV * 2
+        ptx::mbar_arrive_expect_tx(bar_qkv, 2 * tile + npad * DV * 2);
+        for (int r = 0; r < npad; r += 16) {
+            for (int s = 0; s < slabs; ++s)
+                ptx::tma_load_3d(ptx::smem_addr(sQ + s * P.npad_max * 128 + r * 128), &tm_q,
+                                 s * 64, h, off + r, bar_qkv);
+            ptx::tma_load_3d(ptx::smem_addr(sK) + r * dk * 2, &tm_k, 0, h, off + r, bar_qkv);
+            ptx::tma_load_3d(ptx::smem_addr(sV) + r * DV * 2, &tm_v, 0, h, off + r, bar_qkv);
+        }
+    }
+    ptx::grid_launch_dependents();
+
+    // ---- tree checks and per-node decays while the copies fly
+    bool ok = have_nodes;
+    if (have_nodes) {
+        for (int i = tid; i < n; i += kThreads) sG[i] = a.g[(size_t)(off + i) * H + h];
+        ok = load_check_tree(a.parent, a.depth, off, n, md, sPar, sDep, sFlag);
+        if (!ok) {
+            for (int e = tid; e < n * DV; e += kThreads)
+                a.out[((size_t)(off + e / DV) * H + h) * DV + e % DV] = 0.f;
+            if (tid == 0 && h == 0) report(a.status, TV_ERR_TREE);
+        }
+    }
+
+    // ---- wait for the copies (always, so no copy outlives the CTA)
+    bool landed = ptx::mbar_wait(bar_h0, 0, kWaitLimit);
+    if (have_nodes) landed = landed && ptx::mbar_wait(bar_qkv, 0, kWaitLimit);
+    const bool all_landed = __syncthreads_and(landed);
+    if (!all_landed && tid == 0) report(a.status, TV_ERR_TIMEOUT);
+    bool run = ok && all_landed;
+
+    // ---- ancestor scores w_ij = e^{G_i - G_j} (q_i . k_j) and e^{G_i}, from shared memory
+    if (run) {
+        const int per_lane = dk / 32;               // 2 or 4 channels per lane
+        const int c0 = lane * per_lane;             // within one 16-byte chunk
         for (int i = warp; i < n; i += kThreads / 32) {
-            const size_t row_i = (size_t)(off + i) * H + h;
+            // q row i sits in a 128-byte-swizzled tile: chunk (c%64)/8 of row i moves to
+            // chunk ((c%64)/8) ^ (i%8)
+            const int slab = c0 / 64, cc = c0 % 64;
+            const uint8_t *qrow = sQ + slab * P.npad_max * 128 + i * 128;
+            const uint8_t *qp = qrow + ((((cc / 8) ^ (i & 7)) * 16) + (cc % 8) * 2);
             float qv[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-                qv[m] = m < per_lane ? __bfloat162float(q[row_i * dk + lane * per_lane + m]) : 0.f;
+            if (per_lane == 4) {
+                const uint2 raw = *reinterpret_cast<const uint2 *>(qp);
+                const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+                const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+                qv[0] = __low2float(p0); qv[1] = __high2float(p0);
+                qv[2] = __low2float(p1); qv[3] = __high2float(p1);
+            } else {
+                const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(qp);
+                qv[0] = __low2float(p0); qv[1] = __high2float(p0);
+                qv[2] = qv[3] = 0.f;
+            }
             float s = 0.f;  // sum of g over the path nodes below the current ancestor
             int j = i, d = 0;
             while (j >= 0) {
-                const size_t row_j = (size_t)(off + j) * H + h;
-                float part = 0.f;
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    if (m < per_lane)
-                        part += qv[m] * __bfloat162float(k[row_j * dk + lane * per_lane + m]);
+                const __nv_bfloat16 *kr = sK + j * dk + c0;
+                float part;
+                if (per_lane == 4) {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(kr);
+                    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+                    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+                    part = qv[0] * __low2float(p0) + qv[1] * __high2float(p0) +
+                           qv[2] * __low2float(p1) + qv[3] * __high2float(p1);
+                } else {
+                    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(kr);
+                    part = qv[0] * __low2float(p0) + qv[1] * __high2float(p0);
+                }
                 part = warp_sum(part);
                 if (lane == 0) sW[i * md + d] = expf(s) * part;
-                s += a.g[row_j];
+                s += sG[j];
                 j = sPar[j];
                 ++d;
             }
             if (lane == 0) sEG[i] = expf(s);
         }
-    } else {
-        for (int e = tid; e < n * DV; e += kThreads)
-            a.out[((size_t)(off + e / DV) * H + h) * DV + e % DV] = 0.f;
-        if (tid == 0 && h == 0) report(a.status, TV_ERR_TREE);
     }
-
-    // ---- wait for H0 and q
-    const bool landed = ptx::mbar_wait(bar_load, 0, kWaitLimit);
-    const bool all_landed = __syncthreads_and(landed);
-    if (!all_landed) {
-        if (tid == 0) report(a.status, TV_ERR_TIMEOUT);
-        ptx::mbar_wait(bar_load, 0, kWaitLimit);
-    }
-    bool run = ok && all_landed;
 
     // ---- split H0 (fp32, [dk][DV]) into bf16 hi/lo, rewritten as K-major A rows
-    constexpr int kItems = DV * 128 / 8 / kThreads;  // (channel, 8-key) items per thread, dk<=128
+    constexpr int kItems = DV * 128 / 8 / kThreads;  // (channel, 8-key) items per thread
     const int items = DV * (dk / 8);
     float hold[kItems][8];
     if (run) {
@@ -221,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- context term on the tensor core
     if (run && tid == 0) {
         const uint32_t idesc = ptx::idesc_bf16_f32(128, npad);
-        const uint32_t a0 = ptx::smem_addr(sA), b0 = ptx::smem_addr(sB);
+        const uint32_t a0 = ptx::smem_addr(sA), b0 = ptx::smem_addr(sQ);
         const int ksteps = dk / 16;
         const int passes = DV == 64 ? 1 : 2;  // DV = 128: hi operand, then lo operand
         for (int p = 0; p < passes; ++p) {
@@ -236,9 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(bar_mma);
     }
     bool mma_ok = true;
-    if (run) {
-        mma_ok = ptx::mbar_wait(bar_mma, 0, kWaitLimit);
-    }
+    if (run) mma_ok = ptx::mbar_wait(bar_mma, 0, kWaitLimit);
     const bool all_mma = __syncthreads_and(mma_ok);
     if (run && !all_mma && tid == 0) report(a.status, TV_ERR_TIMEOUT);
     run = run && all_mma;
@@ -275,8 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o *= sEG[i];
                 int j = i, d = 0;
                 while (j >= 0) {
-                    o += sW[i * md + d] *
-                         __bfloat162float(v[((size_t)(off + j) * H + h) * DV + c]);
+                    o += sW[i * md + d] * __bfloat162float(sV[j * DV + c]);
                     j = sPar[j];
                     ++d;
                 }
@@ -285,7 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    ptx::grid_launch_dependents();
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) ptx::tmem_dealloc(tmem, P.tmem_cols);
@@ -313,18 +349,26 @@ int tmem_columns(int npad_max) {
     return c;
 }
 
+bool encode_rows(CUtensorMap *tm, const void *base, int width, int H, int T, int box_w,
+                 CUtensorMapSwizzle swz) {
+    // rows of `width` bf16 per (node, head): dims (width, H, T), one head per box
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * H};
+    const cuuint32_t box[3] = {(cuuint32_t)box_w, 1, 16};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode_fn()(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DV>
 cudaError_t launch_dv(const VerifyArgs &a, cudaStream_t s) {
-    CUtensorMap tm;
-    const cuuint64_t dims[3] = {(cuuint64_t)a.dk, (cuuint64_t)a.H, (cuuint64_t)a.T};
-    const cuuint64_t strides[2] = {(cuuint64_t)a.dk * 2, (cuuint64_t)a.dk * 2 * a.H};
-    const cuuint32_t box[3] = {64, 1, 16};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = encode_fn()(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.q),
-                             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    CUtensorMap tq, tk, tv_;
+    if (!encode_rows(&tq, a.q, a.dk, a.H, a.T, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_rows(&tk, a.k, a.dk, a.H, a.T, a.dk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_rows(&tv_, a.v, DV, a.H, a.T, DV, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
 
     TcParams P;
     P.a = a;
@@ -364,7 +408,7 @@ cudaError_t launch_dv(const VerifyArgs &a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, tm, P);
+    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv_, P);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
