@@ -186,6 +186,15 @@ tv_status tv_commit(const tv_problem *p, const float *H0, const float *g, const 
                     const void *v, const int32_t *path, const int32_t *accept_len,
                     float *H_new, int32_t *dev_status, void *stream);
 
+/*
+ * tv_verify_variant -- the kernel tv_verify (TV_VARIANT_AUTO) would launch for
+ * this problem: TV_VARIANT_TC or TV_VARIANT_SIMT.  Reads only the sizes and
+ * kinds in *p (no device memory); returns the negative tv_status of an invalid
+ * problem (e.g. -TV_ERR_SHAPE).  The tensor-core kernel takes bf16 q/k/v with
+ * dk, dv in {64, 128} when its shared-memory plan for max_nodes fits one CTA.
+ */
+int32_t tv_verify_variant(const tv_problem *p);
+
 /* Human-readable name of a status code (static string). */
 const char *tv_status_string(int32_t status);
 

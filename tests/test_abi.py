@@ -29,8 +29,8 @@ def declared_functions():
 
 def test_header_declares_the_abi():
     names = declared_functions()
-    assert {"tv_verify", "tv_verify_ex", "tv_accept_greedy", "tv_commit", "tv_status_string",
-            "tv_version"} <= set(names)
+    assert {"tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
+            "tv_status_string", "tv_version"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -102,6 +102,13 @@ def test_verify_forced_tc_on_unsupported_shape(lib):
     # fp32 q/k/v and dk=16 are outside the tensor-core kernel
     assert verify_rc(prob(qkv_dtype=tv.TV_F32), variant=tv.TV_VARIANT_TC) == tv.TV_ERR_UNSUPPORTED
     assert verify_rc(prob(), variant=9) == tv.TV_ERR_DTYPE
+
+
+def test_variant_query_rejects_bad_problems(lib):
+    assert tv.tv_verify_variant(prob(dk=12)) == -tv.TV_ERR_SHAPE
+    assert tv.tv_verify_variant(prob(decay=5)) == -tv.TV_ERR_DTYPE
+    assert tv.tv_verify_variant(prob(qkv_dtype=tv.TV_F32)) == tv.TV_VARIANT_SIMT
+    assert tv.tv_verify_variant(prob(dk=96)) == tv.TV_VARIANT_SIMT
 
 
 def test_empty_batches_are_no_ops(lib):

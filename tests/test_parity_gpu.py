@@ -26,9 +26,13 @@ def _lib():
 
 
 def _tc_supported(batch):
-    """Shapes the tcgen05 kernel takes (it reports TV_ERR_UNSUPPORTED otherwise)."""
-    return (batch.qkv_dtype == "bf16" and batch.decay == "scalar" and batch.dk in (64, 128)
-            and batch.dv in (64, 128))
+    """Whether the library takes this shape on the tcgen05 kernel (it reports
+    TV_ERR_UNSUPPORTED for a forced tensor-core run otherwise)."""
+    import tree_speculative_verify_tv_gb300 as tv
+    p = tv.make_problem(batch.B, batch.H, batch.dk, batch.dv, batch.T, batch.max_nodes,
+                        batch.max_depth, tv.TV_DECAY_DIAG if batch.decay == "diag" else 0,
+                        tv.TV_BF16 if batch.qkv_dtype == "bf16" else tv.TV_F32, 16, 16, 16)
+    return tv.tv_verify_variant(p) == tv.TV_VARIANT_TC
 
 
 def _full_check(batch, variant="auto", units=None):
@@ -48,9 +52,11 @@ def test_config_full_size(c, variant):
     _full_check(workloads.make_config(c), variant)
 
 
-@pytest.mark.parametrize("c", [2, 4])
+@pytest.mark.parametrize("c", [2, 3, 4])
 def test_config_full_size_tensor_core(c):
-    _full_check(workloads.make_config(c), "tc")
+    b = workloads.make_config(c)
+    assert _tc_supported(b)
+    _full_check(b, "tc")
 
 
 @pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64), (128, 128)])
@@ -59,6 +65,17 @@ def test_tensor_core_ragged_scalar(dk, dv):
     sizes = [1, 16, 17, 0, 200, 64, 31, 256, 5]
     b = workloads.random_batch(rng, sizes, 3, dk, dv, decay="scalar", qkv_dtype="bf16",
                                depth_cap=32, max_depth=32, max_nodes=256)
+    assert _tc_supported(b)
+    _full_check(b, "tc")
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64), (128, 128)])
+def test_tensor_core_ragged_diagonal(dk, dv):
+    rng = np.random.default_rng(3 * dk + dv)
+    sizes = [1, 16, 17, 0, 64, 31, 5, 48]
+    b = workloads.random_batch(rng, sizes, 3, dk, dv, decay="diag", qkv_dtype="bf16",
+                               depth_cap=16, max_depth=16, max_nodes=64)
+    assert _tc_supported(b)
     _full_check(b, "tc")
 
 
@@ -72,7 +89,8 @@ def test_tensor_core_agrees_with_simt():
 
 def test_tensor_core_rejects_unsupported_shapes():
     import tree_speculative_verify_tv_gb300 as tv
-    b = workloads.config3(B=2, H=2)   # diagonal decay
+    b = workloads.config5(B=1, layers=1, heads=2)   # 256-node diagonal-decay trees
+    assert not _tc_supported(b)
     with pytest.raises(tv.TVError) as ei:
         run_library(b, variant=2, steps=("verify",))
     assert ei.value.code == tv.TV_ERR_UNSUPPORTED

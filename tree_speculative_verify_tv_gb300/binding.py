@@ -26,8 +26,8 @@ TV_BF16, TV_F32 = 0, 1
 TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC = 0, 1, 2
 TV_MAX_NODES, TV_MAX_DEPTH, TV_MAX_DIM = 256, 32, 256
 
-EXPORTED = ("tv_verify", "tv_verify_ex", "tv_accept_greedy", "tv_commit", "tv_status_string",
-            "tv_version")
+EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
+            "tv_status_string", "tv_version")
 
 
 class tv_problem(ctypes.Structure):
@@ -72,6 +72,8 @@ def load(path: Optional[str] = None):
         L.tv_status_string.restype = ctypes.c_char_p
         L.tv_version.argtypes = []
         L.tv_version.restype = i32
+        L.tv_verify_variant.argtypes = [P]
+        L.tv_verify_variant.restype = i32
         if path is None:
             _lib = L
         return L
@@ -103,6 +105,11 @@ tv_status_string = status_string
 
 def tv_version() -> int:
     return load().tv_version()
+
+
+def tv_verify_variant(problem: tv_problem) -> int:
+    """Kernel tv_verify would choose (TV_VARIANT_TC / TV_VARIANT_SIMT), or -status."""
+    return load().tv_verify_variant(ctypes.byref(problem))
 
 
 def make_problem(B, H, dk, dv, total_nodes, max_nodes, max_depth, decay, qkv_dtype,
@@ -193,6 +200,9 @@ class DeviceBatch:
         self.status = torch.zeros(4, dtype=torch.int32, device=dev)
         if pin:
             self.status = self.status.pin_memory()
+
+    def variant(self) -> int:
+        return tv_verify_variant(self.problem())
 
     def problem(self) -> tv_problem:
         return make_problem(self.B, self.H, self.dk, self.dv, self.T, self.max_nodes,

@@ -57,6 +57,15 @@ const char *tv_status_string(int32_t s) {
 
 int32_t tv_version(void) { return TV_VERSION; }
 
+int32_t tv_verify_variant(const tv_problem *p) {
+    tv_status st = check_dims(p);
+    if (st != TV_OK) return -static_cast<int32_t>(st);
+    tv::VerifyArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
+                     p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
+                     nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    return tv::verify_tc_supported(a) ? TV_VARIANT_TC : TV_VARIANT_SIMT;
+}
+
 tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, const void *k,
                        const void *v, const float *g, float *out, int32_t *dev_status,
                        void *stream, int32_t variant) {

@@ -39,17 +39,25 @@ __host__ __device__ constexpr uint32_t align_up(uint32_t x, uint32_t a) {
     return (x + a - 1) / a * a;
 }
 
-// Shared-memory plan, identical on host and device.  TMA destinations are
-// 1024-byte aligned.
+// Shared-memory plan, identical on host and device.  TMA destinations and
+// 128-byte-swizzled operands are 1024-byte aligned.
+//   scalar decay: q arrives swizzled and is the B operand itself; g is gathered.
+//   diagonal decay: q arrives as dense rows; B = bf16 hi/lo of e^{G_i} * q_i is
+//   written by the warps in the swizzled layout; g arrives as dense fp32 rows and
+//   is turned into exp(g) in place.
 struct TcLayout {
-    uint32_t a_off, q_off, k_off, v_off, x_off, w_off, eg_off, g_off, par_off, dep_off, bar_off,
-        misc_off, total;
-    __host__ __device__ TcLayout(int dk, int dv, int npad_max, int max_depth) {
-        a_off = 0;                                               // H0 fp32 -> A bf16 hi,lo
-        q_off = align_up(a_off + dk * dv * 4, 1024);             // q tiles, 128B-swizzled
-        k_off = align_up(q_off + (dk / 64) * npad_max * 128, 1024);  // k rows [n][dk]
-        v_off = align_up(k_off + npad_max * dk * 2, 1024);       // v rows [n][dv]
-        x_off = align_up(v_off + npad_max * dv * 2, 16);         // lo-part exchange (dv = 64)
+    uint32_t a_off, b_off, blo_off, q_off, k_off, v_off, e_off, x_off, w_off, eg_off, g_off,
+        par_off, dep_off, bar_off, misc_off, total;
+    __host__ __device__ TcLayout(int dk, int dv, int npad_max, int max_depth, bool diag) {
+        const uint32_t swz_tile = (dk / 64) * npad_max * 128;  // one swizzled [n][dk] bf16 tile
+        a_off = 0;                                             // H0 fp32 -> A bf16 hi,lo
+        b_off = align_up(a_off + dk * dv * 4, 1024);           // B (hi) operand
+        blo_off = align_up(b_off + swz_tile, 1024);            // B lo operand (diag)
+        q_off = align_up(blo_off + (diag ? swz_tile : 0), 1024);  // dense q rows (diag)
+        k_off = align_up(q_off + (diag ? npad_max * dk * 2 : 0), 1024);
+        v_off = align_up(k_off + npad_max * dk * 2, 1024);
+        e_off = align_up(v_off + npad_max * dv * 2, 1024);      // g -> exp(g) rows (diag)
+        x_off = align_up(e_off + (diag ? npad_max * dk * 4 : 0), 16);  // lo exchange (dv 64)
         w_off = align_up(x_off + (dv == 64 ? npad_max * 64 * 4 : 0), 16);
         eg_off = align_up(w_off + npad_max * max_depth * 4, 16);
         g_off = align_up(eg_off + npad_max * 4, 16);
@@ -67,22 +75,53 @@ struct TcParams {
     int tmem_cols;
 };
 
-template <int DV>
+__device__ __forceinline__ void load_bf16x(const __nv_bfloat16 *p, int cnt, float (&x)[4]) {
+    if (cnt == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+        x[0] = __low2float(p0); x[1] = __high2float(p0);
+        x[2] = __low2float(p1); x[3] = __high2float(p1);
+    } else {
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(p);
+        x[0] = __low2float(p0); x[1] = __high2float(p0);
+        x[2] = x[3] = 0.f;
+    }
+}
+
+// Byte offset of bf16 element (row, c) in a 128-byte-swizzled K-major tile:
+// slab c/64 of `slab_bytes`, row of 128 bytes, 16-byte chunk (c%64)/8 XOR row%8.
+__device__ __forceinline__ uint32_t swz_offset(int row, int c, uint32_t slab_bytes) {
+    const int cc = c % 64;
+    return (c / 64) * slab_bytes + row * 128 + ((((cc / 8) ^ (row & 7)) * 16) + (cc % 8) * 2);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+}
+
+template <int DV, bool DIAG>
 __global__ void __launch_bounds__(kThreads, 1)
-    verify_tc_scalar_kernel(const __grid_constant__ CUtensorMap tm_q,
-                            const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, const TcParams P) {
+    verify_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_g, const TcParams P) {
     const VerifyArgs &a = P.a;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int dk = a.dk, H = a.H, md = a.max_depth;
-    const TcLayout L(dk, DV, P.npad_max, md);
+    const TcLayout L(dk, DV, P.npad_max, md, DIAG);
+    const uint32_t slab_bytes = P.npad_max * 128;
     float *sH0 = reinterpret_cast<float *>(smem + L.a_off);
     uint8_t *sA = smem + L.a_off;
-    uint8_t *sQ = smem + L.q_off;
+    uint8_t *sB = smem + L.b_off;
+    uint8_t *sBlo = smem + L.blo_off;
+    const __nv_bfloat16 *sQ = reinterpret_cast<const __nv_bfloat16 *>(smem + L.q_off);
     const __nv_bfloat16 *sK = reinterpret_cast<const __nv_bfloat16 *>(smem + L.k_off);
     const __nv_bfloat16 *sV = reinterpret_cast<const __nv_bfloat16 *>(smem + L.v_off);
+    float *sE = reinterpret_cast<float *>(smem + L.e_off);
     float *sX = reinterpret_cast<float *>(smem + L.x_off);
     float *sW = reinterpret_cast<float *>(smem + L.w_off);
     float *sEG = reinterpret_cast<float *>(smem + L.eg_off);
@@ -96,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x, b = unit / H, h = unit % H;
     const uint32_t bar_h0 = ptx::smem_addr(&bars[0]);
-    const uint32_t bar_qkv = ptx::smem_addr(&bars[1]);
+    const uint32_t bar_in = ptx::smem_addr(&bars[1]);
     const uint32_t bar_mma = ptx::smem_addr(&bars[2]);
 
     // ---- prologue that touches no input: barriers, tensor memory
@@ -104,8 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
+        if (DIAG) ptx::prefetch_tensormap(&tm_g);
         ptx::mbar_init(bar_h0, 1);
-        ptx::mbar_init(bar_qkv, 1);
+        ptx::mbar_init(bar_in, 1);
         ptx::mbar_init(bar_mma, 1);
         ptx::fence_mbar_init();
     }
@@ -132,22 +172,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int slabs = dk / 64;
     const bool have_nodes = range_ok && n > 0;
     if (have_nodes && tid == 0) {
-        const uint32_t tile = slabs * npad * 128;  // q or k bytes; v: npad * DV * 2
-        ptx::mbar_arrive_expect_tx(bar_qkv, 2 * tile + npad * DV * 2);
+        const uint32_t rows_bf16 = npad * dk * 2;  // q or k bytes
+        const uint32_t bytes = 2 * rows_bf16 + npad * DV * 2 + (DIAG ? npad * dk * 4 : 0);
+        ptx::mbar_arrive_expect_tx(bar_in, bytes);
         for (int r = 0; r < npad; r += 16) {
-            for (int s = 0; s < slabs; ++s)
-                ptx::tma_load_3d(ptx::smem_addr(sQ + s * P.npad_max * 128 + r * 128), &tm_q,
-                                 s * 64, h, off + r, bar_qkv);
-            ptx::tma_load_3d(ptx::smem_addr(sK) + r * dk * 2, &tm_k, 0, h, off + r, bar_qkv);
-            ptx::tma_load_3d(ptx::smem_addr(sV) + r * DV * 2, &tm_v, 0, h, off + r, bar_qkv);
+            if (DIAG) {
+                ptx::tma_load_3d(ptx::smem_addr(sQ) + r * dk * 2, &tm_q, 0, h, off + r, bar_in);
+                ptx::tma_load_3d(ptx::smem_addr(sE) + r * dk * 4, &tm_g, 0, h, off + r, bar_in);
+            } else {
+                for (int s = 0; s < slabs; ++s)
+                    ptx::tma_load_3d(ptx::smem_addr(sB + s * slab_bytes + r * 128), &tm_q, s * 64,
+                                     h, off + r, bar_in);
+            }
+            ptx::tma_load_3d(ptx::smem_addr(sK) + r * dk * 2, &tm_k, 0, h, off + r, bar_in);
+            ptx::tma_load_3d(ptx::smem_addr(sV) + r * DV * 2, &tm_v, 0, h, off + r, bar_in);
         }
     }
     ptx::grid_launch_dependents();
 
-    // ---- tree checks and per-node decays while the copies fly
+    // ---- tree checks while the copies fly
     bool ok = have_nodes;
     if (have_nodes) {
-        for (int i = tid; i < n; i += kThreads) sG[i] = a.g[(size_t)(off + i) * H + h];
+        if (!DIAG)
+            for (int i = tid; i < n; i += kThreads) sG[i] = a.g[(size_t)(off + i) * H + h];
         ok = load_check_tree(a.parent, a.depth, off, n, md, sPar, sDep, sFlag);
         if (!ok) {
             for (int e = tid; e < n * DV; e += kThreads)
@@ -158,55 +205,80 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- wait for the copies (always, so no copy outlives the CTA)
     bool landed = ptx::mbar_wait(bar_h0, 0, kWaitLimit);
-    if (have_nodes) landed = landed && ptx::mbar_wait(bar_qkv, 0, kWaitLimit);
+    if (have_nodes) landed = ptx::mbar_wait(bar_in, 0, kWaitLimit) && landed;
     const bool all_landed = __syncthreads_and(landed);
     if (!all_landed && tid == 0) report(a.status, TV_ERR_TIMEOUT);
     bool run = ok && all_landed;
 
-    // ---- ancestor scores w_ij = e^{G_i - G_j} (q_i . k_j) and e^{G_i}, from shared memory
+    const int per_lane = dk / 32;    // 2 or 4 key channels per lane
+    const int c0 = lane * per_lane;  // within one 16-byte chunk
+    if (DIAG && run) {
+        for (int e = tid; e < n * dk; e += kThreads) sE[e] = expf(sE[e]);
+        __syncthreads();
+    }
+    // ---- ancestor scores w_ij, and the decayed query, one warp per node
     if (run) {
-        const int per_lane = dk / 32;               // 2 or 4 channels per lane
-        const int c0 = lane * per_lane;             // within one 16-byte chunk
         for (int i = warp; i < n; i += kThreads / 32) {
-            // q row i sits in a 128-byte-swizzled tile: chunk (c%64)/8 of row i moves to
-            // chunk ((c%64)/8) ^ (i%8)
-            const int slab = c0 / 64, cc = c0 % 64;
-            const uint8_t *qrow = sQ + slab * P.npad_max * 128 + i * 128;
-            const uint8_t *qp = qrow + ((((cc / 8) ^ (i & 7)) * 16) + (cc % 8) * 2);
             float qv[4];
-            if (per_lane == 4) {
-                const uint2 raw = *reinterpret_cast<const uint2 *>(qp);
-                const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
-                const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
-                qv[0] = __low2float(p0); qv[1] = __high2float(p0);
-                qv[2] = __low2float(p1); qv[3] = __high2float(p1);
-            } else {
-                const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(qp);
-                qv[0] = __low2float(p0); qv[1] = __high2float(p0);
-                qv[2] = qv[3] = 0.f;
-            }
-            float s = 0.f;  // sum of g over the path nodes below the current ancestor
+            if (DIAG)
+                load_bf16x(sQ + i * dk + c0, per_lane, qv);
+            else
+                load_bf16x(reinterpret_cast<const __nv_bfloat16 *>(sB + swz_offset(i, c0, slab_bytes)),
+                           per_lane, qv);
+            // f = e^{G_i - G_j} for the current ancestor j: per channel (diagonal) or
+            // one value (scalar, carried as the running log sum s)
+            float f[4] = {1.f, 1.f, 1.f, 1.f};
+            float s = 0.f;
             int j = i, d = 0;
             while (j >= 0) {
-                const __nv_bfloat16 *kr = sK + j * dk + c0;
-                float part;
-                if (per_lane == 4) {
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(kr);
-                    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
-                    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
-                    part = qv[0] * __low2float(p0) + qv[1] * __high2float(p0) +
-                           qv[2] * __low2float(p1) + qv[3] * __high2float(p1);
-                } else {
-                    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(kr);
-                    part = qv[0] * __low2float(p0) + qv[1] * __high2float(p0);
-                }
+                float kv[4];
+                load_bf16x(sK + j * dk + c0, per_lane, kv);
+                float part = 0.f;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) part += qv[m] * kv[m] * f[m];
                 part = warp_sum(part);
-                if (lane == 0) sW[i * md + d] = expf(s) * part;
-                s += sG[j];
+                if (lane == 0) sW[i * md + d] = DIAG ? part : expf(s) * part;
+                if (DIAG) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        if (m < per_lane) f[m] *= sE[j * dk + c0 + m];
+                } else {
+                    s += sG[j];
+                }
                 j = sPar[j];
                 ++d;
             }
-            if (lane == 0) sEG[i] = expf(s);
+            if (DIAG) {
+                // B = bf16 hi/lo of e^{G_i} * q_i in the swizzled K-major layout
+                float hi[4], lo[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float x = qv[m] * f[m];
+                    hi[m] = __bfloat162float(__float2bfloat16_rn(x));
+                    lo[m] = x - hi[m];
+                }
+                const uint32_t o = swz_offset(i, c0, slab_bytes);
+                if (per_lane == 4) {
+                    *reinterpret_cast<uint2 *>(sB + o) = make_uint2(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]));
+                    *reinterpret_cast<uint2 *>(sBlo + o) = make_uint2(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]));
+                } else {
+                    *reinterpret_cast<uint32_t *>(sB + o) = pack_bf16(hi[0], hi[1]);
+                    *reinterpret_cast<uint32_t *>(sBlo + o) = pack_bf16(lo[0], lo[1]);
+                }
+            } else if (lane == 0) {
+                sEG[i] = expf(s);
+            }
+        }
+        if (DIAG) {
+            // rows n..npad-1 of B feed unused output columns; keep them finite
+            for (int e = n * 64 + tid; e < npad * 64; e += kThreads) {
+                const int i = e / 64, cq = (e % 64) * 2;
+                const uint32_t o = swz_offset(i, cq, slab_bytes);
+                if (cq < dk) {
+                    *reinterpret_cast<uint32_t *>(sB + o) = 0u;
+                    *reinterpret_cast<uint32_t *>(sBlo + o) = 0u;
+                }
+            }
         }
     }
 
@@ -237,11 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float x0 = hold[t][2 * e], x1 = hold[t][2 * e + 1];
-                    const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                    const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
-                    const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
-                    hi[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-                    lo[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                    const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+                    const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+                    hi[e] = pack_bf16(h0, h1);
+                    lo[e] = pack_bf16(x0 - h0, x1 - h1);
                 }
                 // hi part: rows 0..DV-1; lo part: rows DV..2DV-1 (stacked) for DV = 64,
                 // or a second 128-row operand right after the first for DV = 128.
@@ -258,18 +329,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after_sync();
 
-    // ---- context term on the tensor core
+    // ---- context term on the tensor core: D[c][i] = sum_r A[c][r] B[i][r]
     if (run && tid == 0) {
         const uint32_t idesc = ptx::idesc_bf16_f32(128, npad);
-        const uint32_t a0 = ptx::smem_addr(sA), b0 = ptx::smem_addr(sQ);
+        const uint32_t a_hi = ptx::smem_addr(sA), a_lo = a_hi + 16 * sbo_a;
+        const uint32_t b_hi = ptx::smem_addr(sB), b_lo = ptx::smem_addr(sBlo);
+        // (A, B) operand pairs: products hi*hi, lo*hi (and hi*lo for the decayed query)
+        uint32_t pa[3], pb[3];
+        int npass = 0;
+        if (DV == 64) {  // A stacks hi (rows 0-63) over lo (rows 64-127)
+            pa[npass] = a_hi; pb[npass++] = b_hi;
+            if (DIAG) { pa[npass] = a_hi; pb[npass++] = b_lo; }
+        } else {
+            pa[npass] = a_hi; pb[npass++] = b_hi;
+            pa[npass] = a_lo; pb[npass++] = b_hi;
+            if (DIAG) { pa[npass] = a_hi; pb[npass++] = b_lo; }
+        }
         const int ksteps = dk / 16;
-        const int passes = DV == 64 ? 1 : 2;  // DV = 128: hi operand, then lo operand
-        for (int p = 0; p < passes; ++p) {
-            const uint32_t abase = a0 + p * 16 * sbo_a;  // 128 rows further on
+        for (int p = 0; p < npass; ++p) {
             for (int kk = 0; kk < ksteps; ++kk) {
-                const uint64_t ad = ptx::desc_kmajor_noswizzle(abase + kk * 256, 128, sbo_a);
-                const uint64_t bd = ptx::desc_kmajor_sw128(
-                    b0 + (kk / 4) * P.npad_max * 128 + (kk % 4) * 32, 1024);
+                const uint64_t ad = ptx::desc_kmajor_noswizzle(pa[p] + kk * 256, 128, sbo_a);
+                const uint64_t bd =
+                    ptx::desc_kmajor_sw128(pb[p] + (kk / 4) * slab_bytes + (kk % 4) * 32, 1024);
                 ptx::mma_bf16(tmem, ad, bd, idesc, (p > 0 || kk > 0) ? 1u : 0u);
             }
         }
@@ -310,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i >= n) break;
                 float o = vals[e];
                 if (DV == 64) o += sX[i * 64 + c];
-                o *= sEG[i];
+                if (!DIAG) o *= sEG[i];
                 int j = i, d = 0;
                 while (j >= 0) {
                     o += sW[i * md + d] * __bfloat162float(sV[j * DV + c]);
@@ -349,34 +430,47 @@ int tmem_columns(int npad_max) {
     return c;
 }
 
-bool encode_rows(CUtensorMap *tm, const void *base, int width, int H, int T, int box_w,
-                 CUtensorMapSwizzle swz) {
-    // rows of `width` bf16 per (node, head): dims (width, H, T), one head per box
+bool encode_rows(CUtensorMap *tm, const void *base, CUtensorMapDataType dt, int esize, int width,
+                 int H, int T, int box_w, CUtensorMapSwizzle swz) {
+    // rows of `width` elements per (node, head): dims (width, H, T), one head per box
     const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)H, (cuuint64_t)T};
-    const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * H};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * esize, (cuuint64_t)width * esize * H};
     const cuuint32_t box[3] = {(cuuint32_t)box_w, 1, 16};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return encode_fn()(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return encode_fn()(tm, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DV>
-cudaError_t launch_dv(const VerifyArgs &a, cudaStream_t s) {
-    CUtensorMap tq, tk, tv_;
-    if (!encode_rows(&tq, a.q, a.dk, a.H, a.T, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_rows(&tk, a.k, a.dk, a.H, a.T, a.dk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_rows(&tv_, a.v, DV, a.H, a.T, DV, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
+constexpr size_t kSmemLimit = 227 * 1024;
+
+size_t tc_smem_bytes(const VerifyArgs &a) {
+    const int npad_max = (a.max_nodes + 15) & ~15;
+    return TcLayout(a.dk, a.dv, npad_max, a.max_depth, a.decay == TV_DECAY_DIAG).total;
+}
+
+template <int DV, bool DIAG>
+cudaError_t launch_tc(const VerifyArgs &a, cudaStream_t s) {
+    const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tq, tk, tv_, tg;
+    bool enc = encode_rows(&tk, a.k, BF, 2, a.dk, a.H, a.T, a.dk, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+               encode_rows(&tv_, a.v, BF, 2, DV, a.H, a.T, DV, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (DIAG) {
+        enc = enc && encode_rows(&tq, a.q, BF, 2, a.dk, a.H, a.T, a.dk, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              encode_rows(&tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dk, a.H, a.T, a.dk,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+        enc = enc && encode_rows(&tq, a.q, BF, 2, a.dk, a.H, a.T, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+        tg = tk;  // unused
+    }
+    if (!enc) return cudaErrorInvalidValue;
 
     TcParams P;
     P.a = a;
     P.npad_max = (a.max_nodes + 15) & ~15;
     P.tmem_cols = tmem_columns(P.npad_max);
-    const TcLayout L(a.dk, DV, P.npad_max, a.max_depth);
-    size_t smem = L.total;
-    auto kern = verify_tc_scalar_kernel<DV>;
+    size_t smem = tc_smem_bytes(a);
+    auto kern = verify_tc_kernel<DV, DIAG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
@@ -408,7 +502,7 @@ cudaError_t launch_dv(const VerifyArgs &a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv_, P);
+    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv_, tg, P);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -416,13 +510,15 @@ cudaError_t launch_dv(const VerifyArgs &a, cudaStream_t s) {
 }  // namespace
 
 bool verify_tc_supported(const VerifyArgs &a) {
-    return a.qkv_dtype == TV_BF16 && a.decay == TV_DECAY_SCALAR && (a.dk == 64 || a.dk == 128) &&
-           (a.dv == 64 || a.dv == 128) && a.max_nodes <= kMaxNodes && encode_fn() != nullptr;
+    return a.qkv_dtype == TV_BF16 && (a.dk == 64 || a.dk == 128) && (a.dv == 64 || a.dv == 128) &&
+           a.max_nodes <= kMaxNodes && tc_smem_bytes(a) <= kSmemLimit && encode_fn() != nullptr;
 }
 
 cudaError_t launch_verify_tc(const VerifyArgs &a, cudaStream_t s) {
     if (!verify_tc_supported(a)) return cudaErrorNotSupported;
-    return a.dv == 64 ? launch_dv<64>(a, s) : launch_dv<128>(a, s);
+    const bool diag = a.decay == TV_DECAY_DIAG;
+    if (a.dv == 64) return diag ? launch_tc<64, true>(a, s) : launch_tc<64, false>(a, s);
+    return diag ? launch_tc<128, true>(a, s) : launch_tc<128, false>(a, s);
 }
 
 }  // namespace tv
