@@ -10,75 +10,84 @@
 // thread reads float4s of H0, applies the update and writes the float4s of
 // H_new, so H_new may be H0 itself.
 //
-// Launch: grid (B*H, ceil(dk/32)), 256 threads; one CTA = 32 key rows of one
-// (request, head).  Each thread issues its H0 loads first, so their latency
-// overlaps the path checks and the factor gathers, which are all independent
-// loads issued in parallel.
+// Launch: grid (B*H, ceil(dk/rows)), 256 threads; one CTA = 8192/dv key rows of
+// one (request, head) (all 128 at dv = 64), 8 float4s per thread.  Memory round trips before the stream are kept to two: the
+// H0 float4s, the request's offsets, the accepted length and path go out
+// together; then the path's parents (for the root-path check) and its factor
+// rows are gathered together.
 #include "tv_internal.cuh"
 
 namespace tv {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRows = 32;
-constexpr int kMaxItems = kRows * (kMaxDim / 4) / kThreads;  // float4s per thread
+constexpr int kItems = 8;                                 // float4s per thread
+constexpr int kRowsMax = kItems * kThreads * 4 / 64;      // 128 key rows at dv = 64
+
+// Key rows per CTA: kItems float4s per thread cover 8192 / dv rows.
+__host__ __device__ inline int rows_per_cta(int dk, int dv) {
+    const int r = kItems * kThreads * 4 / dv;
+    return r < dk ? r : dk;
+}
 
 template <typename E, bool DIAG>
 __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
     __shared__ int s_path[kMaxDepth];
-    __shared__ int s_flag;
-    __shared__ float s_k[kMaxDepth][kRows];
-    __shared__ float s_g[kMaxDepth][kRows];
-    __shared__ float s_a[kMaxDepth][kRows];
-    __shared__ float s_alpha[kRows];
+    __shared__ int s_bad, s_bad2, s_L, s_off;
+    __shared__ float s_k[kMaxDepth][kRowsMax];
+    __shared__ float s_g[kMaxDepth][kRowsMax];
+    __shared__ float s_alpha[kRowsMax];
     extern __shared__ float s_v[];  // [L][dv] value rows of the path
 
     const int unit = blockIdx.x;
     const int b = unit / a.H, h = unit % a.H;
-    const int r0 = blockIdx.y * kRows;
-    const int rows = min(kRows, a.dk - r0);
+    const int rpc = rows_per_cta(a.dk, a.dv);
+    const int r0 = blockIdx.y * rpc;
+    const int rows = min(rpc, a.dk - r0);
     const int tid = threadIdx.x, lane = tid & 31;
-    const int dk = a.dk, dv = a.dv, H = a.H;
+    const int dk = a.dk, dv = a.dv, H = a.H, md = a.max_depth;
     const E *k = static_cast<const E *>(a.k);
     const E *v = static_cast<const E *>(a.v);
 
-    // this thread's H0 float4s, loaded before anything else
+    // round trip 1: this thread's H0 float4s, the offsets, the length and the path
     const int c4n = dv / 4;
     const int items = rows * c4n;
     const float4 *src = reinterpret_cast<const float4 *>(a.H0 + ((size_t)unit * dk + r0) * dv);
-    float4 x[kMaxItems];
+    float4 x[kItems];
 #pragma unroll
-    for (int t = 0; t < kMaxItems; ++t)
+    for (int t = 0; t < kItems; ++t)
         if (tid + t * kThreads < items) x[t] = src[tid + t * kThreads];
-
-    int off, n;
-    if (!request_range(a.node_offsets, b, a.T, a.max_nodes, off, n)) {
-        if (tid == 0 && h == 0 && blockIdx.y == 0) report(a.status, TV_ERR_TREE);
-        return;
-    }
-    const int L = a.len[b];
     if (tid < 32) {
-        // the path must be a root path of request b's tree, at most max_depth long
-        bool bad = (L < 0 || L > a.max_depth);
-        int p = -1, par = -2;
-        if (!bad && lane < L) {
-            p = a.path[(size_t)b * a.max_depth + lane];
-            if (p < 0 || p >= n) bad = true;
-            else par = a.parent[off + p];
-        }
-        const int prev = __shfl_up_sync(0xffffffffu, p, 1);
-        if (!bad && lane < L && par != (lane == 0 ? -1 : prev)) bad = true;
+        int off, n;
+        const bool range = request_range(a.node_offsets, b, a.T, a.max_nodes, off, n);
+        const int L = a.len[b];
+        const int p = lane < md ? a.path[(size_t)b * md + lane] : -1;
+        bool bad = !range || L < 0 || L > md || (lane < L && (p < 0 || p >= n));
         bad = __any_sync(0xffffffffu, bad);
         if (lane < L && !bad) s_path[lane] = p;
-        if (lane == 0) s_flag = bad;
+        if (lane == 0) {
+            s_bad = bad;
+            s_L = bad ? 0 : L;
+            s_off = off;
+        }
     }
     __syncthreads();
-    if (s_flag) {
+    if (s_bad) {
         if (tid == 0 && h == 0 && blockIdx.y == 0) report(a.status, TV_ERR_TREE);
         return;
     }
+    const int L = s_L, off = s_off;
 
-    // gather the path's factor rows (independent loads, all threads)
+    // round trip 2: root-path check and the path's factor rows
+    if (tid < 32) {
+        bool bad = false;
+        if (lane < L) {
+            const int par = a.parent[off + s_path[lane]];
+            bad = par != (lane == 0 ? -1 : s_path[lane - 1]);
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) s_bad2 = bad;
+    }
     for (int e = tid; e < L * dv; e += kThreads) {
         const int m = e / dv, c = e % dv;
         s_v[e] = ldg_f(v, ((size_t)(off + s_path[m]) * H + h) * dv + c);
@@ -90,11 +99,16 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
         s_g[m][r] = DIAG ? a.g[row * dk + r0 + r] : a.g[row];
     }
     __syncthreads();
+    if (s_bad2) {
+        if (tid == 0 && h == 0 && blockIdx.y == 0) report(a.status, TV_ERR_TREE);
+        return;
+    }
     if (tid < rows) {
         float s = 0.f;  // sum of g over the path nodes after m
         for (int m = L - 1; m >= 0; --m) {
-            s_a[m][tid] = expf(s) * s_k[m][tid];
-            s += s_g[m][tid];
+            const float gm = s_g[m][tid];
+            s_k[m][tid] *= expf(s);  // a_{m,r}
+            s += gm;
         }
         s_alpha[tid] = expf(s);
     }
@@ -102,7 +116,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
 
     float4 *dst = reinterpret_cast<float4 *>(a.H_new + ((size_t)unit * dk + r0) * dv);
 #pragma unroll
-    for (int t = 0; t < kMaxItems; ++t) {
+    for (int t = 0; t < kItems; ++t) {
         const int item = tid + t * kThreads;
         if (item >= items) break;
         const int r = item / c4n, c = (item % c4n) * 4;
@@ -110,7 +124,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
         const float al = s_alpha[r];
         y.x *= al; y.y *= al; y.z *= al; y.w *= al;
         for (int m = 0; m < L; ++m) {
-            const float am = s_a[m][r];
+            const float am = s_k[m][r];
             const float4 vm = *reinterpret_cast<const float4 *>(s_v + m * dv + c);
             y.x += am * vm.x; y.y += am * vm.y; y.z += am * vm.z; y.w += am * vm.w;
         }
@@ -120,8 +134,13 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
 
 template <typename E, bool DIAG>
 cudaError_t launch_typed(const CommitArgs &a, cudaStream_t s) {
-    dim3 grid((unsigned)(a.B * a.H), (unsigned)((a.dk + kRows - 1) / kRows));
+    const int rpc = rows_per_cta(a.dk, a.dv);
+    dim3 grid((unsigned)(a.B * a.H), (unsigned)((a.dk + rpc - 1) / rpc));
     size_t smem = (size_t)a.max_depth * a.dv * sizeof(float);
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        commit_kernel<E, DIAG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        kMaxDepth * kMaxDim * (int)sizeof(float));
+    if (attr != cudaSuccess) return attr;
     commit_kernel<E, DIAG><<<grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }

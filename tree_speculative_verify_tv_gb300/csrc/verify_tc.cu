@@ -39,32 +39,41 @@ __host__ __device__ constexpr uint32_t align_up(uint32_t x, uint32_t a) {
     return (x + a - 1) / a * a;
 }
 
+constexpr int kChunkRows = 32;  // H0 key rows per streamed chunk
+constexpr int kMaxChunks = 4;   // dk <= 128
+
 // Shared-memory plan, identical on host and device.  TMA destinations and
 // 128-byte-swizzled operands are 1024-byte aligned.
+//   A region: H0 streams in as kChunkRows-row fp32 chunks; each chunk is split in
+//     place into bf16 hi/lo K-major operand rows (value channels) of the same size.
 //   scalar decay: q arrives swizzled and is the B operand itself; g is gathered.
 //   diagonal decay: q arrives as dense rows; B = bf16 hi/lo of e^{G_i} * q_i is
-//   written by the warps in the swizzled layout; g arrives as dense fp32 rows and
-//   is turned into exp(g) in place.
+//     written by the warps in the swizzled layout; g arrives as dense fp32 rows and
+//     becomes exp(g) in place.
+//   The lo-part exchange (dv = 64) reuses the A region when it is large enough.
 struct TcLayout {
     uint32_t a_off, b_off, blo_off, q_off, k_off, v_off, e_off, x_off, w_off, eg_off, g_off,
         par_off, dep_off, bar_off, misc_off, total;
     __host__ __device__ TcLayout(int dk, int dv, int npad_max, int max_depth, bool diag) {
         const uint32_t swz_tile = (dk / 64) * npad_max * 128;  // one swizzled [n][dk] bf16 tile
-        a_off = 0;                                             // H0 fp32 -> A bf16 hi,lo
-        b_off = align_up(a_off + dk * dv * 4, 1024);           // B (hi) operand
+        const uint32_t a_bytes = dk * dv * 4;
+        const bool x_in_a = dv != 64 || (uint32_t)npad_max * 64 * 4 <= a_bytes;
+        a_off = 0;
+        b_off = align_up(a_off + a_bytes, 1024);               // B (hi) operand
         blo_off = align_up(b_off + swz_tile, 1024);            // B lo operand (diag)
         q_off = align_up(blo_off + (diag ? swz_tile : 0), 1024);  // dense q rows (diag)
         k_off = align_up(q_off + (diag ? npad_max * dk * 2 : 0), 1024);
         v_off = align_up(k_off + npad_max * dk * 2, 1024);
         e_off = align_up(v_off + npad_max * dv * 2, 1024);      // g -> exp(g) rows (diag)
-        x_off = align_up(e_off + (diag ? npad_max * dk * 4 : 0), 16);  // lo exchange (dv 64)
-        w_off = align_up(x_off + (dv == 64 ? npad_max * 64 * 4 : 0), 16);
+        x_off = align_up(e_off + (diag ? npad_max * dk * 4 : 0), 16);
+        w_off = align_up(x_off + (x_in_a ? 0 : npad_max * 64 * 4), 16);
+        if (x_in_a) x_off = a_off;
         eg_off = align_up(w_off + npad_max * max_depth * 4, 16);
         g_off = align_up(eg_off + npad_max * 4, 16);
         par_off = align_up(g_off + npad_max * 4, 16);
         dep_off = align_up(par_off + npad_max * 4, 16);
         bar_off = align_up(dep_off + npad_max * 4, 16);
-        misc_off = bar_off + 32;
+        misc_off = bar_off + 8 * 8;
         total = align_up(misc_off + 16, 16) + 1024;  // + slack for 1024-byte base alignment
     }
 };
@@ -114,7 +123,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dk = a.dk, H = a.H, md = a.max_depth;
     const TcLayout L(dk, DV, P.npad_max, md, DIAG);
     const uint32_t slab_bytes = P.npad_max * 128;
-    float *sH0 = reinterpret_cast<float *>(smem + L.a_off);
     uint8_t *sA = smem + L.a_off;
     uint8_t *sB = smem + L.b_off;
     uint8_t *sBlo = smem + L.blo_off;
@@ -134,9 +142,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x, b = unit / H, h = unit % H;
-    const uint32_t bar_h0 = ptx::smem_addr(&bars[0]);
-    const uint32_t bar_in = ptx::smem_addr(&bars[1]);
-    const uint32_t bar_mma = ptx::smem_addr(&bars[2]);
+    const int nchunks = dk / kChunkRows;
+    const uint32_t chunk_bytes = kChunkRows * DV * 4;  // fp32 in == bf16 hi + lo out
+    // barriers: 0..3 H0 chunks, 4 factor tiles, 5 MMA completion
+    const uint32_t bar0 = ptx::smem_addr(&bars[0]);
+    const uint32_t bar_in = ptx::smem_addr(&bars[kMaxChunks]);
+    const uint32_t bar_mma = ptx::smem_addr(&bars[kMaxChunks + 1]);
 
     // ---- prologue that touches no input: barriers, tensor memory
     if (tid == 0) {
@@ -144,9 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
         if (DIAG) ptx::prefetch_tensormap(&tm_g);
-        ptx::mbar_init(bar_h0, 1);
-        ptx::mbar_init(bar_in, 1);
-        ptx::mbar_init(bar_mma, 1);
+        for (int c = 0; c < kMaxChunks + 2; ++c) ptx::mbar_init(bar0 + 8 * c, 1);
         ptx::fence_mbar_init();
     }
     if (warp == 0) {
@@ -161,8 +170,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // inputs may be written by the previous kernel in the stream
     ptx::grid_dependency_wait();
     if (tid == 0) {
-        ptx::mbar_arrive_expect_tx(bar_h0, dk * DV * 4);
-        ptx::bulk_g2s(ptx::smem_addr(sH0), a.H0 + (size_t)unit * dk * DV, dk * DV * 4, bar_h0);
+        // H0 (contiguous dk x DV fp32) streams in as row chunks, each on its own barrier
+        const float *src = a.H0 + (size_t)unit * dk * DV;
+        for (int c = 0; c < nchunks; ++c) {
+            ptx::mbar_arrive_expect_tx(bar0 + 8 * c, chunk_bytes);
+            ptx::bulk_g2s(ptx::smem_addr(sA) + c * chunk_bytes, src + c * kChunkRows * DV,
+                          chunk_bytes, bar0 + 8 * c);
+        }
     }
 
     int off = 0, n = 0;
@@ -203,12 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // ---- wait for the copies (always, so no copy outlives the CTA)
-    bool landed = ptx::mbar_wait(bar_h0, 0, kWaitLimit);
-    if (have_nodes) landed = ptx::mbar_wait(bar_in, 0, kWaitLimit) && landed;
-    const bool all_landed = __syncthreads_and(landed);
-    if (!all_landed && tid == 0) report(a.status, TV_ERR_TIMEOUT);
-    bool run = ok && all_landed;
+    // ---- factor tiles (q, k, v, g) land first: ancestor scores while H0 streams
+    bool landed = true;
+    if (have_nodes) landed = ptx::mbar_wait(bar_in, 0, kWaitLimit);
+    bool run = __syncthreads_and(landed) ;
+    if (!run && tid == 0) report(a.status, TV_ERR_TIMEOUT);
+    run = run && ok;
 
     const int per_lane = dk / 32;    // 2 or 4 key channels per lane
     const int c0 = lane * per_lane;  // within one 16-byte chunk
@@ -216,7 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = tid; e < n * dk; e += kThreads) sE[e] = expf(sE[e]);
         __syncthreads();
     }
-    // ---- ancestor scores w_ij, and the decayed query, one warp per node
     if (run) {
         for (int i = warp; i < n; i += kThreads / 32) {
             float qv[4];
@@ -279,32 +292,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint32_t *>(sBlo + o) = 0u;
                 }
             }
+            ptx::fence_proxy_async_smem();
         }
     }
 
-    // ---- split H0 (fp32, [dk][DV]) into bf16 hi/lo, rewritten as K-major A rows
-    constexpr int kItems = DV * 128 / 8 / kThreads;  // (channel, 8-key) items per thread
-    const int items = DV * (dk / 8);
-    float hold[kItems][8];
-    if (run) {
+    // ---- H0 chunk by chunk: split in place into bf16 hi/lo K-major rows, then MMA.
+    // Chunk layout (kChunkRows keys): operand rows (value channels) in 8-row groups
+    // of 512 bytes (4 core matrices of 8 rows x 8 keys); DV = 64 stacks hi rows
+    // 0..63 over lo rows 64..127; DV = 128 keeps a hi operand and a lo operand of
+    // 128 rows, 8 KB each.  D[c][i] accumulates sum_r A[c][r] B[i][r] in TMEM.
+    constexpr int kItems = DV * (kChunkRows / 8) / kThreads;  // (channel, 8-key) items per thread
+    const uint32_t idesc = ptx::idesc_bf16_f32(128, npad);
+    const uint32_t b_hi = ptx::smem_addr(sB), b_lo = ptx::smem_addr(sBlo);
+    for (int c = 0; c < nchunks; ++c) {
+        uint8_t *chunk = sA + c * chunk_bytes;
+        const float *f32 = reinterpret_cast<const float *>(chunk);
+        const bool got = ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit);
+        float hold[kItems][8];
+        if (run && got) {
 #pragma unroll
-        for (int t = 0; t < kItems; ++t) {
-            const int it = tid + t * kThreads;
-            if (it < items) {
-                const int c = it % DV, kq = it / DV;
+            for (int t = 0; t < kItems; ++t) {
+                const int it = tid + t * kThreads;
+                const int ch = it % DV, kq = it / DV;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) hold[t][e] = sH0[(kq * 8 + e) * DV + c];
+                for (int e = 0; e < 8; ++e) hold[t][e] = f32[(kq * 8 + e) * DV + ch];
             }
         }
-    }
-    __syncthreads();
-    const uint32_t sbo_a = dk * 16;  // bytes per 8-row group of A
-    if (run) {
+        if (!__syncthreads_and(got)) {
+            if (tid == 0 && run) report(a.status, TV_ERR_TIMEOUT);
+            run = false;
+        }
+        if (run) {
 #pragma unroll
-        for (int t = 0; t < kItems; ++t) {
-            const int it = tid + t * kThreads;
-            if (it < items) {
-                const int c = it % DV, kq = it / DV;
+            for (int t = 0; t < kItems; ++t) {
+                const int it = tid + t * kThreads;
+                const int ch = it % DV, kq = it / DV;
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -314,48 +336,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     hi[e] = pack_bf16(h0, h1);
                     lo[e] = pack_bf16(x0 - h0, x1 - h1);
                 }
-                // hi part: rows 0..DV-1; lo part: rows DV..2DV-1 (stacked) for DV = 64,
-                // or a second 128-row operand right after the first for DV = 128.
-                const int r_hi = c, r_lo = DV + c;
-                uint4 *ph = reinterpret_cast<uint4 *>(sA + (r_hi / 8) * sbo_a + kq * 128 + (r_hi % 8) * 16);
-                uint4 *pl = reinterpret_cast<uint4 *>(sA + (r_lo / 8) * sbo_a + kq * 128 + (r_lo % 8) * 16);
-                *ph = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *pl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                const int r_hi = ch;
+                const int r_lo = DV == 64 ? 64 + ch : ch;
+                uint8_t *lo_base = DV == 64 ? chunk : chunk + 8192;
+                *reinterpret_cast<uint4 *>(chunk + (r_hi / 8) * 512 + kq * 128 + (r_hi % 8) * 16) =
+                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(lo_base + (r_lo / 8) * 512 + kq * 128 + (r_lo % 8) * 16) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            ptx::fence_proxy_async_smem();
+        }
+        ptx::tc_fence_before_sync();
+        __syncthreads();
+        ptx::tc_fence_after_sync();
+        if (run && tid == 0) {
+            const uint32_t a_hi = ptx::smem_addr(chunk);
+            const uint32_t a_lo = DV == 64 ? a_hi : a_hi + 8192;
+            uint32_t pa[3], pb[3];
+            int npass = 0;
+            pa[npass] = a_hi; pb[npass++] = b_hi;  // DV = 64: hi and lo rows together
+            if (DV == 128) { pa[npass] = a_lo; pb[npass++] = b_hi; }
+            if (DIAG) { pa[npass] = a_hi; pb[npass++] = b_lo; }
+            for (int p = 0; p < npass; ++p) {
+                for (int s2 = 0; s2 < kChunkRows / 16; ++s2) {
+                    const int kk = c * (kChunkRows / 16) + s2;  // global 16-key step
+                    const uint64_t ad = ptx::desc_kmajor_noswizzle(pa[p] + s2 * 256, 128, 512);
+                    const uint64_t bd = ptx::desc_kmajor_sw128(
+                        pb[p] + (kk / 4) * slab_bytes + (kk % 4) * 32, 1024);
+                    ptx::mma_bf16(tmem, ad, bd, idesc, (c > 0 || p > 0 || s2 > 0) ? 1u : 0u);
+                }
             }
         }
-        ptx::fence_proxy_async_smem();
     }
-    ptx::tc_fence_before_sync();
-    __syncthreads();
-    ptx::tc_fence_after_sync();
-
-    // ---- context term on the tensor core: D[c][i] = sum_r A[c][r] B[i][r]
-    if (run && tid == 0) {
-        const uint32_t idesc = ptx::idesc_bf16_f32(128, npad);
-        const uint32_t a_hi = ptx::smem_addr(sA), a_lo = a_hi + 16 * sbo_a;
-        const uint32_t b_hi = ptx::smem_addr(sB), b_lo = ptx::smem_addr(sBlo);
-        // (A, B) operand pairs: products hi*hi, lo*hi (and hi*lo for the decayed query)
-        uint32_t pa[3], pb[3];
-        int npass = 0;
-        if (DV == 64) {  // A stacks hi (rows 0-63) over lo (rows 64-127)
-            pa[npass] = a_hi; pb[npass++] = b_hi;
-            if (DIAG) { pa[npass] = a_hi; pb[npass++] = b_lo; }
-        } else {
-            pa[npass] = a_hi; pb[npass++] = b_hi;
-            pa[npass] = a_lo; pb[npass++] = b_hi;
-            if (DIAG) { pa[npass] = a_hi; pb[npass++] = b_lo; }
-        }
-        const int ksteps = dk / 16;
-        for (int p = 0; p < npass; ++p) {
-            for (int kk = 0; kk < ksteps; ++kk) {
-                const uint64_t ad = ptx::desc_kmajor_noswizzle(pa[p] + kk * 256, 128, sbo_a);
-                const uint64_t bd =
-                    ptx::desc_kmajor_sw128(pb[p] + (kk / 4) * slab_bytes + (kk % 4) * 32, 1024);
-                ptx::mma_bf16(tmem, ad, bd, idesc, (p > 0 || kk > 0) ? 1u : 0u);
-            }
-        }
-        ptx::mma_commit(bar_mma);
-    }
+    if (run && tid == 0) ptx::mma_commit(bar_mma);
     bool mma_ok = true;
     if (run) mma_ok = ptx::mbar_wait(bar_mma, 0, kWaitLimit);
     const bool all_mma = __syncthreads_and(mma_ok);
