@@ -33,24 +33,46 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tree-verify node-head updates/s"
 UNIT = "node-head/s"
-WORKLOAD = ("Mamba-2-like layer: B=16 requests, H=24 heads, dk=128, dv=64, 16-node top-4 "
-            "draft tree (4 chains of depth 4), bf16 q/k/v, fp32 H0, scalar decay")
+WORKLOADS = {
+    1: "single request, 1 head, dk=dv=16, fp32 q/k/v, 8-node random tree, scalar decay",
+    2: ("Mamba-2-like layer: B=16 requests, H=24 heads, dk=128, dv=64, 16-node top-4 draft "
+        "tree (4 chains of depth 4), bf16 q/k/v, fp32 H0, scalar decay"),
+    3: ("GLA-like layer: B=32, H=16, dk=dv=128, bf16 q/k/v, fp32 H0, per-channel decay, "
+        "64-node best-first trees (depth <= 8, Dirichlet(0.3))"),
+    4: ("mixed-budget batch: B=128, H=32, dk=dv=128, bf16 q/k/v, fp32 H0, scalar decay, "
+        "tree sizes in {4..128}, depth cap 12"),
+    5: ("large-tree stack: B=8, 36 layers x 32 heads (H=1152), dk=dv=128, bf16 q/k/v, fp32 H0, "
+        "per-channel decay, 256-node best-first trees (depth <= 16, Dirichlet(0.2))"),
+}
+WORKLOAD = WORKLOADS[2]
 KERNEL_SOURCES = ["tree_speculative_verify_tv_gb300/csrc/verify_tc.cu",
                   "tree_speculative_verify_tv_gb300/csrc/verify_simt.cu",
                   "tree_speculative_verify_tv_gb300/csrc/tv_internal.cuh"]
 
 
+DEFAULT_STEPS = {1: 40000, 2: 40000, 3: 5000, 4: 400, 5: 40}
+DEFAULT_WARMUP = {1: 200, 2: 200, 3: 50, 4: 10, 5: 3}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 40000 for config 2, fewer for the larger configs)")
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sets", type=int, default=0, help="rotated input sets (0 = auto, >4x L2)")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--variant", type=int, default=0, help="tv_verify variant (0 auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
+                    help="workload (default 2: the configuration the HBM target is quoted on)")
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.config]
+    if args.warmup is None:
+        args.warmup = DEFAULT_WARMUP[args.config]
+    return args
 
 
 # ---------------------------------------------------------------- byte accounting
@@ -283,7 +305,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     import workloads
-    b = workloads.config2()
+    b = workloads.make_config(args.config)
     threads = cpu_cores()
     steps = args.steps + args.warmup
     value, upl, n, dt, threads = time_oracle(b, steps, 60.0, threads)
@@ -292,8 +314,8 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD, "B": b.B, "H": b.H, "dk": b.dk, "dv": b.dv,
-                       "nodes_per_request": 16},
+            "config": {"workload": WORKLOADS[args.config], "B": b.B, "H": b.H, "dk": b.dk,
+                       "dv": b.dv, "max_nodes": b.max_nodes},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": "%d steps, each the fp64 oracle on %d of the %d "
                                        "(request, head) units (verify + greedy walk of all "
@@ -320,10 +342,13 @@ def run_ours(args, world, rank, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
 
-    base = workloads.config2(seed=1002 + 7919 * rank)
+    cfg = args.config
+    base = workloads.make_config(cfg, seed=1000 + cfg + 7919 * rank)
     per_set = verify_bytes(base) + base.B * base.H * base.dk * base.dv * 4 * 2
-    R = args.sets or max(4, int(np.ceil(4.0 * l2 / per_set)) + 1)
-    sets = [workloads.config2(seed=1002 + 7919 * rank + 101 * r) for r in range(R)]
+    # enough distinct sets that one cycle touches > 4x L2 (one set when it alone does)
+    R = args.sets or (1 if per_set >= 4 * l2 else max(4, int(np.ceil(4.0 * l2 / per_set)) + 1))
+    sets = [base] + [workloads.make_config(cfg, seed=1000 + cfg + 7919 * rank + 101 * r)
+                     for r in range(1, R)]
     dbs = [tv.DeviceBatch(s, device=dev) for s in sets]
     stream = torch.cuda.Stream(device=dev)
     node_heads = base.T * base.H
@@ -441,8 +466,10 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "B": base.B, "H": base.H, "dk": base.dk,
-                       "dv": base.dv, "nodes_per_request": 16, "node_heads_per_step": node_heads,
+            "config": {"workload": WORKLOADS[cfg], "B": base.B, "H": base.H, "dk": base.dk,
+                       "dv": base.dv, "max_nodes": base.max_nodes,
+                       "node_heads_per_step": node_heads,
+                       "verify_kernel": "tcgen05" if dbs[0].variant() == 2 else "simt",
                        "inputs": "bf16 q/k/v, fp32 g/H0/out/H_new",
                        "l2": "inputs larger than L2: %d input sets rotated, %.0f MB touched per "
                              "cycle vs %.0f MB L2" % (R, R * per_set / 1e6, l2 / 1e6),
@@ -478,7 +505,8 @@ def run_e2e(args, host_batch, dev, stream, tv, world):
     outs = ["out", "H_new", "accept_len", "path", "bonus", "status"]
     h2d = sum(getattr(hb, n).numel() * getattr(hb, n).element_size() for n in ins)
     d2h = sum(getattr(db, n).numel() * getattr(db, n).element_size() for n in outs)
-    K = max(1, args.e2e_steps)
+    # about 2 GB of host<->device traffic at most (at least 3 steps)
+    K = max(1, min(args.e2e_steps, max(3, int(2e9 / max(h2d + d2h, 1)))))
 
     def one():
         for n in ins:

@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
     __shared__ int s_tgt[kWarps][kMaxNodes];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int b = blockIdx.x * kWarps + w;
+    pdl_wait();
+    pdl_launch_next();
     if (b >= a.B) return;
     const int md = a.max_depth;
     int32_t *path = a.path + (size_t)b * md;
@@ -88,8 +90,7 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
 
 cudaError_t launch_accept(const AcceptArgs &a, cudaStream_t s) {
     dim3 grid((unsigned)((a.B + kWarps - 1) / kWarps));
-    accept_kernel<<<grid, kWarps * 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(accept_kernel, grid, dim3(kWarps * 32), 0, s, a);
 }
 
 }  // namespace tv

@@ -24,9 +24,10 @@ constexpr int kThreads = 256;
 constexpr int kItems = 8;                                 // float4s per thread
 constexpr int kRowsMax = kItems * kThreads * 4 / 64;      // 128 key rows at dv = 64
 
-// Key rows per CTA: kItems float4s per thread cover 8192 / dv rows.
+// Key rows per CTA: kItems float4s per thread cover 8192 / dv rows, at most kRowsMax.
 __host__ __device__ inline int rows_per_cta(int dk, int dv) {
-    const int r = kItems * kThreads * 4 / dv;
+    int r = kItems * kThreads * 4 / dv;
+    if (r > kRowsMax) r = kRowsMax;
     return r < dk ? r : dk;
 }
 
@@ -49,6 +50,8 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
     const E *k = static_cast<const E *>(a.k);
     const E *v = static_cast<const E *>(a.v);
 
+    pdl_wait();
+    pdl_launch_next();
     // round trip 1: this thread's H0 float4s, the offsets, the length and the path
     const int c4n = dv / 4;
     const int items = rows * c4n;
@@ -141,8 +144,7 @@ cudaError_t launch_typed(const CommitArgs &a, cudaStream_t s) {
         commit_kernel<E, DIAG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         kMaxDepth * kMaxDim * (int)sizeof(float));
     if (attr != cudaSuccess) return attr;
-    commit_kernel<E, DIAG><<<grid, kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(commit_kernel<E, DIAG>, grid, dim3(kThreads), smem, s, a);
 }
 
 }  // namespace

@@ -81,24 +81,31 @@ __device__ __forceinline__ bool request_range(const int32_t *offs, int b, int T,
 
 namespace tv {
 
-// Loads one request's parent[] (and depth[] when s_dep != nullptr) into shared
-// memory and checks the tree: parent[i] in [-1, i) (parents precede children,
-// so every root path ends at the context) and depth[i] = depth[parent]+1 (1 for
-// a child of the context) with depth <= max_depth.  Every thread of the block
-// must call it; returns the same verdict in all threads.
+// Loads one request's parent[] and depth[] (and, when g != nullptr, the scalar
+// decays g[(off+i)*H + h]) into shared memory in one memory round trip and
+// checks the tree: parent[i] in [-1, i) (parents precede children, so every
+// root path ends at the context) and depth[i] = depth[parent]+1 (1 for a child
+// of the context) with depth <= max_depth.  Every thread of the block must call
+// it; returns the same verdict in all threads.
 __device__ __forceinline__ bool load_check_tree(const int32_t *parent, const int32_t *depth,
                                                 int off, int n, int max_depth, int *s_par,
-                                                int *s_dep, int *s_flag) {
+                                                int *s_dep, int *s_flag,
+                                                const float *g = nullptr, int H = 0, int h = 0,
+                                                float *s_g = nullptr) {
     if (threadIdx.x == 0) *s_flag = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        int p = parent[off + i];
+        const int p = parent[off + i];
+        const int d = depth[off + i];
+        float gv = 0.f;
+        if (g) gv = g[(size_t)(off + i) * H + h];
         s_par[i] = p;
-        if (s_dep) s_dep[i] = depth[off + i];
+        s_dep[i] = d;
+        if (g) s_g[i] = gv;
         if (p < -1 || p >= i) *s_flag = 1;
     }
     __syncthreads();
-    if (s_dep && *s_flag == 0) {
+    if (*s_flag == 0) {
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
             int p = s_par[i];
             int want = p < 0 ? 1 : s_dep[p] + 1;
@@ -107,6 +114,32 @@ __device__ __forceinline__ bool load_check_tree(const int32_t *parent, const int
     }
     __syncthreads();
     return *s_flag == 0;
+}
+
+// Programmatic dependent launch: wait for the previous kernel in the stream
+// (no-op when launched without the attribute), and let the next one launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_next() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kern` on `s` with programmatic stream serialization allowed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 }  // namespace tv

@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kThreads) verify_simt_kernel(VerifyArgs a) {
     const E *k = static_cast<const E *>(a.k);
     const E *v = static_cast<const E *>(a.v);
 
+    pdl_wait();
+    pdl_launch_next();
     int off, n;
     if (!request_range(a.node_offsets, b, a.T, a.max_nodes, off, n)) {
         if (tid == 0 && h == 0 && blockIdx.y == 0) report(a.status, TV_ERR_TREE);
@@ -150,8 +152,7 @@ template <typename E, bool DIAG>
 cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s) {
     dim3 grid((unsigned)(a.B * a.H), (unsigned)((a.max_nodes + kTile - 1) / kTile));
     size_t smem = (size_t)kTile * a.dk * sizeof(float);
-    verify_simt_kernel<E, DIAG><<<grid, kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(verify_simt_kernel<E, DIAG>, grid, dim3(kThreads), smem, s, a);
 }
 
 }  // namespace

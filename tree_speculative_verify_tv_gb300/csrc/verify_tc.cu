@@ -204,12 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::grid_launch_dependents();
 
-    // ---- tree checks while the copies fly
+    // ---- tree checks (and scalar decays) in one round trip while the copies fly
     bool ok = have_nodes;
     if (have_nodes) {
-        if (!DIAG)
-            for (int i = tid; i < n; i += kThreads) sG[i] = a.g[(size_t)(off + i) * H + h];
-        ok = load_check_tree(a.parent, a.depth, off, n, md, sPar, sDep, sFlag);
+        ok = load_check_tree(a.parent, a.depth, off, n, md, sPar, sDep, sFlag,
+                             DIAG ? nullptr : a.g, H, h, sG);
         if (!ok) {
             for (int e = tid; e < n * DV; e += kThreads)
                 a.out[((size_t)(off + e / DV) * H + h) * DV + e % DV] = 0.f;
@@ -304,25 +303,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kItems = DV * (kChunkRows / 8) / kThreads;  // (channel, 8-key) items per thread
     const uint32_t idesc = ptx::idesc_bf16_f32(128, npad);
     const uint32_t b_hi = ptx::smem_addr(sB), b_lo = ptx::smem_addr(sBlo);
-    for (int c = 0; c < nchunks; ++c) {
-        uint8_t *chunk = sA + c * chunk_bytes;
-        const float *f32 = reinterpret_cast<const float *>(chunk);
-        const bool got = ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit);
-        float hold[kItems][8];
-        if (run && got) {
+    float hold[2][kItems][8];
+    // read chunk c (fp32 rows) into hold[c & 1]
+    auto read_chunk = [&](int c) {
+        const float *f32 = reinterpret_cast<const float *>(sA + c * chunk_bytes);
 #pragma unroll
-            for (int t = 0; t < kItems; ++t) {
-                const int it = tid + t * kThreads;
-                const int ch = it % DV, kq = it / DV;
+        for (int t = 0; t < kItems; ++t) {
+            const int it = tid + t * kThreads;
+            const int ch = it % DV, kq = it / DV;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) hold[t][e] = f32[(kq * 8 + e) * DV + ch];
-            }
+            for (int e = 0; e < 8; ++e) hold[c & 1][t][e] = f32[(kq * 8 + e) * DV + ch];
         }
-        if (!__syncthreads_and(got)) {
+    };
+    bool got = ptx::mbar_wait(bar0, 0, kWaitLimit);
+    if (run && got) read_chunk(0);
+    bool all_got = __syncthreads_and(got);
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) {
+        if (c >= nchunks) break;
+        if (!all_got) {
             if (tid == 0 && run) report(a.status, TV_ERR_TIMEOUT);
             run = false;
         }
+        uint8_t *chunk = sA + c * chunk_bytes;
         if (run) {
+            // write chunk c in place as bf16 hi/lo operand rows
 #pragma unroll
             for (int t = 0; t < kItems; ++t) {
                 const int it = tid + t * kThreads;
@@ -330,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float x0 = hold[t][2 * e], x1 = hold[t][2 * e + 1];
+                    const float x0 = hold[c & 1][t][2 * e], x1 = hold[c & 1][t][2 * e + 1];
                     const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
                     const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
                     hi[e] = pack_bf16(h0, h1);
@@ -346,8 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::fence_proxy_async_smem();
         }
+        // read ahead the next chunk before the barrier that publishes this one
+        got = true;
+        if (c + 1 < nchunks) {
+            got = ptx::mbar_wait(bar0 + 8 * (c + 1), 0, kWaitLimit);
+            if (run && got) read_chunk(c + 1);
+        }
         ptx::tc_fence_before_sync();
-        __syncthreads();
+        all_got = __syncthreads_and(got);
         ptx::tc_fence_after_sync();
         if (run && tid == 0) {
             const uint32_t a_hi = ptx::smem_addr(chunk);
