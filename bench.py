@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--variant", type=int, default=0, help="tv_verify variant (0 auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fold", type=int, default=32,
+                    help="also time one verify launch over this many config-2 layers folded "
+                         "into the head axis (0 = skip)")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
                     help="workload (default 2: the configuration the HBM target is quoted on)")
     args = ap.parse_args()
@@ -86,6 +89,14 @@ def verify_bytes(b) -> int:
     per_node_head = 2 * b.dk * qk + b.dv * qk + g + 4 * b.dv
     return (b.B * b.H * 4 * b.dk * b.dv + b.T * b.H * per_node_head + 8 * b.T
             + 4 * (b.B + 1))
+
+
+def verify_bytes_of(d) -> int:
+    """verify_bytes for a DeviceBatch."""
+    qk = 2 if d.qkv_dtype == 0 else 4
+    g = 4 if d.decay == 0 else 4 * d.dk
+    per_node_head = 2 * d.dk * qk + d.dv * qk + g + 4 * d.dv
+    return d.B * d.H * 4 * d.dk * d.dv + d.T * d.H * per_node_head + 8 * d.T + 4 * (d.B + 1)
 
 
 def commit_bytes(b, lens) -> int:
@@ -438,6 +449,41 @@ def run_ours(args, world, rank, local):
     # ---------------- end to end through the binding with pinned host buffers
     e2e = run_e2e(args, sets[0], dev, stream, tv, world)
 
+    # ---------------- one verify launch over `fold` layers folded into the head axis
+    folded = None
+    if cfg == 2 and args.fold > 1 and rank == 0:
+        fb = workloads.config2(seed=77, H=base.H * args.fold)
+        fd = tv.DeviceBatch(fb, device=dev)
+        del fb
+        with torch.cuda.stream(stream):
+            fd.status.zero_()
+            for _ in range(3):
+                fd.verify(stream=stream, variant=args.variant)
+        stream.synchronize()
+        KF = max(10, min(200, K // 100))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(KF):
+                fd.verify(stream=stream, variant=args.variant)
+        g.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        if int(fd.status[0].item()) != 0:
+            raise SystemExit("device status %d in folded run" % int(fd.status[0].item()))
+        fb_bytes = verify_bytes_of(fd)
+        t_f = e0.elapsed_time(e1) * 1e-3 / KF
+        folded = {"layers": args.fold, "H": fd.H, "launches": KF,
+                  "bytes_per_launch": fb_bytes, "launch_us": t_f * 1e6,
+                  "node_heads_per_s": fd.T * fd.H / t_f,
+                  "gbs": fb_bytes / t_f / 1e9}
+        del fd, g
+        torch.cuda.empty_cache()
+
     # ---------------- roofline of the dominant kernel (verify)
     peaks, peak_kind = measured_peaks()
     vb = verify_bytes(base)
@@ -484,10 +530,13 @@ def run_ours(args, world, rank, local):
                            "commit": t_commit / K * 1e6},
             "verify_only": {"value": node_heads / v_launch, "unit": UNIT,
                             "gbs": achieved},
+            "verify_folded_layers": (dict(folded, frac=folded["gbs"] / peak) if folded
+                                     else None),
             "commit_gbs": cb / (t_commit / K) / 1e9,
             "transient_bytes": {"library_workspace": 0,
-                                "factors": int(base.T * base.H * (2 * base.dk * 2 + base.dv * 2
-                                                                 + 4)),
+                                "factors": int(base.T * base.H * (
+                                    (2 * base.dk + base.dv) * (2 if base.qkv_dtype == "bf16" else 4)
+                                    + (4 if base.decay == "scalar" else 4 * base.dk))),
                                 "naive_per_node_states": int(base.T * base.H * base.dk * base.dv
                                                              * 4)},
         }

@@ -52,12 +52,14 @@ constexpr int kMaxChunks = 4;   // dk <= 128
 //     becomes exp(g) in place.
 //   The lo-part exchange (dv = 64) reuses the A region when it is large enough.
 struct TcLayout {
-    uint32_t a_off, b_off, blo_off, q_off, k_off, v_off, e_off, x_off, w_off, eg_off, g_off,
-        par_off, dep_off, bar_off, misc_off, total;
+    uint32_t a_off, b_off, blo_off, q_off, k_off, v_off, e_off, x_off, w_off, anc_off, eg_off,
+        g_off, par_off, dep_off, bar_off, misc_off, total;
     __host__ __device__ TcLayout(int dk, int dv, int npad_max, int max_depth, bool diag) {
         const uint32_t swz_tile = (dk / 64) * npad_max * 128;  // one swizzled [n][dk] bf16 tile
         const uint32_t a_bytes = dk * dv * 4;
-        const bool x_in_a = dv != 64 || (uint32_t)npad_max * 64 * 4 <= a_bytes;
+        // dv = 64: the epilogue dumps both 64-row halves of D, npad x 128 fp32
+        const uint32_t x_bytes = dv == 64 ? npad_max * 128 * 4 : 0;
+        const bool x_in_a = x_bytes <= a_bytes;
         a_off = 0;
         b_off = align_up(a_off + a_bytes, 1024);               // B (hi) operand
         blo_off = align_up(b_off + swz_tile, 1024);            // B lo operand (diag)
@@ -66,9 +68,10 @@ struct TcLayout {
         v_off = align_up(k_off + npad_max * dk * 2, 1024);
         e_off = align_up(v_off + npad_max * dv * 2, 1024);      // g -> exp(g) rows (diag)
         x_off = align_up(e_off + (diag ? npad_max * dk * 4 : 0), 16);
-        w_off = align_up(x_off + (x_in_a ? 0 : npad_max * 64 * 4), 16);
+        w_off = align_up(x_off + (x_in_a ? 0 : x_bytes), 16);
         if (x_in_a) x_off = a_off;
-        eg_off = align_up(w_off + npad_max * max_depth * 4, 16);
+        anc_off = align_up(w_off + npad_max * max_depth * 4, 16);   // root paths
+        eg_off = align_up(anc_off + npad_max * max_depth * 4, 16);
         g_off = align_up(eg_off + npad_max * 4, 16);
         par_off = align_up(g_off + npad_max * 4, 16);
         dep_off = align_up(par_off + npad_max * 4, 16);
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *sE = reinterpret_cast<float *>(smem + L.e_off);
     float *sX = reinterpret_cast<float *>(smem + L.x_off);
     float *sW = reinterpret_cast<float *>(smem + L.w_off);
+    int *sAnc = reinterpret_cast<int *>(smem + L.anc_off);
     float *sEG = reinterpret_cast<float *>(smem + L.eg_off);
     float *sG = reinterpret_cast<float *>(smem + L.g_off);
     int *sPar = reinterpret_cast<int *>(smem + L.par_off);
@@ -223,24 +227,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!run && tid == 0) report(a.status, TV_ERR_TIMEOUT);
     run = run && ok;
 
-    const int per_lane = dk / 32;    // 2 or 4 key channels per lane
-    const int c0 = lane * per_lane;  // within one 16-byte chunk
     if (DIAG && run) {
         for (int e = tid; e < n * dk; e += kThreads) sE[e] = expf(sE[e]);
         __syncthreads();
     }
-    if (run) {
+    if (run && !DIAG) {
+        // root path of each node with the decay factor of every (node, ancestor) pair:
+        // anc_d(i) = the ancestor d steps up, e^{G_i - G_{anc_d}} = exp(sum of g over the
+        // path nodes below it), and e^{G_i}
+        for (int i = tid; i < n; i += kThreads) {
+            float s = 0.f;
+            int j = i, d = 0;
+            while (j >= 0) {
+                sAnc[i * md + d] = j;
+                sW[i * md + d] = expf(s);
+                s += sG[j];
+                j = sPar[j];
+                ++d;
+            }
+            sEG[i] = expf(s);
+        }
+        __syncthreads();
+        // w_ij = decay * (q_i . k_j): one 8-lane group per node, its ancestors in turn.
+        // Loop bounds are uniform across the warp (the shuffles need every lane).
+        const int sub = lane & 7;
+        const int per = dk / 8;  // 16 or 8 key channels per lane, whole 16-byte chunks
+        for (int base = warp * 4; base < n; base += kThreads / 8) {
+            const int i = base + (lane >> 3);
+            const bool valid = i < n;
+            float qv[16];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (valid && u * 8 < per) {
+                    const int c = sub * per + u * 8;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(sB + swz_offset(i, c, slab_bytes));
+                    const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        qv[u * 8 + 2 * e] = __low2float(p2[e]);
+                        qv[u * 8 + 2 * e + 1] = __high2float(p2[e]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qv[u * 8 + e] = 0.f;
+                }
+            }
+            const int di = valid ? sDep[i] : 0;
+            const int dmax = __reduce_max_sync(0xffffffffu, di);
+            for (int d = 0; d < dmax; ++d) {
+                const bool act = d < di;
+                float part = 0.f;
+                if (act) {
+                    const int j = sAnc[i * md + d];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        if (u * 8 < per) {
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(sK + j * dk + sub * per + u * 8);
+                            const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                part += qv[u * 8 + 2 * e] * __low2float(p2[e]) +
+                                        qv[u * 8 + 2 * e + 1] * __high2float(p2[e]);
+                        }
+                    }
+                }
+                part += __shfl_xor_sync(0xffffffffu, part, 4);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                if (act && sub == 0) sW[i * md + d] *= part;
+            }
+        }
+    }
+    if (run && DIAG) {
+        // one warp per node walks its root path with a per-channel decay product
+        const int per_lane = dk / 32;    // 2 or 4 key channels per lane
+        const int c0 = lane * per_lane;  // within one 16-byte chunk
         for (int i = warp; i < n; i += kThreads / 32) {
             float qv[4];
-            if (DIAG)
-                load_bf16x(sQ + i * dk + c0, per_lane, qv);
-            else
-                load_bf16x(reinterpret_cast<const __nv_bfloat16 *>(sB + swz_offset(i, c0, slab_bytes)),
-                           per_lane, qv);
-            // f = e^{G_i - G_j} for the current ancestor j: per channel (diagonal) or
-            // one value (scalar, carried as the running log sum s)
-            float f[4] = {1.f, 1.f, 1.f, 1.f};
-            float s = 0.f;
+            load_bf16x(sQ + i * dk + c0, per_lane, qv);
+            float f[4] = {1.f, 1.f, 1.f, 1.f};  // e^{G_i - G_j} per channel
             int j = i, d = 0;
             while (j >= 0) {
                 float kv[4];
@@ -249,93 +314,87 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int m = 0; m < 4; ++m) part += qv[m] * kv[m] * f[m];
                 part = warp_sum(part);
-                if (lane == 0) sW[i * md + d] = DIAG ? part : expf(s) * part;
-                if (DIAG) {
-#pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        if (m < per_lane) f[m] *= sE[j * dk + c0 + m];
-                } else {
-                    s += sG[j];
+                if (lane == 0) {
+                    sW[i * md + d] = part;
+                    sAnc[i * md + d] = j;
                 }
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    if (m < per_lane) f[m] *= sE[j * dk + c0 + m];
                 j = sPar[j];
                 ++d;
             }
-            if (DIAG) {
-                // B = bf16 hi/lo of e^{G_i} * q_i in the swizzled K-major layout
-                float hi[4], lo[4];
+            // B = bf16 hi/lo of e^{G_i} * q_i in the swizzled K-major layout
+            float hi[4], lo[4];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float x = qv[m] * f[m];
-                    hi[m] = __bfloat162float(__float2bfloat16_rn(x));
-                    lo[m] = x - hi[m];
-                }
-                const uint32_t o = swz_offset(i, c0, slab_bytes);
-                if (per_lane == 4) {
-                    *reinterpret_cast<uint2 *>(sB + o) = make_uint2(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]));
-                    *reinterpret_cast<uint2 *>(sBlo + o) = make_uint2(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]));
-                } else {
-                    *reinterpret_cast<uint32_t *>(sB + o) = pack_bf16(hi[0], hi[1]);
-                    *reinterpret_cast<uint32_t *>(sBlo + o) = pack_bf16(lo[0], lo[1]);
-                }
-            } else if (lane == 0) {
-                sEG[i] = expf(s);
+            for (int m = 0; m < 4; ++m) {
+                const float x = qv[m] * f[m];
+                hi[m] = __bfloat162float(__float2bfloat16_rn(x));
+                lo[m] = x - hi[m];
+            }
+            const uint32_t o = swz_offset(i, c0, slab_bytes);
+            if (per_lane == 4) {
+                *reinterpret_cast<uint2 *>(sB + o) = make_uint2(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]));
+                *reinterpret_cast<uint2 *>(sBlo + o) = make_uint2(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]));
+            } else {
+                *reinterpret_cast<uint32_t *>(sB + o) = pack_bf16(hi[0], hi[1]);
+                *reinterpret_cast<uint32_t *>(sBlo + o) = pack_bf16(lo[0], lo[1]);
             }
         }
-        if (DIAG) {
-            // rows n..npad-1 of B feed unused output columns; keep them finite
-            for (int e = n * 64 + tid; e < npad * 64; e += kThreads) {
-                const int i = e / 64, cq = (e % 64) * 2;
-                const uint32_t o = swz_offset(i, cq, slab_bytes);
-                if (cq < dk) {
-                    *reinterpret_cast<uint32_t *>(sB + o) = 0u;
-                    *reinterpret_cast<uint32_t *>(sBlo + o) = 0u;
-                }
+        // rows n..npad-1 of B feed unused output columns; keep them finite
+        for (int e = n * 64 + tid; e < npad * 64; e += kThreads) {
+            const int i = e / 64, cq = (e % 64) * 2;
+            const uint32_t o = swz_offset(i, cq, slab_bytes);
+            if (cq < dk) {
+                *reinterpret_cast<uint32_t *>(sB + o) = 0u;
+                *reinterpret_cast<uint32_t *>(sBlo + o) = 0u;
             }
-            ptx::fence_proxy_async_smem();
         }
+        ptx::fence_proxy_async_smem();
     }
 
-    // ---- H0 chunk by chunk: split in place into bf16 hi/lo K-major rows, then MMA.
-    // Chunk layout (kChunkRows keys): operand rows (value channels) in 8-row groups
-    // of 512 bytes (4 core matrices of 8 rows x 8 keys); DV = 64 stacks hi rows
-    // 0..63 over lo rows 64..127; DV = 128 keeps a hi operand and a lo operand of
-    // 128 rows, 8 KB each.  D[c][i] accumulates sum_r A[c][r] B[i][r] in TMEM.
-    constexpr int kItems = DV * (kChunkRows / 8) / kThreads;  // (channel, 8-key) items per thread
-    const uint32_t idesc = ptx::idesc_bf16_f32(128, npad);
-    const uint32_t b_hi = ptx::smem_addr(sB), b_lo = ptx::smem_addr(sBlo);
-    float hold[2][kItems][8];
-    // read chunk c (fp32 rows) into hold[c & 1]
-    auto read_chunk = [&](int c) {
-        const float *f32 = reinterpret_cast<const float *>(sA + c * chunk_bytes);
+    // ---- H0: once every chunk has landed, split it in place into bf16 hi/lo K-major
+    // operand rows.  Chunk layout (kChunkRows keys): operand rows (value channels) in
+    // 8-row groups of 512 bytes (4 core matrices of 8 rows x 8 keys); DV = 64 stacks
+    // hi rows 0..63 over lo rows 64..127; DV = 128 keeps a hi and a lo operand of 128
+    // rows, 8 KB each.
+    constexpr int kPerChunk = DV * (kChunkRows / 8) / kThreads;  // items per thread per chunk
+    float hold[kMaxChunks][kPerChunk][8];
+    bool got = true;
 #pragma unroll
-        for (int t = 0; t < kItems; ++t) {
-            const int it = tid + t * kThreads;
-            const int ch = it % DV, kq = it / DV;
+    for (int c = 0; c < kMaxChunks; ++c)
+        if (c < nchunks) got = ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit) && got;
+    if (run && got) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) hold[c & 1][t][e] = f32[(kq * 8 + e) * DV + ch];
+        for (int c = 0; c < kMaxChunks; ++c) {
+            if (c >= nchunks) break;
+            const float *f32 = reinterpret_cast<const float *>(sA + c * chunk_bytes);
+#pragma unroll
+            for (int t = 0; t < kPerChunk; ++t) {
+                const int it = tid + t * kThreads;
+                const int ch = it % DV, kq = it / DV;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) hold[c][t][e] = f32[(kq * 8 + e) * DV + ch];
+            }
         }
-    };
-    bool got = ptx::mbar_wait(bar0, 0, kWaitLimit);
-    if (run && got) read_chunk(0);
-    bool all_got = __syncthreads_and(got);
+    }
+    if (!__syncthreads_and(got)) {
+        if (tid == 0 && run) report(a.status, TV_ERR_TIMEOUT);
+        run = false;
+    }
+    if (run) {
 #pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) {
-        if (c >= nchunks) break;
-        if (!all_got) {
-            if (tid == 0 && run) report(a.status, TV_ERR_TIMEOUT);
-            run = false;
-        }
-        uint8_t *chunk = sA + c * chunk_bytes;
-        if (run) {
-            // write chunk c in place as bf16 hi/lo operand rows
+        for (int c = 0; c < kMaxChunks; ++c) {
+            if (c >= nchunks) break;
+            uint8_t *chunk = sA + c * chunk_bytes;
 #pragma unroll
-            for (int t = 0; t < kItems; ++t) {
+            for (int t = 0; t < kPerChunk; ++t) {
                 const int it = tid + t * kThreads;
                 const int ch = it % DV, kq = it / DV;
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float x0 = hold[c & 1][t][2 * e], x1 = hold[c & 1][t][2 * e + 1];
+                    const float x0 = hold[c][t][2 * e], x1 = hold[c][t][2 * e + 1];
                     const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
                     const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
                     hi[e] = pack_bf16(h0, h1);
@@ -349,19 +408,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(lo_base + (r_lo / 8) * 512 + kq * 128 + (r_lo % 8) * 16) =
                     make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
-            ptx::fence_proxy_async_smem();
         }
-        // read ahead the next chunk before the barrier that publishes this one
-        got = true;
-        if (c + 1 < nchunks) {
-            got = ptx::mbar_wait(bar0 + 8 * (c + 1), 0, kWaitLimit);
-            if (run && got) read_chunk(c + 1);
-        }
-        ptx::tc_fence_before_sync();
-        all_got = __syncthreads_and(got);
-        ptx::tc_fence_after_sync();
-        if (run && tid == 0) {
-            const uint32_t a_hi = ptx::smem_addr(chunk);
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+
+    // ---- context term on the tensor core: D[c][i] = sum_r A[c][r] B[i][r]
+    if (run && tid == 0) {
+        const uint32_t idesc = ptx::idesc_bf16_f32(128, npad);
+        const uint32_t b_hi = ptx::smem_addr(sB), b_lo = ptx::smem_addr(sBlo);
+        for (int c = 0; c < nchunks; ++c) {
+            const uint32_t a_hi = ptx::smem_addr(sA + c * chunk_bytes);
             const uint32_t a_lo = DV == 64 ? a_hi : a_hi + 8192;
             uint32_t pa[3], pb[3];
             int npass = 0;
@@ -378,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        ptx::mma_commit(bar_mma);
     }
-    if (run && tid == 0) ptx::mma_commit(bar_mma);
     bool mma_ok = true;
     if (run) mma_ok = ptx::mbar_wait(bar_mma, 0, kWaitLimit);
     const bool all_mma = __syncthreads_and(mma_ok);
@@ -387,24 +446,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     run = run && all_mma;
     ptx::tc_fence_after_sync();
 
-    // ---- epilogue: lane = value channel, columns = nodes
+    // ---- epilogue: o_i = [e^{G_i}] * D[:, i] + sum_d w_{i,d} v_{anc_d(i)}
     const int quad = warp & 3, half = warp >> 2;
-    const int ncols_half = npad / 2;  // multiple of 8
     const uint32_t tq = tmem + (static_cast<uint32_t>(32 * quad) << 16);
     if (DV == 64) {
-        // quadrants 2,3 hold the lo part of channels 0..63: hand it over through smem
-        if (run && quad >= 2) {
-            const int c = 32 * (quad - 2) + lane;
+        // every warp dumps its quadrant (hi rows 0..63, lo rows 64..127) for half the
+        // columns; then all threads form outputs (node, channel), channels fastest
+        const int ncols_half = npad / 2;  // multiple of 8
+        if (run) {
+            const int row = 32 * quad + lane;
             for (int col = half * ncols_half; col < (half + 1) * ncols_half; col += 8) {
                 float vals[8];
                 ptx::tmem_ld_x8(tq + col, vals);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) sX[(col + e) * 64 + c] = vals[e];
+                for (int e = 0; e < 8; ++e) sX[(col + e) * 128 + row] = vals[e];
             }
         }
         __syncthreads();
-    }
-    if (run && (DV == 128 || quad < 2)) {
+        if (run) {
+            const int c = tid & 63;
+            for (int i = tid >> 6; i < n; i += kThreads / 64) {
+                float o = sX[i * 128 + c] + sX[i * 128 + 64 + c];
+                if (!DIAG) o *= sEG[i];
+                const int di = sDep[i];
+                for (int d = 0; d < di; ++d)
+                    o += sW[i * md + d] * __bfloat162float(sV[sAnc[i * md + d] * DV + c]);
+                a.out[((size_t)(off + i) * H + h) * DV + c] = o;
+            }
+        }
+    } else if (run) {
+        const int ncols_half = npad / 2;
         const int c = 32 * quad + lane;
         for (int col = half * ncols_half; col < (half + 1) * ncols_half; col += 8) {
             float vals[8];
@@ -414,14 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int i = col + e;
                 if (i >= n) break;
                 float o = vals[e];
-                if (DV == 64) o += sX[i * 64 + c];
                 if (!DIAG) o *= sEG[i];
-                int j = i, d = 0;
-                while (j >= 0) {
-                    o += sW[i * md + d] * __bfloat162float(sV[j * DV + c]);
-                    j = sPar[j];
-                    ++d;
-                }
+                const int di = sDep[i];
+                for (int d = 0; d < di; ++d)
+                    o += sW[i * md + d] * __bfloat162float(sV[sAnc[i * md + d] * DV + c]);
                 a.out[((size_t)(off + i) * H + h) * DV + c] = o;
             }
         }
