@@ -403,23 +403,27 @@ def run_ours(args, world, rank, local):
         remg = capture([one(i) for i in range(rem)]) if rem else None
         return full, K // R, remg
 
-    def timed(kind, K, sampler=None):
+    def timed(kind, K):
+        """Seconds for exactly K launches of `kind`, replayed on `stream` between CUDA
+        events recorded on that same stream (barrier and synchronize on both sides)."""
         full, reps, remg = graphs_for(kind, K)
-        full.replay()  # upload / warm
-        if remg is not None:
-            remg.replay()
+        with torch.cuda.stream(stream):
+            full.replay()  # upload / warm
+            if remg is not None:
+                remg.replay()
         stream.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         t_host0 = time.time()
-        e0.record(stream)
-        for _ in range(reps):
-            full.replay()
-        if remg is not None:
-            remg.replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                full.replay()
+            if remg is not None:
+                remg.replay()
+            e1.record(stream)
         e1.synchronize()
         t_host1 = time.time()
         torch.cuda.synchronize()
@@ -465,13 +469,15 @@ def run_ours(args, world, rank, local):
         with torch.cuda.graph(g, stream=stream):
             for _ in range(KF):
                 fd.verify(stream=stream, variant=args.variant)
-        g.replay()
+        with torch.cuda.stream(stream):
+            g.replay()
         stream.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
         e1.synchronize()
         if int(fd.status[0].item()) != 0:
             raise SystemExit("device status %d in folded run" % int(fd.status[0].item()))

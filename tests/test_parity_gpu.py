@@ -62,10 +62,9 @@ def test_config_full_size_tensor_core(c):
 @pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64), (128, 128)])
 def test_tensor_core_ragged_scalar(dk, dv):
     rng = np.random.default_rng(dk + 7 * dv)
-    big = 256 if dk == 64 else 128    # largest tree whose shared-memory plan fits one CTA
-    sizes = [1, 16, 17, 0, big - 56, 64, 31, big, 5]
+    sizes = [1, 16, 17, 0, 72, 64, 31, 128, 5]   # 128 nodes: the largest the forced runs use
     b = workloads.random_batch(rng, sizes, 3, dk, dv, decay="scalar", qkv_dtype="bf16",
-                               depth_cap=32, max_depth=32 if dk == 64 else 12, max_nodes=big)
+                               depth_cap=16, max_depth=16, max_nodes=128)
     assert _tc_supported(b)
     _full_check(b, "tc")
 

@@ -113,6 +113,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
 }
 
+// Split two floats into bf16 hi + lo parts: hi keeps the upper 16 bits (exact
+// truncation), so x - hi is exact in fp32 and only lo is rounded (to nearest):
+// |x - hi - lo| <= 2^-16 |x|.  Returns packed pairs (element 0 in the low half).
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+    const float h0 = __uint_as_float(b0 & 0xFFFF0000u), h1 = __uint_as_float(b1 & 0xFFFF0000u);
+    hi = __byte_perm(b0, b1, 0x7632);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - h0, x1 - h1);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
 template <int DV, bool DIAG>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -161,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (DIAG) ptx::prefetch_tensormap(&tm_g);
         for (int c = 0; c < kMaxChunks + 2; ++c) ptx::mbar_init(bar0 + 8 * c, 1);
         ptx::fence_mbar_init();
+        *sFlag = 0;
     }
     if (warp == 0) {
         ptx::tmem_alloc(ptx::smem_addr(sTmem), P.tmem_cols);
@@ -208,24 +220,123 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::grid_launch_dependents();
 
-    // ---- tree checks (and scalar decays) in one round trip while the copies fly
-    bool ok = have_nodes;
-    if (have_nodes) {
-        ok = load_check_tree(a.parent, a.depth, off, n, md, sPar, sDep, sFlag,
-                             DIAG ? nullptr : a.g, H, h, sG);
-        if (!ok) {
-            for (int e = tid; e < n * DV; e += kThreads)
-                a.out[((size_t)(off + e / DV) * H + h) * DV + e % DV] = 0.f;
-            if (tid == 0 && h == 0) report(a.status, TV_ERR_TREE);
-        }
+    // ---- this thread's tree entry (n <= 256 = blockDim), loaded while H0 lands
+    int t_par = 0, t_dep = 0;
+    float t_g = 0.f;
+    if (have_nodes && tid < n) {
+        t_par = a.parent[off + tid];
+        t_dep = a.depth[off + tid];
+        if (!DIAG) t_g = a.g[(size_t)(off + tid) * H + h];
     }
 
-    // ---- factor tiles (q, k, v, g) land first: ancestor scores while H0 streams
+    // ---- H0: once every chunk has landed, split it in place into bf16 hi/lo K-major
+    // operand rows.  Chunk layout (kChunkRows keys): operand rows (value channels) in
+    // 8-row groups of 512 bytes (4 core matrices of 8 rows x 8 keys); DV = 64 stacks
+    // hi rows 0..63 over lo rows 64..127; DV = 128 keeps a hi and a lo operand of 128
+    // rows, 8 KB each.
+    constexpr int kPerChunk = DV * (kChunkRows / 8) / kThreads;  // items per thread per chunk
+    float hold[kMaxChunks][kPerChunk][8];
+    bool got = true;
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c)
+        if (c < nchunks) got = ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit) && got;
+    if (got) {
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c) {
+            if (c >= nchunks) break;
+            const float *f32 = reinterpret_cast<const float *>(sA + c * chunk_bytes);
+#pragma unroll
+            for (int t = 0; t < kPerChunk; ++t) {
+                const int it = tid + t * kThreads;
+                const int ch = it % DV, kq = it / DV;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) hold[c][t][e] = f32[(kq * 8 + e) * DV + ch];
+            }
+        }
+    }
+    if (have_nodes && tid < n) {  // tree entry to shared memory; parents must precede
+        sPar[tid] = t_par;
+        sDep[tid] = t_dep;
+        if (!DIAG) sG[tid] = t_g;
+        if (t_par < -1 || t_par >= tid) *sFlag = 1;
+    }
+    bool run = __syncthreads_and(got);
+    if (!run && tid == 0) report(a.status, TV_ERR_TIMEOUT);
+    run = run && have_nodes;
+    if (run) {
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c) {
+            if (c >= nchunks) break;
+            uint8_t *chunk = sA + c * chunk_bytes;
+#pragma unroll
+            for (int t = 0; t < kPerChunk; ++t) {
+                const int it = tid + t * kThreads;
+                const int ch = it % DV, kq = it / DV;
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    split_pair(hold[c][t][2 * e], hold[c][t][2 * e + 1], hi[e], lo[e]);
+                const int r_hi = ch;
+                const int r_lo = DV == 64 ? 64 + ch : ch;
+                uint8_t *lo_base = DV == 64 ? chunk : chunk + 8192;
+                *reinterpret_cast<uint4 *>(chunk + (r_hi / 8) * 512 + kq * 128 + (r_hi % 8) * 16) =
+                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(lo_base + (r_lo / 8) * 512 + kq * 128 + (r_lo % 8) * 16) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+
+    // D[c][i] = sum_r A[c][r] B[i][r] on the tensor core, one thread issues
+    auto issue_mma = [&]() {
+        const uint32_t idesc = ptx::idesc_bf16_f32(128, npad);
+        const uint32_t b_hi = ptx::smem_addr(sB), b_lo = ptx::smem_addr(sBlo);
+        for (int c = 0; c < nchunks; ++c) {
+            const uint32_t a_hi = ptx::smem_addr(sA + c * chunk_bytes);
+            const uint32_t a_lo = DV == 64 ? a_hi : a_hi + 8192;
+            uint32_t pa[3], pb[3];
+            int npass = 0;
+            pa[npass] = a_hi; pb[npass++] = b_hi;  // DV = 64: hi and lo rows together
+            if (DV == 128) { pa[npass] = a_lo; pb[npass++] = b_hi; }
+            if (DIAG) { pa[npass] = a_hi; pb[npass++] = b_lo; }
+            for (int p = 0; p < npass; ++p) {
+                for (int s2 = 0; s2 < kChunkRows / 16; ++s2) {
+                    const int kk = c * (kChunkRows / 16) + s2;  // global 16-key step
+                    const uint64_t ad = ptx::desc_kmajor_noswizzle(pa[p] + s2 * 256, 128, 512);
+                    const uint64_t bd = ptx::desc_kmajor_sw128(
+                        pb[p] + (kk / 4) * slab_bytes + (kk % 4) * 32, 1024);
+                    ptx::mma_bf16(tmem, ad, bd, idesc, (c > 0 || p > 0 || s2 > 0) ? 1u : 0u);
+                }
+            }
+        }
+        ptx::mma_commit(bar_mma);
+    };
+
+    // ---- factor tiles: the scalar-decay context term needs only q, so its MMAs go
+    // out now and run under the tree checks and ancestor scores
     bool landed = true;
     if (have_nodes) landed = ptx::mbar_wait(bar_in, 0, kWaitLimit);
-    bool run = __syncthreads_and(landed) ;
-    if (!run && tid == 0) report(a.status, TV_ERR_TIMEOUT);
-    run = run && ok;
+    bool mma_issued = false;
+    if (!DIAG && run && tid == 0 && landed) issue_mma();
+    if (!DIAG) mma_issued = __syncthreads_or(tid == 0 && run && landed);
+    // tree: depth[i] = depth[parent] + 1 (1 at the context), within max_depth
+    if (have_nodes && tid < n && *sFlag == 0) {
+        const int want = t_par < 0 ? 1 : sDep[t_par] + 1;
+        if (t_dep != want || t_dep > md) *sFlag = 1;
+    }
+    const bool all_landed = __syncthreads_and(landed);
+    if (!all_landed && tid == 0 && run) report(a.status, TV_ERR_TIMEOUT);
+    const bool tree_ok = *sFlag == 0;
+    if (have_nodes && !tree_ok) {
+        for (int e = tid; e < n * DV; e += kThreads)
+            a.out[((size_t)(off + e / DV) * H + h) * DV + e % DV] = 0.f;
+        if (tid == 0 && h == 0) report(a.status, TV_ERR_TREE);
+    }
+    run = run && all_landed && tree_ok;
 
     if (DIAG && run) {
         for (int e = tid; e < n * dk; e += kThreads) sE[e] = expf(sE[e]);
@@ -235,17 +346,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // root path of each node with the decay factor of every (node, ancestor) pair:
         // anc_d(i) = the ancestor d steps up, e^{G_i - G_{anc_d}} = exp(sum of g over the
         // path nodes below it), and e^{G_i}
-        for (int i = tid; i < n; i += kThreads) {
+        if (tid < n) {
             float s = 0.f;
-            int j = i, d = 0;
+            int j = tid, d = 0;
             while (j >= 0) {
-                sAnc[i * md + d] = j;
-                sW[i * md + d] = expf(s);
+                sAnc[tid * md + d] = j;
+                sW[tid * md + d] = expf(s);
                 s += sG[j];
                 j = sPar[j];
                 ++d;
             }
-            sEG[i] = expf(s);
+            sEG[tid] = expf(s);
         }
         __syncthreads();
         // w_ij = decay * (q_i . k_j): one 8-lane group per node, its ancestors in turn.
@@ -325,20 +436,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++d;
             }
             // B = bf16 hi/lo of e^{G_i} * q_i in the swizzled K-major layout
-            float hi[4], lo[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float x = qv[m] * f[m];
-                hi[m] = __bfloat162float(__float2bfloat16_rn(x));
-                lo[m] = x - hi[m];
-            }
+            uint32_t hi[2], lo[2];
+            split_pair(qv[0] * f[0], qv[1] * f[1], hi[0], lo[0]);
+            split_pair(qv[2] * f[2], qv[3] * f[3], hi[1], lo[1]);
             const uint32_t o = swz_offset(i, c0, slab_bytes);
             if (per_lane == 4) {
-                *reinterpret_cast<uint2 *>(sB + o) = make_uint2(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]));
-                *reinterpret_cast<uint2 *>(sBlo + o) = make_uint2(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]));
+                *reinterpret_cast<uint2 *>(sB + o) = make_uint2(hi[0], hi[1]);
+                *reinterpret_cast<uint2 *>(sBlo + o) = make_uint2(lo[0], lo[1]);
             } else {
-                *reinterpret_cast<uint32_t *>(sB + o) = pack_bf16(hi[0], hi[1]);
-                *reinterpret_cast<uint32_t *>(sBlo + o) = pack_bf16(lo[0], lo[1]);
+                *reinterpret_cast<uint32_t *>(sB + o) = hi[0];
+                *reinterpret_cast<uint32_t *>(sBlo + o) = lo[0];
             }
         }
         // rows n..npad-1 of B feed unused output columns; keep them finite
@@ -352,101 +459,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::fence_proxy_async_smem();
     }
-
-    // ---- H0: once every chunk has landed, split it in place into bf16 hi/lo K-major
-    // operand rows.  Chunk layout (kChunkRows keys): operand rows (value channels) in
-    // 8-row groups of 512 bytes (4 core matrices of 8 rows x 8 keys); DV = 64 stacks
-    // hi rows 0..63 over lo rows 64..127; DV = 128 keeps a hi and a lo operand of 128
-    // rows, 8 KB each.
-    constexpr int kPerChunk = DV * (kChunkRows / 8) / kThreads;  // items per thread per chunk
-    float hold[kMaxChunks][kPerChunk][8];
-    bool got = true;
-#pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c)
-        if (c < nchunks) got = ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit) && got;
-    if (run && got) {
-#pragma unroll
-        for (int c = 0; c < kMaxChunks; ++c) {
-            if (c >= nchunks) break;
-            const float *f32 = reinterpret_cast<const float *>(sA + c * chunk_bytes);
-#pragma unroll
-            for (int t = 0; t < kPerChunk; ++t) {
-                const int it = tid + t * kThreads;
-                const int ch = it % DV, kq = it / DV;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) hold[c][t][e] = f32[(kq * 8 + e) * DV + ch];
-            }
-        }
-    }
-    if (!__syncthreads_and(got)) {
-        if (tid == 0 && run) report(a.status, TV_ERR_TIMEOUT);
-        run = false;
-    }
-    if (run) {
-#pragma unroll
-        for (int c = 0; c < kMaxChunks; ++c) {
-            if (c >= nchunks) break;
-            uint8_t *chunk = sA + c * chunk_bytes;
-#pragma unroll
-            for (int t = 0; t < kPerChunk; ++t) {
-                const int it = tid + t * kThreads;
-                const int ch = it % DV, kq = it / DV;
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float x0 = hold[c][t][2 * e], x1 = hold[c][t][2 * e + 1];
-                    const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-                    const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-                    hi[e] = pack_bf16(h0, h1);
-                    lo[e] = pack_bf16(x0 - h0, x1 - h1);
-                }
-                const int r_hi = ch;
-                const int r_lo = DV == 64 ? 64 + ch : ch;
-                uint8_t *lo_base = DV == 64 ? chunk : chunk + 8192;
-                *reinterpret_cast<uint4 *>(chunk + (r_hi / 8) * 512 + kq * 128 + (r_hi % 8) * 16) =
-                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(lo_base + (r_lo / 8) * 512 + kq * 128 + (r_lo % 8) * 16) =
-                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-        }
-        ptx::fence_proxy_async_smem();
-    }
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
+    if (DIAG && run && tid == 0) issue_mma();
+    if (DIAG) mma_issued = run;
 
-    // ---- context term on the tensor core: D[c][i] = sum_r A[c][r] B[i][r]
-    if (run && tid == 0) {
-        const uint32_t idesc = ptx::idesc_bf16_f32(128, npad);
-        const uint32_t b_hi = ptx::smem_addr(sB), b_lo = ptx::smem_addr(sBlo);
-        for (int c = 0; c < nchunks; ++c) {
-            const uint32_t a_hi = ptx::smem_addr(sA + c * chunk_bytes);
-            const uint32_t a_lo = DV == 64 ? a_hi : a_hi + 8192;
-            uint32_t pa[3], pb[3];
-            int npass = 0;
-            pa[npass] = a_hi; pb[npass++] = b_hi;  // DV = 64: hi and lo rows together
-            if (DV == 128) { pa[npass] = a_lo; pb[npass++] = b_hi; }
-            if (DIAG) { pa[npass] = a_hi; pb[npass++] = b_lo; }
-            for (int p = 0; p < npass; ++p) {
-                for (int s2 = 0; s2 < kChunkRows / 16; ++s2) {
-                    const int kk = c * (kChunkRows / 16) + s2;  // global 16-key step
-                    const uint64_t ad = ptx::desc_kmajor_noswizzle(pa[p] + s2 * 256, 128, 512);
-                    const uint64_t bd = ptx::desc_kmajor_sw128(
-                        pb[p] + (kk / 4) * slab_bytes + (kk % 4) * 32, 1024);
-                    ptx::mma_bf16(tmem, ad, bd, idesc, (c > 0 || p > 0 || s2 > 0) ? 1u : 0u);
-                }
-            }
-        }
-        ptx::mma_commit(bar_mma);
-    }
+    // ---- wait for the tensor core (always, once its MMAs are out)
     bool mma_ok = true;
-    if (run) mma_ok = ptx::mbar_wait(bar_mma, 0, kWaitLimit);
+    if (mma_issued) mma_ok = ptx::mbar_wait(bar_mma, 0, kWaitLimit);
     const bool all_mma = __syncthreads_and(mma_ok);
-    if (run && !all_mma && tid == 0) report(a.status, TV_ERR_TIMEOUT);
+    if (mma_issued && !all_mma && tid == 0) report(a.status, TV_ERR_TIMEOUT);
     run = run && all_mma;
     ptx::tc_fence_after_sync();
 
+    // after a timed-out wait, give the copies one more bounded wait before the CTA
+    // (and its shared memory) goes away
+    if (!got)
+        for (int c = 0; c < nchunks; ++c) ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit);
+    if (have_nodes && !all_landed) ptx::mbar_wait(bar_in, 0, kWaitLimit);
+
     // ---- epilogue: o_i = [e^{G_i}] * D[:, i] + sum_d w_{i,d} v_{anc_d(i)}
+    auto ancestor_sum = [&](int i, int c, float o) {
+        const int di = sDep[i];
+        const int *ap = sAnc + i * md;
+        const float *wp = sW + i * md;
+        for (int d0 = 0; d0 < di; d0 += 4) {
+            int jj[4];
+            float ww[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const bool in = d0 + u < di;
+                jj[u] = in ? ap[d0 + u] : 0;
+                ww[u] = in ? wp[d0 + u] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) o += ww[u] * __bfloat162float(sV[jj[u] * DV + c]);
+        }
+        return o;
+    };
     const int quad = warp & 3, half = warp >> 2;
     const uint32_t tq = tmem + (static_cast<uint32_t>(32 * quad) << 16);
     if (DV == 64) {
@@ -468,10 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = tid >> 6; i < n; i += kThreads / 64) {
                 float o = sX[i * 128 + c] + sX[i * 128 + 64 + c];
                 if (!DIAG) o *= sEG[i];
-                const int di = sDep[i];
-                for (int d = 0; d < di; ++d)
-                    o += sW[i * md + d] * __bfloat162float(sV[sAnc[i * md + d] * DV + c]);
-                a.out[((size_t)(off + i) * H + h) * DV + c] = o;
+                a.out[((size_t)(off + i) * H + h) * DV + c] = ancestor_sum(i, c, o);
             }
         }
     } else if (run) {
@@ -486,10 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i >= n) break;
                 float o = vals[e];
                 if (!DIAG) o *= sEG[i];
-                const int di = sDep[i];
-                for (int d = 0; d < di; ++d)
-                    o += sW[i * md + d] * __bfloat162float(sV[sAnc[i * md + d] * DV + c]);
-                a.out[((size_t)(off + i) * H + h) * DV + c] = o;
+                a.out[((size_t)(off + i) * H + h) * DV + c] = ancestor_sum(i, c, o);
             }
         }
     }
