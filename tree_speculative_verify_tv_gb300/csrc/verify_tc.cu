@@ -236,10 +236,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows, 8 KB each.
     constexpr int kPerChunk = DV * (kChunkRows / 8) / kThreads;  // items per thread per chunk
     float hold[kMaxChunks][kPerChunk][8];
+    // one thread waits on the copies; the others park at the block barrier
     bool got = true;
+    if (tid == 0) {
 #pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c)
-        if (c < nchunks) got = ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit) && got;
+        for (int c = 0; c < kMaxChunks; ++c)
+            if (c < nchunks) got = ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit) && got;
+    }
+    if (have_nodes && tid < n) {  // tree entry to shared memory; parents must precede
+        sPar[tid] = t_par;
+        sDep[tid] = t_dep;
+        if (!DIAG) sG[tid] = t_g;
+        if (t_par < -1 || t_par >= tid) *sFlag = 1;
+    }
+    got = __syncthreads_and(got);
     if (got) {
 #pragma unroll
         for (int c = 0; c < kMaxChunks; ++c) {
@@ -254,13 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    if (have_nodes && tid < n) {  // tree entry to shared memory; parents must precede
-        sPar[tid] = t_par;
-        sDep[tid] = t_dep;
-        if (!DIAG) sG[tid] = t_g;
-        if (t_par < -1 || t_par >= tid) *sFlag = 1;
-    }
-    bool run = __syncthreads_and(got);
+    __syncthreads();  // every H0 read is done before the in-place rewrite
+    bool run = got;
     if (!run && tid == 0) report(a.status, TV_ERR_TIMEOUT);
     run = run && have_nodes;
     if (run) {
@@ -319,16 +324,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- factor tiles: the scalar-decay context term needs only q, so its MMAs go
     // out now and run under the tree checks and ancestor scores
     bool landed = true;
-    if (have_nodes) landed = ptx::mbar_wait(bar_in, 0, kWaitLimit);
-    bool mma_issued = false;
+    if (tid == 0 && have_nodes) landed = ptx::mbar_wait(bar_in, 0, kWaitLimit);
     if (!DIAG && run && tid == 0 && landed) issue_mma();
-    if (!DIAG) mma_issued = __syncthreads_or(tid == 0 && run && landed);
     // tree: depth[i] = depth[parent] + 1 (1 at the context), within max_depth
     if (have_nodes && tid < n && *sFlag == 0) {
         const int want = t_par < 0 ? 1 : sDep[t_par] + 1;
         if (t_dep != want || t_dep > md) *sFlag = 1;
     }
     const bool all_landed = __syncthreads_and(landed);
+    bool mma_issued = !DIAG && run && all_landed;
     if (!all_landed && tid == 0 && run) report(a.status, TV_ERR_TIMEOUT);
     const bool tree_ok = *sFlag == 0;
     if (have_nodes && !tree_ok) {
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- wait for the tensor core (always, once its MMAs are out)
     bool mma_ok = true;
-    if (mma_issued) mma_ok = ptx::mbar_wait(bar_mma, 0, kWaitLimit);
+    if (mma_issued && tid == 0) mma_ok = ptx::mbar_wait(bar_mma, 0, kWaitLimit);
     const bool all_mma = __syncthreads_and(mma_ok);
     if (mma_issued && !all_mma && tid == 0) report(a.status, TV_ERR_TIMEOUT);
     run = run && all_mma;
@@ -475,9 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // after a timed-out wait, give the copies one more bounded wait before the CTA
     // (and its shared memory) goes away
-    if (!got)
+    if (tid == 0 && !got)
         for (int c = 0; c < nchunks; ++c) ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit);
-    if (have_nodes && !all_landed) ptx::mbar_wait(bar_in, 0, kWaitLimit);
+    if (tid == 0 && have_nodes && !all_landed) ptx::mbar_wait(bar_in, 0, kWaitLimit);
 
     // ---- epilogue: o_i = [e^{G_i}] * D[:, i] + sum_d w_{i,d} v_{anc_d(i)}
     auto ancestor_sum = [&](int i, int c, float o) {
