@@ -548,6 +548,347 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) ptx::tmem_dealloc(tmem, P.tmem_cols);
 }
 
+__device__ __forceinline__ void named_barrier(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Scalar-decay verification, warp-specialized so that independent phases overlap:
+//   warps 0-3 stream H0 in chunks, split each chunk in place into bf16 hi/lo operand
+//     rows as it lands, then issue the context MMA (D = H0^T q) as soon as q has landed;
+//   warps 4-7 read the request's offsets and tree, issue the q/k/v tile copies,
+//     validate the tree and compute the ancestor scores
+//     w_{i,d} = e^{G_i - G_{anc_d(i)}} (q_i . k_{anc_d(i)}) and e^{G_i};
+//   all eight warps then form o_i = e^{G_i} D[:, i] + sum_d w_{i,d} v_{anc_d(i)}.
+// Same shared-memory plan, operand layouts and error behaviour as verify_tc_kernel.
+template <int DV>
+__global__ void __launch_bounds__(kThreads, 1)
+    verify_tc_scalar_ws_kernel(const __grid_constant__ CUtensorMap tm_q,
+                               const __grid_constant__ CUtensorMap tm_k,
+                               const __grid_constant__ CUtensorMap tm_v, const TcParams P) {
+    constexpr int kGroup = kThreads / 2;  // threads per specialized group
+    const VerifyArgs &a = P.a;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int dk = a.dk, H = a.H, md = a.max_depth;
+    const TcLayout L(dk, DV, P.npad_max, md, false);
+    const uint32_t slab_bytes = P.npad_max * 128;
+    uint8_t *sA = smem + L.a_off;
+    uint8_t *sB = smem + L.b_off;
+    const __nv_bfloat16 *sK = reinterpret_cast<const __nv_bfloat16 *>(smem + L.k_off);
+    const __nv_bfloat16 *sV = reinterpret_cast<const __nv_bfloat16 *>(smem + L.v_off);
+    float *sX = reinterpret_cast<float *>(smem + L.x_off);
+    float *sW = reinterpret_cast<float *>(smem + L.w_off);
+    int *sAnc = reinterpret_cast<int *>(smem + L.anc_off);
+    float *sEG = reinterpret_cast<float *>(smem + L.eg_off);
+    float *sG = reinterpret_cast<float *>(smem + L.g_off);
+    int *sPar = reinterpret_cast<int *>(smem + L.par_off);
+    int *sDep = reinterpret_cast<int *>(smem + L.dep_off);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+    uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + L.misc_off);
+    int *sFlag = reinterpret_cast<int *>(smem + L.misc_off + 4);   // tree error
+    int *sState = reinterpret_cast<int *>(smem + L.misc_off + 8);  // copy/MMA progress bits
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.x, b = unit / H, h = unit % H;
+    const int nchunks = dk / kChunkRows;
+    const uint32_t chunk_bytes = kChunkRows * DV * 4;
+    const uint32_t bar0 = ptx::smem_addr(&bars[0]);
+    const uint32_t bar_in = ptx::smem_addr(&bars[kMaxChunks]);
+    const uint32_t bar_mma = ptx::smem_addr(&bars[kMaxChunks + 1]);
+    // progress bits; each is written by one group only, before that group's barrier
+    enum { kH0Late = 1, kQkvLateTree = 2, kMmaOut = 4, kQkvLateMma = 8 };
+
+    // ---- prologue that touches no input: barriers, tensor memory
+    if (tid == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+        for (int c = 0; c < kMaxChunks + 2; ++c) ptx::mbar_init(bar0 + 8 * c, 1);
+        ptx::fence_mbar_init();
+        *sFlag = 0;
+        *sState = 0;
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(ptx::smem_addr(sTmem), P.tmem_cols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *sTmem;
+
+    ptx::grid_dependency_wait();  // inputs may be written by the previous kernel
+    if (tid == 0) {
+        const float *src = a.H0 + (size_t)unit * dk * DV;
+        for (int c = 0; c < nchunks; ++c) {
+            ptx::mbar_arrive_expect_tx(bar0 + 8 * c, chunk_bytes);
+            ptx::bulk_g2s(ptx::smem_addr(sA) + c * chunk_bytes, src + c * kChunkRows * DV,
+                          chunk_bytes, bar0 + 8 * c);
+        }
+    }
+    int off = 0, n = 0;
+    const bool range_ok = request_range(a.node_offsets, b, a.T, a.max_nodes, off, n);
+    const int npad = (n + 15) & ~15;
+    const bool have_nodes = range_ok && n > 0;
+    ptx::grid_launch_dependents();
+
+    if (warp < 4) {
+        // ================= H0 group: split chunks as they land, then the MMA
+        constexpr int kPer = DV * (kChunkRows / 8) / kGroup;  // (channel, 8-key) items
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c) {
+            if (c >= nchunks) break;
+            if (tid == 0 && !ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit)) atomicOr(sState, kH0Late);
+            named_barrier(1, kGroup);
+            const bool ok = (*sState & kH0Late) == 0 && have_nodes;
+            uint8_t *chunk = sA + c * chunk_bytes;
+            float hold[kPer][8];
+            if (ok) {
+                const float *f32 = reinterpret_cast<const float *>(chunk);
+#pragma unroll
+                for (int t = 0; t < kPer; ++t) {
+                    const int it = tid + t * kGroup;
+                    const int ch = it % DV, kq = it / DV;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) hold[t][e] = f32[(kq * 8 + e) * DV + ch];
+                }
+            }
+            named_barrier(1, kGroup);  // the chunk is read before it is rewritten in place
+            if (ok) {
+#pragma unroll
+                for (int t = 0; t < kPer; ++t) {
+                    const int it = tid + t * kGroup;
+                    const int ch = it % DV, kq = it / DV;
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        split_pair(hold[t][2 * e], hold[t][2 * e + 1], hi[e], lo[e]);
+                    const int r_lo = DV == 64 ? 64 + ch : ch;
+                    uint8_t *lo_base = DV == 64 ? chunk : chunk + 8192;
+                    *reinterpret_cast<uint4 *>(chunk + (ch / 8) * 512 + kq * 128 + (ch % 8) * 16) =
+                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(lo_base + (r_lo / 8) * 512 + kq * 128 + (r_lo % 8) * 16) =
+                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before_sync();
+        named_barrier(1, kGroup);
+        ptx::tc_fence_after_sync();
+        if (tid == 0 && have_nodes && (*sState & kH0Late) == 0) {
+            if (ptx::mbar_wait(bar_in, 0, kWaitLimit)) {
+                const uint32_t idesc = ptx::idesc_bf16_f32(128, npad);
+                const uint32_t b0 = ptx::smem_addr(sB);
+                for (int c = 0; c < nchunks; ++c) {
+                    const uint32_t a_hi = ptx::smem_addr(sA + c * chunk_bytes);
+                    const int npass = DV == 64 ? 1 : 2;  // DV = 128: hi operand, then lo
+                    for (int p = 0; p < npass; ++p) {
+                        const uint32_t a_op = a_hi + p * 8192;
+                        for (int s2 = 0; s2 < kChunkRows / 16; ++s2) {
+                            const int kk = c * (kChunkRows / 16) + s2;
+                            const uint64_t ad = ptx::desc_kmajor_noswizzle(a_op + s2 * 256, 128, 512);
+                            const uint64_t bd = ptx::desc_kmajor_sw128(
+                                b0 + (kk / 4) * slab_bytes + (kk % 4) * 32, 1024);
+                            ptx::mma_bf16(tmem, ad, bd, idesc, (c > 0 || p > 0 || s2 > 0) ? 1u : 0u);
+                        }
+                    }
+                }
+                ptx::mma_commit(bar_mma);
+                atomicOr(sState, kMmaOut);
+            } else {
+                atomicOr(sState, kQkvLateMma);
+            }
+        }
+    } else {
+        // ================= tree group: tree, factor tiles, ancestor scores
+        const int t = tid - kGroup;
+        if (t == 0 && have_nodes) {
+            const int slabs = dk / 64;
+            ptx::mbar_arrive_expect_tx(bar_in, 2 * npad * dk * 2 + npad * DV * 2);
+            for (int r = 0; r < npad; r += 16) {
+                for (int s = 0; s < slabs; ++s)
+                    ptx::tma_load_3d(ptx::smem_addr(sB + s * slab_bytes + r * 128), &tm_q, s * 64,
+                                     h, off + r, bar_in);
+                ptx::tma_load_3d(ptx::smem_addr(sK) + r * dk * 2, &tm_k, 0, h, off + r, bar_in);
+                ptx::tma_load_3d(ptx::smem_addr(sV) + r * DV * 2, &tm_v, 0, h, off + r, bar_in);
+            }
+        }
+        if (have_nodes) {
+            for (int i = t; i < n; i += kGroup) {
+                const int p = a.parent[off + i], d = a.depth[off + i];
+                const float gv = a.g[(size_t)(off + i) * H + h];
+                sPar[i] = p;
+                sDep[i] = d;
+                sG[i] = gv;
+                if (p < -1 || p >= i) *sFlag = 1;
+            }
+        }
+        named_barrier(2, kGroup);
+        if (have_nodes && *sFlag == 0)
+            for (int i = t; i < n; i += kGroup) {
+                const int p = sPar[i];
+                const int want = p < 0 ? 1 : sDep[p] + 1;
+                if (sDep[i] != want || sDep[i] > md) *sFlag = 1;
+            }
+        if (t == 0 && have_nodes && !ptx::mbar_wait(bar_in, 0, kWaitLimit))
+            atomicOr(sState, kQkvLateTree);
+        named_barrier(2, kGroup);
+        if (have_nodes && *sFlag == 0 && (*sState & kQkvLateTree) == 0) {
+            // root paths with the decay factor of every (node, ancestor) pair
+            for (int i = t; i < n; i += kGroup) {
+                float s = 0.f;
+                int j = i, d = 0;
+                while (j >= 0) {
+                    sAnc[i * md + d] = j;
+                    sW[i * md + d] = expf(s);
+                    s += sG[j];
+                    j = sPar[j];
+                    ++d;
+                }
+                sEG[i] = expf(s);
+            }
+            named_barrier(2, kGroup);
+            // w *= q_i . k_j: one 8-lane group per node, warp-uniform loop bounds
+            const int sub = lane & 7;
+            const int per = dk / 8;
+            const int gw = warp - 4;
+            for (int base = gw * 4; base < n; base += kGroup / 8) {
+                const int i = base + (lane >> 3);
+                const bool valid = i < n;
+                float qv[16];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (valid && u * 8 < per) {
+                        const int c = sub * per + u * 8;
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(sB + swz_offset(i, c, slab_bytes));
+                        const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            qv[u * 8 + 2 * e] = __low2float(p2[e]);
+                            qv[u * 8 + 2 * e + 1] = __high2float(p2[e]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) qv[u * 8 + e] = 0.f;
+                    }
+                }
+                const int di = valid ? sDep[i] : 0;
+                const int dmax = __reduce_max_sync(0xffffffffu, di);
+                for (int d = 0; d < dmax; ++d) {
+                    const bool act = d < di;
+                    float p0 = 0.f, p1 = 0.f;
+                    if (act) {
+                        const int j = sAnc[i * md + d];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            if (u * 8 < per) {
+                                const uint4 raw = *reinterpret_cast<const uint4 *>(sK + j * dk + sub * per + u * 8);
+                                const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    p0 += qv[u * 8 + 2 * e] * __low2float(p2[e]);
+                                    p1 += qv[u * 8 + 2 * e + 1] * __high2float(p2[e]);
+                                }
+                            }
+                        }
+                    }
+                    float part = p0 + p1;
+                    part += __shfl_xor_sync(0xffffffffu, part, 4);
+                    part += __shfl_xor_sync(0xffffffffu, part, 2);
+                    part += __shfl_xor_sync(0xffffffffu, part, 1);
+                    if (act && sub == 0) sW[i * md + d] *= part;
+                }
+            }
+        }
+    }
+
+    // ================= join
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const int st = *sState;
+    const bool tree_ok = *sFlag == 0;
+    const bool mma_out = (st & kMmaOut) != 0;
+    if (tid == 0) {
+        if (!range_ok && h == 0) report(a.status, TV_ERR_TREE);
+        if (have_nodes && !tree_ok && h == 0) report(a.status, TV_ERR_TREE);
+        if (st & (kH0Late | kQkvLateTree | kQkvLateMma)) report(a.status, TV_ERR_TIMEOUT);
+    }
+    if (have_nodes && !tree_ok)
+        for (int e = tid; e < n * DV; e += kThreads)
+            a.out[((size_t)(off + e / DV) * H + h) * DV + e % DV] = 0.f;
+    bool mma_ok = true;
+    if (mma_out && tid == 0) mma_ok = ptx::mbar_wait(bar_mma, 0, kWaitLimit);
+    mma_ok = __syncthreads_and(mma_ok);
+    if (mma_out && !mma_ok && tid == 0) report(a.status, TV_ERR_TIMEOUT);
+    ptx::tc_fence_after_sync();
+    const bool run = have_nodes && tree_ok && mma_out && mma_ok && !(st & kQkvLateTree);
+
+    // ---- epilogue
+    auto ancestor_sum = [&](int i, int c, float o) {
+        const int di = sDep[i];
+        const int *ap = sAnc + i * md;
+        const float *wp = sW + i * md;
+        for (int d0 = 0; d0 < di; d0 += 4) {
+            int jj[4];
+            float ww[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const bool in = d0 + u < di;
+                jj[u] = in ? ap[d0 + u] : 0;
+                ww[u] = in ? wp[d0 + u] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) o += ww[u] * __bfloat162float(sV[jj[u] * DV + c]);
+        }
+        return o;
+    };
+    const int quad = warp & 3, half = warp >> 2;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(32 * quad) << 16);
+    const int ncols_half = npad / 2;  // multiple of 8
+    if (DV == 64) {
+        if (run) {
+            const int row = 32 * quad + lane;
+            for (int col = half * ncols_half; col < (half + 1) * ncols_half; col += 8) {
+                float vals[8];
+                ptx::tmem_ld_x8(tq + col, vals);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) sX[(col + e) * 128 + row] = vals[e];
+            }
+        }
+        __syncthreads();
+        if (run) {
+            const int c = tid & 63;
+            for (int i = tid >> 6; i < n; i += kThreads / 64) {
+                const float o = (sX[i * 128 + c] + sX[i * 128 + 64 + c]) * sEG[i];
+                a.out[((size_t)(off + i) * H + h) * DV + c] = ancestor_sum(i, c, o);
+            }
+        }
+    } else if (run) {
+        const int c = 32 * quad + lane;
+        for (int col = half * ncols_half; col < (half + 1) * ncols_half; col += 8) {
+            float vals[8];
+            ptx::tmem_ld_x8(tq + col, vals);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int i = col + e;
+                if (i >= n) break;
+                a.out[((size_t)(off + i) * H + h) * DV + c] = ancestor_sum(i, c, vals[e] * sEG[i]);
+            }
+        }
+    }
+
+    // a timed-out copy gets one more bounded wait before the CTA's memory goes away
+    if (tid == 0 && (st & kH0Late))
+        for (int c = 0; c < nchunks; ++c) ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit);
+    if (tid == 0 && (st & (kQkvLateTree | kQkvLateMma))) ptx::mbar_wait(bar_in, 0, kWaitLimit);
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) ptx::tmem_dealloc(tmem, P.tmem_cols);
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -589,6 +930,33 @@ size_t tc_smem_bytes(const VerifyArgs &a) {
     return TcLayout(a.dk, a.dv, npad_max, a.max_depth, a.decay == TV_DECAY_DIAG).total;
 }
 
+// Shared-memory opt-in, a residency cap that keeps co-resident CTAs within the 512
+// tensor-memory columns of an SM, and a programmatic-dependent launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_tc_kernel(void (*kern)(KArgs...), const TcParams &P, size_t smem,
+                             unsigned grid, cudaStream_t s, Args &&...args) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const int max_ctas = 512 / P.tmem_cols;
+    if (per_sm > max_ctas) {
+        // enlarge the request so that max_ctas + 1 blocks no longer fit on one SM
+        int dev = 0, smem_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        const size_t need = (size_t)smem_sm / (max_ctas + 1) + 1;
+        if (need > smem) {
+            smem = need;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, static_cast<Args &&>(args)...);
+}
+
 template <int DV, bool DIAG>
 cudaError_t launch_tc(const VerifyArgs &a, cudaStream_t s) {
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -609,42 +977,12 @@ cudaError_t launch_tc(const VerifyArgs &a, cudaStream_t s) {
     P.a = a;
     P.npad_max = (a.max_nodes + 15) & ~15;
     P.tmem_cols = tmem_columns(P.npad_max);
-    size_t smem = tc_smem_bytes(a);
-    auto kern = verify_tc_kernel<DV, DIAG>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    // keep co-resident CTAs within the 512 tensor-memory columns of an SM
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-    if (e != cudaSuccess) return e;
-    const int max_ctas = 512 / P.tmem_cols;
-    if (per_sm > max_ctas) {
-        // enlarge the request so that max_ctas + 1 blocks no longer fit on one SM
-        int dev = 0, smem_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-        size_t need = (size_t)smem_sm / (max_ctas + 1) + 1;
-        if (need > smem) {
-            smem = need;
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-        }
-    }
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.B * a.H));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv_, tg, P);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    const size_t smem = tc_smem_bytes(a);
+    const unsigned grid = (unsigned)(a.B * a.H);
+    if constexpr (DIAG)
+        return launch_tc_kernel(verify_tc_kernel<DV, true>, P, smem, grid, s, tq, tk, tv_, tg, P);
+    else
+        return launch_tc_kernel(verify_tc_scalar_ws_kernel<DV>, P, smem, grid, s, tq, tk, tv_, P);
 }
 
 }  // namespace
