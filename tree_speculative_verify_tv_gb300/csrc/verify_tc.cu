@@ -53,7 +53,7 @@ constexpr int kMaxChunks = 4;   // dk <= 128
 //   The lo-part exchange (dv = 64) reuses the A region when it is large enough.
 struct TcLayout {
     uint32_t a_off, b_off, blo_off, q_off, k_off, v_off, e_off, x_off, w_off, anc_off, eg_off,
-        g_off, par_off, dep_off, bar_off, misc_off, total;
+        g_off, par_off, dep_off, poff_off, pnode_off, bar_off, misc_off, total;
     __host__ __device__ TcLayout(int dk, int dv, int npad_max, int max_depth, bool diag) {
         const uint32_t swz_tile = (dk / 64) * npad_max * 128;  // one swizzled [n][dk] bf16 tile
         const uint32_t a_bytes = dk * dv * 4;
@@ -75,7 +75,9 @@ struct TcLayout {
         g_off = align_up(eg_off + npad_max * 4, 16);
         par_off = align_up(g_off + npad_max * 4, 16);
         dep_off = align_up(par_off + npad_max * 4, 16);
-        bar_off = align_up(dep_off + npad_max * 4, 16);
+        poff_off = align_up(dep_off + npad_max * 4, 16);          // first pair of each node
+        pnode_off = align_up(poff_off + (npad_max + 1) * 4, 16);  // node of each pair (u8)
+        bar_off = align_up(pnode_off + npad_max * max_depth, 16);
         misc_off = bar_off + 8 * 8;
         total = align_up(misc_off + 16, 16) + 1024;  // + slack for 1024-byte base alignment
     }
@@ -588,6 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + L.misc_off);
     int *sFlag = reinterpret_cast<int *>(smem + L.misc_off + 4);   // tree error
     int *sState = reinterpret_cast<int *>(smem + L.misc_off + 8);  // copy/MMA progress bits
+    int *sPairOff = reinterpret_cast<int *>(smem + L.poff_off);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x, b = unit / H, h = unit % H;
@@ -732,74 +735,91 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int want = p < 0 ? 1 : sDep[p] + 1;
                 if (sDep[i] != want || sDep[i] > md) *sFlag = 1;
             }
-        if (t == 0 && have_nodes && !ptx::mbar_wait(bar_in, 0, kWaitLimit))
-            atomicOr(sState, kQkvLateTree);
         named_barrier(2, kGroup);
-        if (have_nodes && *sFlag == 0 && (*sState & kQkvLateTree) == 0) {
-            // root paths with the decay factor of every (node, ancestor) pair
+        const bool tree_ok = have_nodes && *sFlag == 0;
+        if (tree_ok && warp == 4) {
+            // (node, ancestor) pairs numbered node by node: exclusive scan of depths
+            const int per = (n + 31) / 32;
+            int local = 0;
+            for (int u = 0; u < per; ++u) {
+                const int i = lane * per + u;
+                if (i < n) local += sDep[i];
+            }
+            int incl = local;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            int run_sum = incl - local;
+            for (int u = 0; u < per; ++u) {
+                const int i = lane * per + u;
+                if (i < n) {
+                    sPairOff[i] = run_sum;
+                    run_sum += sDep[i];
+                }
+            }
+            if (lane == 31) sPairOff[n] = incl;
+        }
+        named_barrier(2, kGroup);
+        uint8_t *sPairNode = smem + L.pnode_off;
+        if (tree_ok) {
+            // root paths with the decay factor of every (node, ancestor) pair:
+            // anc_d(i), e^{G_i - G_{anc_d(i)}} and e^{G_i}; needs only the tree and g
             for (int i = t; i < n; i += kGroup) {
                 float s = 0.f;
                 int j = i, d = 0;
+                const int p0 = sPairOff[i];
                 while (j >= 0) {
                     sAnc[i * md + d] = j;
                     sW[i * md + d] = expf(s);
+                    sPairNode[p0 + d] = static_cast<uint8_t>(i);
                     s += sG[j];
                     j = sPar[j];
                     ++d;
                 }
                 sEG[i] = expf(s);
             }
-            named_barrier(2, kGroup);
-            // w *= q_i . k_j: one 8-lane group per node, warp-uniform loop bounds
+        }
+        if (t == 0 && have_nodes && !ptx::mbar_wait(bar_in, 0, kWaitLimit))
+            atomicOr(sState, kQkvLateTree);
+        named_barrier(2, kGroup);
+        if (tree_ok && (*sState & kQkvLateTree) == 0) {
+            // w_{i,d} *= q_i . k_{anc_d(i)}: one 8-lane group per pair; the pair count
+            // is uniform, so every lane of a warp takes each shuffle
+            const int npairs = sPairOff[n];
             const int sub = lane & 7;
-            const int per = dk / 8;
-            const int gw = warp - 4;
-            for (int base = gw * 4; base < n; base += kGroup / 8) {
-                const int i = base + (lane >> 3);
-                const bool valid = i < n;
-                float qv[16];
+            const int per = dk / 8;  // 16 or 8 key channels per lane, whole 16-byte chunks
+            for (int base = (warp - 4) * 4; base < npairs; base += kGroup / 8) {
+                const int pr = base + (lane >> 3);
+                const bool act = pr < npairs;
+                float p0 = 0.f, p1 = 0.f;
+                int i = 0, d = 0;
+                if (act) {
+                    i = sPairNode[pr];
+                    d = pr - sPairOff[i];
+                    const int j = sAnc[i * md + d];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    if (valid && u * 8 < per) {
-                        const int c = sub * per + u * 8;
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(sB + swz_offset(i, c, slab_bytes));
-                        const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                    for (int u = 0; u < 2; ++u) {
+                        if (u * 8 < per) {
+                            const int c = sub * per + u * 8;
+                            const uint4 qr = *reinterpret_cast<const uint4 *>(sB + swz_offset(i, c, slab_bytes));
+                            const uint4 kr = *reinterpret_cast<const uint4 *>(sK + j * dk + c);
+                            const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qr);
+                            const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            qv[u * 8 + 2 * e] = __low2float(p2[e]);
-                            qv[u * 8 + 2 * e + 1] = __high2float(p2[e]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) qv[u * 8 + e] = 0.f;
-                    }
-                }
-                const int di = valid ? sDep[i] : 0;
-                const int dmax = __reduce_max_sync(0xffffffffu, di);
-                for (int d = 0; d < dmax; ++d) {
-                    const bool act = d < di;
-                    float p0 = 0.f, p1 = 0.f;
-                    if (act) {
-                        const int j = sAnc[i * md + d];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            if (u * 8 < per) {
-                                const uint4 raw = *reinterpret_cast<const uint4 *>(sK + j * dk + sub * per + u * 8);
-                                const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    p0 += qv[u * 8 + 2 * e] * __low2float(p2[e]);
-                                    p1 += qv[u * 8 + 2 * e + 1] * __high2float(p2[e]);
-                                }
+                            for (int e = 0; e < 4; ++e) {
+                                p0 += __low2float(q2[e]) * __low2float(k2[e]);
+                                p1 += __high2float(q2[e]) * __high2float(k2[e]);
                             }
                         }
                     }
-                    float part = p0 + p1;
-                    part += __shfl_xor_sync(0xffffffffu, part, 4);
-                    part += __shfl_xor_sync(0xffffffffu, part, 2);
-                    part += __shfl_xor_sync(0xffffffffu, part, 1);
-                    if (act && sub == 0) sW[i * md + d] *= part;
                 }
+                float part = p0 + p1;
+                part += __shfl_xor_sync(0xffffffffu, part, 4);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                if (act && sub == 0) sW[i * md + d] *= part;
             }
         }
     }
@@ -826,58 +846,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after_sync();
     const bool run = have_nodes && tree_ok && mma_out && mma_ok && !(st & kQkvLateTree);
 
-    // ---- epilogue
-    auto ancestor_sum = [&](int i, int c, float o) {
-        const int di = sDep[i];
-        const int *ap = sAnc + i * md;
-        const float *wp = sW + i * md;
-        for (int d0 = 0; d0 < di; d0 += 4) {
-            int jj[4];
-            float ww[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const bool in = d0 + u < di;
-                jj[u] = in ? ap[d0 + u] : 0;
-                ww[u] = in ? wp[d0 + u] : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) o += ww[u] * __bfloat162float(sV[jj[u] * DV + c]);
-        }
-        return o;
-    };
+    // ---- epilogue, 32 node columns at a time: every warp copies its tensor-memory
+    // quadrant (rows = value channels; dv = 64 keeps hi rows 0-63 and lo rows 64-127)
+    // into shared memory; then each thread forms 4 consecutive channels of one node:
+    // o_i = e^{G_i} D[:, i] + sum_d w_{i,d} v_{anc_d(i)}, stored as a float4
+    float *sXc = reinterpret_cast<float *>(sA);  // A is free once the MMAs completed
     const int quad = warp & 3, half = warp >> 2;
     const uint32_t tq = tmem + (static_cast<uint32_t>(32 * quad) << 16);
-    const int ncols_half = npad / 2;  // multiple of 8
-    if (DV == 64) {
+    constexpr int kQuads = DV / 4;
+    for (int c0 = 0; c0 < npad; c0 += 32) {  // npad is uniform
+        const int ncol = min(32, npad - c0);  // 16 or 32
         if (run) {
             const int row = 32 * quad + lane;
-            for (int col = half * ncols_half; col < (half + 1) * ncols_half; col += 8) {
+            for (int col = half * (ncol / 2); col < (half + 1) * (ncol / 2); col += 8) {
                 float vals[8];
-                ptx::tmem_ld_x8(tq + col, vals);
+                ptx::tmem_ld_x8(tq + c0 + col, vals);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) sX[(col + e) * 128 + row] = vals[e];
+                for (int e = 0; e < 8; ++e) sXc[(col + e) * 128 + row] = vals[e];
             }
         }
         __syncthreads();
         if (run) {
-            const int c = tid & 63;
-            for (int i = tid >> 6; i < n; i += kThreads / 64) {
-                const float o = (sX[i * 128 + c] + sX[i * 128 + 64 + c]) * sEG[i];
-                a.out[((size_t)(off + i) * H + h) * DV + c] = ancestor_sum(i, c, o);
+            const int ntask = min(ncol, n - c0) * kQuads;
+            for (int task = tid; task < ntask; task += kThreads) {
+                const int il = task / kQuads, c = (task % kQuads) * 4;
+                const int i = c0 + il;
+                float4 o = *reinterpret_cast<const float4 *>(sXc + il * 128 + c);
+                if (DV == 64) {
+                    const float4 lo = *reinterpret_cast<const float4 *>(sXc + il * 128 + 64 + c);
+                    o.x += lo.x; o.y += lo.y; o.z += lo.z; o.w += lo.w;
+                }
+                const float eg = sEG[i];
+                o.x *= eg; o.y *= eg; o.z *= eg; o.w *= eg;
+                const int di = sDep[i];
+                for (int d = 0; d < di; ++d) {
+                    const float w = sW[i * md + d];
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(sV + sAnc[i * md + d] * DV + c);
+                    const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+                    const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+                    o.x += w * __low2float(v01); o.y += w * __high2float(v01);
+                    o.z += w * __low2float(v23); o.w += w * __high2float(v23);
+                }
+                *reinterpret_cast<float4 *>(a.out + ((size_t)(off + i) * H + h) * DV + c) = o;
             }
         }
-    } else if (run) {
-        const int c = 32 * quad + lane;
-        for (int col = half * ncols_half; col < (half + 1) * ncols_half; col += 8) {
-            float vals[8];
-            ptx::tmem_ld_x8(tq + col, vals);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = col + e;
-                if (i >= n) break;
-                a.out[((size_t)(off + i) * H + h) * DV + c] = ancestor_sum(i, c, vals[e] * sEG[i]);
-            }
-        }
+        __syncthreads();  // the staging buffer is reused by the next column chunk
     }
 
     // a timed-out copy gets one more bounded wait before the CTA's memory goes away
