@@ -1,5 +1,6 @@
 """Benchmark of the tree-verification hot path on GB300: one step = tv_verify +
-tv_accept_greedy + tv_commit over one batch of the Mamba-2-like workload
+tv_accept_commit (greedy acceptance and path commit in one launch) over one
+batch of the Mamba-2-like workload
 (B=16 requests, H=24 heads, dk=128, dv=64, 16-node top-4 draft trees, bf16
 q/k/v, fp32 states, scalar decay).
 
@@ -46,7 +47,7 @@ WORKLOADS = {
 }
 WORKLOAD = WORKLOADS[2]
 KERNEL_SOURCES = ["tree_speculative_verify_tv_gb300/csrc/verify_tc.cu",
-                  "tree_speculative_verify_tv_gb300/csrc/verify_simt.cu",
+                  "tree_speculative_verify_tv_gb300/csrc/tc_ptx.cuh",
                   "tree_speculative_verify_tv_gb300/csrc/tv_internal.cuh"]
 
 
@@ -365,9 +366,9 @@ def run_ours(args, world, rank, local):
     node_heads = base.T * base.H
 
     def step(d):
+        # one pass of the hot path: verify, then greedy accept + commit in one launch
         d.verify(stream=stream, variant=args.variant)
-        d.accept(stream=stream)
-        d.commit(stream=stream)
+        d.accept_commit(stream=stream)
 
     with torch.cuda.stream(stream):
         for d in dbs:
@@ -397,6 +398,8 @@ def run_ours(args, world, rank, local):
                 return lambda d=d: d.verify(stream=stream, variant=args.variant)
             if kind == "accept":
                 return lambda d=d: d.accept(stream=stream)
+            if kind == "accept_commit":
+                return lambda d=d: d.accept_commit(stream=stream)
             return lambda d=d: d.commit(stream=stream)
         full = capture([one(i) for i in range(R)])
         rem = K % R
@@ -439,6 +442,7 @@ def run_ours(args, world, rank, local):
     t_verify, _, _ = timed("verify", K)
     t_accept, _, _ = timed("accept", K)
     t_commit, _, _ = timed("commit", K)
+    t_acom, _, _ = timed("accept_commit", K)
     sampler.stop()
     for d in dbs:
         st = int(d.status[0].item())
@@ -530,10 +534,12 @@ def run_ours(args, world, rank, local):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 3 * K,
+            "gpu_launches": 2 * K,
             "clocks": clocks,
-            "kernels_us": {"verify": t_verify / K * 1e6, "accept": t_accept / K * 1e6,
-                           "commit": t_commit / K * 1e6},
+            "kernels_us": {"verify": t_verify / K * 1e6, "accept_commit": t_acom / K * 1e6,
+                           "accept (separate call)": t_accept / K * 1e6,
+                           "commit (separate call)": t_commit / K * 1e6},
+            "step_kernels": ["tv_verify", "tv_accept_commit"],
             "verify_only": {"value": node_heads / v_launch, "unit": UNIT,
                             "gbs": achieved},
             "verify_folded_layers": (dict(folded, frac=folded["gbs"] / peak) if folded
@@ -568,8 +574,7 @@ def run_e2e(args, host_batch, dev, stream, tv, world):
             getattr(db, n).copy_(getattr(hb, n), non_blocking=True)
         db.status.zero_()
         db.verify(stream=stream, variant=args.variant)
-        db.accept(stream=stream)
-        db.commit(stream=stream)
+        db.accept_commit(stream=stream)
         for n in outs:
             getattr(hb, n).copy_(getattr(db, n), non_blocking=True)
 

@@ -187,6 +187,27 @@ tv_status tv_commit(const tv_problem *p, const float *H0, const float *g, const 
                     float *H_new, int32_t *dev_status, void *stream);
 
 /*
+ * tv_accept_commit -- tv_accept_greedy and tv_commit in one launch.
+ * Same results as tv_accept_greedy followed by tv_commit with the path it found:
+ * every commit block re-runs its request's greedy walk (LLM Primer VI ch. 9
+ * §9.1) on shared memory and restores the accepted path's state from the
+ * factors (Bole summary page, "Core techniques" §2), so the state update does
+ * not wait for a separate acceptance launch.
+ *
+ *   p, H0, g, k, v, H_new          as in tv_commit (H_new may equal H0)
+ *   draft_tokens, target_argmax, root_argmax, accept_len, path, bonus
+ *                                  as in tv_accept_greedy
+ * Device-detected errors (bad offsets, a parent outside [-1, i), a walk longer
+ * than max_depth): TV_ERR_TREE; that request gets accept_len = 0, path = -1,
+ * bonus = -1 and its H_new is left untouched.
+ */
+tv_status tv_accept_commit(const tv_problem *p, const float *H0, const float *g, const void *k,
+                           const void *v, const int32_t *draft_tokens,
+                           const int32_t *target_argmax, const int32_t *root_argmax,
+                           int32_t *accept_len, int32_t *path, int32_t *bonus, float *H_new,
+                           int32_t *dev_status, void *stream);
+
+/*
  * tv_verify_variant -- the kernel tv_verify (TV_VARIANT_AUTO) would launch for
  * this problem: TV_VARIANT_TC or TV_VARIANT_SIMT.  Reads only the sizes and
  * kinds in *p (no device memory); returns the negative tv_status of an invalid

@@ -24,15 +24,19 @@ def run_library(batch, variant=0, commit_in_place=False, steps=("verify", "accep
         if not commit_in_place:
             d.H_new.fill_(float("nan"))
         d.commit(in_place=commit_in_place)
+    if "accept_commit" in steps:
+        if not commit_in_place:
+            d.H_new.fill_(float("nan"))
+        d.accept_commit(in_place=commit_in_place)
     torch.cuda.synchronize()
     res = {"status": int(d.status[0].item())}
     if "verify" in steps:
         res["out"] = d.out[:batch.T].cpu().numpy().astype(np.float64)
-    if "accept" in steps:
+    if "accept" in steps or "accept_commit" in steps:
         res["len"] = d.accept_len[:batch.B].cpu().numpy()
         res["path"] = d.path[:batch.B].cpu().numpy()
         res["bonus"] = d.bonus[:batch.B].cpu().numpy()
-    if "commit" in steps:
+    if "commit" in steps or "accept_commit" in steps:
         res["H_new"] = (d.H0 if commit_in_place else d.H_new).cpu().numpy().astype(np.float64)
     return res
 

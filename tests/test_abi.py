@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert {"tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
-            "tv_status_string", "tv_version"} <= set(names)
+            "tv_accept_commit", "tv_status_string", "tv_version"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -148,6 +148,22 @@ def test_commit_rejects_bad_arguments(lib):
     assert rc(Hn=None) == tv.TV_ERR_NULL
     assert rc(Hn=P[3] + 16) == tv.TV_ERR_SHAPE      # overlaps H0 without being H0
     assert rc(Hn=P[12] + 4) == tv.TV_ERR_ALIGN
+
+
+def test_accept_commit_rejects_bad_arguments(lib):
+    def rc(p=None, **kw):
+        a = dict(H0=P[3], g=P[7], k=P[5], v=P[6], dr=P[13], tg=P[14], root=P[15], ln=P[11],
+                 path=P[10], bonus=P[4], Hn=P[12], st=P[9])
+        a.update(kw)
+        return tv.tv_accept_commit(p or prob(), a["H0"], a["g"], a["k"], a["v"], a["dr"], a["tg"],
+                                   a["root"], a["ln"], a["path"], a["bonus"], a["Hn"], a["st"],
+                                   stream=0, check=False)
+    assert rc(prob(dk=12)) == tv.TV_ERR_SHAPE
+    assert rc(dr=None) == tv.TV_ERR_NULL
+    assert rc(bonus=None) == tv.TV_ERR_NULL
+    assert rc(Hn=P[3] + 16) == tv.TV_ERR_SHAPE
+    assert rc(root=P[15] + 4) == tv.TV_ERR_ALIGN
+    assert rc(prob(B=0, total_nodes=0)) == tv.TV_OK
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

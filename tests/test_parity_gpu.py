@@ -167,6 +167,59 @@ def test_strong_decay_and_zero_decay():
         _full_check(b, "auto")
 
 
+@pytest.mark.parametrize("c", [1, 2, 3, 4])
+def test_accept_commit_fused_matches_oracle(c):
+    b = workloads.make_config(c)
+    res = run_library(b, steps=("verify", "accept_commit"))
+    assert res["status"] == 0
+    ln, path = check_accept(b, res)
+    check_commit(b, res["H_new"], ln, path)
+
+
+def test_accept_commit_fused_equals_separate_calls():
+    b = workloads.config5(B=2, layers=2, heads=4, seed=3)
+    r1 = run_library(b, steps=("accept", "commit"))
+    r2 = run_library(b, steps=("accept_commit",))
+    assert r1["status"] == 0 and r2["status"] == 0
+    for key in ("len", "path", "bonus"):
+        assert np.array_equal(r1[key], r2[key])
+    assert np.array_equal(r1["H_new"], r2["H_new"])
+    r3 = run_library(b, steps=("accept_commit",), commit_in_place=True)
+    assert np.array_equal(r1["H_new"], r3["H_new"])
+
+
+def test_accept_commit_fused_malformed_tree():
+    b = _bad_tree_batch()
+    s0 = b.node_offsets[1]
+    b.parent[s0 + 2] = 4                                  # request 1: parent after child
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    d = tv.DeviceBatch(b)
+    d.status.zero_()
+    d.H_new.fill_(5.0)
+    d.accept_commit()
+    torch.cuda.synchronize()
+    assert int(d.status[0]) == 6
+    assert int(d.accept_len[1]) == 0 and int(d.bonus[1]) == -1
+    assert bool(torch.all(d.path[1] == -1))
+    assert bool(torch.all(d.H_new[1] == 5.0))             # request 1 untouched
+    # requests 0 and 2 are committed as the oracle does
+    import oracle
+    keep = [0, 2]
+    ln = d.accept_len[:b.B].cpu().numpy()
+    path = d.path[:b.B].cpu().numpy()
+    for bb in keep:
+        s, e = b.node_offsets[bb], b.node_offsets[bb + 1]
+        L, p, bo = oracle.accept(b.parent[s:e], b.draft[s:e], b.target[s:e], b.root_argmax[bb],
+                                 b.max_depth)
+        assert L == ln[bb] and np.array_equal(p, path[bb]) and bo == int(d.bonus[bb])
+    ref = oracle.commit(b, ln, path, units=[u for u in range(b.B * b.H) if u // b.H in keep])
+    Hn = d.H_new.cpu().numpy().astype(np.float64)
+    for u, Hr in ref.items():
+        bb, h = divmod(u, b.H)
+        assert mat_rel_err(Hn[bb, h], Hr) <= TOL
+
+
 def test_commit_in_place():
     b = workloads.config2(seed=4)
     res = run_library(b, commit_in_place=True)

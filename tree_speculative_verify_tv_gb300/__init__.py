@@ -6,12 +6,14 @@ include/treeverify.h; this package is the ctypes binding):
 * ``tv_verify``        outputs of every draft-tree node, tree closed form
 * ``tv_accept_greedy`` greedy acceptance walk over each request's tree
 * ``tv_commit``        state after the accepted path, rebuilt from the factors
+* ``tv_accept_commit`` the two above in one launch
 
 ``build()`` compiles the CUDA sources in-tree for sm_103a.
 """
 from ._build import build, LIB
 from .binding import (  # noqa: F401
-    DeviceBatch, TVError, load, make_problem, status_string, tv_accept_greedy, tv_commit,
+    DeviceBatch, TVError, load, make_problem, status_string, tv_accept_commit, tv_accept_greedy,
+    tv_commit,
     tv_problem, tv_status_string, tv_verify, tv_verify_variant, tv_version, EXPORTED,
     TV_OK, TV_ERR_NULL, TV_ERR_SHAPE, TV_ERR_DTYPE, TV_ERR_ALIGN, TV_ERR_UNSUPPORTED,
     TV_ERR_TREE, TV_ERR_CUDA, TV_ERR_TIMEOUT, TV_DECAY_SCALAR, TV_DECAY_DIAG, TV_BF16, TV_F32,

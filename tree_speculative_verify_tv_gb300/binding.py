@@ -27,7 +27,7 @@ TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC = 0, 1, 2
 TV_MAX_NODES, TV_MAX_DEPTH, TV_MAX_DIM = 256, 32, 256
 
 EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
-            "tv_status_string", "tv_version")
+            "tv_accept_commit", "tv_status_string", "tv_version")
 
 
 class tv_problem(ctypes.Structure):
@@ -66,7 +66,9 @@ def load(path: Optional[str] = None):
         L.tv_verify_ex.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, i32]
         L.tv_accept_greedy.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.tv_commit.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]
-        for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit):
+        L.tv_accept_commit.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit,
+                  L.tv_accept_commit):
             f.restype = ctypes.c_int32
         L.tv_status_string.argtypes = [i32]
         L.tv_status_string.restype = ctypes.c_char_p
@@ -150,6 +152,16 @@ def tv_commit(problem: tv_problem, H0, g, k, v, path, accept_len, H_new, dev_sta
     return _check(rc, "tv_commit", check)
 
 
+def tv_accept_commit(problem: tv_problem, H0, g, k, v, draft_tokens, target_argmax, root_argmax,
+                     accept_len, path, bonus, H_new, dev_status, stream=None,
+                     check: bool = True) -> int:
+    rc = load().tv_accept_commit(ctypes.byref(problem), _ptr(H0), _ptr(g), _ptr(k), _ptr(v),
+                                 _ptr(draft_tokens), _ptr(target_argmax), _ptr(root_argmax),
+                                 _ptr(accept_len), _ptr(path), _ptr(bonus), _ptr(H_new),
+                                 _ptr(dev_status), _stream(stream))
+    return _check(rc, "tv_accept_commit", check)
+
+
 # ---------------------------------------------------------------- device batches
 
 
@@ -219,6 +231,12 @@ class DeviceBatch:
                                 self.parent, self.draft, self.target, self.root_argmax,
                                 self.accept_len, self.path, self.bonus, self.status, stream,
                                 check)
+
+    def accept_commit(self, stream=None, in_place=False, check=True):
+        dst = self.H0 if in_place else self.H_new
+        return tv_accept_commit(self.problem(), self.H0, self.g, self.k, self.v, self.draft,
+                                self.target, self.root_argmax, self.accept_len, self.path,
+                                self.bonus, dst, self.status, stream, check)
 
     def commit(self, stream=None, in_place=False, check=True):
         dst = self.H0 if in_place else self.H_new

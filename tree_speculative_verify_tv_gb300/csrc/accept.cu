@@ -10,7 +10,7 @@
 // memory), then the walk runs on shared memory: children of node c all have
 // larger indices than c, so each step scans the nodes after the current one 32
 // at a time and a ballot finds the lowest matching index.  Integer-only, exact.
-#include "tv_internal.cuh"
+#include "greedy_walk.cuh"
 
 namespace tv {
 namespace {
@@ -31,49 +31,12 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
     int *par = s_par[w], *drf = s_drf[w], *tgt = s_tgt[w];
 
     int off, n;
-    bool ok = request_range(a.node_offsets, b, a.T, a.max_nodes, off, n);
-    const int32_t root = a.root[b];
-    if (ok) {
-        // parents precede children: parent[i] in [-1, i)
-        bool bad = false;
-        for (int i = lane; i < n; i += 32) {
-            const int p = a.parent[off + i];
-            par[i] = p;
-            drf[i] = a.draft[off + i];
-            tgt[i] = a.target[off + i];
-            bad |= (p < -1 || p >= i);
-        }
-        ok = !__any_sync(0xffffffffu, bad);
-    }
-    __syncwarp();
-
-    int L = 0;
-    int32_t t = root;
-    if (ok) {
-        int cur = -1;
-        for (;;) {
-            int found = -1;
-            for (int base = cur + 1; base < n; base += 32) {
-                const int i = base + lane;
-                const bool hit = i < n && par[i] == cur && drf[i] == t;
-                const unsigned m = __ballot_sync(0xffffffffu, hit);
-                if (m) {
-                    found = base + __ffs(m) - 1;
-                    break;
-                }
-            }
-            if (found < 0) break;
-            if (L >= md) {  // deeper than the caller's bound: not a valid tree for it
-                ok = false;
-                break;
-            }
-            if (lane == 0) path[L] = found;
-            ++L;
-            t = tgt[found];
-            cur = found;
-        }
-    }
-    if (!ok) {
+    int L = -1;
+    int32_t t = -1;
+    if (request_range(a.node_offsets, b, a.T, a.max_nodes, off, n))
+        L = warp_greedy_walk(a.parent, a.draft, a.target, off, n, md, a.root[b], par, drf, tgt,
+                             path, &t);
+    if (L < 0) {
         if (lane == 0) report(a.status, TV_ERR_TREE);
         L = 0;
         t = -1;

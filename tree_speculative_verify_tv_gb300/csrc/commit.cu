@@ -15,7 +15,7 @@
 // H0 float4s, the request's offsets, the accepted length and path go out
 // together; then the path's parents (for the root-path check) and its factor
 // rows are gathered together.
-#include "tv_internal.cuh"
+#include "greedy_walk.cuh"
 
 namespace tv {
 namespace {
@@ -31,10 +31,16 @@ __host__ __device__ inline int rows_per_cta(int dk, int dv) {
     return r < dk ? r : dk;
 }
 
-template <typename E, bool DIAG>
+// FUSED: run the greedy walk of the request in warp 0 instead of reading an
+// accepted path (tv_accept_commit); the CTA of head 0 and the first row tile
+// writes the request's acceptance outputs.
+template <typename E, bool DIAG, bool FUSED>
 __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
     __shared__ int s_path[kMaxDepth];
+    __shared__ int s_par[FUSED ? kMaxNodes : 1], s_drf[FUSED ? kMaxNodes : 1],
+        s_tgt[FUSED ? kMaxNodes : 1];
     __shared__ int s_bad, s_bad2, s_L, s_off;
+    if (FUSED && threadIdx.x == 0) s_bad2 = 0;
     __shared__ float s_k[kMaxDepth][kRowsMax];
     __shared__ float s_g[kMaxDepth][kRowsMax];
     __shared__ float s_alpha[kRowsMax];
@@ -63,15 +69,38 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
     if (tid < 32) {
         int off, n;
         const bool range = request_range(a.node_offsets, b, a.T, a.max_nodes, off, n);
-        const int L = a.len[b];
-        const int p = lane < md ? a.path[(size_t)b * md + lane] : -1;
-        bool bad = !range || L < 0 || L > md || (lane < L && (p < 0 || p >= n));
-        bad = __any_sync(0xffffffffu, bad);
-        if (lane < L && !bad) s_path[lane] = p;
-        if (lane == 0) {
-            s_bad = bad;
-            s_L = bad ? 0 : L;
-            s_off = off;
+        if (FUSED) {
+            int L = -1;
+            int32_t t = -1;
+            if (range)
+                L = warp_greedy_walk(a.parent, a.draft, a.target, off, n, md, a.root[b], s_par,
+                                     s_drf, s_tgt, s_path, &t);
+            const bool bad = L < 0;
+            __syncwarp();
+            if (h == 0 && blockIdx.y == 0) {  // the request's acceptance outputs, once
+                for (int m = lane; m < md; m += 32)
+                    a.path_out[(size_t)b * md + m] = (!bad && m < L) ? s_path[m] : -1;
+                if (lane == 0) {
+                    a.len_out[b] = bad ? 0 : L;
+                    a.bonus_out[b] = bad ? -1 : t;
+                }
+            }
+            if (lane == 0) {
+                s_bad = bad;
+                s_L = bad ? 0 : L;
+                s_off = off;
+            }
+        } else {
+            const int L = a.len[b];
+            const int p = lane < md ? a.path[(size_t)b * md + lane] : -1;
+            bool bad = !range || L < 0 || L > md || (lane < L && (p < 0 || p >= n));
+            bad = __any_sync(0xffffffffu, bad);
+            if (lane < L && !bad) s_path[lane] = p;
+            if (lane == 0) {
+                s_bad = bad;
+                s_L = bad ? 0 : L;
+                s_off = off;
+            }
         }
     }
     __syncthreads();
@@ -81,8 +110,9 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
     }
     const int L = s_L, off = s_off;
 
-    // round trip 2: root-path check and the path's factor rows
-    if (tid < 32) {
+    // round trip 2: root-path check (a walked path is one by construction) and the
+    // path's factor rows
+    if (!FUSED && tid < 32) {
         bool bad = false;
         if (lane < L) {
             const int par = a.parent[off + s_path[lane]];
@@ -135,25 +165,33 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
     }
 }
 
-template <typename E, bool DIAG>
+template <typename E, bool DIAG, bool FUSED>
 cudaError_t launch_typed(const CommitArgs &a, cudaStream_t s) {
     const int rpc = rows_per_cta(a.dk, a.dv);
     dim3 grid((unsigned)(a.B * a.H), (unsigned)((a.dk + rpc - 1) / rpc));
     size_t smem = (size_t)a.max_depth * a.dv * sizeof(float);
     static const cudaError_t attr = cudaFuncSetAttribute(
-        commit_kernel<E, DIAG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        commit_kernel<E, DIAG, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         kMaxDepth * kMaxDim * (int)sizeof(float));
     if (attr != cudaSuccess) return attr;
-    return launch_pdl(commit_kernel<E, DIAG>, grid, dim3(kThreads), smem, s, a);
+    return launch_pdl(commit_kernel<E, DIAG, FUSED>, grid, dim3(kThreads), smem, s, a);
+}
+
+template <bool FUSED>
+cudaError_t launch_any(const CommitArgs &a, cudaStream_t s) {
+    const bool diag = a.decay == TV_DECAY_DIAG;
+    if (a.qkv_dtype == TV_BF16)
+        return diag ? launch_typed<__nv_bfloat16, true, FUSED>(a, s)
+                    : launch_typed<__nv_bfloat16, false, FUSED>(a, s);
+    return diag ? launch_typed<float, true, FUSED>(a, s) : launch_typed<float, false, FUSED>(a, s);
 }
 
 }  // namespace
 
-cudaError_t launch_commit(const CommitArgs &a, cudaStream_t s) {
-    const bool diag = a.decay == TV_DECAY_DIAG;
-    if (a.qkv_dtype == TV_BF16)
-        return diag ? launch_typed<__nv_bfloat16, true>(a, s) : launch_typed<__nv_bfloat16, false>(a, s);
-    return diag ? launch_typed<float, true>(a, s) : launch_typed<float, false>(a, s);
+cudaError_t launch_commit(const CommitArgs &a, cudaStream_t s) { return launch_any<false>(a, s); }
+
+cudaError_t launch_accept_commit(const CommitArgs &a, cudaStream_t s) {
+    return launch_any<true>(a, s);
 }
 
 }  // namespace tv

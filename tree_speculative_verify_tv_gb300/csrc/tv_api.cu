@@ -140,8 +140,40 @@ tv_status tv_commit(const tv_problem *p, const float *H0, const float *g, const 
     }
     tv::CommitArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
                      p->decay, p->qkv_dtype, p->node_offsets, p->parent, H0, g, k, v, path,
-                     accept_len, H_new, dev_status};
+                     accept_len, H_new, dev_status, nullptr, nullptr, nullptr,
+                     nullptr, nullptr, nullptr};
     cudaError_t e = tv::launch_commit(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+tv_status tv_accept_commit(const tv_problem *p, const float *H0, const float *g, const void *k,
+                           const void *v, const int32_t *draft_tokens,
+                           const int32_t *target_argmax, const int32_t *root_argmax,
+                           int32_t *accept_len, int32_t *path, int32_t *bonus, float *H_new,
+                           int32_t *dev_status, void *stream) {
+    tv_status st = check_dims(p);
+    if (st != TV_OK) return st;
+    if (!dev_status || !H0 || !H_new || !path || !accept_len || !bonus || !root_argmax)
+        return TV_ERR_NULL;
+    if (p->total_nodes > 0 && (!g || !k || !v || !draft_tokens || !target_argmax))
+        return TV_ERR_NULL;
+    if (p->B == 0) return TV_OK;
+    const size_t bytes = (size_t)p->B * p->H * p->dk * p->dv * sizeof(float);
+    const char *h0 = reinterpret_cast<const char *>(H0);
+    const char *hn = reinterpret_cast<const char *>(H_new);
+    if (hn != h0 && hn < h0 + bytes && h0 < hn + bytes) return TV_ERR_SHAPE;
+    st = check_ptrs({H0, H_new, path, accept_len, bonus, root_argmax, p->node_offsets,
+                     dev_status});
+    if (st != TV_OK) return st;
+    if (p->total_nodes > 0) {
+        st = check_ptrs({g, k, v, p->parent, draft_tokens, target_argmax});
+        if (st != TV_OK) return st;
+    }
+    tv::CommitArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
+                     p->decay, p->qkv_dtype, p->node_offsets, p->parent, H0, g, k, v, nullptr,
+                     nullptr, H_new, dev_status, draft_tokens, target_argmax, root_argmax,
+                     path, accept_len, bonus};
+    cudaError_t e = tv::launch_accept_commit(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 

@@ -35,9 +35,12 @@ struct CommitArgs {
     const int32_t *node_offsets, *parent;
     const float *H0, *g;
     const void *k, *v;
-    const int32_t *path, *len;
+    const int32_t *path, *len;  // accepted paths (tv_commit)
     float *H_new;
     int32_t *status;
+    // tv_accept_commit: the walk's inputs and its outputs
+    const int32_t *draft, *target, *root;
+    int32_t *path_out, *len_out, *bonus_out;
 };
 
 cudaError_t launch_verify_simt(const VerifyArgs &a, cudaStream_t s);
@@ -46,6 +49,7 @@ cudaError_t launch_verify_tc(const VerifyArgs &a, cudaStream_t s);
 bool verify_tc_supported(const VerifyArgs &a);
 cudaError_t launch_accept(const AcceptArgs &a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs &a, cudaStream_t s);
+cudaError_t launch_accept_commit(const CommitArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------- device helpers
 
