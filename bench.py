@@ -1,8 +1,14 @@
-"""Benchmark of the tree-verification hot path on GB300: one step = tv_verify +
-tv_accept_commit (greedy acceptance and path commit in one launch) over one
-batch of the Mamba-2-like workload
-(B=16 requests, H=24 heads, dk=128, dv=64, 16-node top-4 draft trees, bf16
-q/k/v, fp32 states, scalar decay).
+"""Benchmark of the tree-verification hot path on GB300 over one batch of the
+Mamba-2-like workload (B=16 requests, H=24 heads, dk=128, dv=64, 16-node top-4
+draft trees, bf16 q/k/v, fp32 states, scalar decay).  One step verifies the
+tree, runs the greedy acceptance walk and commits the accepted path:
+
+  --pipeline fused (default): tv_commit_verify (the previous step's accepted
+      paths applied to the state in place, then the tree verified against it)
+      + tv_accept_greedy.  In steady state every step does one commit, one
+      verification and one walk; the state stays resident and is streamed once.
+  --pipeline separate: tv_verify + tv_accept_commit (walk and commit in one
+      launch), the state streamed by both kernels.
 
 Prints one JSON line (rank 0).  Metric: tree-verify node-head updates per
 second (node-heads = nodes x heads per batch), whole job.
@@ -47,8 +53,11 @@ WORKLOADS = {
 }
 WORKLOAD = WORKLOADS[2]
 KERNEL_SOURCES = ["tree_speculative_verify_tv_gb300/csrc/verify_tc.cu",
+                  "tree_speculative_verify_tv_gb300/csrc/verify_tc_stream.cu",
+                  "tree_speculative_verify_tv_gb300/csrc/tc_common.cuh",
                   "tree_speculative_verify_tv_gb300/csrc/tc_ptx.cuh",
                   "tree_speculative_verify_tv_gb300/csrc/tv_internal.cuh"]
+KERNEL_NAMES = {1: "simt", 2: "tcgen05 one unit per CTA", 3: "tcgen05 streaming"}
 
 
 DEFAULT_STEPS = {1: 40000, 2: 40000, 3: 5000, 4: 400, 5: 40}
@@ -69,6 +78,12 @@ def parse():
     ap.add_argument("--fold", type=int, default=32,
                     help="also time one verify launch over this many config-2 layers folded "
                          "into the head axis (0 = skip)")
+    ap.add_argument("--profile-folded", type=int, default=None, metavar="VARIANT",
+                    help="profiling aid: only run 3 verify launches of this tv_variant over "
+                         "--fold config-2 layers folded into the head axis, then exit")
+    ap.add_argument("--pipeline", default="fused", choices=["fused", "separate"],
+                    help="step as tv_commit_verify + tv_accept_greedy (fused) or as "
+                         "tv_verify + tv_accept_commit (separate)")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
                     help="workload (default 2: the configuration the HBM target is quoted on)")
     args = ap.parse_args()
@@ -100,6 +115,19 @@ def verify_bytes_of(d) -> int:
     return d.B * d.H * 4 * d.dk * d.dv + d.T * d.H * per_node_head + 8 * d.T + 4 * (d.B + 1)
 
 
+def commit_verify_bytes(b, lens) -> int:
+    """Algorithmic HBM bytes of one tv_commit_verify launch: those of tv_verify, the
+    committed state rows written back (requests with a non-empty path), and the
+    path's factor rows, offsets, lengths and paths."""
+    qk = 2 if b.qkv_dtype == "bf16" else 4
+    g = 4 if b.decay == "scalar" else 4 * b.dk
+    lens = np.asarray(lens)
+    written = int(np.count_nonzero(lens)) * b.H * 4 * b.dk * b.dv
+    L = int(np.sum(lens))
+    return (verify_bytes(b) + written + L * b.H * (b.dk * qk + b.dv * qk + g) + 4 * L
+            + 4 * (b.B + 1) + 4 * b.B + 4 * b.B * b.max_depth)
+
+
 def commit_bytes(b, lens) -> int:
     """H0 read + H_new written, plus the accepted path's factor rows."""
     qk = 2 if b.qkv_dtype == "bf16" else 4
@@ -117,10 +145,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """Per-launch DRAM bytes of the verify kernel from the committed ncu summary,
-    valid only while the kernel sources are unchanged since the capture."""
-    fp = os.path.join(ROOT, "profiles", "verify_c2_dram_traffic.txt")
+def recorded_traffic(name: str):
+    """Per-launch DRAM bytes of a kernel on the config-2 workload from the committed
+    ncu summary profiles/<name>_c2_dram_traffic.txt, valid only while the kernel
+    sources are unchanged since the capture."""
+    fp = os.path.join(ROOT, "profiles", "%s_c2_dram_traffic.txt" % name)
     if not os.path.exists(fp):
         return None
     vals = {}
@@ -365,14 +394,26 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(device=dev)
     node_heads = base.T * base.H
 
-    def step(d):
+    fused = args.pipeline == "fused"
+
+    def step_fused(d):
+        # one pass of the hot path: the commit of this set's previous accepted paths
+        # and the verification in one launch, then the greedy walk (its paths are the
+        # commit pending for the set's next step; the state stays resident in d.H0)
+        d.commit_verify(d, stream=stream)
+        d.accept(stream=stream)
+
+    def step_separate(d):
         # one pass of the hot path: verify, then greedy accept + commit in one launch
         d.verify(stream=stream, variant=args.variant)
         d.accept_commit(stream=stream)
 
+    step = step_fused if fused else step_separate
+
     with torch.cuda.stream(stream):
         for d in dbs:
             d.status.zero_()
+            d.accept(stream=stream)  # the first pending commit of every set
         for w in range(args.warmup):
             step(dbs[w % R])
     stream.synchronize()
@@ -394,6 +435,10 @@ def run_ours(args, world, rank, local):
             d = dbs[i % R]
             if kind == "step":
                 return lambda d=d: step(d)
+            if kind == "step_separate":
+                return lambda d=d: step_separate(d)
+            if kind == "commit_verify":
+                return lambda d=d: d.commit_verify(d, stream=stream)
             if kind == "verify":
                 return lambda d=d: d.verify(stream=stream, variant=args.variant)
             if kind == "accept":
@@ -443,6 +488,8 @@ def run_ours(args, world, rank, local):
     t_accept, _, _ = timed("accept", K)
     t_commit, _, _ = timed("commit", K)
     t_acom, _, _ = timed("accept_commit", K)
+    t_cv, _, _ = timed("commit_verify", K)
+    t_sep = timed("step_separate", K)[0] if fused else t_step
     sampler.stop()
     for d in dbs:
         st = int(d.status[0].item())
@@ -455,60 +502,73 @@ def run_ours(args, world, rank, local):
     ms_per_step = t_step_max / K * 1e3
 
     # ---------------- end to end through the binding with pinned host buffers
-    e2e = run_e2e(args, sets[0], dev, stream, tv, world)
+    e2e = run_e2e(args, sets[0], dev, stream, tv, world, fused)
 
     # ---------------- one verify launch over `fold` layers folded into the head axis
-    folded = None
+    folded = {}
     if cfg == 2 and args.fold > 1 and rank == 0:
         fb = workloads.config2(seed=77, H=base.H * args.fold)
         fd = tv.DeviceBatch(fb, device=dev)
         del fb
-        with torch.cuda.stream(stream):
-            fd.status.zero_()
-            for _ in range(3):
-                fd.verify(stream=stream, variant=args.variant)
-        stream.synchronize()
-        KF = max(10, min(200, K // 100))
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for _ in range(KF):
-                fd.verify(stream=stream, variant=args.variant)
-        with torch.cuda.stream(stream):
-            g.replay()
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-        e1.synchronize()
-        if int(fd.status[0].item()) != 0:
-            raise SystemExit("device status %d in folded run" % int(fd.status[0].item()))
         fb_bytes = verify_bytes_of(fd)
-        t_f = e0.elapsed_time(e1) * 1e-3 / KF
-        folded = {"layers": args.fold, "H": fd.H, "launches": KF,
-                  "bytes_per_launch": fb_bytes, "launch_us": t_f * 1e6,
-                  "node_heads_per_s": fd.T * fd.H / t_f,
-                  "gbs": fb_bytes / t_f / 1e9}
-        del fd, g
+        auto_variant = fd.variant()
+        for name, var in (("auto", args.variant), ("one_unit_kernel", 2)):
+            with torch.cuda.stream(stream):
+                fd.status.zero_()
+                for _ in range(3):
+                    fd.verify(stream=stream, variant=var)
+            stream.synchronize()
+            KF = max(10, min(200, K // 100))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(KF):
+                    fd.verify(stream=stream, variant=var)
+            with torch.cuda.stream(stream):
+                g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            e1.synchronize()
+            if int(fd.status[0].item()) != 0:
+                raise SystemExit("device status %d in folded run" % int(fd.status[0].item()))
+            t_f = e0.elapsed_time(e1) * 1e-3 / KF
+            used = var if var else auto_variant
+            folded[name] = {"layers": args.fold, "H": fd.H, "launches": KF,
+                            "kernel": KERNEL_NAMES.get(used, str(used)),
+                            "bytes_per_launch": fb_bytes, "launch_us": t_f * 1e6,
+                            "node_heads_per_s": fd.T * fd.H / t_f,
+                            "gbs": fb_bytes / t_f / 1e9}
+            del g
+        del fd
         torch.cuda.empty_cache()
 
-    # ---------------- roofline of the dominant kernel (verify)
+    # ---------------- roofline of the dominant kernel of the step
     peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
     vb = verify_bytes(base)
     v_launch = t_verify / K
-    achieved = vb / v_launch / 1e9
-    peak = float(peaks.get("hbm_gbs", 6800.0))
     lens = [int(x) for x in dbs[0].accept_len[:base.B].cpu().numpy()]
     cb = commit_bytes(base, lens)
+    cvb = commit_verify_bytes(base, lens)
+    cv_launch = t_cv / K
     used_variant = args.variant if args.variant else dbs[0].variant()
-    # the recorded capture is of the tensor-core kernel on the config-2 workload
-    traffic = recorded_traffic() if (cfg == 2 and used_variant == 2) else None
+    # the recorded captures are of the tensor-core kernels on the config-2 workload
+    tc2 = cfg == 2 and used_variant == 2
+    if fused:
+        dom_bytes, dom_t, dom_name = cvb, cv_launch, "tv_commit_verify"
+        traffic = recorded_traffic("commit_verify") if tc2 else None
+    else:
+        dom_bytes, dom_t, dom_name = vb, v_launch, "tv_verify"
+        traffic = recorded_traffic("verify") if tc2 else None
+    achieved = dom_bytes / dom_t / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "tv_verify", "bytes_per_launch": vb,
-                "launch_us": v_launch * 1e6, "peak_kind": "%s (hbm_gbs burst copy)" % peak_kind}
+                "kernel": dom_name, "bytes_per_launch": dom_bytes,
+                "launch_us": dom_t * 1e6, "peak_kind": "%s (hbm_gbs burst copy)" % peak_kind}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -528,7 +588,10 @@ def run_ours(args, world, rank, local):
             "config": {"workload": WORKLOADS[cfg], "B": base.B, "H": base.H, "dk": base.dk,
                        "dv": base.dv, "max_nodes": base.max_nodes,
                        "node_heads_per_step": node_heads,
-                       "verify_kernel": "tcgen05" if used_variant == 2 else "simt",
+                       "verify_kernel": KERNEL_NAMES.get(used_variant, str(used_variant)),
+                       "pipeline": ("tv_commit_verify + tv_accept_greedy; state resident in "
+                                    "HBM, updated in place" if fused else
+                                    "tv_verify + tv_accept_commit"),
                        "inputs": "bf16 q/k/v, fp32 g/H0/out/H_new",
                        "l2": "inputs larger than L2: %d input sets rotated, %.0f MB touched per "
                              "cycle vs %.0f MB L2" % (R, R * per_set / 1e6, l2 / 1e6),
@@ -540,13 +603,19 @@ def run_ours(args, world, rank, local):
             "gpu_launches": 2 * K,
             "clocks": clocks,
             "kernels_us": {"verify": t_verify / K * 1e6, "accept_commit": t_acom / K * 1e6,
+                           "commit_verify": t_cv / K * 1e6,
                            "accept (separate call)": t_accept / K * 1e6,
                            "commit (separate call)": t_commit / K * 1e6},
-            "step_kernels": ["tv_verify", "tv_accept_commit"],
+            "step_kernels": (["tv_commit_verify", "tv_accept_greedy"] if fused
+                             else ["tv_verify", "tv_accept_commit"]),
+            "step_us": {"fused": t_step / K * 1e6 if fused else None,
+                        "separate": t_sep / K * 1e6},
             "verify_only": {"value": node_heads / v_launch, "unit": UNIT,
-                            "gbs": achieved},
-            "verify_folded_layers": (dict(folded, frac=folded["gbs"] / peak) if folded
-                                     else None),
+                            "gbs": vb / v_launch / 1e9, "bytes_per_launch": vb,
+                            "frac": vb / v_launch / 1e9 / peak,
+                            "traffic": recorded_traffic("verify") if tc2 else None},
+            "verify_folded_layers": ({k: dict(v, frac=v["gbs"] / peak)
+                                      for k, v in folded.items()} if folded else None),
             "commit_gbs": cb / (t_commit / K) / 1e9,
             "transient_bytes": {"library_workspace": 0,
                                 "factors": int(base.T * base.H * (
@@ -558,15 +627,21 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, host_batch, dev, stream, tv, world):
+def run_e2e(args, host_batch, dev, stream, tv, world, fused):
     """The step through the binding with host buffers: pinned host -> device copies
-    of the step's inputs, the three calls, device -> pinned host copies of its results."""
+    of the step's inputs, the calls, device -> pinned host copies of its results.
+    Fused pipeline: the state is resident on the device (tv_commit_verify updates it
+    in place), so the inputs are the tree, factors and tokens and the results the
+    outputs and acceptance; separate pipeline: the state is copied in and H_new out."""
     import torch
     hb = tv.DeviceBatch(host_batch, pin=True)
     db = tv.DeviceBatch(host_batch, device=dev)
-    ins = ["node_offsets", "parent", "depth", "q", "k", "v", "g", "H0", "draft", "target",
+    ins = ["node_offsets", "parent", "depth", "q", "k", "v", "g", "draft", "target",
            "root_argmax"]
-    outs = ["out", "H_new", "accept_len", "path", "bonus", "status"]
+    outs = ["out", "accept_len", "path", "bonus", "status"]
+    if not fused:
+        ins.append("H0")
+        outs.append("H_new")
     h2d = sum(getattr(hb, n).numel() * getattr(hb, n).element_size() for n in ins)
     d2h = sum(getattr(db, n).numel() * getattr(db, n).element_size() for n in outs)
     # about 2 GB of host<->device traffic at most (at least 3 steps)
@@ -576,12 +651,17 @@ def run_e2e(args, host_batch, dev, stream, tv, world):
         for n in ins:
             getattr(db, n).copy_(getattr(hb, n), non_blocking=True)
         db.status.zero_()
-        db.verify(stream=stream, variant=args.variant)
-        db.accept_commit(stream=stream)
+        if fused:
+            db.commit_verify(db, stream=stream)
+            db.accept(stream=stream)
+        else:
+            db.verify(stream=stream, variant=args.variant)
+            db.accept_commit(stream=stream)
         for n in outs:
             getattr(hb, n).copy_(getattr(db, n), non_blocking=True)
 
     with torch.cuda.stream(stream):
+        db.accept(stream=stream)  # the first pending commit
         for _ in range(5):
             one()
         stream.synchronize()
@@ -598,11 +678,33 @@ def run_e2e(args, host_batch, dev, stream, tv, world):
         raise SystemExit("device status %d in e2e" % int(hb.status[0]))
     nh = sum_over_ranks(host_batch.T * host_batch.H * K, world)
     return {"value": nh / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": dt / K * 1e3}
+            "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": dt / K * 1e3,
+            "state": "resident in HBM" if fused else "copied in and out every step"}
+
+
+def profile_folded(args):
+    """Three verify launches over `--fold` folded config-2 layers (for ncu captures)."""
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    import workloads
+    tv.build()
+    tv.load()
+    fd = tv.DeviceBatch(workloads.config2(seed=77, H=24 * args.fold))
+    fd.status.zero_()
+    for _ in range(3):
+        fd.verify(variant=args.profile_folded)
+    torch.cuda.synchronize()
+    st = int(fd.status[0].item())
+    print(json.dumps({"profile_folded": args.profile_folded, "layers": args.fold, "status": st}))
+    if st != 0:
+        raise SystemExit("device status %d" % st)
 
 
 def main():
     args = parse()
+    if args.profile_folded is not None:
+        profile_folded(args)
+        return
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -81,8 +81,13 @@ typedef enum tv_dtype {
 typedef enum tv_variant {
     TV_VARIANT_AUTO = 0,    /* tensor-core kernel where it applies, else SIMT */
     TV_VARIANT_SIMT = 1,    /* CUDA-core kernel, every supported shape */
-    TV_VARIANT_TC = 2       /* tcgen05 tensor-core kernel: bf16 q/k/v, dk in {64,128},
-                               dv in {64,128}; TV_ERR_UNSUPPORTED otherwise */
+    TV_VARIANT_TC = 2,      /* tcgen05 tensor-core kernel, one (request, head) per CTA:
+                               bf16 q/k/v, dk in {64,128}, dv in {64,128};
+                               TV_ERR_UNSUPPORTED otherwise */
+    TV_VARIANT_TC_STREAM = 3 /* persistent tcgen05 kernel streaming many (request, head)
+                               units per CTA through double-buffered shared memory:
+                               as TV_VARIANT_TC but scalar decay only, and only where two
+                               units' operands fit one CTA's shared memory */
 } tv_variant;
 
 /*
@@ -208,11 +213,60 @@ tv_status tv_accept_commit(const tv_problem *p, const float *H0, const float *g,
                            int32_t *dev_status, void *stream);
 
 /*
+ * tv_pending -- a commit that has not been applied yet: the accepted paths of
+ * the previous step and that step's tree and factors.  B, H, dk, dv, decay and
+ * qkv_dtype are those of the tv_problem it is passed with; the other sizes and
+ * all arrays are the previous step's (they may be the current step's buffers).
+ *
+ *   total_nodes, max_nodes, max_depth   sizes of the previous step's batch
+ *   node_offsets [B+1], parent [T']     its packed tree (local parents)
+ *   g, k, v      its factors, layouts as in tv_verify
+ *   path [B][max_depth], accept_len [B] its accepted paths (tv_accept_greedy)
+ */
+typedef struct tv_pending {
+    int32_t total_nodes;
+    int32_t max_nodes;
+    int32_t max_depth;
+    const int32_t *node_offsets;
+    const int32_t *parent;
+    const float *g;
+    const void *k;
+    const void *v;
+    const int32_t *path;
+    const int32_t *accept_len;
+} tv_pending;
+
+/*
+ * tv_commit_verify -- apply the pending commit to the state in place, then
+ * verify the current tree against the updated state.
+ * Same results as tv_commit(pending's problem, H, ..., H_new = H) followed by
+ * tv_verify(p, H, ...): the commit is the restore of the accepted path's state
+ * from its factors (Bole summary page, "Core techniques" §2) and the
+ * verification is the tree closed form (§1).  The state is the only operand
+ * both steps stream, so for scalar decay with bf16 q/k/v and dk, dv in
+ * {64, 128} one kernel reads H once, writes the updated rows back and feeds
+ * them to the context term; other shapes run the two kernels in sequence.
+ *
+ *   p, q, k, v, g, out   the current step, as in tv_verify
+ *   pend       the previous step's accepted paths and factors; NULL for none
+ *              (then this is tv_verify with H0 = H)
+ *   H          [B][H][dk][dv] fp32, read and written (the committed state)
+ * Device-detected errors: a malformed pending path (as in tv_commit) gives
+ * TV_ERR_TREE and leaves that request's state untouched, and its outputs are
+ * computed from the untouched state; a malformed current tree is handled as in
+ * tv_verify.  Requests without current nodes still get their pending commit.
+ */
+tv_status tv_commit_verify(const tv_problem *p, const tv_pending *pend, float *H, const void *q,
+                           const void *k, const void *v, const float *g, float *out,
+                           int32_t *dev_status, void *stream);
+
+/*
  * tv_verify_variant -- the kernel tv_verify (TV_VARIANT_AUTO) would launch for
- * this problem: TV_VARIANT_TC or TV_VARIANT_SIMT.  Reads only the sizes and
- * kinds in *p (no device memory); returns the negative tv_status of an invalid
- * problem (e.g. -TV_ERR_SHAPE).  The tensor-core kernel takes bf16 q/k/v with
- * dk, dv in {64, 128} when its shared-memory plan for max_nodes fits one CTA.
+ * this problem: TV_VARIANT_TC_STREAM, TV_VARIANT_TC or TV_VARIANT_SIMT.  Reads
+ * only the sizes and kinds in *p (no device memory; the current device's SM count
+ * and shared memory); returns the negative tv_status of an invalid problem (e.g.
+ * -TV_ERR_SHAPE).  The tensor-core kernels take bf16 q/k/v with dk, dv in
+ * {64, 128} when their shared-memory plan for max_nodes fits one CTA.
  */
 int32_t tv_verify_variant(const tv_problem *p);
 

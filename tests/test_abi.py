@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert {"tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
-            "tv_accept_commit", "tv_status_string", "tv_version"} <= set(names)
+            "tv_accept_commit", "tv_commit_verify", "tv_status_string", "tv_version"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -164,6 +164,42 @@ def test_accept_commit_rejects_bad_arguments(lib):
     assert rc(Hn=P[3] + 16) == tv.TV_ERR_SHAPE
     assert rc(root=P[15] + 4) == tv.TV_ERR_ALIGN
     assert rc(prob(B=0, total_nodes=0)) == tv.TV_OK
+
+
+def pend(**kw):
+    d = dict(total_nodes=5, max_nodes=4, max_depth=3, node_offsets=P[0], parent=P[1], g=P[7],
+             k=P[5], v=P[6], path=P[10], accept_len=P[11])
+    d.update(kw)
+    return tv.make_pending(**d)
+
+
+def test_commit_verify_rejects_bad_arguments(lib):
+    def rc(p=None, pe="default", **kw):
+        a = dict(H=P[3], q=P[4], k=P[5], v=P[6], g=P[7], out=P[8], st=P[9])
+        a.update(kw)
+        pe = pend() if pe == "default" else pe
+        return tv.tv_commit_verify(p or prob(), pe, a["H"], a["q"], a["k"], a["v"], a["g"],
+                                   a["out"], a["st"], stream=0, check=False)
+    assert rc(prob(dk=12)) == tv.TV_ERR_SHAPE
+    assert rc(prob(depth=None)) == tv.TV_ERR_NULL
+    assert rc(H=None) == tv.TV_ERR_NULL
+    assert rc(st=None) == tv.TV_ERR_NULL
+    assert rc(q=None) == tv.TV_ERR_NULL
+    assert rc(pe=pend(path=None)) == tv.TV_ERR_NULL
+    assert rc(pe=pend(accept_len=None)) == tv.TV_ERR_NULL
+    assert rc(pe=pend(k=None)) == tv.TV_ERR_NULL
+    assert rc(pe=pend(max_depth=0)) == tv.TV_ERR_SHAPE
+    assert rc(pe=pend(max_depth=33)) == tv.TV_ERR_UNSUPPORTED
+    assert rc(pe=pend(max_nodes=300)) == tv.TV_ERR_UNSUPPORTED
+    assert rc(pe=pend(total_nodes=9)) == tv.TV_ERR_SHAPE
+    assert rc(pe=pend(path=P[10] + 4)) == tv.TV_ERR_ALIGN
+    assert rc(pe=pend(v=P[6] + 8)) == tv.TV_ERR_ALIGN
+    assert rc(H=P[3] + 4) == tv.TV_ERR_ALIGN
+    assert rc(g=P[7] + 8) == tv.TV_ERR_ALIGN
+    assert rc(prob(B=0, total_nodes=0), pe=pend(total_nodes=0)) == tv.TV_OK
+    # without a pending commit the call is tv_verify and checks like it
+    assert rc(pe=None, q=None) == tv.TV_ERR_NULL
+    assert rc(prob(dv=0), pe=None) == tv.TV_ERR_SHAPE
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -32,7 +32,7 @@ def _tc_supported(batch):
     p = tv.make_problem(batch.B, batch.H, batch.dk, batch.dv, batch.T, batch.max_nodes,
                         batch.max_depth, tv.TV_DECAY_DIAG if batch.decay == "diag" else 0,
                         tv.TV_BF16 if batch.qkv_dtype == "bf16" else tv.TV_F32, 16, 16, 16)
-    return tv.tv_verify_variant(p) == tv.TV_VARIANT_TC
+    return tv.tv_verify_variant(p) in (tv.TV_VARIANT_TC, tv.TV_VARIANT_TC_STREAM)
 
 
 def _full_check(batch, variant="auto", units=None):

@@ -23,11 +23,11 @@ TV_OK, TV_ERR_NULL, TV_ERR_SHAPE, TV_ERR_DTYPE, TV_ERR_ALIGN = 0, 1, 2, 3, 4
 TV_ERR_UNSUPPORTED, TV_ERR_TREE, TV_ERR_CUDA, TV_ERR_TIMEOUT = 5, 6, 7, 8
 TV_DECAY_SCALAR, TV_DECAY_DIAG = 0, 1
 TV_BF16, TV_F32 = 0, 1
-TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC = 0, 1, 2
+TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC, TV_VARIANT_TC_STREAM = 0, 1, 2, 3
 TV_MAX_NODES, TV_MAX_DEPTH, TV_MAX_DIM = 256, 32, 256
 
 EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
-            "tv_accept_commit", "tv_status_string", "tv_version")
+            "tv_accept_commit", "tv_commit_verify", "tv_status_string", "tv_version")
 
 
 class tv_problem(ctypes.Structure):
@@ -37,6 +37,14 @@ class tv_problem(ctypes.Structure):
                 ("decay", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32),
                 ("node_offsets", ctypes.c_void_p), ("parent", ctypes.c_void_p),
                 ("depth", ctypes.c_void_p)]
+
+
+class tv_pending(ctypes.Structure):
+    _fields_ = [("total_nodes", ctypes.c_int32), ("max_nodes", ctypes.c_int32),
+                ("max_depth", ctypes.c_int32), ("node_offsets", ctypes.c_void_p),
+                ("parent", ctypes.c_void_p), ("g", ctypes.c_void_p), ("k", ctypes.c_void_p),
+                ("v", ctypes.c_void_p), ("path", ctypes.c_void_p),
+                ("accept_len", ctypes.c_void_p)]
 
 
 class TVError(RuntimeError):
@@ -67,8 +75,10 @@ def load(path: Optional[str] = None):
         L.tv_accept_greedy.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.tv_commit.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.tv_accept_commit.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.tv_commit_verify.argtypes = [P, ctypes.POINTER(tv_pending), vp, vp, vp, vp, vp, vp, vp,
+                                       vp]
         for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit,
-                  L.tv_accept_commit):
+                  L.tv_accept_commit, L.tv_commit_verify):
             f.restype = ctypes.c_int32
         L.tv_status_string.argtypes = [i32]
         L.tv_status_string.restype = ctypes.c_char_p
@@ -162,6 +172,21 @@ def tv_accept_commit(problem: tv_problem, H0, g, k, v, draft_tokens, target_argm
     return _check(rc, "tv_accept_commit", check)
 
 
+def make_pending(total_nodes, max_nodes, max_depth, node_offsets, parent, g, k, v, path,
+                 accept_len) -> tv_pending:
+    """tv_pending from sizes and device arrays; keeps no reference to tensors."""
+    return tv_pending(int(total_nodes), int(max_nodes), int(max_depth), _ptr(node_offsets),
+                      _ptr(parent), _ptr(g), _ptr(k), _ptr(v), _ptr(path), _ptr(accept_len))
+
+
+def tv_commit_verify(problem: tv_problem, pending: Optional[tv_pending], H, q, k, v, g, out,
+                     dev_status, stream=None, check: bool = True) -> int:
+    pp = ctypes.byref(pending) if pending is not None else None
+    rc = load().tv_commit_verify(ctypes.byref(problem), pp, _ptr(H), _ptr(q), _ptr(k), _ptr(v),
+                                 _ptr(g), _ptr(out), _ptr(dev_status), _stream(stream))
+    return _check(rc, "tv_commit_verify", check)
+
+
 # ---------------------------------------------------------------- device batches
 
 
@@ -237,6 +262,18 @@ class DeviceBatch:
         return tv_accept_commit(self.problem(), self.H0, self.g, self.k, self.v, self.draft,
                                 self.target, self.root_argmax, self.accept_len, self.path,
                                 self.bonus, dst, self.status, stream, check)
+
+    def pending(self) -> tv_pending:
+        """This batch's accepted paths and factors as the commit still to apply."""
+        return make_pending(self.T, self.max_nodes, self.max_depth, self.node_offsets,
+                            self.parent, self.g, self.k, self.v, self.path, self.accept_len)
+
+    def commit_verify(self, pending: "Optional[DeviceBatch]", stream=None, check=True):
+        """Apply `pending`'s accepted paths to this batch's state H0 in place, then
+        verify this batch's tree against the updated state."""
+        pend = pending.pending() if pending is not None else None
+        return tv_commit_verify(self.problem(), pend, self.H0, self.q, self.k, self.v, self.g,
+                                self.out, self.status, stream, check)
 
     def commit(self, stream=None, in_place=False, check=True):
         dst = self.H0 if in_place else self.H_new

@@ -1,0 +1,117 @@
+// tc_common.cuh -- pieces shared by the tcgen05 verify kernels: the bf16 hi/lo
+// split of fp32 state values, the 128-byte-swizzled operand layout, named
+// barriers, and host helpers for tensor maps and tensor-memory sizing.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tc_ptx.cuh"
+#include "tv_internal.cuh"
+
+namespace tv {
+namespace tcc {
+
+constexpr long long kWaitLimit = 2000000000LL;  // ~1 s at 2 GHz
+
+__host__ __device__ constexpr uint32_t align_up(uint32_t x, uint32_t a) {
+    return (x + a - 1) / a * a;
+}
+
+constexpr int kChunkRows = 32;  // H0 key rows per streamed chunk
+constexpr int kMaxChunks = 4;   // dk <= 128
+
+__device__ __forceinline__ void load_bf16x(const __nv_bfloat16 *p, int cnt, float (&x)[4]) {
+    if (cnt == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+        x[0] = __low2float(p0); x[1] = __high2float(p0);
+        x[2] = __low2float(p1); x[3] = __high2float(p1);
+    } else {
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(p);
+        x[0] = __low2float(p0); x[1] = __high2float(p0);
+        x[2] = x[3] = 0.f;
+    }
+}
+
+// Byte offset of bf16 element (row, c) in a 128-byte-swizzled K-major tile:
+// slab c/64 of `slab_bytes`, row of 128 bytes, 16-byte chunk (c%64)/8 XOR row%8.
+__device__ __forceinline__ uint32_t swz_offset(int row, int c, uint32_t slab_bytes) {
+    const int cc = c % 64;
+    return (c / 64) * slab_bytes + row * 128 + ((((cc / 8) ^ (row & 7)) * 16) + (cc % 8) * 2);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+}
+
+// Split two floats into bf16 hi + lo parts: hi keeps the upper 16 bits (exact
+// truncation), so x - hi is exact in fp32 and only lo is rounded (to nearest):
+// |x - hi - lo| <= 2^-16 |x|.  Returns packed pairs (element 0 in the low half).
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+    const float h0 = __uint_as_float(b0 & 0xFFFF0000u), h1 = __uint_as_float(b1 & 0xFFFF0000u);
+    hi = __byte_perm(b0, b1, 0x7632);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - h0, x1 - h1);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+__device__ __forceinline__ void named_barrier(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Barrier among `count` threads and reduce: true iff `pred` holds in all of them.
+__device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// ---------------------------------------------------------------- host side
+
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+inline int tmem_columns(int npad_max) {
+    int c = 32;
+    while (c < npad_max) c <<= 1;
+    return c;
+}
+
+inline bool encode_rows(CUtensorMap *tm, const void *base, CUtensorMapDataType dt, int esize, int width,
+                        int H, int T, int box_w, CUtensorMapSwizzle swz) {
+    // rows of `width` elements per (node, head): dims (width, H, T), one head per box
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * esize, (cuuint64_t)width * esize * H};
+    const cuuint32_t box[3] = {(cuuint32_t)box_w, 1, 16};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode_fn()(tm, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t kSmemLimit = 227 * 1024;
+
+}  // namespace tcc
+}  // namespace tv

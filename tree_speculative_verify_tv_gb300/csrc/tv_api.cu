@@ -36,6 +36,14 @@ tv_status check_ptrs(std::initializer_list<const void *> ptrs) {
     return TV_OK;
 }
 
+// The kernel TV_VARIANT_AUTO picks: the one-unit tensor-core kernel where it
+// applies (the streaming kernel only when it is the faster one), else SIMT.
+cudaError_t launch_verify_auto(const tv::VerifyArgs &a, cudaStream_t s) {
+    if (tv::verify_tc_stream_preferred(a)) return tv::launch_verify_tc_stream(a, s);
+    if (tv::verify_tc_supported(a)) return tv::launch_verify_tc(a, s);
+    return tv::launch_verify_simt(a, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -63,6 +71,7 @@ int32_t tv_verify_variant(const tv_problem *p) {
     tv::VerifyArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
                      p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
                      nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    if (tv::verify_tc_stream_preferred(a)) return TV_VARIANT_TC_STREAM;
     return tv::verify_tc_supported(a) ? TV_VARIANT_TC : TV_VARIANT_SIMT;
 }
 
@@ -72,7 +81,7 @@ tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, cons
     tv_status st = check_dims(p);
     if (st != TV_OK) return st;
     if (!p->depth && p->total_nodes > 0) return TV_ERR_NULL;
-    if (variant < TV_VARIANT_AUTO || variant > TV_VARIANT_TC) return TV_ERR_DTYPE;
+    if (variant < TV_VARIANT_AUTO || variant > TV_VARIANT_TC_STREAM) return TV_ERR_DTYPE;
     if (!dev_status) return TV_ERR_NULL;
     if (p->B == 0 || p->total_nodes == 0) return TV_OK;
     st = check_ptrs({H0, q, k, v, g, out, p->node_offsets, p->parent, p->depth, dev_status});
@@ -82,10 +91,19 @@ tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, cons
                      p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
                      H0, q, k, v, g, out, dev_status};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool tc_ok = tv::verify_tc_supported(a);
-    if (variant == TV_VARIANT_TC && !tc_ok) return TV_ERR_UNSUPPORTED;
-    const bool use_tc = variant == TV_VARIANT_TC || (variant == TV_VARIANT_AUTO && tc_ok);
-    cudaError_t e = use_tc ? tv::launch_verify_tc(a, s) : tv::launch_verify_simt(a, s);
+    cudaError_t e;
+    switch (variant) {
+        case TV_VARIANT_SIMT: e = tv::launch_verify_simt(a, s); break;
+        case TV_VARIANT_TC:
+            if (!tv::verify_tc_supported(a)) return TV_ERR_UNSUPPORTED;
+            e = tv::launch_verify_tc(a, s);
+            break;
+        case TV_VARIANT_TC_STREAM:
+            if (!tv::verify_tc_stream_supported(a)) return TV_ERR_UNSUPPORTED;
+            e = tv::launch_verify_tc_stream(a, s);
+            break;
+        default: e = launch_verify_auto(a, s);
+    }
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
@@ -174,6 +192,57 @@ tv_status tv_accept_commit(const tv_problem *p, const float *H0, const float *g,
                      nullptr, H_new, dev_status, draft_tokens, target_argmax, root_argmax,
                      path, accept_len, bonus};
     cudaError_t e = tv::launch_accept_commit(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+tv_status tv_commit_verify(const tv_problem *p, const tv_pending *pend, float *H, const void *q,
+                           const void *k, const void *v, const float *g, float *out,
+                           int32_t *dev_status, void *stream) {
+    if (!pend) return tv_verify(p, H, q, k, v, g, out, dev_status, stream);
+    tv_status st = check_dims(p);
+    if (st != TV_OK) return st;
+    if (!p->depth && p->total_nodes > 0) return TV_ERR_NULL;
+    if (!dev_status || !H || !pend->node_offsets || !pend->path || !pend->accept_len)
+        return TV_ERR_NULL;
+    if (pend->total_nodes < 0 || pend->max_nodes < 1 || pend->max_depth < 1) return TV_ERR_SHAPE;
+    if (pend->max_nodes > TV_MAX_NODES || pend->max_depth > TV_MAX_DEPTH)
+        return TV_ERR_UNSUPPORTED;
+    if ((int64_t)pend->total_nodes > (int64_t)p->B * pend->max_nodes) return TV_ERR_SHAPE;
+    if (pend->total_nodes > 0 && (!pend->parent || !pend->g || !pend->k || !pend->v))
+        return TV_ERR_NULL;
+    if (p->total_nodes > 0 && (!q || !k || !v || !g || !out)) return TV_ERR_NULL;
+    if (p->B == 0) return TV_OK;
+    st = check_ptrs({H, dev_status, p->node_offsets, pend->node_offsets, pend->path,
+                     pend->accept_len});
+    if (st != TV_OK) return st;
+    if (pend->total_nodes > 0) {
+        st = check_ptrs({pend->parent, pend->g, pend->k, pend->v});
+        if (st != TV_OK) return st;
+    }
+    if (p->total_nodes > 0) {
+        st = check_ptrs({q, k, v, g, out, p->parent, p->depth});
+        if (st != TV_OK) return st;
+    }
+
+    tv::VerifyArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
+                     p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
+                     H, q, k, v, g, out, dev_status};
+    tv::PendingArgs pa{pend->total_nodes, pend->max_nodes, pend->max_depth, pend->node_offsets,
+                       pend->parent, pend->g, pend->k, pend->v, pend->path, pend->accept_len};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->total_nodes > 0 && tv::commit_verify_tc_supported(a, pa)) {
+        cudaError_t e = tv::launch_commit_verify_tc(a, pa, H, s);
+        return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+    }
+    // other shapes: the commit kernel in place, then the verify kernel
+    tv::CommitArgs c{p->B, p->H, p->dk, p->dv, pend->total_nodes, pend->max_nodes,
+                     pend->max_depth, p->decay, p->qkv_dtype, pend->node_offsets, pend->parent,
+                     H, pend->g, pend->k, pend->v, pend->path, pend->accept_len, H, dev_status,
+                     nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    cudaError_t e = tv::launch_commit(c, s);
+    if (e != cudaSuccess) return TV_ERR_CUDA;
+    if (p->total_nodes == 0) return TV_OK;
+    e = launch_verify_auto(a, s);
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 

@@ -43,10 +43,27 @@ struct CommitArgs {
     int32_t *path_out, *len_out, *bonus_out;
 };
 
+// A commit carried into the next verification (tv_commit_verify).
+struct PendingArgs {
+    int32_t T, max_nodes, max_depth;
+    const int32_t *node_offsets, *parent;
+    const float *g;
+    const void *k, *v;
+    const int32_t *path, *len;
+};
+
 cudaError_t launch_verify_simt(const VerifyArgs &a, cudaStream_t s);
 // Returns cudaErrorNotSupported when the shape is outside the tensor-core kernel.
 cudaError_t launch_verify_tc(const VerifyArgs &a, cudaStream_t s);
 bool verify_tc_supported(const VerifyArgs &a);
+// Persistent tensor-core kernel (scalar decay): many units per CTA, double-buffered.
+bool verify_tc_stream_supported(const VerifyArgs &a);
+bool verify_tc_stream_preferred(const VerifyArgs &a);  // what TV_VARIANT_AUTO picks
+cudaError_t launch_verify_tc_stream(const VerifyArgs &a, cudaStream_t s);
+// One-kernel commit + verify (scalar decay, tensor cores); H is read and written.
+bool commit_verify_tc_supported(const VerifyArgs &a, const PendingArgs &p);
+cudaError_t launch_commit_verify_tc(const VerifyArgs &a, const PendingArgs &p, float *H,
+                                    cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs &a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs &a, cudaStream_t s);
 cudaError_t launch_accept_commit(const CommitArgs &a, cudaStream_t s);

@@ -22,26 +22,13 @@
 //     e^{G_i}, adds sum_j w_ij v_j and stores fp32 rows, 128 bytes per warp.
 // Every wait is bounded (TV_ERR_TIMEOUT); malformed trees zero their rows and
 // set TV_ERR_TREE.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
-#include "tc_ptx.cuh"
-#include "tv_internal.cuh"
+#include "tc_common.cuh"
 
 namespace tv {
 namespace {
+using namespace tcc;
 
 constexpr int kThreads = 256;
-constexpr long long kWaitLimit = 2000000000LL;  // ~1 s at 2 GHz
-
-__host__ __device__ constexpr uint32_t align_up(uint32_t x, uint32_t a) {
-    return (x + a - 1) / a * a;
-}
-
-constexpr int kChunkRows = 32;  // H0 key rows per streamed chunk
-constexpr int kMaxChunks = 4;   // dk <= 128
-
 // Shared-memory plan, identical on host and device.  TMA destinations and
 // 128-byte-swizzled operands are 1024-byte aligned.
 //   A region: H0 streams in as kChunkRows-row fp32 chunks; each chunk is split in
@@ -51,10 +38,14 @@ constexpr int kMaxChunks = 4;   // dk <= 128
 //     written by the warps in the swizzled layout; g arrives as dense fp32 rows and
 //     becomes exp(g) in place.
 //   The lo-part exchange (dv = 64) reuses the A region when it is large enough.
+//   pending commit (pend_depth > 0): the previous step's path factors, k rows
+//     scaled by their suffix decays and v rows, both fp32, plus the path itself.
 struct TcLayout {
     uint32_t a_off, b_off, blo_off, q_off, k_off, v_off, e_off, x_off, w_off, anc_off, eg_off,
-        g_off, par_off, dep_off, poff_off, pnode_off, bar_off, misc_off, total;
-    __host__ __device__ TcLayout(int dk, int dv, int npad_max, int max_depth, bool diag) {
+        g_off, par_off, dep_off, poff_off, pnode_off, bar_off, misc_off, pk_off, pv_off, pg_off,
+        ppath_off, pmisc_off, total;
+    __host__ __device__ TcLayout(int dk, int dv, int npad_max, int max_depth, bool diag,
+                                 int pend_depth = 0) {
         const uint32_t swz_tile = (dk / 64) * npad_max * 128;  // one swizzled [n][dk] bf16 tile
         const uint32_t a_bytes = dk * dv * 4;
         // dv = 64: the epilogue dumps both 64-row halves of D, npad x 128 fp32
@@ -79,7 +70,17 @@ struct TcLayout {
         pnode_off = align_up(poff_off + (npad_max + 1) * 4, 16);  // node of each pair (u8)
         bar_off = align_up(pnode_off + npad_max * max_depth, 16);
         misc_off = bar_off + 8 * 8;
-        total = align_up(misc_off + 16, 16) + 1024;  // + slack for 1024-byte base alignment
+        pk_off = align_up(misc_off + 16, 16);
+        if (pend_depth > 0) {
+            pv_off = pk_off + pend_depth * dk * 4;
+            pg_off = pv_off + pend_depth * dv * 4;
+            ppath_off = pg_off + kMaxDepth * 4;
+            pmisc_off = ppath_off + kMaxDepth * 4;
+            total = align_up(pmisc_off + 32, 16) + 1024;
+        } else {
+            pv_off = pg_off = ppath_off = pmisc_off = pk_off;
+            total = pk_off + 1024;  // + slack for 1024-byte base alignment
+        }
     }
 };
 
@@ -87,44 +88,9 @@ struct TcParams {
     VerifyArgs a;
     int npad_max;
     int tmem_cols;
+    PendingArgs pend;  // commit + verify only
+    float *H_w;        // the state rows written back (commit + verify only)
 };
-
-__device__ __forceinline__ void load_bf16x(const __nv_bfloat16 *p, int cnt, float (&x)[4]) {
-    if (cnt == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(p);
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
-        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
-        x[0] = __low2float(p0); x[1] = __high2float(p0);
-        x[2] = __low2float(p1); x[3] = __high2float(p1);
-    } else {
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(p);
-        x[0] = __low2float(p0); x[1] = __high2float(p0);
-        x[2] = x[3] = 0.f;
-    }
-}
-
-// Byte offset of bf16 element (row, c) in a 128-byte-swizzled K-major tile:
-// slab c/64 of `slab_bytes`, row of 128 bytes, 16-byte chunk (c%64)/8 XOR row%8.
-__device__ __forceinline__ uint32_t swz_offset(int row, int c, uint32_t slab_bytes) {
-    const int cc = c % 64;
-    return (c / 64) * slab_bytes + row * 128 + ((((cc / 8) ^ (row & 7)) * 16) + (cc % 8) * 2);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
-}
-
-// Split two floats into bf16 hi + lo parts: hi keeps the upper 16 bits (exact
-// truncation), so x - hi is exact in fp32 and only lo is rounded (to nearest):
-// |x - hi - lo| <= 2^-16 |x|.  Returns packed pairs (element 0 in the low half).
-__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
-    const float h0 = __uint_as_float(b0 & 0xFFFF0000u), h1 = __uint_as_float(b1 & 0xFFFF0000u);
-    hi = __byte_perm(b0, b1, 0x7632);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - h0, x1 - h1);
-    lo = *reinterpret_cast<const uint32_t *>(&l);
-}
 
 template <int DV, bool DIAG>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -550,10 +516,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) ptx::tmem_dealloc(tmem, P.tmem_cols);
 }
 
-__device__ __forceinline__ void named_barrier(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // Scalar-decay verification, warp-specialized so that independent phases overlap:
 //   warps 0-3 stream H0 in chunks, split each chunk in place into bf16 hi/lo operand
 //     rows as it lands, then issue the context MMA (D = H0^T q) as soon as q has landed;
@@ -562,8 +524,18 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 //     w_{i,d} = e^{G_i - G_{anc_d(i)}} (q_i . k_{anc_d(i)}) and e^{G_i};
 //   all eight warps then form o_i = e^{G_i} D[:, i] + sum_d w_{i,d} v_{anc_d(i)}.
 // Same shared-memory plan, operand layouts and error behaviour as verify_tc_kernel.
-template <int DV>
-__global__ void __launch_bounds__(kThreads, 1)
+//
+// PEND (tv_commit_verify): before the state is split, the previous step's accepted
+// path p_1..p_L is applied to it (Bole summary page, "Core techniques" §2):
+//   H[r][c] <- e^{G_L} H[r][c] + sum_m e^{G_L - G_{p_m}} k_{p_m}[r] v_{p_m}[c],
+// the updated rows are written back to the state in HBM and the context term is
+// formed from them.  The H0 group reads the path and gathers its factor rows while
+// the first chunk is in flight; a request with L = 0 writes nothing.
+// Residency at dv = 64: 45 KB of shared memory per CTA at 16-node trees, so four
+// CTAs fit an SM and registers are capped to match (the launch asks for the whole
+// shared-memory carveout); the pending-commit variant keeps three.
+template <int DV, bool PEND>
+__global__ void __launch_bounds__(kThreads, PEND ? 3 : (DV == 64 ? 4 : 1))
     verify_tc_scalar_ws_kernel(const __grid_constant__ CUtensorMap tm_q,
                                const __grid_constant__ CUtensorMap tm_k,
                                const __grid_constant__ CUtensorMap tm_v, const TcParams P) {
@@ -573,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int dk = a.dk, H = a.H, md = a.max_depth;
-    const TcLayout L(dk, DV, P.npad_max, md, false);
+    const TcLayout L(dk, DV, P.npad_max, md, false, PEND ? P.pend.max_depth : 0);
     const uint32_t slab_bytes = P.npad_max * 128;
     uint8_t *sA = smem + L.a_off;
     uint8_t *sB = smem + L.b_off;
@@ -639,15 +611,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) {
         // ================= H0 group: split chunks as they land, then the MMA
         constexpr int kPer = DV * (kChunkRows / 8) / kGroup;  // (channel, 8-key) items
+        // pending commit: path length pL, e^{G_L} and the path's scaled factor rows
+        int pL = 0;
+        float palpha = 1.f;
+        float *sPK = reinterpret_cast<float *>(smem + L.pk_off);  // [pL][dk] e^{G_L-G_m} k_m
+        float *sPV = reinterpret_cast<float *>(smem + L.pv_off);  // [pL][DV] v_m
+        if constexpr (PEND) {
+            const PendingArgs &pa = P.pend;
+            const int mdp = pa.max_depth;
+            float *sPG = reinterpret_cast<float *>(smem + L.pg_off);
+            int *sPath = reinterpret_cast<int *>(smem + L.ppath_off);
+            // L, bad range/length/entry, offset, not a root path, e^{G_L} (float bits)
+            int *sPM = reinterpret_cast<int *>(smem + L.pmisc_off);
+            if (warp == 0) {
+                int poff = 0, pn = 0;
+                const bool prange =
+                    request_range(pa.node_offsets, b, pa.T, pa.max_nodes, poff, pn);
+                const int Lp = pa.len[b];
+                const int pnode = lane < mdp ? pa.path[(size_t)b * mdp + lane] : -1;
+                bool bad = !prange || Lp < 0 || Lp > mdp || (lane < Lp && (pnode < 0 || pnode >= pn));
+                bad = __any_sync(0xffffffffu, bad);
+                if (!bad && lane < Lp) sPath[lane] = pnode;
+                if (lane == 0) {
+                    sPM[0] = bad ? 0 : Lp;
+                    sPM[1] = bad;
+                    sPM[2] = poff;
+                    sPM[3] = 0;
+                }
+            }
+            named_barrier(1, kGroup);
+            const int Lp = sPM[0], poff = sPM[2];
+            if (Lp > 0) {
+                // the path must be a root path of the previous tree; its factor rows
+                if (warp == 0) {
+                    bool bad = false;
+                    if (lane < Lp)
+                        bad = pa.parent[poff + sPath[lane]] != (lane == 0 ? -1 : sPath[lane - 1]);
+                    bad = __any_sync(0xffffffffu, bad);
+                    if (lane == 0) sPM[3] = bad;
+                }
+                const __nv_bfloat16 *pk = static_cast<const __nv_bfloat16 *>(pa.k);
+                const __nv_bfloat16 *pv = static_cast<const __nv_bfloat16 *>(pa.v);
+                const int k8 = dk / 8, v8 = DV / 8;
+                for (int e = tid; e < Lp * (k8 + v8); e += kGroup) {
+                    const bool isk = e < Lp * k8;
+                    const int e2 = isk ? e : e - Lp * k8;
+                    const int per = isk ? k8 : v8;
+                    const int m = e2 / per, c8 = (e2 % per) * 8;
+                    const size_t row = (size_t)(poff + sPath[m]) * H + h;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(
+                        isk ? pk + row * dk + c8 : pv + row * DV + c8);
+                    const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                    float *dst = isk ? sPK + m * dk + c8 : sPV + m * DV + c8;
 #pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        dst[2 * u] = __low2float(x2[u]);
+                        dst[2 * u + 1] = __high2float(x2[u]);
+                    }
+                }
+                if (tid < Lp) sPG[tid] = pa.g[(size_t)(poff + sPath[tid]) * H + h];
+                named_barrier(1, kGroup);
+                if (sPM[3] == 0) {
+                    // a_{m,r} = e^{sum of g after p_m} k_{p_m}[r]; e^{G_L} once per row
+                    for (int r = tid; r < dk; r += kGroup) {
+                        float sg = 0.f;
+                        for (int m = Lp - 1; m >= 0; --m) {
+                            sPK[m * dk + r] *= expf(sg);
+                            sg += sPG[m];
+                        }
+                        if (r == 0) reinterpret_cast<float *>(sPM)[4] = expf(sg);
+                    }
+                }
+                named_barrier(1, kGroup);
+                if (sPM[3] == 0) {
+                    pL = Lp;
+                    palpha = reinterpret_cast<const float *>(sPM)[4];
+                }
+            }
+        }
+        float *Hw = PEND ? P.H_w + (size_t)unit * dk * DV : nullptr;
+        // the pending update makes the loop body long: keep one copy of it in the
+        // instruction cache
+        constexpr int kUnrollChunks = PEND ? 1 : kMaxChunks;
+#pragma unroll kUnrollChunks
         for (int c = 0; c < kMaxChunks; ++c) {
             if (c >= nchunks) break;
             if (tid == 0 && !ptx::mbar_wait(bar0 + 8 * c, 0, kWaitLimit)) atomicOr(sState, kH0Late);
             named_barrier(1, kGroup);
-            const bool ok = (*sState & kH0Late) == 0 && have_nodes;
+            const bool landed = (*sState & kH0Late) == 0;
+            const bool ok = landed && have_nodes;
             uint8_t *chunk = sA + c * chunk_bytes;
             float hold[kPer][8];
-            if (ok) {
+            if (landed && (have_nodes || pL > 0)) {
                 const float *f32 = reinterpret_cast<const float *>(chunk);
 #pragma unroll
                 for (int t = 0; t < kPer; ++t) {
@@ -655,6 +710,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int ch = it % DV, kq = it / DV;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) hold[t][e] = f32[(kq * 8 + e) * DV + ch];
+                }
+            }
+            if (PEND && landed && pL > 0) {
+                // the pending rank-pL update; each thread owns 8 consecutive rows x 1
+                // channel per item, so a warp's stores of one row are 128 contiguous bytes
+#pragma unroll
+                for (int t = 0; t < kPer; ++t)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) hold[t][e] *= palpha;
+                for (int m = 0; m < pL; ++m) {
+#pragma unroll
+                    for (int t = 0; t < kPer; ++t) {
+                        const int it = tid + t * kGroup;
+                        const int ch = it % DV, kq = it / DV;
+                        const float vm = sPV[m * DV + ch];
+                        const float4 k0 = *reinterpret_cast<const float4 *>(
+                            sPK + m * dk + c * kChunkRows + kq * 8);
+                        const float4 k1 = *reinterpret_cast<const float4 *>(
+                            sPK + m * dk + c * kChunkRows + kq * 8 + 4);
+                        hold[t][0] += k0.x * vm; hold[t][1] += k0.y * vm;
+                        hold[t][2] += k0.z * vm; hold[t][3] += k0.w * vm;
+                        hold[t][4] += k1.x * vm; hold[t][5] += k1.y * vm;
+                        hold[t][6] += k1.z * vm; hold[t][7] += k1.w * vm;
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < kPer; ++t) {
+                    const int it = tid + t * kGroup;
+                    const int ch = it % DV, kq = it / DV;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        Hw[(size_t)(c * kChunkRows + kq * 8 + e) * DV + ch] = hold[t][e];
                 }
             }
             named_barrier(1, kGroup);  // the chunk is read before it is rewritten in place
@@ -835,6 +922,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!range_ok && h == 0) report(a.status, TV_ERR_TREE);
         if (have_nodes && !tree_ok && h == 0) report(a.status, TV_ERR_TREE);
         if (st & (kH0Late | kQkvLateTree | kQkvLateMma)) report(a.status, TV_ERR_TIMEOUT);
+        if constexpr (PEND) {
+            const int *sPM = reinterpret_cast<const int *>(smem + L.pmisc_off);
+            if ((sPM[1] || sPM[3]) && h == 0) report(a.status, TV_ERR_TREE);
+        }
     }
     if (have_nodes && !tree_ok)
         for (int e = tid; e < n * DV; e += kThreads)
@@ -904,43 +995,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-int tmem_columns(int npad_max) {
-    int c = 32;
-    while (c < npad_max) c <<= 1;
-    return c;
-}
-
-bool encode_rows(CUtensorMap *tm, const void *base, CUtensorMapDataType dt, int esize, int width,
-                 int H, int T, int box_w, CUtensorMapSwizzle swz) {
-    // rows of `width` elements per (node, head): dims (width, H, T), one head per box
-    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)H, (cuuint64_t)T};
-    const cuuint64_t strides[2] = {(cuuint64_t)width * esize, (cuuint64_t)width * esize * H};
-    const cuuint32_t box[3] = {(cuuint32_t)box_w, 1, 16};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return encode_fn()(tm, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-constexpr size_t kSmemLimit = 227 * 1024;
-
-size_t tc_smem_bytes(const VerifyArgs &a) {
+size_t tc_smem_bytes(const VerifyArgs &a, int pend_depth = 0) {
     const int npad_max = (a.max_nodes + 15) & ~15;
-    return TcLayout(a.dk, a.dv, npad_max, a.max_depth, a.decay == TV_DECAY_DIAG).total;
+    return TcLayout(a.dk, a.dv, npad_max, a.max_depth, a.decay == TV_DECAY_DIAG, pend_depth).total;
 }
 
 // Shared-memory opt-in, a residency cap that keeps co-resident CTAs within the 512
@@ -950,6 +1007,11 @@ cudaError_t launch_tc_kernel(void (*kern)(KArgs...), const TcParams &P, size_t s
                              unsigned grid, cudaStream_t s, Args &&...args) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
+    if (e != cudaSuccess) return e;
+    // without this the driver may configure a smaller shared-memory carveout and fit
+    // fewer CTAs than registers and shared memory allow
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
@@ -970,8 +1032,11 @@ cudaError_t launch_tc_kernel(void (*kern)(KArgs...), const TcParams &P, size_t s
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, static_cast<Args &&>(args)...);
 }
 
-template <int DV, bool DIAG>
-cudaError_t launch_tc(const VerifyArgs &a, cudaStream_t s) {
+// PEND: the scalar kernel with the pending commit of *pend applied to H first.
+template <int DV, bool DIAG, bool PEND = false>
+cudaError_t launch_tc(const VerifyArgs &a, cudaStream_t s, const PendingArgs *pend = nullptr,
+                      float *H = nullptr) {
+    static_assert(!(DIAG && PEND), "the pending commit runs in the scalar-decay kernel");
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tq, tk, tv_, tg;
     bool enc = encode_rows(&tk, a.k, BF, 2, a.dk, a.H, a.T, a.dk, CU_TENSOR_MAP_SWIZZLE_NONE) &&
@@ -990,12 +1055,15 @@ cudaError_t launch_tc(const VerifyArgs &a, cudaStream_t s) {
     P.a = a;
     P.npad_max = (a.max_nodes + 15) & ~15;
     P.tmem_cols = tmem_columns(P.npad_max);
-    const size_t smem = tc_smem_bytes(a);
+    P.pend = pend ? *pend : PendingArgs{};
+    P.H_w = H;
+    const size_t smem = tc_smem_bytes(a, pend ? pend->max_depth : 0);
     const unsigned grid = (unsigned)(a.B * a.H);
     if constexpr (DIAG)
         return launch_tc_kernel(verify_tc_kernel<DV, true>, P, smem, grid, s, tq, tk, tv_, tg, P);
     else
-        return launch_tc_kernel(verify_tc_scalar_ws_kernel<DV>, P, smem, grid, s, tq, tk, tv_, P);
+        return launch_tc_kernel(verify_tc_scalar_ws_kernel<DV, PEND>, P, smem, grid, s, tq, tk,
+                                tv_, P);
 }
 
 }  // namespace
@@ -1010,6 +1078,18 @@ cudaError_t launch_verify_tc(const VerifyArgs &a, cudaStream_t s) {
     const bool diag = a.decay == TV_DECAY_DIAG;
     if (a.dv == 64) return diag ? launch_tc<64, true>(a, s) : launch_tc<64, false>(a, s);
     return diag ? launch_tc<128, true>(a, s) : launch_tc<128, false>(a, s);
+}
+
+bool commit_verify_tc_supported(const VerifyArgs &a, const PendingArgs &p) {
+    return a.decay == TV_DECAY_SCALAR && verify_tc_supported(a) &&
+           tc_smem_bytes(a, p.max_depth) <= kSmemLimit;
+}
+
+cudaError_t launch_commit_verify_tc(const VerifyArgs &a, const PendingArgs &p, float *H,
+                                    cudaStream_t s) {
+    if (!commit_verify_tc_supported(a, p)) return cudaErrorNotSupported;
+    if (a.dv == 64) return launch_tc<64, false, true>(a, s, &p, H);
+    return launch_tc<128, false, true>(a, s, &p, H);
 }
 
 }  // namespace tv
