@@ -394,6 +394,23 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(device=dev)
     node_heads = base.T * base.H
 
+    # target logits for the argmax + walk call (config 2's 32000-token vocabulary; the
+    # others draw their tokens from 32), rows planted so the argmax is the target
+    vocab = 32000 if cfg == 2 else 64
+    logits = []
+    for r, hb in enumerate(sets):
+        rl, nl = workloads.target_logits(hb, vocab, seed=31 + r)
+        logits.append((torch.from_numpy(rl.view(np.int16)).to(dev),
+                       torch.from_numpy(nl.view(np.int16)).to(dev)))
+    root_am = torch.empty(base.B, dtype=torch.int32, device=dev)
+    tgt_am = torch.empty(max(base.T, 1), dtype=torch.int32, device=dev)
+
+    def accept_logits(i):
+        d, (rl, nl) = dbs[i], logits[i]
+        tv.tv_accept_greedy_logits(d.B, d.T, d.max_nodes, d.max_depth, vocab, d.node_offsets,
+                                   d.parent, d.draft, rl, nl, root_am, tgt_am, d.accept_len,
+                                   d.path, d.bonus, d.status, stream)
+
     fused = args.pipeline == "fused"
 
     def step_fused(d):
@@ -443,6 +460,10 @@ def run_ours(args, world, rank, local):
                 return lambda d=d: d.verify(stream=stream, variant=args.variant)
             if kind == "accept":
                 return lambda d=d: d.accept(stream=stream)
+            if kind == "accept_logits":
+                return lambda i=i: accept_logits(i % R)
+            if kind == "step_logits":
+                return lambda d=d, i=i: (d.commit_verify(d, stream=stream), accept_logits(i % R))
             if kind == "accept_commit":
                 return lambda d=d: d.accept_commit(stream=stream)
             return lambda d=d: d.commit(stream=stream)
@@ -489,6 +510,8 @@ def run_ours(args, world, rank, local):
     t_commit, _, _ = timed("commit", K)
     t_acom, _, _ = timed("accept_commit", K)
     t_cv, _, _ = timed("commit_verify", K)
+    t_al, _, _ = timed("accept_logits", K)
+    t_sl, _, _ = timed("step_logits", K)
     t_sep = timed("step_separate", K)[0] if fused else t_step
     sampler.stop()
     for d in dbs:
@@ -554,6 +577,9 @@ def run_ours(args, world, rank, local):
     lens = [int(x) for x in dbs[0].accept_len[:base.B].cpu().numpy()]
     cb = commit_bytes(base, lens)
     cvb = commit_verify_bytes(base, lens)
+    # logits rows read once, tree arrays, acceptance outputs and argmax outputs
+    al_bytes = ((base.B + base.T) * vocab * 2 + 8 * base.T + 4 * (base.B + 1)
+                + 4 * base.B * (3 + base.max_depth) + 4 * base.T)
     cv_launch = t_cv / K
     used_variant = args.variant if args.variant else dbs[0].variant()
     # the recorded captures are of the tensor-core kernels on the config-2 workload
@@ -617,6 +643,13 @@ def run_ours(args, world, rank, local):
             "verify_folded_layers": ({k: dict(v, frac=v["gbs"] / peak)
                                       for k, v in folded.items()} if folded else None),
             "commit_gbs": cb / (t_commit / K) / 1e9,
+            "accept_from_logits": {
+                "call": "tv_accept_greedy_logits", "vocab": vocab,
+                "bytes_per_launch": al_bytes, "launch_us": t_al / K * 1e6,
+                "gbs": al_bytes / (t_al / K) / 1e9,
+                "frac": al_bytes / (t_al / K) / 1e9 / peak,
+                "step_us_with_it": t_sl / K * 1e6,
+                "step": "tv_commit_verify + tv_accept_greedy_logits"},
             "transient_bytes": {"library_workspace": 0,
                                 "factors": int(base.T * base.H * (
                                     (2 * base.dk + base.dv) * (2 if base.qkv_dtype == "bf16" else 4)

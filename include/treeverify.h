@@ -170,6 +170,32 @@ tv_status tv_accept_greedy(int32_t B, int32_t total_nodes, int32_t max_nodes, in
                            int32_t *bonus, int32_t *dev_status, void *stream);
 
 /*
+ * tv_accept_greedy_logits -- tv_accept_greedy with the target's choices taken
+ * from its logits: the target argmax at the committed context and after every
+ * draft node (LLM Primer VI ch. 9 §9.1: the target model's own most likely
+ * token decides), computed and walked in one launch.
+ *
+ *   vocab        V >= 1, the row length of the logits
+ *   root_logits  [B][V] bf16   the target's logits at the committed context
+ *   node_logits  [T][V] bf16   the target's logits after each draft node
+ *   root_argmax  [B] out, may be NULL: argmax of each root row
+ *   target_argmax [T] out, may be NULL: argmax of each node row
+ *   other arguments as in tv_accept_greedy (the walk uses the computed argmaxes)
+ * Argmax: the first index of the largest value; a NaN counts as larger than any
+ * number, -0 equals +0.  Rows are read with 16-byte loads when V is a multiple
+ * of 8 (logit pointers must be 16-byte aligned in any case).  Device-detected
+ * errors and outputs of a malformed request as in tv_accept_greedy.  Results are
+ * exact.
+ */
+tv_status tv_accept_greedy_logits(int32_t B, int32_t total_nodes, int32_t max_nodes,
+                                  int32_t max_depth, int32_t vocab, const int32_t *node_offsets,
+                                  const int32_t *parent, const int32_t *draft_tokens,
+                                  const void *root_logits, const void *node_logits,
+                                  int32_t *root_argmax, int32_t *target_argmax,
+                                  int32_t *accept_len, int32_t *path, int32_t *bonus,
+                                  int32_t *dev_status, void *stream);
+
+/*
  * tv_commit -- state after the accepted path, rebuilt from the factors.
  * Bole summary page, "Core techniques" §2: only the accepted path's state is
  * restored, h_k = Chain(S_k..S_1) h_0 + accumulated updates; here

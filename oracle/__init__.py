@@ -251,6 +251,31 @@ def accept_batch(batch, max_depth: Optional[int] = None, root_argmax=None, targe
     return ln[:b.B], path[:b.B * md].reshape(b.B, md), bonus[:b.B]
 
 
+def argmax_rows(bits) -> np.ndarray:
+    """Target argmax of every row of bf16 logits (uint16 bit patterns, [rows][V]).
+
+    The greedy rule takes the target's most likely token (LLM Primer VI ch. 9,
+    §9.1).  Written as numpy's argmax over the exactly widened values: the first
+    index among equal maxima; a NaN counts as larger than any number (the first
+    NaN wins); -0 equals +0."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    if b.ndim != 2 or b.shape[1] == 0:
+        raise OracleError("argmax_rows needs a [rows][V] array with V >= 1")
+    x = (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return np.argmax(x, axis=1).astype(np.int32)
+
+
+def accept_from_logits(batch, root_logits, node_logits, max_depth: Optional[int] = None):
+    """Greedy walk with the target's choices taken as the argmax of its logits:
+    root_logits [B][V] at the committed context, node_logits [T][V] after each
+    node.  Returns (len[B], path[B,max_depth], bonus[B], root_argmax[B],
+    target_argmax[T])."""
+    root = argmax_rows(root_logits) if batch.B else np.zeros(0, np.int32)
+    tgt = argmax_rows(node_logits) if batch.T else np.zeros(0, np.int32)
+    ln, path, bonus = accept_batch(batch, max_depth=max_depth, root_argmax=root, target=tgt)
+    return ln, path, bonus, root, tgt
+
+
 def commit(batch, accept_len, path, units: Optional[Sequence[int]] = None, threads: int = 1,
            packed=None):
     """H_new of the listed units: dict u -> [dk, dv] float64."""

@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert {"tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
-            "tv_accept_commit", "tv_commit_verify", "tv_status_string", "tv_version"} <= set(names)
+            "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_status_string",
+            "tv_version"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -200,6 +201,27 @@ def test_commit_verify_rejects_bad_arguments(lib):
     # without a pending commit the call is tv_verify and checks like it
     assert rc(pe=None, q=None) == tv.TV_ERR_NULL
     assert rc(prob(dv=0), pe=None) == tv.TV_ERR_SHAPE
+
+
+def test_accept_logits_rejects_bad_arguments(lib):
+    def rc(**kw):
+        a = dict(B=2, T=5, mn=4, md=3, V=32000, offs=P[0], par=P[1], dr=P[2], rl=P[3], nl=P[4],
+                 ra=P[5], ta=P[6], ln=P[7], path=P[8], bonus=P[9], st=P[10])
+        a.update(kw)
+        return tv.tv_accept_greedy_logits(a["B"], a["T"], a["mn"], a["md"], a["V"], a["offs"],
+                                          a["par"], a["dr"], a["rl"], a["nl"], a["ra"], a["ta"],
+                                          a["ln"], a["path"], a["bonus"], a["st"], stream=0,
+                                          check=False)
+    assert rc(V=0) == tv.TV_ERR_SHAPE
+    assert rc(B=-1) == tv.TV_ERR_SHAPE
+    assert rc(md=33) == tv.TV_ERR_UNSUPPORTED
+    assert rc(T=9) == tv.TV_ERR_SHAPE
+    assert rc(rl=None) == tv.TV_ERR_NULL
+    assert rc(nl=None) == tv.TV_ERR_NULL
+    assert rc(st=None) == tv.TV_ERR_NULL
+    assert rc(nl=P[4] + 2) == tv.TV_ERR_ALIGN
+    assert rc(ta=P[6] + 4) == tv.TV_ERR_ALIGN
+    assert rc(B=0, T=0) == tv.TV_OK
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -27,7 +27,8 @@ TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC, TV_VARIANT_TC_STREAM = 0, 1, 2,
 TV_MAX_NODES, TV_MAX_DEPTH, TV_MAX_DIM = 256, 32, 256
 
 EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
-            "tv_accept_commit", "tv_commit_verify", "tv_status_string", "tv_version")
+            "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_status_string",
+            "tv_version")
 
 
 class tv_problem(ctypes.Structure):
@@ -77,8 +78,9 @@ def load(path: Optional[str] = None):
         L.tv_accept_commit.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.tv_commit_verify.argtypes = [P, ctypes.POINTER(tv_pending), vp, vp, vp, vp, vp, vp, vp,
                                        vp]
+        L.tv_accept_greedy_logits.argtypes = [i32, i32, i32, i32, i32] + [vp] * 12
         for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit,
-                  L.tv_accept_commit, L.tv_commit_verify):
+                  L.tv_accept_commit, L.tv_commit_verify, L.tv_accept_greedy_logits):
             f.restype = ctypes.c_int32
         L.tv_status_string.argtypes = [i32]
         L.tv_status_string.restype = ctypes.c_char_p
@@ -153,6 +155,19 @@ def tv_accept_greedy(B, total_nodes, max_nodes, max_depth, node_offsets, parent,
                                  _ptr(target_argmax), _ptr(root_argmax), _ptr(accept_len),
                                  _ptr(path), _ptr(bonus), _ptr(dev_status), _stream(stream))
     return _check(rc, "tv_accept_greedy", check)
+
+
+def tv_accept_greedy_logits(B, total_nodes, max_nodes, max_depth, vocab, node_offsets, parent,
+                            draft_tokens, root_logits, node_logits, root_argmax, target_argmax,
+                            accept_len, path, bonus, dev_status, stream=None,
+                            check: bool = True) -> int:
+    rc = load().tv_accept_greedy_logits(int(B), int(total_nodes), int(max_nodes), int(max_depth),
+                                        int(vocab), _ptr(node_offsets), _ptr(parent),
+                                        _ptr(draft_tokens), _ptr(root_logits), _ptr(node_logits),
+                                        _ptr(root_argmax), _ptr(target_argmax), _ptr(accept_len),
+                                        _ptr(path), _ptr(bonus), _ptr(dev_status),
+                                        _stream(stream))
+    return _check(rc, "tv_accept_greedy_logits", check)
 
 
 def tv_commit(problem: tv_problem, H0, g, k, v, path, accept_len, H_new, dev_status, stream=None,

@@ -11,28 +11,15 @@
 
 namespace tv {
 
-// Copies request rows [off, off+n) of parent/draft/target into the warp's shared
-// buffers (one round trip of independent loads), checks parent[i] in [-1, i), then
-// walks on shared memory: children of node c all have larger indices, so each step
-// scans the nodes after the current one 32 at a time and a ballot finds the lowest
-// matching index.  Writes path[0..L) (lane 0) and returns L, with *bonus = final
-// token; returns -1 for a malformed tree or a walk longer than max_depth.
-// Every lane of the warp must call it.
-__device__ __forceinline__ int warp_greedy_walk(const int32_t *parent, const int32_t *draft,
-                                                const int32_t *target, int off, int n,
-                                                int max_depth, int32_t root, int *par, int *drf,
-                                                int *tgt, int *path, int32_t *bonus) {
+// The walk on shared memory, parents already checked to lie in [-1, i): children
+// of node c all have larger indices, so each step scans the nodes after the
+// current one 32 at a time and a ballot finds the lowest matching index.  Writes
+// path[0..L) (lane 0) and returns L, with *bonus = final token; returns -1 for a
+// walk longer than max_depth.  Every lane of the warp must call it.
+__device__ __forceinline__ int warp_greedy_walk_shared(const int *par, const int *drf,
+                                                       const int *tgt, int n, int max_depth,
+                                                       int32_t root, int *path, int32_t *bonus) {
     const int lane = threadIdx.x & 31;
-    bool bad = false;
-    for (int i = lane; i < n; i += 32) {
-        const int p = parent[off + i];
-        par[i] = p;
-        drf[i] = draft[off + i];
-        tgt[i] = target[off + i];
-        bad |= (p < -1 || p >= i);
-    }
-    if (__any_sync(0xffffffffu, bad)) return -1;
-    __syncwarp();
     int L = 0, cur = -1;
     int32_t t = root;
     for (;;) {
@@ -55,6 +42,28 @@ __device__ __forceinline__ int warp_greedy_walk(const int32_t *parent, const int
     }
     *bonus = t;
     return L;
+}
+
+// Copies request rows [off, off+n) of parent/draft/target into the warp's shared
+// buffers (one round trip of independent loads), checks parent[i] in [-1, i), then
+// runs warp_greedy_walk_shared.  Returns -1 for a malformed tree or a walk longer
+// than max_depth.  Every lane of the warp must call it.
+__device__ __forceinline__ int warp_greedy_walk(const int32_t *parent, const int32_t *draft,
+                                                const int32_t *target, int off, int n,
+                                                int max_depth, int32_t root, int *par, int *drf,
+                                                int *tgt, int *path, int32_t *bonus) {
+    const int lane = threadIdx.x & 31;
+    bool bad = false;
+    for (int i = lane; i < n; i += 32) {
+        const int p = parent[off + i];
+        par[i] = p;
+        drf[i] = draft[off + i];
+        tgt[i] = target[off + i];
+        bad |= (p < -1 || p >= i);
+    }
+    if (__any_sync(0xffffffffu, bad)) return -1;
+    __syncwarp();
+    return warp_greedy_walk_shared(par, drf, tgt, n, max_depth, root, path, bonus);
 }
 
 }  // namespace tv

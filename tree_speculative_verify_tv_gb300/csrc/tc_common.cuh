@@ -63,6 +63,72 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// w_p *= q_i . k_j for every (node, ancestor) pair p = (i, j) of a request, pairs
+// numbered node by node (sPairOff[n] of them; sPairNode[p] = i, sAnc[p] = j).  q is
+// the 128-byte-swizzled bf16 B operand tile (slabs of 64 channels, `slab_bytes`
+// apart), k dense bf16 rows of dk.  16 groups of 8 lanes (`grp` = this lane's
+// group, the 128 threads of one warp group) take two pairs each per round, so the
+// loads of a round are independent; the round count is uniform, so every lane of a
+// warp takes each shuffle.  Lanes 4-7 of a group visit their two 16-byte pieces in
+// the other order, which keeps each quarter-warp's loads of a k row and of the
+// swizzled q row on distinct banks.
+__device__ __forceinline__ void pair_scores(const uint8_t *sB, const __nv_bfloat16 *sK,
+                                            const int *sPairOff, const uint8_t *sPairNode,
+                                            const int *sAnc, float *sW, int n, int dk,
+                                            uint32_t slab_bytes, int grp, int lane) {
+    constexpr int kGroups = 16;
+    const int npairs = sPairOff[n];
+    const int sub = lane & 7;
+    const int per = dk / 8;  // 16 or 8 key channels per lane, whole 16-byte chunks
+    for (int base = 0; base < npairs; base += 2 * kGroups) {
+        int pr[2], ii[2], jj[2];
+        float acc[2];
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            pr[x] = base + x * kGroups + grp;
+            ii[x] = 0;
+            jj[x] = 0;
+            acc[x] = 0.f;
+            if (pr[x] < npairs) {
+                ii[x] = sPairNode[pr[x]];
+                jj[x] = sAnc[pr[x]];
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            if (pr[x] < npairs) {
+                float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (u * 8 < per) {
+                        const int uu = per == 16 ? ((u + (sub >> 2)) & 1) : u;
+                        const int c = sub * per + uu * 8;
+                        const uint4 qr =
+                            *reinterpret_cast<const uint4 *>(sB + swz_offset(ii[x], c, slab_bytes));
+                        const uint4 kr = *reinterpret_cast<const uint4 *>(sK + jj[x] * dk + c);
+                        const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qr);
+                        const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            p0 += __low2float(q2[e]) * __low2float(k2[e]);
+                            p1 += __high2float(q2[e]) * __high2float(k2[e]);
+                        }
+                    }
+                }
+                acc[x] = p0 + p1;
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            float part = acc[x];
+            part += __shfl_xor_sync(0xffffffffu, part, 4);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            if (pr[x] < npairs && sub == 0) sW[pr[x]] *= part;
+        }
+    }
+}
+
 // Barrier among `count` threads and reduce: true iff `pred` holds in all of them.
 __device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
     uint32_t r;

@@ -137,6 +137,39 @@ tv_status tv_accept_greedy(int32_t B, int32_t total_nodes, int32_t max_nodes, in
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+tv_status tv_accept_greedy_logits(int32_t B, int32_t total_nodes, int32_t max_nodes,
+                                  int32_t max_depth, int32_t vocab, const int32_t *node_offsets,
+                                  const int32_t *parent, const int32_t *draft_tokens,
+                                  const void *root_logits, const void *node_logits,
+                                  int32_t *root_argmax, int32_t *target_argmax,
+                                  int32_t *accept_len, int32_t *path, int32_t *bonus,
+                                  int32_t *dev_status, void *stream) {
+    if (B < 0 || total_nodes < 0 || max_nodes < 1 || max_depth < 1 || vocab < 1)
+        return TV_ERR_SHAPE;
+    if (max_nodes > TV_MAX_NODES || max_depth > TV_MAX_DEPTH) return TV_ERR_UNSUPPORTED;
+    if ((int64_t)total_nodes > (int64_t)B * max_nodes) return TV_ERR_SHAPE;
+    if ((int64_t)B * 8 > 0x7fffffffLL) return TV_ERR_UNSUPPORTED;
+    if (!node_offsets || !root_logits || !accept_len || !path || !bonus || !dev_status)
+        return TV_ERR_NULL;
+    if (total_nodes > 0 && (!parent || !draft_tokens || !node_logits)) return TV_ERR_NULL;
+    if (B == 0) return TV_OK;
+    tv_status st = check_ptrs({node_offsets, root_logits, accept_len, path, bonus, dev_status});
+    if (st != TV_OK) return st;
+    if (total_nodes > 0) {
+        st = check_ptrs({parent, draft_tokens, node_logits});
+        if (st != TV_OK) return st;
+    }
+    for (const void *q : {static_cast<const void *>(root_argmax),
+                          static_cast<const void *>(target_argmax)})
+        if (q && !aligned16(q)) return TV_ERR_ALIGN;
+    tv::LogitsArgs a{B, total_nodes, max_nodes, max_depth, vocab, node_offsets, parent,
+                     draft_tokens, static_cast<const uint16_t *>(root_logits),
+                     static_cast<const uint16_t *>(node_logits), root_argmax, target_argmax,
+                     accept_len, path, bonus, dev_status};
+    cudaError_t e = tv::launch_accept_logits(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 tv_status tv_commit(const tv_problem *p, const float *H0, const float *g, const void *k,
                     const void *v, const int32_t *path, const int32_t *accept_len,
                     float *H_new, int32_t *dev_status, void *stream) {

@@ -43,6 +43,16 @@ struct CommitArgs {
     int32_t *path_out, *len_out, *bonus_out;
 };
 
+// Target argmax from logits + greedy walk (tv_accept_greedy_logits).
+struct LogitsArgs {
+    int32_t B, T, max_nodes, max_depth, V;
+    const int32_t *node_offsets, *parent, *draft;
+    const uint16_t *root_logits, *node_logits;  // bf16 bit patterns
+    int32_t *root_out, *target_out;             // optional argmax outputs
+    int32_t *len, *path, *bonus, *status;
+};
+cudaError_t launch_accept_logits(const LogitsArgs &a, cudaStream_t s);
+
 // A commit carried into the next verification (tv_commit_verify).
 struct PendingArgs {
     int32_t T, max_nodes, max_depth;

@@ -552,6 +552,8 @@ __global__ void __launch_bounds__(kThreads, PEND ? 3 : (DV == 64 ? 4 : 1))
     const __nv_bfloat16 *sK = reinterpret_cast<const __nv_bfloat16 *>(smem + L.k_off);
     const __nv_bfloat16 *sV = reinterpret_cast<const __nv_bfloat16 *>(smem + L.v_off);
     float *sX = reinterpret_cast<float *>(smem + L.x_off);
+    // per (node, ancestor) pair p, numbered node by node (sPairOff): the ancestor,
+    // its weight w_p and its node
     float *sW = reinterpret_cast<float *>(smem + L.w_off);
     int *sAnc = reinterpret_cast<int *>(smem + L.anc_off);
     float *sEG = reinterpret_cast<float *>(smem + L.eg_off);
@@ -858,8 +860,8 @@ __global__ void __launch_bounds__(kThreads, PEND ? 3 : (DV == 64 ? 4 : 1))
                 int j = i, d = 0;
                 const int p0 = sPairOff[i];
                 while (j >= 0) {
-                    sAnc[i * md + d] = j;
-                    sW[i * md + d] = expf(s);
+                    sAnc[p0 + d] = j;
+                    sW[p0 + d] = expf(s);
                     sPairNode[p0 + d] = static_cast<uint8_t>(i);
                     s += sG[j];
                     j = sPar[j];
@@ -872,42 +874,8 @@ __global__ void __launch_bounds__(kThreads, PEND ? 3 : (DV == 64 ? 4 : 1))
             atomicOr(sState, kQkvLateTree);
         named_barrier(2, kGroup);
         if (tree_ok && (*sState & kQkvLateTree) == 0) {
-            // w_{i,d} *= q_i . k_{anc_d(i)}: one 8-lane group per pair; the pair count
-            // is uniform, so every lane of a warp takes each shuffle
-            const int npairs = sPairOff[n];
-            const int sub = lane & 7;
-            const int per = dk / 8;  // 16 or 8 key channels per lane, whole 16-byte chunks
-            for (int base = (warp - 4) * 4; base < npairs; base += kGroup / 8) {
-                const int pr = base + (lane >> 3);
-                const bool act = pr < npairs;
-                float p0 = 0.f, p1 = 0.f;
-                int i = 0, d = 0;
-                if (act) {
-                    i = sPairNode[pr];
-                    d = pr - sPairOff[i];
-                    const int j = sAnc[i * md + d];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        if (u * 8 < per) {
-                            const int c = sub * per + u * 8;
-                            const uint4 qr = *reinterpret_cast<const uint4 *>(sB + swz_offset(i, c, slab_bytes));
-                            const uint4 kr = *reinterpret_cast<const uint4 *>(sK + j * dk + c);
-                            const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qr);
-                            const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                p0 += __low2float(q2[e]) * __low2float(k2[e]);
-                                p1 += __high2float(q2[e]) * __high2float(k2[e]);
-                            }
-                        }
-                    }
-                }
-                float part = p0 + p1;
-                part += __shfl_xor_sync(0xffffffffu, part, 4);
-                part += __shfl_xor_sync(0xffffffffu, part, 2);
-                part += __shfl_xor_sync(0xffffffffu, part, 1);
-                if (act && sub == 0) sW[i * md + d] *= part;
-            }
+            pair_scores(sB, sK, sPairOff, sPairNode, sAnc, sW, n, dk, slab_bytes,
+                        (warp - 4) * 4 + (lane >> 3), lane);
         }
     }
 
@@ -969,10 +937,10 @@ __global__ void __launch_bounds__(kThreads, PEND ? 3 : (DV == 64 ? 4 : 1))
                 }
                 const float eg = sEG[i];
                 o.x *= eg; o.y *= eg; o.z *= eg; o.w *= eg;
-                const int di = sDep[i];
+                const int di = sDep[i], p0 = sPairOff[i];
                 for (int d = 0; d < di; ++d) {
-                    const float w = sW[i * md + d];
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(sV + sAnc[i * md + d] * DV + c);
+                    const float w = sW[p0 + d];
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(sV + sAnc[p0 + d] * DV + c);
                     const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
                     const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
                     o.x += w * __low2float(v01); o.y += w * __high2float(v01);

@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                         int x = j, d = 0;
                         const int p0 = sPairOff[j];
                         while (x >= 0) {
-                            sAnc[j * md + d] = x;
-                            sW[j * md + d] = expf(sg);
+                            sAnc[p0 + d] = x;
+                            sW[p0 + d] = expf(sg);
                             sPairNode[p0 + d] = static_cast<uint8_t>(j);
                             sg += sG[x];
                             x = sPar[x];
@@ -387,42 +387,8 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                     atomicOr(sState, kQkvLateTree);
                 named_barrier(2, kGroup);
                 if (tree_ok && (*sState & kQkvLateTree) == 0) {
-                    // w_{j,d} *= q_j . k_{anc_d(j)}: one 8-lane group per pair
-                    const int npairs = sPairOff[n];
-                    const int sub = lane & 7;
-                    const int per = dk / 8;
-                    for (int base = (warp - 4) * 4; base < npairs; base += kGroup / 8) {
-                        const int pr = base + (lane >> 3);
-                        const bool act = pr < npairs;
-                        float p0 = 0.f, p1 = 0.f;
-                        int j = 0, d = 0;
-                        if (act) {
-                            j = sPairNode[pr];
-                            d = pr - sPairOff[j];
-                            const int x = sAnc[j * md + d];
-#pragma unroll
-                            for (int q = 0; q < 2; ++q) {
-                                if (q * 8 < per) {
-                                    const int c = sub * per + q * 8;
-                                    const uint4 qr = *reinterpret_cast<const uint4 *>(
-                                        sB + swz_offset(j, c, slab_bytes));
-                                    const uint4 kr = *reinterpret_cast<const uint4 *>(sK + x * dk + c);
-                                    const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qr);
-                                    const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        p0 += __low2float(q2[e]) * __low2float(k2[e]);
-                                        p1 += __high2float(q2[e]) * __high2float(k2[e]);
-                                    }
-                                }
-                            }
-                        }
-                        float part = p0 + p1;
-                        part += __shfl_xor_sync(0xffffffffu, part, 4);
-                        part += __shfl_xor_sync(0xffffffffu, part, 2);
-                        part += __shfl_xor_sync(0xffffffffu, part, 1);
-                        if (act && sub == 0) sW[j * md + d] *= part;
-                    }
+                    pair_scores(sB, sK, sPairOff, sPairNode, sAnc, sW, n, dk, slab_bytes,
+                                (warp - 4) * 4 + (lane >> 3), lane);
                 }
             }
 
@@ -476,10 +442,10 @@ __global__ void __launch_bounds__(kThreadsS, 2)
                     }
                     const float eg = sEG[j];
                     o.x *= eg; o.y *= eg; o.z *= eg; o.w *= eg;
-                    const int dj = sDep[j];
+                    const int dj = sDep[j], p0 = sPairOff[j];
                     for (int d = 0; d < dj; ++d) {
-                        const float w = sW[j * md + d];
-                        const uint2 raw = *reinterpret_cast<const uint2 *>(sV + sAnc[j * md + d] * DV + c);
+                        const float w = sW[p0 + d];
+                        const uint2 raw = *reinterpret_cast<const uint2 *>(sV + sAnc[p0 + d] * DV + c);
                         const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
                         const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
                         o.x += w * __low2float(v01); o.y += w * __high2float(v01);

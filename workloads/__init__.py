@@ -386,6 +386,36 @@ def make_config(c: int, seed: Optional[int] = None, **kw) -> Batch:
     return CONFIGS[c](seed, **kw)
 
 
+def target_logits(batch: Batch, vocab: int, seed: Optional[int] = None, *,
+                  levels: Optional[int] = None):
+    """bf16 target logits for the greedy walk (uint16 bits): root_logits [B][vocab]
+    at the committed context and node_logits [T][vocab] after each node.
+
+    Default: values N(0, 2) with the row's target token (batch.root_argmax /
+    batch.target) set 1 above the row's largest other value, so the argmax of each
+    row is that token and the planted acceptance paths are reproduced.
+    levels=k: values drawn from k equally spaced levels (many ties, targets not
+    planted), for exercising the first-index rule."""
+    rng = np.random.default_rng(0 if seed is None else seed)
+    rows = batch.B + batch.T
+
+    def draw(n):
+        if levels:
+            return rng.integers(0, levels, (n, vocab)).astype(np.float32) * np.float32(0.5)
+        return rng.normal(0.0, 2.0, (n, vocab)).astype(np.float32)
+
+    x = draw(rows)
+    if not levels:
+        tok = np.concatenate([batch.root_argmax, batch.target]).astype(np.int64)
+        if rows and int(tok.max()) >= vocab:
+            raise ValueError("a target token is outside the vocabulary")
+        r = np.arange(rows)
+        x[r, tok] = -np.inf
+        x[r, tok] = np.max(x, axis=1) + np.float32(1.0)
+    bits = f32_to_bf16_bits(x)
+    return bits[:batch.B], bits[batch.B:]
+
+
 def random_batch(rng, sizes: Sequence[int], H: int, dk: int, dv: int, *, decay="scalar",
                  qkv_dtype="bf16", g_kind=None, depth_cap: int = 32, vocab: int = 4,
                  h0_std: float = 0.05, max_depth: Optional[int] = None,
