@@ -405,6 +405,11 @@ def run_ours(args, world, rank, local):
     root_am = torch.empty(base.B, dtype=torch.int32, device=dev)
     tgt_am = torch.empty(max(base.T, 1), dtype=torch.int32, device=dev)
 
+    # workspace of the naive serial baseline (per-node states), when it is modest
+    serial_bytes = tv.tv_verify_serial_workspace_bytes(dbs[0].problem())
+    serial_ws = (torch.empty(serial_bytes // 4, dtype=torch.float32, device=dev)
+                 if 0 < serial_bytes <= 4 * 2 ** 30 else None)
+
     def accept_logits(i):
         d, (rl, nl) = dbs[i], logits[i]
         tv.tv_accept_greedy_logits(d.B, d.T, d.max_nodes, d.max_depth, vocab, d.node_offsets,
@@ -460,6 +465,8 @@ def run_ours(args, world, rank, local):
                 return lambda d=d: d.verify(stream=stream, variant=args.variant)
             if kind == "accept":
                 return lambda d=d: d.accept(stream=stream)
+            if kind == "serial":
+                return lambda d=d: d.verify_serial(serial_ws, stream=stream)
             if kind == "accept_logits":
                 return lambda i=i: accept_logits(i % R)
             if kind == "step_logits":
@@ -511,6 +518,7 @@ def run_ours(args, world, rank, local):
     t_acom, _, _ = timed("accept_commit", K)
     t_cv, _, _ = timed("commit_verify", K)
     t_al, _, _ = timed("accept_logits", K)
+    t_ser = timed("serial", max(1, K // 8))[0] * 8 if serial_ws is not None else None
     t_sl, _, _ = timed("step_logits", K)
     t_sep = timed("step_separate", K)[0] if fused else t_step
     sampler.stop()
@@ -643,6 +651,12 @@ def run_ours(args, world, rank, local):
             "verify_folded_layers": ({k: dict(v, frac=v["gbs"] / peak)
                                       for k, v in folded.items()} if folded else None),
             "commit_gbs": cb / (t_commit / K) / 1e9,
+            "speedup_over_serial": ({
+                "serial_us": t_ser / K * 1e6, "tree_closed_form_us": t_verify / K * 1e6,
+                "ratio": t_ser / t_verify,
+                "serial": "tv_verify_serial: node after node, per-node states in a %d MB "
+                          "workspace" % (serial_bytes // 2 ** 20)}
+                if t_ser is not None else None),
             "accept_from_logits": {
                 "call": "tv_accept_greedy_logits", "vocab": vocab,
                 "bytes_per_launch": al_bytes, "launch_us": t_al / K * 1e6,

@@ -138,6 +138,29 @@ tv_status tv_verify(const tv_problem *p, const float *H0, const void *q, const v
                     const void *v, const float *g, float *out, int32_t *dev_status,
                     void *stream);
 
+/*
+ * tv_verify_serial -- the same outputs as tv_verify, computed the naive way that
+ * the tree closed form replaces (Bole summary page, "Core techniques" §1-§2 and
+ * the serial baseline it is compared with): inside each (request, head) the nodes
+ * are processed one after another, S_i = diag(exp g_i) S_parent(i) + k_i v_i^T is
+ * formed and stored for every node, and o_i = S_i^T q_i.  A measurement baseline
+ * (speed-up of the closed form over serial verification) and a second evaluator
+ * of the same function; not the fast path.
+ *
+ *   p, H0, q, k, v, g, out, dev_status   as in tv_verify
+ *   workspace        device memory of at least tv_verify_serial_workspace_bytes(p)
+ *                    bytes, 16-byte aligned, owned by the caller; it receives the
+ *                    per-node states [B*H][max_nodes][dk][dv] fp32 (contents are
+ *                    scratch for the caller)
+ *   workspace_bytes  its size
+ * Host errors as tv_verify, plus TV_ERR_NULL for a NULL workspace and TV_ERR_SHAPE
+ * for one that is too small.  Device-detected errors as tv_verify.
+ */
+size_t tv_verify_serial_workspace_bytes(const tv_problem *p);
+tv_status tv_verify_serial(const tv_problem *p, const float *H0, const void *q, const void *k,
+                           const void *v, const float *g, float *out, void *workspace,
+                           size_t workspace_bytes, int32_t *dev_status, void *stream);
+
 /* tv_verify with an explicit kernel choice (tv_variant). */
 tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, const void *k,
                        const void *v, const float *g, float *out, int32_t *dev_status,

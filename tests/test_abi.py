@@ -224,6 +224,26 @@ def test_accept_logits_rejects_bad_arguments(lib):
     assert rc(B=0, T=0) == tv.TV_OK
 
 
+def test_serial_rejects_bad_arguments(lib):
+    p = prob()
+    need = tv.tv_verify_serial_workspace_bytes(p)
+    assert need == 2 * 3 * 4 * 16 * 16 * 4
+    assert tv.tv_verify_serial_workspace_bytes(prob(dk=12)) == 0
+
+    def rc(pp=None, ws=P[11], nbytes=None, **kw):
+        a = dict(H0=P[3], q=P[4], k=P[5], v=P[6], g=P[7], out=P[8], st=P[9])
+        a.update(kw)
+        return tv.tv_verify_serial(pp or p, a["H0"], a["q"], a["k"], a["v"], a["g"], a["out"], ws,
+                                   need if nbytes is None else nbytes, a["st"], stream=0,
+                                   check=False)
+    assert rc(ws=None) == tv.TV_ERR_NULL
+    assert rc(nbytes=need - 1) == tv.TV_ERR_SHAPE
+    assert rc(ws=P[11] + 4) == tv.TV_ERR_ALIGN
+    assert rc(q=None) == tv.TV_ERR_NULL
+    assert rc(prob(dv=12)) == tv.TV_ERR_SHAPE
+    assert rc(prob(total_nodes=0)) == tv.TV_OK
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         tv.load(str(tmp_path / "missing.so"))

@@ -27,8 +27,8 @@ TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC, TV_VARIANT_TC_STREAM = 0, 1, 2,
 TV_MAX_NODES, TV_MAX_DEPTH, TV_MAX_DIM = 256, 32, 256
 
 EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
-            "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_status_string",
-            "tv_version")
+            "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_verify_serial",
+            "tv_verify_serial_workspace_bytes", "tv_status_string", "tv_version")
 
 
 class tv_problem(ctypes.Structure):
@@ -79,8 +79,12 @@ def load(path: Optional[str] = None):
         L.tv_commit_verify.argtypes = [P, ctypes.POINTER(tv_pending), vp, vp, vp, vp, vp, vp, vp,
                                        vp]
         L.tv_accept_greedy_logits.argtypes = [i32, i32, i32, i32, i32] + [vp] * 12
+        L.tv_verify_serial.argtypes = [P] + [vp] * 7 + [ctypes.c_size_t, vp, vp]
+        L.tv_verify_serial_workspace_bytes.argtypes = [P]
+        L.tv_verify_serial_workspace_bytes.restype = ctypes.c_size_t
         for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit,
-                  L.tv_accept_commit, L.tv_commit_verify, L.tv_accept_greedy_logits):
+                  L.tv_accept_commit, L.tv_commit_verify, L.tv_accept_greedy_logits,
+                  L.tv_verify_serial):
             f.restype = ctypes.c_int32
         L.tv_status_string.argtypes = [i32]
         L.tv_status_string.restype = ctypes.c_char_p
@@ -145,6 +149,18 @@ def tv_verify(problem: tv_problem, H0, q, k, v, g, out, dev_status, stream=None,
     rc = load().tv_verify_ex(ctypes.byref(problem), _ptr(H0), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                              _ptr(out), _ptr(dev_status), _stream(stream), int(variant))
     return _check(rc, "tv_verify", check)
+
+
+def tv_verify_serial_workspace_bytes(problem: tv_problem) -> int:
+    return int(load().tv_verify_serial_workspace_bytes(ctypes.byref(problem)))
+
+
+def tv_verify_serial(problem: tv_problem, H0, q, k, v, g, out, workspace, workspace_bytes,
+                     dev_status, stream=None, check: bool = True) -> int:
+    rc = load().tv_verify_serial(ctypes.byref(problem), _ptr(H0), _ptr(q), _ptr(k), _ptr(v),
+                                 _ptr(g), _ptr(out), _ptr(workspace), int(workspace_bytes),
+                                 _ptr(dev_status), _stream(stream))
+    return _check(rc, "tv_verify_serial", check)
 
 
 def tv_accept_greedy(B, total_nodes, max_nodes, max_depth, node_offsets, parent, draft_tokens,
@@ -265,6 +281,13 @@ class DeviceBatch:
     def verify(self, stream=None, variant=TV_VARIANT_AUTO, check=True):
         return tv_verify(self.problem(), self.H0, self.q, self.k, self.v, self.g, self.out,
                          self.status, stream, variant, check)
+
+    def verify_serial(self, workspace, stream=None, check=True):
+        """tv_verify_serial into self.out; `workspace` is a device tensor of at least
+        tv_verify_serial_workspace_bytes bytes."""
+        return tv_verify_serial(self.problem(), self.H0, self.q, self.k, self.v, self.g,
+                                self.out, workspace, workspace.numel() * workspace.element_size(),
+                                self.status, stream, check)
 
     def accept(self, stream=None, check=True):
         return tv_accept_greedy(self.B, self.T, self.max_nodes, self.max_depth, self.node_offsets,

@@ -107,6 +107,34 @@ tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, cons
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+size_t tv_verify_serial_workspace_bytes(const tv_problem *p) {
+    if (check_dims(p) != TV_OK) return 0;
+    tv::VerifyArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
+                     p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
+                     nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    return tv::verify_serial_workspace_bytes(a);
+}
+
+tv_status tv_verify_serial(const tv_problem *p, const float *H0, const void *q, const void *k,
+                           const void *v, const float *g, float *out, void *workspace,
+                           size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    tv_status st = check_dims(p);
+    if (st != TV_OK) return st;
+    if (!p->depth && p->total_nodes > 0) return TV_ERR_NULL;
+    if (!dev_status || !workspace) return TV_ERR_NULL;
+    if (p->B == 0 || p->total_nodes == 0) return TV_OK;
+    st = check_ptrs({H0, q, k, v, g, out, p->node_offsets, p->parent, p->depth, dev_status,
+                     workspace});
+    if (st != TV_OK) return st;
+    tv::VerifyArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
+                     p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
+                     H0, q, k, v, g, out, dev_status};
+    if (workspace_bytes < tv::verify_serial_workspace_bytes(a)) return TV_ERR_SHAPE;
+    cudaError_t e = tv::launch_verify_serial(a, static_cast<float *>(workspace),
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 tv_status tv_verify(const tv_problem *p, const float *H0, const void *q, const void *k,
                     const void *v, const float *g, float *out, int32_t *dev_status,
                     void *stream) {

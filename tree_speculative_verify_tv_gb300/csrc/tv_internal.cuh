@@ -43,6 +43,10 @@ struct CommitArgs {
     int32_t *path_out, *len_out, *bonus_out;
 };
 
+// The naive serial baseline with per-node states in a workspace (tv_verify_serial).
+size_t verify_serial_workspace_bytes(const VerifyArgs &a);
+cudaError_t launch_verify_serial(const VerifyArgs &a, float *ws, cudaStream_t s);
+
 // Target argmax from logits + greedy walk (tv_accept_greedy_logits).
 struct LogitsArgs {
     int32_t B, T, max_nodes, max_depth, V;
