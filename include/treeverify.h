@@ -161,6 +161,35 @@ tv_status tv_verify_serial(const tv_problem *p, const float *H0, const void *q, 
                            const void *v, const float *g, float *out, void *workspace,
                            size_t workspace_bytes, int32_t *dev_status, void *stream);
 
+/* Size of the scratch array built into the library for tv_verify_serial_static. */
+#define TV_SERIAL_STATIC_BYTES (16u << 20)
+
+/*
+ * tv_verify_serial_static -- tv_verify_serial for callers that cannot allocate
+ * device memory.  The pages have no counterpart; this entry point exists for the
+ * library's users.  A process whose allocator has already reserved the device
+ * memory for its own pool, or a loop with a fixed memory budget where an
+ * allocation could fail or stall, cannot hand tv_verify_serial a workspace.  This
+ * call needs none: the per-node states go to a scratch array of
+ * TV_SERIAL_STATIC_BYTES (16 MiB) compiled into the library, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ *   arguments, results and errors as tv_verify_serial, without the workspace
+ *   Problems whose states need more than TV_SERIAL_STATIC_BYTES
+ *   (tv_verify_serial_workspace_bytes(p)) are rejected with TV_ERR_UNSUPPORTED
+ *   before anything is launched.
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address there (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  Every call on a device shares the one array, and
+ * it keeps the last call's contents; the kernel writes every state before it
+ * reads it, so nothing has to be cleared between calls.  Calls that overlap on
+ * the same GPU (for instance on two streams) race on the array and give wrong
+ * results: serialize them.  No device memory is allocated or freed.
+ */
+tv_status tv_verify_serial_static(const tv_problem *p, const float *H0, const void *q,
+                                  const void *k, const void *v, const float *g, float *out,
+                                  int32_t *dev_status, void *stream);
+
 /* tv_verify with an explicit kernel choice (tv_variant). */
 tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, const void *k,
                        const void *v, const float *g, float *out, int32_t *dev_status,

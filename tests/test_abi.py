@@ -244,6 +244,19 @@ def test_serial_rejects_bad_arguments(lib):
     assert rc(prob(total_nodes=0)) == tv.TV_OK
 
 
+def test_serial_static_rejects_problems_beyond_its_scratch(lib):
+    # per-node states of 4 x 8 units x 256 nodes x 128 x 128 fp32 = 512 MiB > 16 MiB
+    big = prob(B=4, H=8, dk=128, dv=128, total_nodes=4, max_nodes=256, max_depth=32)
+    assert tv.tv_verify_serial_workspace_bytes(big) > tv.TV_SERIAL_STATIC_BYTES
+    rc = tv.tv_verify_serial_static(big, P[3], P[4], P[5], P[6], P[7], P[8], P[9], stream=0,
+                                    check=False)
+    assert rc == tv.TV_ERR_UNSUPPORTED
+    assert tv.tv_verify_serial_static(prob(dk=12), *P[3:10], stream=0,
+                                      check=False) == tv.TV_ERR_SHAPE
+    assert tv.tv_verify_serial_static(prob(), P[3], P[4], P[5], P[6], P[7], P[8], None,
+                                      stream=0, check=False) == tv.TV_ERR_NULL
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         tv.load(str(tmp_path / "missing.so"))

@@ -19,7 +19,8 @@ from ._build import build, LIB
 from .binding import (  # noqa: F401
     DeviceBatch, TVError, load, make_pending, make_problem, status_string, tv_accept_commit,
     tv_accept_greedy, tv_accept_greedy_logits, tv_commit, tv_commit_verify, tv_pending,
-    tv_verify_serial, tv_verify_serial_workspace_bytes,
+    tv_verify_serial, tv_verify_serial_workspace_bytes, tv_verify_serial_static,
+    TV_SERIAL_STATIC_BYTES,
     tv_problem, tv_status_string, tv_verify, tv_verify_variant, tv_version, EXPORTED,
     TV_OK, TV_ERR_NULL, TV_ERR_SHAPE, TV_ERR_DTYPE, TV_ERR_ALIGN, TV_ERR_UNSUPPORTED,
     TV_ERR_TREE, TV_ERR_CUDA, TV_ERR_TIMEOUT, TV_DECAY_SCALAR, TV_DECAY_DIAG, TV_BF16, TV_F32,

@@ -25,10 +25,12 @@ TV_DECAY_SCALAR, TV_DECAY_DIAG = 0, 1
 TV_BF16, TV_F32 = 0, 1
 TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC, TV_VARIANT_TC_STREAM = 0, 1, 2, 3
 TV_MAX_NODES, TV_MAX_DEPTH, TV_MAX_DIM = 256, 32, 256
+TV_SERIAL_STATIC_BYTES = 16 << 20
 
 EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
             "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_verify_serial",
-            "tv_verify_serial_workspace_bytes", "tv_status_string", "tv_version")
+            "tv_verify_serial_workspace_bytes", "tv_verify_serial_static", "tv_status_string",
+            "tv_version")
 
 
 class tv_problem(ctypes.Structure):
@@ -80,11 +82,12 @@ def load(path: Optional[str] = None):
                                        vp]
         L.tv_accept_greedy_logits.argtypes = [i32, i32, i32, i32, i32] + [vp] * 12
         L.tv_verify_serial.argtypes = [P] + [vp] * 7 + [ctypes.c_size_t, vp, vp]
+        L.tv_verify_serial_static.argtypes = [P] + [vp] * 8
         L.tv_verify_serial_workspace_bytes.argtypes = [P]
         L.tv_verify_serial_workspace_bytes.restype = ctypes.c_size_t
         for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit,
                   L.tv_accept_commit, L.tv_commit_verify, L.tv_accept_greedy_logits,
-                  L.tv_verify_serial):
+                  L.tv_verify_serial, L.tv_verify_serial_static):
             f.restype = ctypes.c_int32
         L.tv_status_string.argtypes = [i32]
         L.tv_status_string.restype = ctypes.c_char_p
@@ -161,6 +164,15 @@ def tv_verify_serial(problem: tv_problem, H0, q, k, v, g, out, workspace, worksp
                                  _ptr(g), _ptr(out), _ptr(workspace), int(workspace_bytes),
                                  _ptr(dev_status), _stream(stream))
     return _check(rc, "tv_verify_serial", check)
+
+
+def tv_verify_serial_static(problem: tv_problem, H0, q, k, v, g, out, dev_status, stream=None,
+                            check: bool = True) -> int:
+    """tv_verify_serial with the library's built-in scratch array (no workspace)."""
+    rc = load().tv_verify_serial_static(ctypes.byref(problem), _ptr(H0), _ptr(q), _ptr(k),
+                                        _ptr(v), _ptr(g), _ptr(out), _ptr(dev_status),
+                                        _stream(stream))
+    return _check(rc, "tv_verify_serial_static", check)
 
 
 def tv_accept_greedy(B, total_nodes, max_nodes, max_depth, node_offsets, parent, draft_tokens,

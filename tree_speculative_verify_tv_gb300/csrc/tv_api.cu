@@ -135,6 +135,24 @@ tv_status tv_verify_serial(const tv_problem *p, const float *H0, const void *q, 
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+tv_status tv_verify_serial_static(const tv_problem *p, const float *H0, const void *q,
+                                  const void *k, const void *v, const float *g, float *out,
+                                  int32_t *dev_status, void *stream) {
+    tv_status st = check_dims(p);
+    if (st != TV_OK) return st;
+    if (!p->depth && p->total_nodes > 0) return TV_ERR_NULL;
+    if (!dev_status) return TV_ERR_NULL;
+    tv::VerifyArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
+                     p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
+                     H0, q, k, v, g, out, dev_status};
+    if (tv::verify_serial_workspace_bytes(a) > TV_SERIAL_STATIC_BYTES) return TV_ERR_UNSUPPORTED;
+    if (p->B == 0 || p->total_nodes == 0) return TV_OK;
+    st = check_ptrs({H0, q, k, v, g, out, p->node_offsets, p->parent, p->depth, dev_status});
+    if (st != TV_OK) return st;
+    cudaError_t e = tv::launch_verify_serial_static(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 tv_status tv_verify(const tv_problem *p, const float *H0, const void *q, const void *k,
                     const void *v, const float *g, float *out, int32_t *dev_status,
                     void *stream) {

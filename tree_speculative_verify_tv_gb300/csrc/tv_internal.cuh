@@ -46,6 +46,8 @@ struct CommitArgs {
 // The naive serial baseline with per-node states in a workspace (tv_verify_serial).
 size_t verify_serial_workspace_bytes(const VerifyArgs &a);
 cudaError_t launch_verify_serial(const VerifyArgs &a, float *ws, cudaStream_t s);
+// The same with the library's built-in scratch array (tv_verify_serial_static).
+cudaError_t launch_verify_serial_static(const VerifyArgs &a, cudaStream_t s);
 
 // Target argmax from logits + greedy walk (tv_accept_greedy_logits).
 struct LogitsArgs {

@@ -14,7 +14,14 @@
 // Per node, each of 256 threads updates its share of the dk x dv state as float4s
 // (dk*dv/1024 float4 each, dv >= 4) and accumulates S_i^T q_i over its rows; the
 // column sums are reduced through shared memory.
+#include <mutex>
+
 #include "tv_internal.cuh"
+
+// Scratch of tv_verify_serial_static: the per-node states of problems that need at
+// most TV_SERIAL_STATIC_BYTES.  One copy lives on every device that loads the
+// library; host code only uses its name to look up that device address.
+static __device__ __align__(256) float g_serial_states[TV_SERIAL_STATIC_BYTES / sizeof(float)];
 
 namespace tv {
 namespace {
@@ -26,7 +33,7 @@ __global__ void __launch_bounds__(kThreadsS) verify_serial_kernel(VerifyArgs a, 
     __shared__ int s_par[kMaxNodes];
     __shared__ int s_dep[kMaxNodes];
     __shared__ int s_flag;
-    extern __shared__ float s_dyn[];  // q_i, k_i, decay_i [dk] each; v_i [dv]; partial [kThreadsS/?][dv]
+    extern __shared__ float s_dyn[];  // q_i, k_i, decay_i [dk] each; v_i [dv]; [row groups][dv]
     const int unit = blockIdx.x;
     const int b = unit / a.H, h = unit % a.H;
     const int tid = threadIdx.x;
@@ -118,12 +125,45 @@ size_t verify_serial_workspace_bytes(const VerifyArgs &a) {
     return (size_t)a.B * a.H * a.max_nodes * a.dk * a.dv * sizeof(float);
 }
 
+namespace {
+
+// Device address of g_serial_states on the current device, looked up once per
+// device with that device current.
+cudaError_t static_states(float **ptr) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static float *addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_serial_states);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<float *>(p);
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_verify_serial(const VerifyArgs &a, float *ws, cudaStream_t s) {
     const bool diag = a.decay == TV_DECAY_DIAG;
     if (a.qkv_dtype == TV_BF16)
         return diag ? launch_typed<__nv_bfloat16, true>(a, ws, s)
                     : launch_typed<__nv_bfloat16, false>(a, ws, s);
     return diag ? launch_typed<float, true>(a, ws, s) : launch_typed<float, false>(a, ws, s);
+}
+
+cudaError_t launch_verify_serial_static(const VerifyArgs &a, cudaStream_t s) {
+    if (verify_serial_workspace_bytes(a) > TV_SERIAL_STATIC_BYTES) return cudaErrorInvalidValue;
+    float *ws = nullptr;
+    const cudaError_t e = static_states(&ws);
+    if (e != cudaSuccess) return e;
+    return launch_verify_serial(a, ws, s);
 }
 
 }  // namespace tv
