@@ -225,13 +225,13 @@ tv_status tv_accept_greedy(int32_t B, int32_t total_nodes, int32_t max_nodes, in
  * tv_accept_greedy_logits -- tv_accept_greedy with the target's choices taken
  * from its logits: the target argmax at the committed context and after every
  * draft node (LLM Primer VI ch. 9 §9.1: the target model's own most likely
- * token decides), computed and walked in one launch.
+ * token decides).  Two kernels on `stream`: the argmax of every row, then the walk.
  *
  *   vocab        V >= 1, the row length of the logits
  *   root_logits  [B][V] bf16   the target's logits at the committed context
  *   node_logits  [T][V] bf16   the target's logits after each draft node
- *   root_argmax  [B] out, may be NULL: argmax of each root row
- *   target_argmax [T] out, may be NULL: argmax of each node row
+ *   root_argmax  [B] out: argmax of each root row
+ *   target_argmax [T] out: argmax of each node row (the walk reads both)
  *   other arguments as in tv_accept_greedy (the walk uses the computed argmaxes)
  * Argmax: the first index of the largest value; a NaN counts as larger than any
  * number, -0 equals +0.  Rows are read with 16-byte loads when V is a multiple

@@ -219,6 +219,8 @@ def test_accept_logits_rejects_bad_arguments(lib):
     assert rc(rl=None) == tv.TV_ERR_NULL
     assert rc(nl=None) == tv.TV_ERR_NULL
     assert rc(st=None) == tv.TV_ERR_NULL
+    assert rc(ra=None) == tv.TV_ERR_NULL
+    assert rc(ta=None) == tv.TV_ERR_NULL
     assert rc(nl=P[4] + 2) == tv.TV_ERR_ALIGN
     assert rc(ta=P[6] + 4) == tv.TV_ERR_ALIGN
     assert rc(B=0, T=0) == tv.TV_OK

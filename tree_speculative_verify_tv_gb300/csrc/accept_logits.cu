@@ -1,5 +1,4 @@
-// accept_logits.cu -- the target's argmax from its logits and the greedy walk, in
-// one launch.
+// accept_logits.cu -- the target's argmax from its logits, then the greedy walk.
 //
 // LLM Primer VI ch. 9 §9.1: greedy verification keeps the longest draft prefix
 // that matches the target model's own choices and then the target's next choice.
@@ -7,22 +6,20 @@
 // context (root row) and after every draft node (node rows); the walk is the one
 // of tv_accept_greedy.
 //
-// Launch: one thread-block cluster of 16 CTAs per request (8 where the device
-// does not allow 16).  The request's n + 1 rows are dealt round-robin to the
-// cluster's CTAs; a CTA reduces a row of V bf16 logits (16-byte loads, 16 per
-// thread in flight) to the first index of its largest value and stores it into
-// the shared memory of the cluster's first CTA.  After one cluster barrier that
-// CTA runs the walk on its shared memory.  The logits are read once; no global
-// scratch memory is used.
+// Two launches on the caller's stream: one CTA per logits row reduces the row to
+// the first index of its largest value and writes it to root_argmax /
+// target_argmax; then the walk kernel of tv_accept_greedy reads those.  The
+// logits are read once.  (A single launch with one thread-block cluster per
+// request was slower: with n + 1 rows over the cluster's CTAs some CTA reduced
+// two rows one after the other.)
 //
 // Order of values: a NaN is larger than any number (the first NaN wins), -0 equals
 // +0, otherwise the numeric order of the bf16 values; ties go to the lower index.
-#include "greedy_walk.cuh"
+#include "tv_internal.cuh"
 
 namespace tv {
 namespace {
 
-constexpr int kClusterMax = 16;  // non-portable cluster size where allowed, else 8
 constexpr int kThreadsL = 256;
 constexpr int kRegs = 16;         // 16-byte pieces per thread held in registers per chunk
 
@@ -145,136 +142,32 @@ __device__ int row_argmax(const uint16_t *row, int V, int *red) {
     return bi;
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-// Store to the shared memory of CTA `rank` of this cluster at the address that
-// `local` has in this CTA.
-__device__ __forceinline__ void st_cluster(int *local, uint32_t rank, int v) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                 : "=r"(remote)
-                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__global__ void __launch_bounds__(kThreadsL) accept_logits_kernel(LogitsArgs a) {
-    __shared__ int s_arg[kMaxNodes + 1];  // first CTA: argmax of every row, root first
-    __shared__ int s_par[kMaxNodes], s_drf[kMaxNodes], s_path[kMaxDepth];
+// One CTA per row: rows 0..B-1 are the root rows, B..B+T-1 the node rows.
+__global__ void __launch_bounds__(kThreadsL) argmax_rows_kernel(LogitsArgs a) {
     __shared__ int s_red[2 * (kThreadsL / 32) + 2];
-    const uint32_t rank = cluster_rank(), csize = cluster_size();
-    const int b = blockIdx.x / (int)csize;
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int md = a.max_depth;
-
+    const int row = blockIdx.x;
     pdl_wait();
     pdl_launch_next();
-    int off = 0, n = 0;
-    const bool range = request_range(a.node_offsets, b, a.T, a.max_nodes, off, n);
-    if (range) {
-        for (int row = (int)rank; row <= n; row += (int)csize) {
-            const uint16_t *src = row == 0 ? a.root_logits + (size_t)b * a.V
-                                           : a.node_logits + (size_t)(off + row - 1) * a.V;
-            const int am = row_argmax(src, a.V, s_red);
-            if (tid == 0) {
-                st_cluster(&s_arg[row], 0, am);
-                if (row == 0 && a.root_out) a.root_out[b] = am;
-                if (row > 0 && a.target_out) a.target_out[off + row - 1] = am;
-            }
-        }
-    }
-    cluster_sync_all();  // every row's argmax is in the first CTA's shared memory
-    if (rank != 0 || tid >= 32) return;
-
-    int32_t *path = a.path + (size_t)b * md;
-    int L = -1;
-    int32_t t = -1;
-    if (range) {
-        bool bad = false;
-        for (int i = lane; i < n; i += 32) {
-            const int p = a.parent[off + i];
-            s_par[i] = p;
-            s_drf[i] = a.draft[off + i];
-            bad |= (p < -1 || p >= i);
-        }
-        if (!__any_sync(0xffffffffu, bad)) {
-            __syncwarp();
-            L = warp_greedy_walk_shared(s_par, s_drf, s_arg + 1, n, md, s_arg[0], s_path, &t);
-        }
-    }
-    if (L < 0) {
-        if (lane == 0) report(a.status, TV_ERR_TREE);
-        L = 0;
-        t = -1;
-    }
-    __syncwarp();
-    for (int m = lane; m < md; m += 32) path[m] = m < L ? s_path[m] : -1;
-    if (lane == 0) {
-        a.len[b] = L;
-        a.bonus[b] = t;
+    const uint16_t *src = row < a.B ? a.root_logits + (size_t)row * a.V
+                                    : a.node_logits + (size_t)(row - a.B) * a.V;
+    const int am = row_argmax(src, a.V, s_red);
+    if (threadIdx.x == 0) {
+        if (row < a.B)
+            a.root_out[row] = am;
+        else
+            a.target_out[row - a.B] = am;
     }
 }
 
 }  // namespace
 
 cudaError_t launch_accept_logits(const LogitsArgs &a, cudaStream_t s) {
-    // 16 CTAs per request where the device allows clusters of 16, else 8
-    static const int cluster = [] {
-        if (cudaFuncSetAttribute(accept_logits_kernel,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-            cudaGetLastError();
-            return 8;
-        }
-        cudaLaunchConfig_t q = {};
-        q.gridDim = dim3(kClusterMax);
-        q.blockDim = dim3(kThreadsL);
-        cudaLaunchAttribute at;
-        at.id = cudaLaunchAttributeClusterDimension;
-        at.val.clusterDim.x = kClusterMax;
-        at.val.clusterDim.y = 1;
-        at.val.clusterDim.z = 1;
-        q.attrs = &at;
-        q.numAttrs = 1;
-        int nclusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&nclusters, accept_logits_kernel, &q) != cudaSuccess ||
-            nclusters < 1) {
-            cudaGetLastError();
-            return 8;
-        }
-        return kClusterMax;
-    }();
-    const int kCluster = cluster;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.B * kCluster));
-    cfg.blockDim = dim3(kThreadsL);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, accept_logits_kernel, a);
+    cudaError_t e = launch_pdl(argmax_rows_kernel, dim3((unsigned)(a.B + a.T)), dim3(kThreadsL), 0,
+                               s, a);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    AcceptArgs w{a.B, a.T, a.max_nodes, a.max_depth, a.node_offsets, a.parent, a.draft,
+                 a.target_out, a.root_out, a.len, a.path, a.bonus, a.status};
+    return launch_accept(w, s);
 }
 
 }  // namespace tv

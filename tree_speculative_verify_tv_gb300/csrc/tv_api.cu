@@ -195,19 +195,19 @@ tv_status tv_accept_greedy_logits(int32_t B, int32_t total_nodes, int32_t max_no
     if (max_nodes > TV_MAX_NODES || max_depth > TV_MAX_DEPTH) return TV_ERR_UNSUPPORTED;
     if ((int64_t)total_nodes > (int64_t)B * max_nodes) return TV_ERR_SHAPE;
     if ((int64_t)B * 8 > 0x7fffffffLL) return TV_ERR_UNSUPPORTED;
-    if (!node_offsets || !root_logits || !accept_len || !path || !bonus || !dev_status)
+    if (!node_offsets || !root_logits || !root_argmax || !accept_len || !path || !bonus ||
+        !dev_status)
         return TV_ERR_NULL;
-    if (total_nodes > 0 && (!parent || !draft_tokens || !node_logits)) return TV_ERR_NULL;
+    if (total_nodes > 0 && (!parent || !draft_tokens || !node_logits || !target_argmax))
+        return TV_ERR_NULL;
     if (B == 0) return TV_OK;
-    tv_status st = check_ptrs({node_offsets, root_logits, accept_len, path, bonus, dev_status});
+    tv_status st = check_ptrs(
+        {node_offsets, root_logits, root_argmax, accept_len, path, bonus, dev_status});
     if (st != TV_OK) return st;
     if (total_nodes > 0) {
-        st = check_ptrs({parent, draft_tokens, node_logits});
+        st = check_ptrs({parent, draft_tokens, node_logits, target_argmax});
         if (st != TV_OK) return st;
     }
-    for (const void *q : {static_cast<const void *>(root_argmax),
-                          static_cast<const void *>(target_argmax)})
-        if (q && !aligned16(q)) return TV_ERR_ALIGN;
     tv::LogitsArgs a{B, total_nodes, max_nodes, max_depth, vocab, node_offsets, parent,
                      draft_tokens, static_cast<const uint16_t *>(root_logits),
                      static_cast<const uint16_t *>(node_logits), root_argmax, target_argmax,

@@ -54,7 +54,7 @@ struct LogitsArgs {
     int32_t B, T, max_nodes, max_depth, V;
     const int32_t *node_offsets, *parent, *draft;
     const uint16_t *root_logits, *node_logits;  // bf16 bit patterns
-    int32_t *root_out, *target_out;             // optional argmax outputs
+    int32_t *root_out, *target_out;             // argmax of every root / node row
     int32_t *len, *path, *bonus, *status;
 };
 cudaError_t launch_accept_logits(const LogitsArgs &a, cudaStream_t s);
