@@ -17,6 +17,7 @@ Parity pins for each function are in ``tests/test_oracle_pins.py``.
 from __future__ import annotations
 
 import ctypes
+import heapq
 import os
 import subprocess
 import threading
@@ -274,6 +275,48 @@ def accept_from_logits(batch, root_logits, node_logits, max_depth: Optional[int]
     tgt = argmax_rows(node_logits) if batch.T else np.zeros(0, np.int32)
     ln, path, bonus = accept_batch(batch, max_depth=max_depth, root_argmax=root, target=tgt)
     return ln, path, bonus, root, tgt
+
+
+def best_first(marginals, n: int, depth_cap: int, cost=None):
+    """Draft tree of one request by best-first expansion (BASTION page, Method §1-§3).
+
+    marginals [depth_cap][C]: the drafter's distribution q_k over C candidates at
+    position k.  A node at depth d holding candidates x_1..x_d has path score
+    rho = prod_k q_k(x_k).  The frontier starts as the C children of the context;
+    the frontier node with the largest rho is added next (equal scores: the one that
+    joined the frontier first; a node's C children join, in candidate order, when it
+    is added and its depth is below depth_cap).  Node index = order of addition.
+    cost (optional) [n+1]: the step cost C(N) with N nodes; the tree then stops
+    growing once the estimated speed-up sum(rho) / C(N) would drop (§3).
+    Returns (parent[N], token[N], rho[N]) with N <= n nodes (float64 rho)."""
+    q = np.asarray(marginals, dtype=np.float64)
+    C = q.shape[1]
+    frontier = []  # (-rho, joined, parent, depth, token)
+    joined = 0
+    for x in range(C):
+        heapq.heappush(frontier, (-float(q[0, x]), joined, -1, 1, x))
+        joined += 1
+    parent, token, rho = [], [], []
+    total = 0.0
+    while len(parent) < n and frontier:
+        negr, _, p, d, x = frontier[0]
+        r = -negr
+        if cost is not None and parent:
+            N = len(parent)
+            if (total + r) / float(cost[N + 1]) < total / float(cost[N]):
+                break
+        heapq.heappop(frontier)
+        i = len(parent)
+        parent.append(p)
+        token.append(x)
+        rho.append(r)
+        total += r
+        if d < depth_cap:
+            for y in range(C):
+                heapq.heappush(frontier, (negr * float(q[d, y]), joined, i, d + 1, y))
+                joined += 1
+    return (np.array(parent, dtype=np.int32), np.array(token, dtype=np.int32),
+            np.array(rho, dtype=np.float64))
 
 
 def commit(batch, accept_len, path, units: Optional[Sequence[int]] = None, threads: int = 1,
