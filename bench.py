@@ -577,6 +577,32 @@ def run_ours(args, world, rank, local):
         del fd
         torch.cuda.empty_cache()
 
+    # ---------------- best-first draft trees (the GLA-like layer's and the large-tree
+    # stack's tree shapes), one launch per batch of requests
+    builder = None
+    if rank == 0:
+        builder = {}
+        for name, (Bt, Ct, cap, nt, alpha) in (("64-node trees, B=32, depth <= 8", (32, 8, 8, 64, 0.3)),
+                                               ("256-node trees, B=8, depth <= 16", (8, 8, 16, 256, 0.2))):
+            marg = torch.from_numpy(np.random.default_rng(3).dirichlet(
+                alpha * np.ones(Ct), size=(Bt, cap))).to(dev)
+            par = torch.empty((Bt, nt), dtype=torch.int32, device=dev)
+            tok = torch.empty((Bt, nt), dtype=torch.int32, device=dev)
+            rho = torch.empty((Bt, nt), dtype=torch.float64, device=dev)
+            cnt = torch.empty(Bt, dtype=torch.int32, device=dev)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    tv.tv_build_tree(Bt, Ct, cap, nt, marg, None, par, tok, rho, cnt, stream)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(20):
+                    tv.tv_build_tree(Bt, Ct, cap, nt, marg, None, par, tok, rho, cnt, stream)
+                e1.record(stream)
+            e1.synchronize()
+            builder[name] = {"call": "tv_build_tree", "launch_us": e0.elapsed_time(e1) * 1e3 / 20,
+                             "candidates": Ct}
+
     # ---------------- roofline of the dominant kernel of the step
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
@@ -657,6 +683,7 @@ def run_ours(args, world, rank, local):
                 "serial": "tv_verify_serial: node after node, per-node states in a %d MB "
                           "workspace" % (serial_bytes // 2 ** 20)}
                 if t_ser is not None else None),
+            "tree_builder": builder,
             "accept_from_logits": {
                 "call": "tv_accept_greedy_logits", "vocab": vocab,
                 "bytes_per_launch": al_bytes, "launch_us": t_al / K * 1e6,

@@ -161,6 +161,36 @@ tv_status tv_verify_serial(const tv_problem *p, const float *H0, const void *q, 
                            const void *v, const float *g, float *out, void *workspace,
                            size_t workspace_bytes, int32_t *dev_status, void *stream);
 
+/*
+ * tv_build_tree -- draft trees by best-first expansion of path scores.
+ * BASTION page, Method §1-§3: for every position k the drafter gives a
+ * distribution q_k over C candidates; a node at depth d holding candidates
+ * x_1..x_d has path score rho = prod_k q_k(x_k).  Starting from the C children of
+ * the context, the frontier node with the largest rho joins the tree next, and its
+ * C children join the frontier (in candidate order) unless it is at depth_cap;
+ * among equal scores the node that joined the frontier first wins.  With a cost
+ * table the growth stops before the node that would lower sum(rho) / cost[N].
+ * Node index = order of addition: parents precede children, ready for tv_verify.
+ *
+ *   B            requests (>= 0)
+ *   C            candidates per position, 1..32
+ *   depth_cap    deepest allowed node, 1..32
+ *   n            node budget per request, 1..256
+ *   marginals    [B][depth_cap][C] fp64, finite and >= 0 (q_k of request b at row k-1)
+ *   cost         [n+1] fp64 > 0, cost[N] = the step cost with N nodes (index 0
+ *                unused); NULL for a fixed budget of n nodes
+ *   parent, token [B][n] int32 out: local parent (-1 = child of the context) and
+ *                candidate of each node; slots past count[b] hold -1
+ *   rho          [B][n] fp64 out: path scores (0 past count[b])
+ *   count        [B] int32 out: nodes built (fewer than n when the frontier empties
+ *                or the cost stop applies)
+ * One warp per request; the choices are made on fp64 products, so equal inputs give
+ * equal trees on every run.
+ */
+tv_status tv_build_tree(int32_t B, int32_t C, int32_t depth_cap, int32_t n,
+                        const double *marginals, const double *cost, int32_t *parent,
+                        int32_t *token, double *rho, int32_t *count, void *stream);
+
 /* Size of the scratch array built into the library for tv_verify_serial_static. */
 #define TV_SERIAL_STATIC_BYTES (16u << 20)
 

@@ -259,6 +259,24 @@ def test_serial_static_rejects_problems_beyond_its_scratch(lib):
                                       stream=0, check=False) == tv.TV_ERR_NULL
 
 
+def test_build_tree_rejects_bad_arguments(lib):
+    def rc(**kw):
+        a = dict(B=2, C=8, cap=8, n=64, m=P[0], cost=None, par=P[1], tok=P[2], rho=P[3], cnt=P[4])
+        a.update(kw)
+        return tv.tv_build_tree(a["B"], a["C"], a["cap"], a["n"], a["m"], a["cost"], a["par"],
+                                a["tok"], a["rho"], a["cnt"], stream=0, check=False)
+    assert rc(C=0) == tv.TV_ERR_SHAPE
+    assert rc(C=33) == tv.TV_ERR_SHAPE
+    assert rc(cap=33) == tv.TV_ERR_SHAPE
+    assert rc(n=257) == tv.TV_ERR_SHAPE
+    assert rc(B=-1) == tv.TV_ERR_SHAPE
+    assert rc(m=None) == tv.TV_ERR_NULL
+    assert rc(cnt=None) == tv.TV_ERR_NULL
+    assert rc(rho=P[3] + 8) == tv.TV_ERR_ALIGN
+    assert rc(cost=P[5] + 8) == tv.TV_ERR_ALIGN
+    assert rc(B=0) == tv.TV_OK
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         tv.load(str(tmp_path / "missing.so"))

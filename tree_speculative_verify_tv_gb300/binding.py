@@ -29,8 +29,8 @@ TV_SERIAL_STATIC_BYTES = 16 << 20
 
 EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
             "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_verify_serial",
-            "tv_verify_serial_workspace_bytes", "tv_verify_serial_static", "tv_status_string",
-            "tv_version")
+            "tv_verify_serial_workspace_bytes", "tv_verify_serial_static", "tv_build_tree",
+            "tv_status_string", "tv_version")
 
 
 class tv_problem(ctypes.Structure):
@@ -83,11 +83,12 @@ def load(path: Optional[str] = None):
         L.tv_accept_greedy_logits.argtypes = [i32, i32, i32, i32, i32] + [vp] * 12
         L.tv_verify_serial.argtypes = [P] + [vp] * 7 + [ctypes.c_size_t, vp, vp]
         L.tv_verify_serial_static.argtypes = [P] + [vp] * 8
+        L.tv_build_tree.argtypes = [i32] * 4 + [vp] * 7
         L.tv_verify_serial_workspace_bytes.argtypes = [P]
         L.tv_verify_serial_workspace_bytes.restype = ctypes.c_size_t
         for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit,
                   L.tv_accept_commit, L.tv_commit_verify, L.tv_accept_greedy_logits,
-                  L.tv_verify_serial, L.tv_verify_serial_static):
+                  L.tv_verify_serial, L.tv_verify_serial_static, L.tv_build_tree):
             f.restype = ctypes.c_int32
         L.tv_status_string.argtypes = [i32]
         L.tv_status_string.restype = ctypes.c_char_p
@@ -173,6 +174,13 @@ def tv_verify_serial_static(problem: tv_problem, H0, q, k, v, g, out, dev_status
                                         _ptr(v), _ptr(g), _ptr(out), _ptr(dev_status),
                                         _stream(stream))
     return _check(rc, "tv_verify_serial_static", check)
+
+
+def tv_build_tree(B, C, depth_cap, n, marginals, cost, parent, token, rho, count, stream=None,
+                  check: bool = True) -> int:
+    rc = load().tv_build_tree(int(B), int(C), int(depth_cap), int(n), _ptr(marginals), _ptr(cost),
+                              _ptr(parent), _ptr(token), _ptr(rho), _ptr(count), _stream(stream))
+    return _check(rc, "tv_build_tree", check)
 
 
 def tv_accept_greedy(B, total_nodes, max_nodes, max_depth, node_offsets, parent, draft_tokens,

@@ -1,0 +1,148 @@
+// build_tree.cu -- draft trees by best-first expansion of path scores, on the GPU.
+//
+// BASTION page, Method §1-§3: the drafter gives, for every position k, a
+// distribution q_k over C candidates; a node at depth d holding x_1..x_d has path
+// score rho = prod_k q_k(x_k); the tree grows by repeatedly adding the frontier
+// node with the largest rho (§2), and, with a step-cost table C(N), stops once the
+// estimated speed-up sum(rho) / C(N) would drop (§3).  Node index = order of
+// addition, so parents precede children and the result feeds tv_verify directly.
+//
+// One warp per request.  The frontier is kept lazily: one entry per node that can
+// still get children (entry 0 is the context, entry i + 1 node i), holding its best
+// child not yet in the tree.  Each step takes the largest entry score; equal scores
+// go to the lower entry, then to the lower candidate index.  That is the order in
+// which a frontier that receives all C children of a node when the node is added
+// (in candidate order) would hand them out.  Scores are fp64 products computed the
+// same way as in that formulation, so every choice is made on identical values.
+#include "tv_internal.cuh"
+
+namespace tv {
+namespace {
+
+constexpr int kWarpsB = 4;
+
+struct WarpBest {
+    double s;
+    int i;
+};
+
+// Largest s, then smallest i, over the warp.
+__device__ __forceinline__ WarpBest warp_best(double s, int i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const double os = __shfl_xor_sync(0xffffffffu, s, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        if (os > s || (os == s && oi < i)) {
+            s = os;
+            i = oi;
+        }
+    }
+    return {s, i};
+}
+
+__global__ void __launch_bounds__(kWarpsB * 32) build_tree_kernel(BuildArgs a) {
+    extern __shared__ double s_dyn[];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int b = blockIdx.x * kWarpsB + w;
+    pdl_wait();
+    pdl_launch_next();
+    if (b >= a.B) return;
+    const int C = a.C, cap = a.depth_cap, n = a.n;
+    // per warp, in doubles: q [cap][C]; per entry rho and score (fp64), best child,
+    // depth and taken mask (three 32-bit words, two doubles of room)
+    const size_t per_warp = (size_t)cap * C + 4 * (size_t)(n + 1);
+    double *sq = s_dyn + w * per_warp;
+    double *erho = sq + cap * C;
+    double *escore = erho + (n + 1);
+    int *ebest = reinterpret_cast<int *>(escore + (n + 1));
+    int *edep = ebest + (n + 1);
+    uint32_t *emask = reinterpret_cast<uint32_t *>(edep + (n + 1));
+
+    const double *marg = a.marginals + (size_t)b * cap * C;
+    for (int e = lane; e < cap * C; e += 32) sq[e] = marg[e];
+    __syncwarp();
+
+    // best child of entry e not yet in the tree: largest erho * q, lowest candidate
+    auto refresh = [&](int e) {
+        const uint32_t taken = emask[e];
+        const int d = edep[e];
+        double s = -1.0;
+        if (lane < C && !((taken >> lane) & 1u)) s = erho[e] * sq[d * C + lane];
+        const WarpBest bb = warp_best(s, lane < C ? lane : 0x7fffffff);
+        if (lane == 0) {
+            escore[e] = bb.s;
+            ebest[e] = bb.i;
+        }
+        __syncwarp();
+    };
+
+    if (lane == 0) {
+        erho[0] = 1.0;
+        edep[0] = 0;
+        emask[0] = 0u;
+    }
+    __syncwarp();
+    refresh(0);
+
+    int32_t *par_out = a.parent + (size_t)b * n;
+    int32_t *tok_out = a.token + (size_t)b * n;
+    double *rho_out = a.rho + (size_t)b * n;
+    double total = 0.0;
+    int count = 0;
+    for (int i = 0; i < n; ++i) {
+        double s = -1.0;
+        int e = 0x7fffffff;
+        for (int k = lane; k <= i; k += 32) {  // entries 0..i exist
+            const double ks = escore[k];
+            if (ks > s) {  // ascending k in a lane: the first maximum is the lowest
+                s = ks;
+                e = k;
+            }
+        }
+        const WarpBest best = warp_best(s, e);
+        if (best.s < 0.0) break;  // the frontier is empty
+        if (a.cost && i >= 1 && (total + best.s) / a.cost[i + 1] < total / a.cost[i]) break;
+        const int ep = best.i;
+        const int y = ebest[ep];
+        const int d = edep[ep] + 1;
+        if (lane == 0) {
+            par_out[i] = ep - 1;
+            tok_out[i] = y;
+            rho_out[i] = best.s;
+            emask[ep] |= 1u << y;
+            // entry of node i: its children join the frontier below the depth cap
+            erho[i + 1] = best.s;
+            edep[i + 1] = d;
+            emask[i + 1] = 0u;
+            escore[i + 1] = -1.0;
+        }
+        total += best.s;
+        count = i + 1;
+        __syncwarp();
+        refresh(ep);
+        if (d < cap) refresh(i + 1);
+    }
+    for (int i = count + lane; i < n; i += 32) {
+        par_out[i] = -1;
+        tok_out[i] = -1;
+        rho_out[i] = 0.0;
+    }
+    if (lane == 0) a.count[b] = count;
+}
+
+}  // namespace
+
+size_t build_tree_smem_bytes(int C, int depth_cap, int n) {
+    return (size_t)kWarpsB * ((size_t)depth_cap * C + 4 * (size_t)(n + 1)) * sizeof(double);
+}
+
+cudaError_t launch_build_tree(const BuildArgs &a, cudaStream_t s) {
+    const size_t smem = build_tree_smem_bytes(a.C, a.depth_cap, a.n);
+    cudaError_t e = cudaFuncSetAttribute(build_tree_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(build_tree_kernel, dim3((unsigned)((a.B + kWarpsB - 1) / kWarpsB)),
+                      dim3(kWarpsB * 32), smem, s, a);
+}
+
+}  // namespace tv

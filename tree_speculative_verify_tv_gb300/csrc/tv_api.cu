@@ -216,6 +216,22 @@ tv_status tv_accept_greedy_logits(int32_t B, int32_t total_nodes, int32_t max_no
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+tv_status tv_build_tree(int32_t B, int32_t C, int32_t depth_cap, int32_t n,
+                        const double *marginals, const double *cost, int32_t *parent,
+                        int32_t *token, double *rho, int32_t *count, void *stream) {
+    if (B < 0 || C < 1 || C > 32 || depth_cap < 1 || depth_cap > TV_MAX_DEPTH || n < 1 ||
+        n > TV_MAX_NODES)
+        return TV_ERR_SHAPE;
+    if (!marginals || !parent || !token || !rho || !count) return TV_ERR_NULL;
+    if (B == 0) return TV_OK;
+    tv_status st = check_ptrs({marginals, parent, token, rho, count});
+    if (st != TV_OK) return st;
+    if (cost && !aligned16(cost)) return TV_ERR_ALIGN;
+    tv::BuildArgs a{B, C, depth_cap, n, marginals, cost, parent, token, count, rho};
+    cudaError_t e = tv::launch_build_tree(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 tv_status tv_commit(const tv_problem *p, const float *H0, const float *g, const void *k,
                     const void *v, const int32_t *path, const int32_t *accept_len,
                     float *H_new, int32_t *dev_status, void *stream) {

@@ -43,6 +43,16 @@ struct CommitArgs {
     int32_t *path_out, *len_out, *bonus_out;
 };
 
+// Best-first draft-tree construction (tv_build_tree).
+struct BuildArgs {
+    int32_t B, C, depth_cap, n;
+    const double *marginals, *cost;  // cost may be null
+    int32_t *parent, *token, *count;
+    double *rho;
+};
+size_t build_tree_smem_bytes(int C, int depth_cap, int n);
+cudaError_t launch_build_tree(const BuildArgs &a, cudaStream_t s);
+
 // The naive serial baseline with per-node states in a workspace (tv_verify_serial).
 size_t verify_serial_workspace_bytes(const VerifyArgs &a);
 cudaError_t launch_verify_serial(const VerifyArgs &a, float *ws, cudaStream_t s);
