@@ -319,6 +319,85 @@ def best_first(marginals, n: int, depth_cap: int, cost=None):
             np.array(rho, dtype=np.float64))
 
 
+def accept_stochastic_request(parent, draft, p_root, q_root, p_nodes, q_nodes, u_accept,
+                              u_bonus: float, max_depth: int, with_margin: bool = False):
+    """Stochastic acceptance of one request's draft tree (LLM Primer VI ch. 9, §9.1).
+
+    The rule on a chain: a token x drawn from the draft distribution q is accepted
+    with probability min(1, p(x)/q(x)), tested as u * q(x) < p(x) with the node's
+    uniform u; after a rejection the target distribution becomes the normalized
+    residual (p - q)_+ and the emitted token is drawn from it.  On a tree (reading):
+    the children of the current node are tried in index order, each against the
+    current residual; the first accepted child becomes the current node (its own
+    p, q); if none is accepted, the bonus token is drawn from the current residual
+    by inverse CDF: the first index whose running sum exceeds u_bonus * total.  A
+    residual that sums to 0 (p <= q everywhere) leaves p unchanged.  fp64 throughout.
+    Returns (L, path[max_depth], bonus), and the smallest decision margin if asked."""
+    par = np.asarray(parent)
+    n = len(par)
+    p = np.asarray(p_root, dtype=np.float64)
+    q = np.asarray(q_root, dtype=np.float64)
+    cur, path, margin = -1, [], np.inf
+    while True:
+        accepted = False
+        for c in range(cur + 1, n):
+            if par[c] != cur:
+                continue
+            x = int(draft[c])
+            lhs, rhs = float(u_accept[c]) * q[x], p[x]
+            margin = min(margin, abs(lhs - rhs) / max(abs(lhs), abs(rhs), 1e-300))
+            if lhs < rhs:
+                if len(path) >= max_depth:
+                    raise OracleError("accepted path longer than max_depth")
+                path.append(c)
+                cur = c
+                p = np.asarray(p_nodes[c], dtype=np.float64)
+                q = np.asarray(q_nodes[c], dtype=np.float64)
+                accepted = True
+                break
+            r = np.maximum(p - q, 0.0)
+            z = r.sum()
+            if z > 0.0:
+                p = r / z
+        if not accepted:
+            break
+    cs = np.cumsum(p)
+    target = float(u_bonus) * cs[-1]
+    idx = int(np.searchsorted(cs, target, side="right"))
+    if idx >= len(p):
+        idx = int(np.nonzero(p > 0)[0][-1])
+    if with_margin:
+        gaps = np.abs(cs - target)
+        margin = min(margin, float(gaps.min()) / max(cs[-1], 1e-300))
+    out = np.full(max(max_depth, 1), -1, np.int32)
+    out[:len(path)] = path
+    if with_margin:
+        return len(path), out, idx, margin
+    return len(path), out, idx
+
+
+def accept_stochastic(batch, root_p, node_p, root_q, node_q, u_accept, u_bonus,
+                      max_depth: Optional[int] = None, with_margin: bool = False):
+    """accept_stochastic_request for every request: (len[B], path[B,md], bonus[B])
+    (and the smallest decision margin over the batch if asked)."""
+    b = batch
+    md = b.max_depth if max_depth is None else max_depth
+    ln = np.zeros(b.B, np.int32)
+    path = np.full((b.B, md), -1, np.int32)
+    bonus = np.zeros(b.B, np.int32)
+    margin = np.inf
+    for r in range(b.B):
+        s, e = int(b.node_offsets[r]), int(b.node_offsets[r + 1])
+        res = accept_stochastic_request(b.parent[s:e], b.draft[s:e], root_p[r], root_q[r],
+                                        node_p[s:e], node_q[s:e], u_accept[s:e], u_bonus[r],
+                                        md, with_margin=True)
+        ln[r], path[r], bonus[r] = res[0], res[1], res[2]
+        margin = min(margin, res[3])
+    if with_margin:
+        return ln, path, bonus, margin
+    return ln, path, bonus
+
+
 def commit(batch, accept_len, path, units: Optional[Sequence[int]] = None, threads: int = 1,
            packed=None):
     """H_new of the listed units: dict u -> [dk, dv] float64."""

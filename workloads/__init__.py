@@ -416,6 +416,39 @@ def target_logits(batch: Batch, vocab: int, seed: Optional[int] = None, *,
     return bits[:batch.B], bits[batch.B:]
 
 
+def stochastic_inputs(batch: Batch, vocab: int, seed: Optional[int] = None,
+                      spread: float = 2.0, draft_noise: float = 1.0):
+    """Inputs of the stochastic acceptance rule for `batch`'s trees: target and draft
+    probability rows (float32) at the context (root_p, root_q [B][vocab]) and after
+    every node (node_p, node_q [T][vocab]), draft tokens drawn from the parent's
+    draft row, uniforms for every acceptance test (u_accept [T]) and every bonus
+    draw (u_bonus [B]), both float64 in [0, 1).  Target logits are N(0, spread);
+    draft logits add N(0, draft_noise) to them.  Returns a dict; the batch's own
+    draft tokens are left unchanged (the dict carries the new ones)."""
+    rng = np.random.default_rng(0 if seed is None else seed)
+    rows = batch.B + batch.T
+
+    def softmax(z):
+        z = z - z.max(axis=1, keepdims=True)
+        e = np.exp(z)
+        return e / e.sum(axis=1, keepdims=True)
+
+    zt = rng.normal(0.0, spread, (rows, vocab))
+    pt = softmax(zt).astype(np.float32)
+    pq = softmax(zt + rng.normal(0.0, draft_noise, (rows, vocab))).astype(np.float32)
+    draft = np.zeros(batch.T, np.int32)
+    for r in range(batch.B):
+        s, e = int(batch.node_offsets[r]), int(batch.node_offsets[r + 1])
+        for i in range(s, e):
+            p = int(batch.parent[i])
+            row = pq[r] if p < 0 else pq[batch.B + s + p]
+            w = row.astype(np.float64)
+            draft[i] = rng.choice(vocab, p=w / w.sum())
+    return dict(root_p=pt[:batch.B], node_p=pt[batch.B:], root_q=pq[:batch.B],
+                node_q=pq[batch.B:], draft=draft,
+                u_accept=rng.random(batch.T), u_bonus=rng.random(batch.B))
+
+
 def random_batch(rng, sizes: Sequence[int], H: int, dk: int, dv: int, *, decay="scalar",
                  qkv_dtype="bf16", g_kind=None, depth_cap: int = 32, vocab: int = 4,
                  h0_std: float = 0.05, max_depth: Optional[int] = None,
