@@ -162,6 +162,38 @@ tv_status tv_verify_serial(const tv_problem *p, const float *H0, const void *q, 
                            size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * tv_accept_stochastic -- stochastic acceptance of every request's draft tree.
+ * LLM Primer VI ch. 9 §9.1: a draft token x drawn from the draft distribution q
+ * is accepted with probability min(1, p(x)/q(x)), p the target's distribution;
+ * after a rejection the emitted token comes from the normalized residual
+ * (p - q)_+, so the output follows the target's distribution.  On a tree: the
+ * children of the current node are tried in index order against the current
+ * residual (each rejection replaces p by (p - q)_+ / sum, unchanged if that sum is
+ * 0); the first accepted child becomes the current node, with its own p and q;
+ * when none is accepted the bonus token is drawn from the current residual: the
+ * first index whose running sum exceeds u_bonus * (sum of the row).
+ *
+ *   vocab              V >= 1
+ *   root_p, root_q     [B][V] fp32: target / draft probabilities at the context
+ *   node_p, node_q     [T][V] fp32: target / draft probabilities after each node
+ *                      (q of a node is the distribution its children were drawn from)
+ *   u_accept           [T] fp64 uniforms in [0,1): child c is accepted when
+ *                      u_accept[c] * q(x_c) < p(x_c) (p the current residual)
+ *   u_bonus            [B] fp64 uniforms in [0,1) for the bonus draw
+ *   other arguments as in tv_accept_greedy (draft tokens must lie in [0, V))
+ * Arithmetic that decides a token is fp64.  Device-detected errors (bad offsets or
+ * parents, a draft token outside the vocabulary, a path longer than max_depth):
+ * TV_ERR_TREE with accept_len 0, path -1, bonus -1 for that request.
+ */
+tv_status tv_accept_stochastic(int32_t B, int32_t total_nodes, int32_t max_nodes,
+                               int32_t max_depth, int32_t vocab, const int32_t *node_offsets,
+                               const int32_t *parent, const int32_t *draft_tokens,
+                               const float *root_p, const float *node_p, const float *root_q,
+                               const float *node_q, const double *u_accept,
+                               const double *u_bonus, int32_t *accept_len, int32_t *path,
+                               int32_t *bonus, int32_t *dev_status, void *stream);
+
+/*
  * tv_build_tree -- draft trees by best-first expansion of path scores.
  * BASTION page, Method §1-§3: for every position k the drafter gives a
  * distribution q_k over C candidates; a node at depth d holding candidates

@@ -259,6 +259,23 @@ def test_serial_static_rejects_problems_beyond_its_scratch(lib):
                                       stream=0, check=False) == tv.TV_ERR_NULL
 
 
+def test_accept_stochastic_rejects_bad_arguments(lib):
+    def rc(**kw):
+        a = dict(B=2, T=5, mn=4, md=3, V=100, offs=P[0], par=P[1], dr=P[2], rp=P[3], np_=P[4],
+                 rq=P[5], nq=P[6], ua=P[7], ub=P[8], ln=P[9], path=P[10], bonus=P[11], st=P[12])
+        a.update(kw)
+        return tv.tv_accept_stochastic(a["B"], a["T"], a["mn"], a["md"], a["V"], a["offs"],
+                                       a["par"], a["dr"], a["rp"], a["np_"], a["rq"], a["nq"],
+                                       a["ua"], a["ub"], a["ln"], a["path"], a["bonus"], a["st"],
+                                       stream=0, check=False)
+    assert rc(V=0) == tv.TV_ERR_SHAPE
+    assert rc(md=40) == tv.TV_ERR_UNSUPPORTED
+    assert rc(rq=None) == tv.TV_ERR_NULL
+    assert rc(ua=None) == tv.TV_ERR_NULL
+    assert rc(ub=P[8] + 8) == tv.TV_ERR_ALIGN
+    assert rc(B=0, T=0) == tv.TV_OK
+
+
 def test_build_tree_rejects_bad_arguments(lib):
     def rc(**kw):
         a = dict(B=2, C=8, cap=8, n=64, m=P[0], cost=None, par=P[1], tok=P[2], rho=P[3], cnt=P[4])

@@ -30,6 +30,7 @@ TV_SERIAL_STATIC_BYTES = 16 << 20
 EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
             "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_verify_serial",
             "tv_verify_serial_workspace_bytes", "tv_verify_serial_static", "tv_build_tree",
+            "tv_accept_stochastic",
             "tv_status_string", "tv_version")
 
 
@@ -84,11 +85,13 @@ def load(path: Optional[str] = None):
         L.tv_verify_serial.argtypes = [P] + [vp] * 7 + [ctypes.c_size_t, vp, vp]
         L.tv_verify_serial_static.argtypes = [P] + [vp] * 8
         L.tv_build_tree.argtypes = [i32] * 4 + [vp] * 7
+        L.tv_accept_stochastic.argtypes = [i32] * 5 + [vp] * 14
         L.tv_verify_serial_workspace_bytes.argtypes = [P]
         L.tv_verify_serial_workspace_bytes.restype = ctypes.c_size_t
         for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit,
                   L.tv_accept_commit, L.tv_commit_verify, L.tv_accept_greedy_logits,
-                  L.tv_verify_serial, L.tv_verify_serial_static, L.tv_build_tree):
+                  L.tv_verify_serial, L.tv_verify_serial_static, L.tv_build_tree,
+                  L.tv_accept_stochastic):
             f.restype = ctypes.c_int32
         L.tv_status_string.argtypes = [i32]
         L.tv_status_string.restype = ctypes.c_char_p
@@ -174,6 +177,19 @@ def tv_verify_serial_static(problem: tv_problem, H0, q, k, v, g, out, dev_status
                                         _ptr(v), _ptr(g), _ptr(out), _ptr(dev_status),
                                         _stream(stream))
     return _check(rc, "tv_verify_serial_static", check)
+
+
+def tv_accept_stochastic(B, total_nodes, max_nodes, max_depth, vocab, node_offsets, parent,
+                         draft_tokens, root_p, node_p, root_q, node_q, u_accept, u_bonus,
+                         accept_len, path, bonus, dev_status, stream=None,
+                         check: bool = True) -> int:
+    rc = load().tv_accept_stochastic(int(B), int(total_nodes), int(max_nodes), int(max_depth),
+                                     int(vocab), _ptr(node_offsets), _ptr(parent),
+                                     _ptr(draft_tokens), _ptr(root_p), _ptr(node_p), _ptr(root_q),
+                                     _ptr(node_q), _ptr(u_accept), _ptr(u_bonus),
+                                     _ptr(accept_len), _ptr(path), _ptr(bonus), _ptr(dev_status),
+                                     _stream(stream))
+    return _check(rc, "tv_accept_stochastic", check)
 
 
 def tv_build_tree(B, C, depth_cap, n, marginals, cost, parent, token, rho, count, stream=None,

@@ -216,6 +216,37 @@ tv_status tv_accept_greedy_logits(int32_t B, int32_t total_nodes, int32_t max_no
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+tv_status tv_accept_stochastic(int32_t B, int32_t total_nodes, int32_t max_nodes,
+                               int32_t max_depth, int32_t vocab, const int32_t *node_offsets,
+                               const int32_t *parent, const int32_t *draft_tokens,
+                               const float *root_p, const float *node_p, const float *root_q,
+                               const float *node_q, const double *u_accept,
+                               const double *u_bonus, int32_t *accept_len, int32_t *path,
+                               int32_t *bonus, int32_t *dev_status, void *stream) {
+    if (B < 0 || total_nodes < 0 || max_nodes < 1 || max_depth < 1 || vocab < 1)
+        return TV_ERR_SHAPE;
+    if (max_nodes > TV_MAX_NODES || max_depth > TV_MAX_DEPTH) return TV_ERR_UNSUPPORTED;
+    if ((int64_t)total_nodes > (int64_t)B * max_nodes) return TV_ERR_SHAPE;
+    if (!node_offsets || !root_p || !root_q || !u_bonus || !accept_len || !path || !bonus ||
+        !dev_status)
+        return TV_ERR_NULL;
+    if (total_nodes > 0 && (!parent || !draft_tokens || !node_p || !node_q || !u_accept))
+        return TV_ERR_NULL;
+    if (B == 0) return TV_OK;
+    tv_status st = check_ptrs({node_offsets, root_p, root_q, u_bonus, accept_len, path, bonus,
+                               dev_status});
+    if (st != TV_OK) return st;
+    if (total_nodes > 0) {
+        st = check_ptrs({parent, draft_tokens, node_p, node_q, u_accept});
+        if (st != TV_OK) return st;
+    }
+    tv::StochArgs a{B, total_nodes, max_nodes, max_depth, vocab, node_offsets, parent,
+                    draft_tokens, root_p, node_p, root_q, node_q, u_accept, u_bonus,
+                    accept_len, path, bonus, dev_status};
+    cudaError_t e = tv::launch_accept_stochastic(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 tv_status tv_build_tree(int32_t B, int32_t C, int32_t depth_cap, int32_t n,
                         const double *marginals, const double *cost, int32_t *parent,
                         int32_t *token, double *rho, int32_t *count, void *stream) {

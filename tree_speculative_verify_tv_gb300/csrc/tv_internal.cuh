@@ -43,6 +43,16 @@ struct CommitArgs {
     int32_t *path_out, *len_out, *bonus_out;
 };
 
+// Stochastic acceptance (tv_accept_stochastic).
+struct StochArgs {
+    int32_t B, T, max_nodes, max_depth, V;
+    const int32_t *node_offsets, *parent, *draft;
+    const float *root_p, *node_p, *root_q, *node_q;
+    const double *u_accept, *u_bonus;
+    int32_t *len, *path, *bonus, *status;
+};
+cudaError_t launch_accept_stochastic(const StochArgs &a, cudaStream_t s);
+
 // Best-first draft-tree construction (tv_build_tree).
 struct BuildArgs {
     int32_t B, C, depth_cap, n;
