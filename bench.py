@@ -603,6 +603,42 @@ def run_ours(args, world, rank, local):
             builder[name] = {"call": "tv_build_tree", "launch_us": e0.elapsed_time(e1) * 1e3 / 20,
                              "candidates": Ct}
 
+    # ---------------- stochastic acceptance on this workload's trees: fp32 target and
+    # draft rows over `vocab` tokens, drafts drawn from the draft rows
+    stochastic = None
+    if rank == 0:
+        sin = workloads.stochastic_inputs(base, vocab, seed=41)
+        cu = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+        sp = {k: cu(v) for k, v in sin.items()}
+        sd = tv.DeviceBatch(base, device=dev)
+        slen = torch.empty(base.B, dtype=torch.int32, device=dev)
+        spath = torch.empty((base.B, base.max_depth), dtype=torch.int32, device=dev)
+        sbon = torch.empty(base.B, dtype=torch.int32, device=dev)
+
+        def stoch():
+            tv.tv_accept_stochastic(base.B, base.T, base.max_nodes, base.max_depth, vocab,
+                                    sd.node_offsets, sd.parent, sp["draft"], sp["root_p"],
+                                    sp["node_p"], sp["root_q"], sp["node_q"], sp["u_accept"],
+                                    sp["u_bonus"], slen, spath, sbon, sd.status, stream)
+        with torch.cuda.stream(stream):
+            sd.status.zero_()
+            for _ in range(3):
+                stoch()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(20):
+                stoch()
+            e1.record(stream)
+        e1.synchronize()
+        if int(sd.status[0].item()) != 0:
+            raise SystemExit("device status %d in stochastic acceptance" % int(sd.status[0].item()))
+        stochastic = {"call": "tv_accept_stochastic", "vocab": vocab,
+                      "launch_us": e0.elapsed_time(e1) * 1e3 / 20,
+                      "mean_accept_len": float(slen.float().mean().item()),
+                      "rows_fp32_mb": (base.B + base.T) * vocab * 8 / 1e6}
+        del sp, sd
+
     # ---------------- roofline of the dominant kernel of the step
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
@@ -684,6 +720,7 @@ def run_ours(args, world, rank, local):
                           "workspace" % (serial_bytes // 2 ** 20)}
                 if t_ser is not None else None),
             "tree_builder": builder,
+            "stochastic_accept": stochastic,
             "accept_from_logits": {
                 "call": "tv_accept_greedy_logits", "vocab": vocab,
                 "bytes_per_launch": al_bytes, "launch_us": t_al / K * 1e6,

@@ -9,8 +9,10 @@ The arithmetic lives in ``oracle.c`` (plain C, double precision): the naive
 serial tree walk that materialises one state matrix per draft node (Bole
 summary page, "Core techniques" §1-§2 and the naive baseline it compares
 against), the greedy acceptance walk (LLM Primer VI ch. 9, §9.1) and the
-commit of the accepted path's state (Bole §2).  This file only builds the C
-source, marshals arrays and splits work over threads.
+commit of the accepted path's state (Bole §2).  This file builds the C source,
+marshals arrays and splits work over threads; the functions for the wider rows
+of the path are plain numpy here: the argmax of logits rows, best-first tree
+construction, stochastic acceptance and tree-masked softmax attention.
 
 Parity pins for each function are in ``tests/test_oracle_pins.py``.
 """
@@ -396,6 +398,63 @@ def accept_stochastic(batch, root_p, node_p, root_q, node_q, u_accept, u_bonus,
     if with_margin:
         return ln, path, bonus, margin
     return ln, path, bonus
+
+
+def tree_attention(node_offsets, parent, q, k_cache, v_cache, ctx_len, k_tree, v_tree,
+                   scale: float):
+    """Softmax attention of one layer over draft trees with the tree mask -- the
+    attention half of a hybrid model's verification pass.
+
+    Pages: the target verifies all candidates in one forward pass over the prefix
+    followed by the candidates (LLM Primer VI ch. 9, §9.1); a candidate tree is
+    verified in one attention pass with a custom mask (§9.2); every branch shares
+    the prefix's KV and adds only its own (Bole summary page, "Why existing tree
+    speculation fails on hybrid models").  Reading: node i of request b, query head
+    h, sees the b's first ctx_len[b] cached positions of KV head h // (H / Hkv) and
+    the tree nodes on its own root path, itself included:
+        o[i, h] = sum_j softmax_j(scale * q[i, h] . k_j) v_j.
+    Shapes: q [T][H][d]; k_cache, v_cache [B][Hkv][P][d]; ctx_len [B];
+    k_tree, v_tree [T][Hkv][d]; node_offsets [B+1]; parent [T] local to the request
+    (-1 = child of the context, parents precede children).  fp64; returns [T][H][d].
+    The mask is written out as a full 0/1 matrix and the softmax takes the row
+    maximum out before exponentiating (exact in real arithmetic)."""
+    q = np.asarray(q, dtype=np.float64)
+    kc = np.asarray(k_cache, dtype=np.float64)
+    vc = np.asarray(v_cache, dtype=np.float64)
+    kt = np.asarray(k_tree, dtype=np.float64)
+    vt = np.asarray(v_tree, dtype=np.float64)
+    T, H, d = q.shape
+    B, Hkv = kc.shape[0], kc.shape[1]
+    if H % Hkv:
+        raise OracleError("query heads must be a multiple of KV heads")
+    grp = H // Hkv
+    out = np.zeros((T, H, d), dtype=np.float64)
+    for b in range(B):
+        s, e = int(node_offsets[b]), int(node_offsets[b + 1])
+        n, L = e - s, int(ctx_len[b])
+        if n == 0:
+            continue
+        # anc[i, j] = 1 iff node j is on node i's root path (i included)
+        anc = np.zeros((n, n), dtype=bool)
+        for i in range(n):
+            j = i
+            while j >= 0:
+                if j > i or int(parent[s + j]) >= j:
+                    raise OracleError("parents must precede children")
+                anc[i, j] = True
+                j = int(parent[s + j])
+        visible = np.concatenate([np.ones((n, L), dtype=bool), anc], axis=1)
+        for h in range(H):
+            kv = h // grp
+            K = np.concatenate([kc[b, kv, :L], kt[s:e, kv]], axis=0)
+            V = np.concatenate([vc[b, kv, :L], vt[s:e, kv]], axis=0)
+            S = scale * (q[s:e, h] @ K.T)
+            S = np.where(visible, S, -np.inf)
+            S = S - S.max(axis=1, keepdims=True)
+            W = np.exp(S)
+            W = W / W.sum(axis=1, keepdims=True)
+            out[s:e, h] = W @ V
+    return out
 
 
 def commit(batch, accept_len, path, units: Optional[Sequence[int]] = None, threads: int = 1,

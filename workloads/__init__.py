@@ -449,6 +449,57 @@ def stochastic_inputs(batch: Batch, vocab: int, seed: Optional[int] = None,
                 u_accept=rng.random(batch.T), u_bonus=rng.random(batch.B))
 
 
+def attention_inputs(batch: Batch, H: int, Hkv: int, d: int, ctx_len: Sequence[int],
+                     P: Optional[int] = None, seed: Optional[int] = None, spike: float = 0.0,
+                     tail_nan: bool = False, widen: bool = True):
+    """Inputs of one attention layer over `batch`'s draft trees (its tree only; its
+    linear-layer factors are not used): queries q [T][H][d], the shared-prefix KV
+    cache k_cache, v_cache [B][Hkv][P][d] with ctx_len[b] valid positions, and the
+    tree nodes' own keys and values k_tree, v_tree [T][Hkv][d].  Every value is
+    N(0, 1) rounded to bf16 (uint16 bits; the "_f32" entries are the exact widened
+    values), so scale * q.k with scale = 1/sqrt(d) is about N(0, 1).
+    spike > 0: one cached key in 64 per (request, KV head) is replaced by
+    spike * (the mean of the group's first query head over the request's nodes) /
+    |that mean| * sqrt(d), giving scores of about +-spike that make the row maximum
+    jump between key tiles.  tail_nan: cache positions at and beyond ctx_len hold
+    NaN (they must not be read into the result).  widen=False leaves out the
+    "_f32" entries."""
+    rng = np.random.default_rng(0 if seed is None else seed)
+    B, T = batch.B, batch.T
+    ctx = np.asarray(ctx_len, dtype=np.int32).reshape(B)
+    P = int(max(1, ctx.max() if B else 1)) if P is None else int(P)
+    if B and int(ctx.max()) > P:
+        raise ValueError("ctx_len exceeds the cache capacity P")
+    q = rng.standard_normal((T, H, d)).astype(np.float32)
+    kc = rng.standard_normal((B, Hkv, P, d)).astype(np.float32)
+    vc = rng.standard_normal((B, Hkv, P, d)).astype(np.float32)
+    kt = rng.standard_normal((T, Hkv, d)).astype(np.float32)
+    vt = rng.standard_normal((T, Hkv, d)).astype(np.float32)
+    grp = H // Hkv
+    if spike > 0:
+        for b in range(B):
+            s, e = int(batch.node_offsets[b]), int(batch.node_offsets[b + 1])
+            if e == s or ctx[b] == 0:
+                continue
+            for kv in range(Hkv):
+                m = q[s:e, kv * grp].astype(np.float64).mean(axis=0)
+                m = m / max(np.linalg.norm(m), 1e-30) * np.sqrt(d) * spike
+                pos = rng.choice(int(ctx[b]), size=max(1, int(ctx[b]) // 64), replace=False)
+                sign = np.where(rng.random(len(pos)) < 0.5, -1.0, 1.0)
+                kc[b, kv, pos] = (sign[:, None] * m[None, :]).astype(np.float32)
+    if tail_nan:
+        for b in range(B):
+            kc[b, :, int(ctx[b]):] = np.nan
+            vc[b, :, int(ctx[b]):] = np.nan
+    out = dict(ctx_len=ctx, scale=float(1.0 / np.sqrt(d)))
+    for name, a in (("q", q), ("k_cache", kc), ("v_cache", vc), ("k_tree", kt), ("v_tree", vt)):
+        bits = f32_to_bf16_bits(a)
+        out[name] = bits
+        if widen:
+            out[name + "_f32"] = bf16_bits_to_f32(bits)
+    return out
+
+
 def random_batch(rng, sizes: Sequence[int], H: int, dk: int, dv: int, *, decay="scalar",
                  qkv_dtype="bf16", g_kind=None, depth_cap: int = 32, vocab: int = 4,
                  h0_std: float = 0.05, max_depth: Optional[int] = None,
