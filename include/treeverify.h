@@ -401,6 +401,60 @@ tv_status tv_commit_verify(const tv_problem *p, const tv_pending *pend, float *H
                            int32_t *dev_status, void *stream);
 
 /*
+ * tv_tree_attention -- softmax attention of one attention layer over every
+ * request's draft tree, the attention layers' share of the verification pass of a
+ * hybrid model.  LLM Primer VI ch. 9: the target runs one forward pass over the
+ * prefix followed by the candidates (§9.1) and checks a candidate tree in one
+ * attention pass with a custom mask (§9.2); Bole summary page ("Why existing tree
+ * speculation fails on hybrid models"): all branches share the prefix's KV and each
+ * adds only its own.  Query row (node i of request b, head h) sees the first
+ * ctx_len[b] cached positions of KV head h / (H / Hkv) and the tree nodes on i's
+ * root path, i included:
+ *     out[i][h] = sum_j softmax_j(scale * q[i][h] . k_j) v_j.
+ *
+ *   B, total_nodes (T), max_nodes   as in tv_problem (max_nodes <= TV_MAX_NODES)
+ *   H, Hkv     query heads and KV heads; H / Hkv a power of two <= 128
+ *   d          head dimension, 64 or 128
+ *   P          positions per (request, KV head) in the cache (capacity), >= 1
+ *   node_offsets [B+1], parent [T]   the trees, as in tv_verify (parents precede
+ *              children; depth is not needed)
+ *   ctx_len    [B] int32 (device): valid cached positions of each request, <= P
+ *   q          [T][H][d] bf16
+ *   k_cache, v_cache  [B][Hkv][P][d] bf16; positions >= ctx_len[b] are never read
+ *              into the result (they may hold anything, NaN included)
+ *   k_tree, v_tree    [T][Hkv][d] bf16: the tree nodes' own keys and values
+ *   scale      softmax scale, positive and finite; usually 1/sqrt(d)
+ *   out        [T][H][d] fp32
+ *   workspace  optional device memory (16-byte aligned, caller-owned scratch) for
+ *              partial results when the context is split over several CTAs, which
+ *              the library does when B * Hkv * ceil(max_nodes * H / Hkv / 128) is
+ *              below half the SM count.  tv_tree_attention_workspace_bytes gives
+ *              the size that allows the library's preferred split; with less (or
+ *              NULL, 0) it splits less (not at all with NULL).  Results do not
+ *              depend on the split beyond fp32 rounding.
+ *   dev_status, stream   see conventions
+ * Arithmetic: bf16 inputs, fp32 scores and accumulation on tensor cores; the
+ * softmax weights enter the weighted sum of values as bf16 (relative rounding
+ * 2^-9), so outputs carry a relative error of order 2^-9.
+ * Host errors: TV_ERR_NULL, TV_ERR_ALIGN as usual; TV_ERR_SHAPE for sizes out of
+ * range (H not a multiple of Hkv, T > B * max_nodes, P < 1, scale not positive and
+ * finite);
+ * TV_ERR_UNSUPPORTED for d not in {64, 128}, H / Hkv not a power of two <= 128 or
+ * max_nodes > TV_MAX_NODES.  Device-detected errors: bad offsets or parents give
+ * TV_ERR_TREE (rows of a request with a bad tree are written as zeros; requests
+ * whose offsets are unusable are left untouched); ctx_len[b] outside [0, P] gives
+ * TV_ERR_SHAPE and zero rows for that request.
+ */
+size_t tv_tree_attention_workspace_bytes(int32_t B, int32_t total_nodes, int32_t max_nodes,
+                                         int32_t H, int32_t Hkv, int32_t d, int32_t P);
+tv_status tv_tree_attention(int32_t B, int32_t total_nodes, int32_t max_nodes, int32_t H,
+                            int32_t Hkv, int32_t d, int32_t P, const int32_t *node_offsets,
+                            const int32_t *parent, const int32_t *ctx_len, const void *q,
+                            const void *k_cache, const void *v_cache, const void *k_tree,
+                            const void *v_tree, float scale, float *out, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
  * tv_verify_variant -- the kernel tv_verify (TV_VARIANT_AUTO) would launch for
  * this problem: TV_VARIANT_TC_STREAM, TV_VARIANT_TC or TV_VARIANT_SIMT.  Reads
  * only the sizes and kinds in *p (no device memory; the current device's SM count

@@ -276,6 +276,34 @@ def test_accept_stochastic_rejects_bad_arguments(lib):
     assert rc(B=0, T=0) == tv.TV_OK
 
 
+def test_tree_attention_rejects_bad_arguments(lib):
+    def rc(**kw):
+        a = dict(B=2, T=5, mn=4, H=8, Hkv=2, d=128, P_=64, offs=P[0], par=P[1], ctx=P[2], q=P[3],
+                 kc=P[4], vc=P[5], kt=P[6], vt=P[7], scale=0.1, out=P[8], ws=None, wsb=0,
+                 st=P[9])
+        a.update(kw)
+        return tv.tv_tree_attention(a["B"], a["T"], a["mn"], a["H"], a["Hkv"], a["d"], a["P_"],
+                                    a["offs"], a["par"], a["ctx"], a["q"], a["kc"], a["vc"],
+                                    a["kt"], a["vt"], a["scale"], a["out"], a["ws"], a["wsb"],
+                                    a["st"], stream=0, check=False)
+    assert rc(H=6, Hkv=4) == tv.TV_ERR_SHAPE         # H not a multiple of Hkv
+    assert rc(H=6, Hkv=2) == tv.TV_ERR_UNSUPPORTED   # a group of 3 query heads
+    assert rc(d=96) == tv.TV_ERR_UNSUPPORTED
+    assert rc(mn=300) == tv.TV_ERR_UNSUPPORTED
+    assert rc(T=9) == tv.TV_ERR_SHAPE                # T > B * max_nodes
+    assert rc(P_=0) == tv.TV_ERR_SHAPE
+    assert rc(scale=float("nan")) == tv.TV_ERR_SHAPE
+    assert rc(scale=float("inf")) == tv.TV_ERR_SHAPE
+    assert rc(scale=0.0) == tv.TV_ERR_SHAPE
+    assert rc(scale=-0.1) == tv.TV_ERR_SHAPE
+    assert rc(q=None) == tv.TV_ERR_NULL
+    assert rc(ctx=None) == tv.TV_ERR_NULL
+    assert rc(kt=P[6] + 4) == tv.TV_ERR_ALIGN
+    assert rc(ws=P[10] + 8, wsb=1024) == tv.TV_ERR_ALIGN
+    assert rc(B=0, T=0) == tv.TV_OK
+    assert rc(T=0, par=None, q=None, kt=None, vt=None, out=None) == tv.TV_OK
+
+
 def test_build_tree_rejects_bad_arguments(lib):
     def rc(**kw):
         a = dict(B=2, C=8, cap=8, n=64, m=P[0], cost=None, par=P[1], tok=P[2], rho=P[3], cnt=P[4])

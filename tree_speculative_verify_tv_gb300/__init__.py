@@ -10,6 +10,8 @@ include/treeverify.h; this package is the ctypes binding):
 * ``tv_accept_greedy_logits`` the target argmax from its logits and the walk
 * ``tv_build_tree``     draft trees by best-first expansion of path scores
 * ``tv_accept_stochastic`` acceptance by min(1, p/q) with residual resampling
+* ``tv_tree_attention`` tree-masked softmax attention over a shared-prefix KV cache
+  (the attention layers of a hybrid model)
 * ``tv_verify_serial``  the naive node-by-node verification with per-node states
   (a baseline for the closed form)
 * ``tv_commit_verify`` the previous step's commit applied to the state in place,
@@ -22,7 +24,7 @@ from .binding import (  # noqa: F401
     DeviceBatch, TVError, load, make_pending, make_problem, status_string, tv_accept_commit,
     tv_accept_greedy, tv_accept_greedy_logits, tv_commit, tv_commit_verify, tv_pending,
     tv_verify_serial, tv_verify_serial_workspace_bytes, tv_verify_serial_static, tv_build_tree,
-    tv_accept_stochastic,
+    tv_accept_stochastic, tv_tree_attention, tv_tree_attention_workspace_bytes,
     TV_SERIAL_STATIC_BYTES,
     tv_problem, tv_status_string, tv_verify, tv_verify_variant, tv_version, EXPORTED,
     TV_OK, TV_ERR_NULL, TV_ERR_SHAPE, TV_ERR_DTYPE, TV_ERR_ALIGN, TV_ERR_UNSUPPORTED,

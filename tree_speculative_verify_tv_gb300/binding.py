@@ -30,7 +30,7 @@ TV_SERIAL_STATIC_BYTES = 16 << 20
 EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
             "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_verify_serial",
             "tv_verify_serial_workspace_bytes", "tv_verify_serial_static", "tv_build_tree",
-            "tv_accept_stochastic",
+            "tv_accept_stochastic", "tv_tree_attention", "tv_tree_attention_workspace_bytes",
             "tv_status_string", "tv_version")
 
 
@@ -86,12 +86,16 @@ def load(path: Optional[str] = None):
         L.tv_verify_serial_static.argtypes = [P] + [vp] * 8
         L.tv_build_tree.argtypes = [i32] * 4 + [vp] * 7
         L.tv_accept_stochastic.argtypes = [i32] * 5 + [vp] * 14
+        L.tv_tree_attention.argtypes = ([i32] * 7 + [vp] * 8 + [ctypes.c_float, vp, vp,
+                                                                ctypes.c_size_t, vp, vp])
+        L.tv_tree_attention_workspace_bytes.argtypes = [i32] * 7
+        L.tv_tree_attention_workspace_bytes.restype = ctypes.c_size_t
         L.tv_verify_serial_workspace_bytes.argtypes = [P]
         L.tv_verify_serial_workspace_bytes.restype = ctypes.c_size_t
         for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit,
                   L.tv_accept_commit, L.tv_commit_verify, L.tv_accept_greedy_logits,
                   L.tv_verify_serial, L.tv_verify_serial_static, L.tv_build_tree,
-                  L.tv_accept_stochastic):
+                  L.tv_accept_stochastic, L.tv_tree_attention):
             f.restype = ctypes.c_int32
         L.tv_status_string.argtypes = [i32]
         L.tv_status_string.restype = ctypes.c_char_p
@@ -190,6 +194,22 @@ def tv_accept_stochastic(B, total_nodes, max_nodes, max_depth, vocab, node_offse
                                      _ptr(accept_len), _ptr(path), _ptr(bonus), _ptr(dev_status),
                                      _stream(stream))
     return _check(rc, "tv_accept_stochastic", check)
+
+
+def tv_tree_attention_workspace_bytes(B, total_nodes, max_nodes, H, Hkv, d, P) -> int:
+    return int(load().tv_tree_attention_workspace_bytes(int(B), int(total_nodes), int(max_nodes),
+                                                        int(H), int(Hkv), int(d), int(P)))
+
+
+def tv_tree_attention(B, total_nodes, max_nodes, H, Hkv, d, P, node_offsets, parent, ctx_len, q,
+                      k_cache, v_cache, k_tree, v_tree, scale, out, workspace=None,
+                      workspace_bytes=0, dev_status=None, stream=None, check: bool = True) -> int:
+    rc = load().tv_tree_attention(int(B), int(total_nodes), int(max_nodes), int(H), int(Hkv),
+                                  int(d), int(P), _ptr(node_offsets), _ptr(parent), _ptr(ctx_len),
+                                  _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_tree),
+                                  _ptr(v_tree), float(scale), _ptr(out), _ptr(workspace),
+                                  int(workspace_bytes), _ptr(dev_status), _stream(stream))
+    return _check(rc, "tv_tree_attention", check)
 
 
 def tv_build_tree(B, C, depth_cap, n, marginals, cost, parent, token, rho, count, stream=None,

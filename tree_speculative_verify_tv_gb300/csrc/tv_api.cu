@@ -247,6 +247,66 @@ tv_status tv_accept_stochastic(int32_t B, int32_t total_nodes, int32_t max_nodes
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+tv_status attn_dims(int32_t B, int32_t T, int32_t max_nodes, int32_t H, int32_t Hkv, int32_t d,
+                    int32_t P) {
+    if (B < 0 || T < 0 || max_nodes < 1 || H < 1 || Hkv < 1 || P < 1 || d < 1) return TV_ERR_SHAPE;
+    if (H % Hkv) return TV_ERR_SHAPE;
+    if ((int64_t)T > (int64_t)B * max_nodes) return TV_ERR_SHAPE;
+    const int32_t grp = H / Hkv;
+    if (d != 64 && d != 128) return TV_ERR_UNSUPPORTED;
+    if (grp > 128 || (grp & (grp - 1))) return TV_ERR_UNSUPPORTED;
+    if (max_nodes > TV_MAX_NODES) return TV_ERR_UNSUPPORTED;
+    if ((int64_t)B * Hkv * P > 0x7fffffffLL || (int64_t)T * H > 0x7fffffffLL)
+        return TV_ERR_UNSUPPORTED;
+    return TV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tv_tree_attention_workspace_bytes(int32_t B, int32_t total_nodes, int32_t max_nodes,
+                                         int32_t H, int32_t Hkv, int32_t d, int32_t P) {
+    if (attn_dims(B, total_nodes, max_nodes, H, Hkv, d, P) != TV_OK || B == 0) return 0;
+    tv::AttnArgs a{};
+    a.B = B;
+    a.T = total_nodes;
+    a.max_nodes = max_nodes;
+    a.H = H;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.P = P;
+    return tv::tree_attention_workspace_bytes(a);
+}
+
+tv_status tv_tree_attention(int32_t B, int32_t total_nodes, int32_t max_nodes, int32_t H,
+                            int32_t Hkv, int32_t d, int32_t P, const int32_t *node_offsets,
+                            const int32_t *parent, const int32_t *ctx_len, const void *q,
+                            const void *k_cache, const void *v_cache, const void *k_tree,
+                            const void *v_tree, float scale, float *out, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    tv_status st = attn_dims(B, total_nodes, max_nodes, H, Hkv, d, P);
+    if (st != TV_OK) return st;
+    if (!(scale > 0.f) || scale > 3.0e38f) return TV_ERR_SHAPE;  // positive and finite
+    if (!node_offsets || !ctx_len || !k_cache || !v_cache || !dev_status) return TV_ERR_NULL;
+    if (total_nodes > 0 && (!parent || !q || !k_tree || !v_tree || !out)) return TV_ERR_NULL;
+    if (B == 0 || total_nodes == 0) return TV_OK;
+    st = check_ptrs({node_offsets, parent, ctx_len, q, k_cache, v_cache, k_tree, v_tree, out,
+                     dev_status});
+    if (st != TV_OK) return st;
+    if (workspace && !aligned16(workspace)) return TV_ERR_ALIGN;
+    tv::AttnArgs a{B, total_nodes, max_nodes, H, Hkv, d, P, node_offsets, parent, ctx_len,
+                   q, k_cache, v_cache, k_tree, v_tree, scale, out,
+                   static_cast<float *>(workspace), workspace ? workspace_bytes : 0, dev_status};
+    cudaError_t e = tv::launch_tree_attention(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return TV_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 tv_status tv_build_tree(int32_t B, int32_t C, int32_t depth_cap, int32_t n,
                         const double *marginals, const double *cost, int32_t *parent,
                         int32_t *token, double *rho, int32_t *count, void *stream) {

@@ -53,6 +53,21 @@ struct StochArgs {
 };
 cudaError_t launch_accept_stochastic(const StochArgs &a, cudaStream_t s);
 
+// Tree-masked softmax attention over a shared-prefix KV cache (tv_tree_attention).
+struct AttnArgs {
+    int32_t B, T, max_nodes, H, Hkv, d, P;
+    const int32_t *node_offsets, *parent, *ctx_len;
+    const void *q, *k_cache, *v_cache, *k_tree, *v_tree;  // bf16
+    float scale;
+    float *out;
+    float *ws;        // split partials (may be null)
+    size_t ws_bytes;
+    int32_t *status;
+};
+// Workspace bytes for the context split the library would pick with room for it.
+size_t tree_attention_workspace_bytes(const AttnArgs &a);
+cudaError_t launch_tree_attention(const AttnArgs &a, cudaStream_t s);
+
 // Best-first draft-tree construction (tv_build_tree).
 struct BuildArgs {
     int32_t B, C, depth_cap, n;
