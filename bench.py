@@ -52,11 +52,15 @@ WORKLOADS = {
         "per-channel decay, 256-node best-first trees (depth <= 16, Dirichlet(0.2))"),
 }
 WORKLOAD = WORKLOADS[2]
-KERNEL_SOURCES = ["tree_speculative_verify_tv_gb300/csrc/verify_tc.cu",
-                  "tree_speculative_verify_tv_gb300/csrc/verify_tc_stream.cu",
-                  "tree_speculative_verify_tv_gb300/csrc/tc_common.cuh",
-                  "tree_speculative_verify_tv_gb300/csrc/tc_ptx.cuh",
-                  "tree_speculative_verify_tv_gb300/csrc/tv_internal.cuh"]
+_CS = "tree_speculative_verify_tv_gb300/csrc/"
+# sources behind each kernel whose DRAM traffic was captured with ncu
+TRAFFIC_SOURCES = {
+    "verify": [_CS + f for f in ("verify_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
+    "commit_verify": [_CS + f for f in ("verify_tc.cu", "tc_common.cuh", "tc_ptx.cuh",
+                                        "tv_internal.cuh")],
+    "tree_attention": [_CS + f for f in ("tree_attention.cu", "tc_common.cuh", "tc_ptx.cuh",
+                                         "tv_internal.cuh")],
+}
 KERNEL_NAMES = {1: "simt", 2: "tcgen05 one unit per CTA", 3: "tcgen05 streaming"}
 
 
@@ -84,6 +88,12 @@ def parse():
     ap.add_argument("--pipeline", default="fused", choices=["fused", "separate"],
                     help="step as tv_commit_verify + tv_accept_greedy (fused) or as "
                          "tv_verify + tv_accept_commit (separate)")
+    ap.add_argument("--attention-ctx", type=int, default=4096,
+                    help="shared-prefix positions per request for the tree-attention line "
+                         "(0 = skip it)")
+    ap.add_argument("--profile-attention", action="store_true",
+                    help="profiling aid: only run 3 tree-attention launches of the attention "
+                         "workload, then exit")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
                     help="workload (default 2: the configuration the HBM target is quoted on)")
     args = ap.parse_args()
@@ -136,9 +146,9 @@ def commit_bytes(b, lens) -> int:
     return b.B * b.H * 8 * b.dk * b.dv + L * b.H * (b.dk * qk + b.dv * qk + g)
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(name: str) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in TRAFFIC_SOURCES[name]:
         fp = os.path.join(ROOT, p)
         if os.path.exists(fp):
             h.update(open(fp, "rb").read())
@@ -147,7 +157,7 @@ def kernel_source_hash() -> str:
 
 def recorded_traffic(name: str):
     """Per-launch DRAM bytes of a kernel on the config-2 workload from the committed
-    ncu summary profiles/<name>_c2_dram_traffic.txt, valid only while the kernel
+    ncu summary profiles/<name>_c2_dram_traffic.txt, valid only while the kernel's
     sources are unchanged since the capture."""
     fp = os.path.join(ROOT, "profiles", "%s_c2_dram_traffic.txt" % name)
     if not os.path.exists(fp):
@@ -157,7 +167,7 @@ def recorded_traffic(name: str):
         if "=" in line and not line.startswith("#"):
             k, _, v = line.partition("=")
             vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_hash") != kernel_source_hash():
+    if vals.get("kernel_source_hash") != kernel_source_hash(name):
         return None
     try:
         return int(vals["dram_bytes_per_launch"])
@@ -367,6 +377,52 @@ def run_reference(args, world, rank):
 
 
 # ---------------------------------------------------------------- GPU arm
+
+
+ATTN_H, ATTN_HKV, ATTN_D = 32, 8, 128
+
+
+def attention_setup(base, ctx, dev, stream):
+    """The attention layers' share of the verification pass on `base`'s trees: 32 query
+    heads over 8 KV heads, d = 128, a `ctx`-position shared prefix per request (bf16
+    cache, seeded N(0, 1) values).  Returns (tree_call, decode_call, bytes_tree,
+    bytes_decode, flops_tree, status); decode_call runs the same cache with one query
+    node per request (the first node of its tree), as a plain decoding step would."""
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    import workloads
+    B, T, H, Hkv, d = base.B, base.T, ATTN_H, ATTN_HKV, ATTN_D
+    ai = workloads.attention_inputs(base, H, Hkv, d, [ctx] * B, P=ctx, seed=51, widen=False)
+    cu = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    kc, vc = cu(ai["k_cache"]), cu(ai["v_cache"])
+    del ai["k_cache"], ai["v_cache"]
+    q, kt, vt, cl = cu(ai["q"]), cu(ai["k_tree"]), cu(ai["v_tree"]), cu(ai["ctx_len"])
+    offs, par = cu(base.node_offsets), cu(base.parent)
+    first = base.node_offsets[:-1].astype(np.int64)
+    q1, kt1, vt1 = cu(ai["q"][first]), cu(ai["k_tree"][first]), cu(ai["v_tree"][first])
+    offs1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    par1 = torch.full((B,), -1, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty((T, H, d), dtype=torch.float32, device=dev)
+    out1 = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+
+    def make(Tn, maxn, o, p, qq, ktt, vtt, oo):
+        wsb = tv.tv_tree_attention_workspace_bytes(B, Tn, maxn, H, Hkv, d, ctx)
+        ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device=dev) if wsb else None
+
+        def call():
+            tv.tv_tree_attention(B, Tn, maxn, H, Hkv, d, ctx, o, p, cl, qq, kc, vc, ktt, vtt,
+                                 ai["scale"], oo, ws, wsb, status, stream)
+        return call
+
+    tree_call = make(T, base.max_nodes, offs, par, q, kt, vt, out)
+    dec_call = make(B, 1, offs1, par1, q1, kt1, vt1, out1)
+    cache = 2 * B * Hkv * ctx * d * 2
+    side = lambda Tn: Tn * H * d * 2 + 2 * Tn * Hkv * d * 2 + Tn * H * d * 4 + 8 * Tn + 8 * B
+    # scores and weighted values over every visible key of every query row
+    path = int(np.asarray(base.depth, dtype=np.int64).sum())
+    flops = 4 * H * d * (T * ctx + path)
+    return tree_call, dec_call, cache + side(T), cache + side(B), flops, status
 
 
 def run_ours(args, world, rank, local):
@@ -639,6 +695,53 @@ def run_ours(args, world, rank, local):
                       "rows_fp32_mb": (base.B + base.T) * vocab * 8 / 1e6}
         del sp, sd
 
+    # ---------------- tree-masked softmax attention (the hybrid target's attention
+    # layers) on this workload's trees, and the same cache with one query per request
+    attention = None
+    if rank == 0 and args.attention_ctx > 0:
+        tcall, dcall, ab, db, aflops, ast = attention_setup(base, args.attention_ctx, dev, stream)
+
+        def time_calls(call, KA=20):
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    call()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(KA):
+                    call()
+            with torch.cuda.stream(stream):
+                g.replay()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1) * 1e-3 / KA
+
+        t_at = time_calls(tcall)
+        t_dec = time_calls(dcall)
+        if int(ast[0].item()) != 0:
+            raise SystemExit("device status %d in tree attention" % int(ast[0].item()))
+        hbm = float(measured_peaks()[0].get("hbm_gbs", 6800.0))
+        attention = {
+            "call": "tv_tree_attention",
+            "workload": "%d requests x config-2 trees (%d nodes), %d query heads over %d KV "
+                        "heads, d=%d, %d-position shared prefix, bf16" % (
+                            base.B, base.T, ATTN_H, ATTN_HKV, ATTN_D, args.attention_ctx),
+            "launch_us": t_at * 1e6, "bytes_per_launch": ab, "gbs": ab / t_at / 1e9,
+            "roofline": {"bound": "hbm", "achieved": ab / t_at / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": ab / t_at / 1e9 / hbm,
+                         "traffic": recorded_traffic("tree_attention")},
+            "tensor_tflops": aflops / t_at / 1e12,
+            "decode_us": t_dec * 1e6, "decode_gbs": db / t_dec / 1e9,
+            "tree_over_decode": t_at / t_dec,
+            "l2": "the %d MB cache is over twice the L2; launches replay back to back"
+                  % (ab // 2 ** 20)}
+        del tcall, dcall
+        torch.cuda.empty_cache()
+
     # ---------------- roofline of the dominant kernel of the step
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
@@ -721,6 +824,7 @@ def run_ours(args, world, rank, local):
                 if t_ser is not None else None),
             "tree_builder": builder,
             "stochastic_accept": stochastic,
+            "tree_attention": attention,
             "accept_from_logits": {
                 "call": "tv_accept_greedy_logits", "vocab": vocab,
                 "bytes_per_launch": al_bytes, "launch_us": t_al / K * 1e6,
@@ -811,8 +915,31 @@ def profile_folded(args):
         raise SystemExit("device status %d" % st)
 
 
+def profile_attention(args):
+    """Three tree-attention launches of the attention workload (for ncu captures)."""
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    import workloads
+    tv.build()
+    tv.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    tcall, _, _, _, _, st = attention_setup(workloads.make_config(args.config, seed=1000 + args.config
+                                                                  ), args.attention_ctx, dev,
+                                            stream)
+    for _ in range(3):
+        tcall()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_attention": args.attention_ctx, "status": int(st[0].item())}))
+    if int(st[0].item()) != 0:
+        raise SystemExit("device status %d" % int(st[0].item()))
+
+
 def main():
     args = parse()
+    if args.profile_attention:
+        profile_attention(args)
+        return
     if args.profile_folded is not None:
         profile_folded(args)
         return

@@ -72,6 +72,18 @@ def test_ragged_trees_and_vocabularies(V, noise):
     check(b, V, seed=V + 1, draft_noise=noise)
 
 
+@pytest.mark.parametrize("V,noise,seed", [(50, 3.0, 11), (32000, 4.0, 12)])
+def test_wide_trees_many_rejections(V, noise, seed):
+    # twelve children of the context and eight of node 0: up to twelve rejections in a
+    # row at one node, each a new residual
+    sizes = [20, 20, 20, 20]
+    b = workloads.random_batch(np.random.default_rng(seed), sizes, 1, 16, 16, decay="scalar",
+                               depth_cap=4, max_depth=4)
+    par = np.concatenate([[-1] * 12 + [0] * 8] * len(sizes)).astype(np.int32)
+    b = dataclasses.replace(b, parent=par, depth=np.where(par < 0, 1, 2).astype(np.int32))
+    check(b, V, seed=seed + 100, draft_noise=noise)
+
+
 def test_empty_trees():
     # no draft nodes at all: every bonus is a draw from the root's target row
     b = workloads.random_batch(np.random.default_rng(8), [0, 0, 0], 1, 16, 16, decay="scalar",

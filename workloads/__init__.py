@@ -33,12 +33,17 @@ import numpy as np
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to bfloat16 (nearest, ties to even); return the bits."""
+    """Round float32 values to bfloat16 (nearest, ties to even); return the bits.
+    A NaN stays a NaN (quiet, same sign)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    lsb = (u >> np.uint64(16)) & np.uint64(1)
-    r = (u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
-    return r.astype(np.uint16)
+    u = x.view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    with np.errstate(over="ignore"):
+        r = ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        r[nan] = ((u[nan] >> np.uint32(16)) | np.uint32(0x0040)).astype(np.uint16)
+    return r
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -470,11 +475,12 @@ def attention_inputs(batch: Batch, H: int, Hkv: int, d: int, ctx_len: Sequence[i
     P = int(max(1, ctx.max() if B else 1)) if P is None else int(P)
     if B and int(ctx.max()) > P:
         raise ValueError("ctx_len exceeds the cache capacity P")
-    q = rng.standard_normal((T, H, d)).astype(np.float32)
-    kc = rng.standard_normal((B, Hkv, P, d)).astype(np.float32)
-    vc = rng.standard_normal((B, Hkv, P, d)).astype(np.float32)
-    kt = rng.standard_normal((T, Hkv, d)).astype(np.float32)
-    vt = rng.standard_normal((T, Hkv, d)).astype(np.float32)
+    draw = lambda shape: rng.standard_normal(shape, dtype=np.float32)
+    q = draw((T, H, d))
+    kc = draw((B, Hkv, P, d))
+    vc = draw((B, Hkv, P, d))
+    kt = draw((T, Hkv, d))
+    vt = draw((T, Hkv, d))
     grp = H // Hkv
     if spike > 0:
         for b in range(B):
