@@ -11,14 +11,18 @@
 // residual by inverse CDF with the request's uniform.  The acceptance test for child c
 // is u_accept[c] * q(x) < p(x).  The uniforms are inputs.
 //
-// One CTA of 1024 threads per request.  Every sibling of a node is tested against the
+// One cluster of 8 CTAs (256 threads each) per request; CTA r owns the r-th eighth
+// of every probability row.  Every sibling of a node is tested against the
 // same q, so the residual after any number of rejections has a closed form:
 //     p_k(y) = max(p(y) - a_k q(y), 0) / b_k,   a_0 = 0, b_0 = 1,
 // and a rejection gives a_{k+1} = a_k + b_k, b_{k+1} = T = sum_y max(p(y) - a_{k+1} q(y), 0)
 // (= b_k Z_{k+1}; a zero sum leaves (a, b) unchanged).  By induction: where
 // p - a_k q <= 0 the next residual is 0 as well, elsewhere max(p_k - q, 0) / Z_{k+1} =
 // max(p - (a_k + b_k) q, 0) / (b_k Z_{k+1}).  So a rejection costs one pass over the
-// row and no scratch memory.
+// row and no scratch memory.  A pass adds its slice in every CTA, the eight slice
+// sums are exchanged through distributed shared memory, and every CTA adds them in
+// rank order, so all CTAs hold bit-identical sums and take identical decisions (the
+// cluster's control flow stays uniform, which the cluster barriers rely on).
 //
 // Precision: a, b, the tested residual p_k(x) and every comparison are fp64.  The
 // row sums T (and the bonus token's running sums) are formed from per-element terms
@@ -27,12 +31,15 @@
 // precision", 1971; Knuth's two-sum) -- which keeps about 48 bits on the fp32 pipe
 // (GB300's fp64 rate is a small fraction of its fp32 rate); partial sums are combined
 // in double-float within a warp and in fp64 across the 32 warps.
+#include <cooperative_groups.h>
+
 #include "tv_internal.cuh"
 
 namespace tv {
 namespace {
 
-constexpr int kThreadsA = 1024;
+constexpr int kCluster = 8;     // CTAs per request
+constexpr int kThreadsA = 256;
 constexpr int kWarpsA = kThreadsA / 32;
 
 struct DF {
@@ -75,7 +82,7 @@ __device__ __forceinline__ DF shfl_up_df(DF v, int o) {
 }
 
 // Sum over the block, returned to every thread: double-float within warps, fp64
-// across the 32 warp sums (one warp).
+// across the warp sums (one warp).
 __device__ __forceinline__ double block_sum(DF v, double *red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -83,7 +90,7 @@ __device__ __forceinline__ double block_sum(DF v, double *red) {
     if (lane == 0) red[warp] = to_double(v);
     __syncthreads();
     if (warp == 0) {
-        double t = red[lane];
+        double t = lane < kWarpsA ? red[lane] : 0.0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
         if (lane == 0) red[kWarpsA] = t;
@@ -94,12 +101,12 @@ __device__ __forceinline__ double block_sum(DF v, double *red) {
     return t;
 }
 
-// T = sum_y max(P[y] - a Q[y], 0) over the row.
-__device__ __forceinline__ double row_sum(const float *P, const float *Q, int V, double a,
-                                          double *red) {
+// This CTA's part of T = sum_y max(P[y] - a Q[y], 0): elements [y0, y1).
+__device__ __forceinline__ double slice_sum(const float *P, const float *Q, int y0, int y1,
+                                            double a, double *red) {
     const float ahi = (float)a, alo = (float)(a - (double)ahi);
     DF acc = {0.f, 0.f};
-    for (int y = threadIdx.x; y < V; y += kThreadsA)
+    for (int y = y0 + threadIdx.x; y < y1; y += kThreadsA)
         acc = df_add(acc, term(__ldg(P + y), __ldg(Q + y), ahi, alo));
     return block_sum(acc, red);
 }
@@ -111,11 +118,18 @@ __device__ __forceinline__ double residual_at(const float *P, const float *Q, in
 }
 
 __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs a) {
+    namespace cg = cooperative_groups;
     __shared__ int s_par[kMaxNodes], s_drf[kMaxNodes], s_path[kMaxDepth];
     __shared__ double s_red[kWarpsA + 1], s_base[kWarpsA + 1];
-    __shared__ int s_bad, s_idx;
-    const int b = blockIdx.x, tid = threadIdx.x;
+    __shared__ double s_slot[2];     // this CTA's slice sum of the last two passes
+    __shared__ double s_tot;         // this CTA's slice total for the bonus draw
+    __shared__ int s_bad, s_idx, s_last;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int b = blockIdx.x / kCluster, tid = threadIdx.x;
     const int V = a.V, md = a.max_depth;
+    const int y0 = (int)((long long)V * rank / kCluster);
+    const int y1 = (int)((long long)V * (rank + 1) / kCluster);
 
     pdl_wait();
     pdl_launch_next();
@@ -132,22 +146,36 @@ __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs 
         }
     __syncthreads();
     int32_t *path = a.path + (size_t)b * md;
-    if (s_bad) {
-        if (tid == 0) {
-            report(a.status, TV_ERR_TREE);
-            a.len[b] = 0;
-            a.bonus[b] = -1;
+    if (s_bad) {  // the same verdict in every CTA of the cluster; nothing shared yet
+        if (rank == 0) {
+            if (tid == 0) {
+                report(a.status, TV_ERR_TREE);
+                a.len[b] = 0;
+                a.bonus[b] = -1;
+            }
+            for (int m = tid; m < md; m += kThreadsA) path[m] = -1;
         }
-        for (int m = tid; m < md; m += kThreadsA) path[m] = -1;
         return;
     }
+
+    // the sum over the whole row of this pass's slice sums, in rank order
+    int pass = 0;
+    auto cluster_sum = [&](double part) {
+        const int slot = pass & 1;
+        ++pass;
+        if (tid == 0) s_slot[slot] = part;
+        cluster.sync();  // a slot is rewritten two passes later, after the next barrier
+        double t = 0.0;
+        for (int r = 0; r < kCluster; ++r) t += *cluster.map_shared_rank(&s_slot[slot], r);
+        return t;
+    };
 
     const float *P = a.root_p + (size_t)b * V;
     const float *Q = a.root_q + (size_t)b * V;
     double ca = 0.0, cb = 1.0;  // residual coefficients at the current node
     int cur = -1, L = 0;
     bool too_deep = false;
-    for (;;) {  // every thread takes the same branches: all values below are uniform
+    for (;;) {  // every thread of the cluster takes the same branches
         bool found = false;
         for (int c = cur + 1; c < n; ++c) {
             if (s_par[c] != cur) continue;
@@ -170,7 +198,7 @@ __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs 
             }
             // rejected: the next residual, unless it sums to zero
             const double na = ca + cb;
-            const double t = row_sum(P, Q, V, na, s_red);
+            const double t = cluster_sum(slice_sum(P, Q, y0, y1, na, s_red));
             if (t > 0.0) {
                 ca = na;
                 cb = t;
@@ -178,89 +206,118 @@ __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs 
         }
         if (!found || too_deep) break;
     }
-    if (too_deep) {
-        if (tid == 0) {
-            report(a.status, TV_ERR_TREE);
-            a.len[b] = 0;
-            a.bonus[b] = -1;
-        }
-        for (int m = tid; m < md; m += kThreadsA) path[m] = -1;
-        return;
-    }
 
-    // bonus token: the first index whose running sum of the residual exceeds u_bonus
-    // times the total (sums of the unnormalized terms; each thread owns a contiguous
-    // chunk of the row)
-    const float ahi = (float)ca, alo = (float)(ca - (double)ahi);
-    const int chunk = (V + kThreadsA - 1) / kThreadsA;
-    const int x0 = min(tid * chunk, V), x1 = min(x0 + chunk, V);
-    DF pacc = {0.f, 0.f};
-    for (int y = x0; y < x1; ++y) pacc = df_add(pacc, term(P[y], Q[y], ahi, alo));
-    // exclusive scan of the chunk sums: double-float within warps, fp64 across them
-    const int lane = tid & 31, warp = tid >> 5;
-    DF incl = pacc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const DF v = shfl_up_df(incl, o);
-        if (lane >= o) incl = df_add(incl, v);
-    }
-    if (lane == 31) s_red[warp] = to_double(incl);
-    if (tid == 0) s_idx = 0x7fffffff;
-    __syncthreads();
-    if (warp == 0) {
-        const double w = s_red[lane];
-        double v = w;
+    int idx = -1;
+    if (!too_deep) {
+        // bonus token: the first index whose running sum of the residual exceeds
+        // u_bonus times the total.  Slice totals give each CTA its base; inside a
+        // slice each thread owns a contiguous chunk.
+        const float ahi = (float)ca, alo = (float)(ca - (double)ahi);
+        const int chunk = (y1 - y0 + kThreadsA - 1) / kThreadsA;
+        const int x0 = min(y0 + tid * chunk, y1), x1 = min(x0 + chunk, y1);
+        DF pacc = {0.f, 0.f};
+        for (int y = x0; y < x1; ++y) pacc = df_add(pacc, term(P[y], Q[y], ahi, alo));
+        const int lane = tid & 31, warp = tid >> 5;
+        DF incl = pacc;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const double u = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += u;
+            const DF v = shfl_up_df(incl, o);
+            if (lane >= o) incl = df_add(incl, v);
         }
-        s_base[lane] = v - w;
-        if (lane == 31) s_base[kWarpsA] = v;
-    }
-    __syncthreads();
-    const double part = to_double(pacc);
-    const double excl = s_base[warp] + (to_double(incl) - part);
-    const double total = s_base[kWarpsA];
-    const double target = a.u_bonus[b] * total;
-    if (excl <= target && target < excl + part) {
-        double run = excl;
-        for (int y = x0; y < x1; ++y) {
-            run += to_double(term(P[y], Q[y], ahi, alo));
-            if (run > target) {
-                atomicMin(&s_idx, y);
-                break;
+        if (lane == 31) s_red[warp] = to_double(incl);
+        if (tid == 0) {
+            s_idx = 0x7fffffff;
+            s_last = -1;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const double w = lane < kWarpsA ? s_red[lane] : 0.0;
+            double v = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (lane < kWarpsA) s_base[lane] = v - w;
+            if (lane == kWarpsA - 1) s_tot = v;
+        }
+        cluster.sync();
+        double base = 0.0, total = 0.0;
+        for (int r = 0; r < kCluster; ++r) {
+            const double tr = *cluster.map_shared_rank(&s_tot, r);
+            if (r < rank) base += tr;
+            total += tr;
+        }
+        const double part = to_double(pacc);
+        const double excl = base + s_base[warp] + (to_double(incl) - part);
+        const double target = a.u_bonus[b] * total;
+        if (excl <= target && target < excl + part) {
+            double run = excl;
+            for (int y = x0; y < x1; ++y) {
+                run += to_double(term(P[y], Q[y], ahi, alo));
+                if (run > target) {
+                    atomicMin(&s_idx, y);
+                    break;
+                }
             }
         }
-    }
-    __syncthreads();
-    int idx = s_idx;
-    if (idx == 0x7fffffff) {
-        // the target fell past the last running sum (rounding): last index with p > 0
+        // for a target past the last running sum (rounding): the last index with p > 0
         int last = -1;
         for (int y = x0; y < x1; ++y) {
             const DF tv = term(P[y], Q[y], ahi, alo);
             if (tv.hi > 0.f || tv.lo > 0.f) last = y;
         }
         last = __reduce_max_sync(0xffffffffu, last);
-        if (lane == 0) s_red[warp] = (double)last;
-        __syncthreads();
-        double m = -1.0;
-        for (int w = 0; w < kWarpsA; ++w) m = fmax(m, s_red[w]);
-        idx = (int)m;
+        if (lane == 0) atomicMax(&s_last, last);
+        cluster.sync();
+        if (rank == 0) {
+            int found = 0x7fffffff, lastc = -1;
+            for (int r = 0; r < kCluster; ++r) {
+                found = min(found, *cluster.map_shared_rank(&s_idx, r));
+                lastc = max(lastc, *cluster.map_shared_rank(&s_last, r));
+            }
+            idx = found != 0x7fffffff ? found : lastc;
+        }
     }
-    __syncthreads();
-    for (int m = tid; m < md; m += kThreadsA) path[m] = m < L ? s_path[m] : -1;
-    if (tid == 0) {
-        a.len[b] = L;
-        a.bonus[b] = idx;
+    if (rank == 0) {
+        if (too_deep) {
+            if (tid == 0) {
+                report(a.status, TV_ERR_TREE);
+                a.len[b] = 0;
+                a.bonus[b] = -1;
+            }
+            for (int m = tid; m < md; m += kThreadsA) path[m] = -1;
+        } else {
+            for (int m = tid; m < md; m += kThreadsA) path[m] = m < L ? s_path[m] : -1;
+            if (tid == 0) {
+                a.len[b] = L;
+                a.bonus[b] = idx;
+            }
+        }
     }
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace
 
 cudaError_t launch_accept_stochastic(const StochArgs &a, cudaStream_t s) {
-    return launch_pdl(accept_stochastic_kernel, dim3((unsigned)a.B), dim3(kThreadsA), 0, s, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.B * kCluster);
+    cfg.blockDim = dim3(kThreadsA);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, accept_stochastic_kernel, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 }  // namespace tv

@@ -14,30 +14,40 @@
 // which a frontier that receives all C children of a node when the node is added
 // (in candidate order) would hand them out.  Scores are fp64 products computed the
 // same way as in that formulation, so every choice is made on identical values.
+// Comparisons run on integer keys: for non-negative doubles the order of the bit
+// patterns is the numeric order (zero of either sign maps to 0, "none" to -1), so
+// they stay off GB300's narrow fp64 pipe; one warp per CTA, so requests do not share
+// an SM's fp64 unit for the products.
 #include "tv_internal.cuh"
 
 namespace tv {
 namespace {
 
-constexpr int kWarpsB = 4;
+constexpr int kWarpsB = 1;
+
+// Order key of a score: a non-negative double's bit pattern, -1 for "none".
+__device__ __forceinline__ long long score_key(double s) {
+    const long long b = __double_as_longlong(s);  // -0.0 is the most negative pattern
+    return b >= 0 ? b : (b == (long long)0x8000000000000000ULL ? 0LL : -1LL);
+}
 
 struct WarpBest {
-    double s;
+    long long k;
     int i;
 };
 
-// Largest s, then smallest i, over the warp.
-__device__ __forceinline__ WarpBest warp_best(double s, int i) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const double os = __shfl_xor_sync(0xffffffffu, s, o);
+// Largest key, then smallest i, over aligned groups of `width` lanes (a power of
+// two; 32 = the whole warp).
+__device__ __forceinline__ WarpBest warp_best(long long k, int i, int width = 32) {
+    for (int o = width >> 1; o > 0; o >>= 1) {
+        const long long ok = __shfl_xor_sync(0xffffffffu, k, o);
         const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-        if (os > s || (os == s && oi < i)) {
-            s = os;
+        if (ok > k || (ok == k && oi < i)) {
+            k = ok;
             i = oi;
         }
     }
-    return {s, i};
+    return {k, i};
 }
 
 __global__ void __launch_bounds__(kWarpsB * 32) build_tree_kernel(BuildArgs a) {
@@ -48,12 +58,14 @@ __global__ void __launch_bounds__(kWarpsB * 32) build_tree_kernel(BuildArgs a) {
     pdl_launch_next();
     if (b >= a.B) return;
     const int C = a.C, cap = a.depth_cap, n = a.n;
-    // per warp, in doubles: q [cap][C]; per entry rho and score (fp64), best child,
-    // depth and taken mask (three 32-bit words, two doubles of room)
+    int cw = 1;  // candidate lanes rounded up to a power of two
+    while (cw < C) cw <<= 1;
+    // per warp, in doubles: q [cap][C]; per entry rho (fp64) and score key (int64),
+    // best child, depth and taken mask (three 32-bit words, two doubles of room)
     const size_t per_warp = (size_t)cap * C + 4 * (size_t)(n + 1);
     double *sq = s_dyn + w * per_warp;
     double *erho = sq + cap * C;
-    double *escore = erho + (n + 1);
+    long long *escore = reinterpret_cast<long long *>(erho + (n + 1));
     int *ebest = reinterpret_cast<int *>(escore + (n + 1));
     int *edep = ebest + (n + 1);
     uint32_t *emask = reinterpret_cast<uint32_t *>(edep + (n + 1));
@@ -66,11 +78,11 @@ __global__ void __launch_bounds__(kWarpsB * 32) build_tree_kernel(BuildArgs a) {
     auto refresh = [&](int e) {
         const uint32_t taken = emask[e];
         const int d = edep[e];
-        double s = -1.0;
-        if (lane < C && !((taken >> lane) & 1u)) s = erho[e] * sq[d * C + lane];
-        const WarpBest bb = warp_best(s, lane < C ? lane : 0x7fffffff);
+        long long k = -1;
+        if (lane < C && !((taken >> lane) & 1u)) k = score_key(erho[e] * sq[d * C + lane]);
+        const WarpBest bb = warp_best(k, lane < C ? lane : 0x7fffffff, cw);
         if (lane == 0) {
-            escore[e] = bb.s;
+            escore[e] = bb.k;
             ebest[e] = bb.i;
         }
         __syncwarp();
@@ -90,33 +102,34 @@ __global__ void __launch_bounds__(kWarpsB * 32) build_tree_kernel(BuildArgs a) {
     double total = 0.0;
     int count = 0;
     for (int i = 0; i < n; ++i) {
-        double s = -1.0;
+        long long s = -1;
         int e = 0x7fffffff;
         for (int k = lane; k <= i; k += 32) {  // entries 0..i exist
-            const double ks = escore[k];
+            const long long ks = escore[k];
             if (ks > s) {  // ascending k in a lane: the first maximum is the lowest
                 s = ks;
                 e = k;
             }
         }
         const WarpBest best = warp_best(s, e);
-        if (best.s < 0.0) break;  // the frontier is empty
-        if (a.cost && i >= 1 && (total + best.s) / a.cost[i + 1] < total / a.cost[i]) break;
+        if (best.k < 0) break;  // the frontier is empty
         const int ep = best.i;
+        const double bs = erho[ep] * sq[edep[ep] * C + ebest[ep]];  // the entry's score
+        if (a.cost && i >= 1 && (total + bs) / a.cost[i + 1] < total / a.cost[i]) break;
         const int y = ebest[ep];
         const int d = edep[ep] + 1;
         if (lane == 0) {
             par_out[i] = ep - 1;
             tok_out[i] = y;
-            rho_out[i] = best.s;
+            rho_out[i] = bs;
             emask[ep] |= 1u << y;
             // entry of node i: its children join the frontier below the depth cap
-            erho[i + 1] = best.s;
+            erho[i + 1] = bs;
             edep[i + 1] = d;
             emask[i + 1] = 0u;
-            escore[i + 1] = -1.0;
+            escore[i + 1] = -1;
         }
-        total += best.s;
+        total += bs;
         count = i + 1;
         __syncwarp();
         refresh(ep);
