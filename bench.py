@@ -61,7 +61,8 @@ TRAFFIC_SOURCES = {
     "tree_attention": [_CS + f for f in ("tree_attention.cu", "tc_common.cuh", "tc_ptx.cuh",
                                          "tv_internal.cuh")],
 }
-KERNEL_NAMES = {1: "simt", 2: "tcgen05 one unit per CTA", 3: "tcgen05 streaming"}
+KERNEL_NAMES = {1: "simt", 2: "tcgen05 one unit per CTA", 3: "tcgen05 streaming",
+                4: "tcgen05 node tiles"}
 
 
 DEFAULT_STEPS = {1: 40000, 2: 40000, 3: 5000, 4: 400, 5: 40}
@@ -91,6 +92,10 @@ def parse():
     ap.add_argument("--attention-ctx", type=int, default=4096,
                     help="shared-prefix positions per request for the tree-attention line "
                          "(0 = skip it)")
+    ap.add_argument("--profile-verify", type=int, default=None, metavar="VARIANT",
+                    help="profiling aid: only run 3 verify launches of this tv_variant on "
+                         "--config's workload (config 5 as 2 layers of 32 heads, 512 units), "
+                         "then exit")
     ap.add_argument("--profile-attention", action="store_true",
                     help="profiling aid: only run 3 tree-attention launches of the attention "
                          "workload, then exit")
@@ -769,6 +774,40 @@ def run_ours(args, world, rank, local):
                 "kernel": dom_name, "bytes_per_launch": dom_bytes,
                 "launch_us": dom_t * 1e6, "peak_kind": "%s (hbm_gbs burst copy)" % peak_kind}
 
+    # context for the roofline: a plain torch read reduction (torch.sum) over the same
+    # number of bytes, timed the same way (graph replays, regions rotated past 4x L2);
+    # at a few tens of MB one launch of any streaming kernel is dominated by launch and
+    # first-byte latency, so this is the practical ceiling at the step's size
+    same_bytes = None
+    if rank == 0:
+        nfl = max(1, int(dom_bytes) // 4)
+        R2 = 1 if dom_bytes >= 4 * l2 else max(4, int(4 * l2 / max(dom_bytes, 1)) + 1)
+        pool = torch.ones(R2 * nfl, dtype=torch.float32, device=dev)
+        acc = torch.empty((), dtype=torch.float32, device=dev)
+        KS2 = R2 * max(1, 200 // R2)
+        with torch.cuda.stream(stream):
+            torch.sum(pool[:nfl], dim=0, out=acc)
+        stream.synchronize()
+        gs = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gs, stream=stream):
+            for k in range(KS2):
+                torch.sum(pool[(k % R2) * nfl:(k % R2 + 1) * nfl], dim=0, out=acc)
+        with torch.cuda.stream(stream):
+            gs.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gs.replay()
+            e1.record(stream)
+        e1.synchronize()
+        t_sum = e0.elapsed_time(e1) * 1e-3 / KS2
+        same_bytes = {"what": "torch.sum over the dominant kernel's byte count", "bytes": int(dom_bytes),
+                      "launch_us": t_sum * 1e6, "gbs": dom_bytes / t_sum / 1e9,
+                      "frac": dom_bytes / t_sum / 1e9 / peak,
+                      "ours_over_it": t_sum / dom_t}
+        del gs, pool
+        torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = cpu_cores()
@@ -797,6 +836,7 @@ def run_ours(args, world, rank, local):
                        "timing": "CUDA graph replays of the K steps, CUDA events on the "
                                  "launching stream"},
             "roofline": roofline,
+            "same_bytes_read_reduction": same_bytes,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 2 * K,
@@ -1016,8 +1056,34 @@ def profile_attention(args):
         raise SystemExit("device status %d" % int(st[0].item()))
 
 
+def profile_verify(args):
+    """Three verify launches of one variant on the configuration's workload (for ncu)."""
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    import workloads
+    tv.build()
+    tv.load()
+    if args.config == 5:
+        b = workloads.config5(B=8, layers=2, heads=32)
+    else:
+        b = workloads.make_config(args.config)
+    d = tv.DeviceBatch(b)
+    d.status.zero_()
+    for _ in range(3):
+        d.verify(variant=args.profile_verify)
+    torch.cuda.synchronize()
+    st = int(d.status[0].item())
+    print(json.dumps({"profile_verify": args.profile_verify, "config": args.config,
+                      "units": b.B * b.H, "status": st}))
+    if st != 0:
+        raise SystemExit("device status %d" % st)
+
+
 def main():
     args = parse()
+    if args.profile_verify is not None:
+        profile_verify(args)
+        return
     if args.profile_attention:
         profile_attention(args)
         return

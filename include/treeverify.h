@@ -84,10 +84,14 @@ typedef enum tv_variant {
     TV_VARIANT_TC = 2,      /* tcgen05 tensor-core kernel, one (request, head) per CTA:
                                bf16 q/k/v, dk in {64,128}, dv in {64,128};
                                TV_ERR_UNSUPPORTED otherwise */
-    TV_VARIANT_TC_STREAM = 3 /* persistent tcgen05 kernel streaming many (request, head)
+    TV_VARIANT_TC_STREAM = 3, /* persistent tcgen05 kernel streaming many (request, head)
                                units per CTA through double-buffered shared memory:
                                as TV_VARIANT_TC but scalar decay only, and only where two
                                units' operands fit one CTA's shared memory */
+    TV_VARIANT_TC_TILED = 4  /* tcgen05 kernel for large trees, one (request, head) per
+                               CTA, nodes in tiles of 64 against an H0 operand kept in
+                               shared memory: bf16 q/k/v, dk = dv = 128, any tree size up
+                               to TV_MAX_NODES; TV_ERR_UNSUPPORTED otherwise */
 } tv_variant;
 
 /*
@@ -456,7 +460,8 @@ tv_status tv_tree_attention(int32_t B, int32_t total_nodes, int32_t max_nodes, i
 
 /*
  * tv_verify_variant -- the kernel tv_verify (TV_VARIANT_AUTO) would launch for
- * this problem: TV_VARIANT_TC_STREAM, TV_VARIANT_TC or TV_VARIANT_SIMT.  Reads
+ * this problem: TV_VARIANT_TC_STREAM, TV_VARIANT_TC, TV_VARIANT_TC_TILED (trees too
+ * large for TV_VARIANT_TC's shared-memory plan) or TV_VARIANT_SIMT.  Reads
  * only the sizes and kinds in *p (no device memory; the current device's SM count
  * and shared memory); returns the negative tv_status of an invalid problem (e.g.
  * -TV_ERR_SHAPE).  The tensor-core kernels take bf16 q/k/v with dk, dv in

@@ -12,7 +12,7 @@ from gpu_util import (TOL, check_accept, check_commit, check_verify, mat_rel_err
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = {"auto": 0, "simt": 1, "tc": 2}
+VARIANTS = {"auto": 0, "simt": 1, "tc": 2, "tiled": 4}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -248,6 +248,57 @@ def test_outputs_stay_inside_their_buffers():
 
 
 # ------------------------------------------------------------------ device-detected errors
+
+
+@pytest.mark.parametrize("decay", ["diag", "scalar"])
+def test_tiled_tensor_core_ragged(decay):
+    """The node-tiled tcgen05 kernel on ragged trees: empty, single-node, one tile
+    exactly, one node over a tile, several tiles and the largest tree."""
+    rng = np.random.default_rng(41 if decay == "diag" else 42)
+    b = workloads.random_batch(rng, [0, 1, 63, 64, 65, 130, 256], 2, 128, 128, decay=decay,
+                               qkv_dtype="bf16", depth_cap=12, max_depth=16)
+    _full_check(b, "tiled")
+
+
+def test_tiled_tensor_core_config3():
+    """The GLA-like configuration (64-node best-first trees, per-channel decay) on
+    the node-tiled kernel."""
+    _full_check(workloads.make_config(3), "tiled")
+
+
+def test_tiled_tensor_core_deepest_chain():
+    b = workloads.random_batch(np.random.default_rng(43), [32, 200], 2, 128, 128,
+                               decay="diag", qkv_dtype="bf16", depth_cap=32, max_depth=32)
+    s = int(b.node_offsets[0])
+    b.parent[s:s + 32] = np.arange(-1, 31, dtype=np.int32)
+    b.depth[s:s + 32] = np.arange(1, 33, dtype=np.int32)
+    _full_check(b, "tiled")
+
+
+def test_tiled_tensor_core_malformed_tree():
+    rng = np.random.default_rng(44)
+    b = workloads.random_batch(rng, [6, 70, 7], 2, 128, 128, decay="diag", qkv_dtype="bf16",
+                               depth_cap=6, max_depth=6)
+    s = b.node_offsets[1]
+    b.parent[s + 66] = 68
+    res = run_library(b, variant=4, steps=("verify",))
+    assert res["status"] == 6  # TV_ERR_TREE
+    e = b.node_offsets[2]
+    assert np.all(res["out"][s:e] == 0.0)
+    import oracle
+    units = [u for u in range(b.B * b.H) if u // b.H != 1]
+    ref = oracle.verify(b, units=units)
+    for u, o in ref.items():
+        bb, h = divmod(u, b.H)
+        ss, ee = b.node_offsets[bb], b.node_offsets[bb + 1]
+        assert row_rel_err(res["out"][ss:ee, h], o) <= TOL
+
+
+def test_tiled_tensor_core_rejects_other_dims():
+    b = workloads.random_batch(np.random.default_rng(45), [4], 1, 64, 64, decay="diag",
+                               qkv_dtype="bf16")
+    with pytest.raises(Exception):
+        run_library(b, variant=4, steps=("verify",))
 
 
 def _bad_tree_batch():

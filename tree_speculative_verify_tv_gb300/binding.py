@@ -24,6 +24,7 @@ TV_ERR_UNSUPPORTED, TV_ERR_TREE, TV_ERR_CUDA, TV_ERR_TIMEOUT = 5, 6, 7, 8
 TV_DECAY_SCALAR, TV_DECAY_DIAG = 0, 1
 TV_BF16, TV_F32 = 0, 1
 TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC, TV_VARIANT_TC_STREAM = 0, 1, 2, 3
+TV_VARIANT_TC_TILED = 4
 TV_MAX_NODES, TV_MAX_DEPTH, TV_MAX_DIM = 256, 32, 256
 TV_SERIAL_STATIC_BYTES = 16 << 20
 

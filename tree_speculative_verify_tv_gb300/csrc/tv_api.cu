@@ -37,11 +37,22 @@ tv_status check_ptrs(std::initializer_list<const void *> ptrs) {
 }
 
 // The kernel TV_VARIANT_AUTO picks: the one-unit tensor-core kernel where it
-// applies (the streaming kernel only when it is the faster one), else SIMT.
+// applies (the streaming kernel only when it is the faster one), the node-tiled
+// tensor-core kernel for trees too large for it, else SIMT.
+int32_t auto_variant(const tv::VerifyArgs &a) {
+    if (tv::verify_tc_stream_preferred(a)) return TV_VARIANT_TC_STREAM;
+    if (tv::verify_tc_supported(a)) return TV_VARIANT_TC;
+    if (tv::verify_tc_big_supported(a)) return TV_VARIANT_TC_TILED;
+    return TV_VARIANT_SIMT;
+}
+
 cudaError_t launch_verify_auto(const tv::VerifyArgs &a, cudaStream_t s) {
-    if (tv::verify_tc_stream_preferred(a)) return tv::launch_verify_tc_stream(a, s);
-    if (tv::verify_tc_supported(a)) return tv::launch_verify_tc(a, s);
-    return tv::launch_verify_simt(a, s);
+    switch (auto_variant(a)) {
+        case TV_VARIANT_TC_STREAM: return tv::launch_verify_tc_stream(a, s);
+        case TV_VARIANT_TC: return tv::launch_verify_tc(a, s);
+        case TV_VARIANT_TC_TILED: return tv::launch_verify_tc_big(a, s);
+        default: return tv::launch_verify_simt(a, s);
+    }
 }
 
 }  // namespace
@@ -71,8 +82,7 @@ int32_t tv_verify_variant(const tv_problem *p) {
     tv::VerifyArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
                      p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
                      nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
-    if (tv::verify_tc_stream_preferred(a)) return TV_VARIANT_TC_STREAM;
-    return tv::verify_tc_supported(a) ? TV_VARIANT_TC : TV_VARIANT_SIMT;
+    return auto_variant(a);
 }
 
 tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, const void *k,
@@ -81,7 +91,7 @@ tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, cons
     tv_status st = check_dims(p);
     if (st != TV_OK) return st;
     if (!p->depth && p->total_nodes > 0) return TV_ERR_NULL;
-    if (variant < TV_VARIANT_AUTO || variant > TV_VARIANT_TC_STREAM) return TV_ERR_DTYPE;
+    if (variant < TV_VARIANT_AUTO || variant > TV_VARIANT_TC_TILED) return TV_ERR_DTYPE;
     if (!dev_status) return TV_ERR_NULL;
     if (p->B == 0 || p->total_nodes == 0) return TV_OK;
     st = check_ptrs({H0, q, k, v, g, out, p->node_offsets, p->parent, p->depth, dev_status});
@@ -101,6 +111,10 @@ tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, cons
         case TV_VARIANT_TC_STREAM:
             if (!tv::verify_tc_stream_supported(a)) return TV_ERR_UNSUPPORTED;
             e = tv::launch_verify_tc_stream(a, s);
+            break;
+        case TV_VARIANT_TC_TILED:
+            if (!tv::verify_tc_big_supported(a)) return TV_ERR_UNSUPPORTED;
+            e = tv::launch_verify_tc_big(a, s);
             break;
         default: e = launch_verify_auto(a, s);
     }

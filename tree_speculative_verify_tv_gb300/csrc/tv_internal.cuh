@@ -107,6 +107,9 @@ cudaError_t launch_verify_simt(const VerifyArgs &a, cudaStream_t s);
 // Returns cudaErrorNotSupported when the shape is outside the tensor-core kernel.
 cudaError_t launch_verify_tc(const VerifyArgs &a, cudaStream_t s);
 bool verify_tc_supported(const VerifyArgs &a);
+// Node-tiled tensor-core kernel for large trees (dk = dv = 128).
+bool verify_tc_big_supported(const VerifyArgs &a);
+cudaError_t launch_verify_tc_big(const VerifyArgs &a, cudaStream_t s);
 // Persistent tensor-core kernel (scalar decay): many units per CTA, double-buffered.
 bool verify_tc_stream_supported(const VerifyArgs &a);
 bool verify_tc_stream_preferred(const VerifyArgs &a);  // what TV_VARIANT_AUTO picks
