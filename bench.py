@@ -331,9 +331,10 @@ def oracle_step(batch, units, threads, packed):
     oracle.commit(batch, ln, path, units=units, threads=threads, packed=packed)
 
 
-def time_oracle(batch, total_steps: int, budget_s: float, threads: int):
-    """Pick a sample size (units per step) so total_steps steps take about budget_s;
-    returns (node_heads_per_s, units_per_step, steps_run, seconds, threads_used)."""
+def time_oracle(batch, total_steps: int, budget_s: float, threads: int, fill_budget=False):
+    """Pick a sample size (units per step) so total_steps steps take about budget_s
+    (fill_budget: then run as many steps of that size as fill budget_s); returns
+    (node_heads_per_s, units_per_step, steps_run, seconds, threads_used)."""
     import oracle
     packed = oracle._Packed(batch)
     n_units = batch.B * batch.H
@@ -345,6 +346,12 @@ def time_oracle(batch, total_steps: int, budget_s: float, threads: int):
     want = budget_s / max(total_steps, 1) / max(per_unit, 1e-9)
     upl = int(min(n_units, max(1, want)))
     units_all = np.arange(n_units, dtype=np.int32)
+    if fill_budget:
+        # one calibration step at that size, then as many steps as fill the budget
+        t0 = time.perf_counter()
+        oracle_step(batch, units_all[:upl], threads, packed)
+        step_t = time.perf_counter() - t0
+        total_steps = int(min(5000, max(3, budget_s / max(step_t, 1e-9))))
     t0 = time.perf_counter()
     nh = 0
     for s in range(total_steps):
@@ -811,7 +818,7 @@ def run_ours(args, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = cpu_cores()
-        v, upl, n, dt, threads = time_oracle(base, 40, 15.0, threads)
+        v, upl, n, dt, threads = time_oracle(base, 40, 15.0, threads, fill_budget=True)
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "%d steps of the fp64 oracle, each on %d of the %d (request, head) "
                          "units (verify + greedy walk + commit), %.1f s" % (n, upl,
