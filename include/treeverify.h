@@ -49,7 +49,7 @@ extern "C" {
 
 #define TV_VERSION 1
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define TV_MAX_NODES 256  /* nodes per request tree */
 #define TV_MAX_DEPTH 32   /* depth of any node (1 = child of the context) */
 #define TV_MAX_DIM   256  /* dk and dv */
@@ -60,7 +60,7 @@ typedef enum tv_status {
     TV_ERR_SHAPE = 2,       /* B, H, dk, dv, T, max_nodes or max_depth out of range */
     TV_ERR_DTYPE = 3,       /* unknown decay kind or element type */
     TV_ERR_ALIGN = 4,       /* an array pointer is not 16-byte aligned */
-    TV_ERR_UNSUPPORTED = 5, /* a limit of this build is exceeded, or a forced variant
+    TV_ERR_UNSUPPORTED = 5, /* a limit of the library is exceeded, or a forced variant
                                cannot run this shape */
     TV_ERR_TREE = 6,        /* device-detected: bad node_offsets, parent, depth or path */
     TV_ERR_CUDA = 7,        /* a CUDA runtime call failed (launch error) */

@@ -66,7 +66,7 @@ const char *tv_status_string(int32_t s) {
         case TV_ERR_SHAPE: return "TV_ERR_SHAPE: a size argument is out of range";
         case TV_ERR_DTYPE: return "TV_ERR_DTYPE: unknown decay kind or element type";
         case TV_ERR_ALIGN: return "TV_ERR_ALIGN: an array pointer is not 16-byte aligned";
-        case TV_ERR_UNSUPPORTED: return "TV_ERR_UNSUPPORTED: a limit of this build is exceeded";
+        case TV_ERR_UNSUPPORTED: return "TV_ERR_UNSUPPORTED: a limit of the library is exceeded";
         case TV_ERR_TREE: return "TV_ERR_TREE: malformed tree, offsets or path";
         case TV_ERR_CUDA: return "TV_ERR_CUDA: a CUDA runtime call failed";
         case TV_ERR_TIMEOUT: return "TV_ERR_TIMEOUT: a bounded device wait expired";
