@@ -88,10 +88,13 @@ typedef enum tv_variant {
                                units per CTA through double-buffered shared memory:
                                as TV_VARIANT_TC but scalar decay only, and only where two
                                units' operands fit one CTA's shared memory */
-    TV_VARIANT_TC_TILED = 4  /* tcgen05 kernel for large trees, one (request, head) per
-                               CTA, nodes in tiles of 64 against an H0 operand kept in
-                               shared memory: bf16 q/k/v, dk = dv = 128, any tree size up
-                               to TV_MAX_NODES; TV_ERR_UNSUPPORTED otherwise */
+    TV_VARIANT_TC_TILED = 4  /* tcgen05 kernels for large trees, one (request, head) per
+                               CTA: bf16 q/k/v, dk = dv = 128, trees up to TV_MAX_NODES.
+                               Where a request's k, decay and v rows fit shared memory
+                               (depth up to 21 at 256 nodes) they are loaded once and
+                               both terms run on the tensor cores; deeper trees walk
+                               their ancestors through the caches in node tiles of 64;
+                               TV_ERR_UNSUPPORTED otherwise */
 } tv_variant;
 
 /*
@@ -461,13 +464,23 @@ tv_status tv_tree_attention(int32_t B, int32_t total_nodes, int32_t max_nodes, i
 /*
  * tv_verify_variant -- the kernel tv_verify (TV_VARIANT_AUTO) would launch for
  * this problem: TV_VARIANT_TC_STREAM, TV_VARIANT_TC, TV_VARIANT_TC_TILED (trees too
- * large for TV_VARIANT_TC's shared-memory plan) or TV_VARIANT_SIMT.  Reads
+ * large for TV_VARIANT_TC's shared-memory plan, and per-channel decay trees of 64
+ * or more nodes, where its staged kernel is the faster) or TV_VARIANT_SIMT.  Reads
  * only the sizes and kinds in *p (no device memory; the current device's SM count
  * and shared memory); returns the negative tv_status of an invalid problem (e.g.
  * -TV_ERR_SHAPE).  The tensor-core kernels take bf16 q/k/v with dk, dv in
  * {64, 128} when their shared-memory plan for max_nodes fits one CTA.
  */
 int32_t tv_verify_variant(const tv_problem *p);
+
+/*
+ * tv_verify_supports -- 1 when tv_verify_ex would take `variant` for this problem
+ * (TV_VARIANT_AUTO and TV_VARIANT_SIMT: any valid problem; the tensor-core
+ * variants: the shapes their kernels take), 0 when it would return
+ * TV_ERR_UNSUPPORTED, and the negative tv_status of an invalid problem or variant.
+ * Reads only the sizes and kinds in *p, like tv_verify_variant.
+ */
+int32_t tv_verify_supports(const tv_problem *p, int32_t variant);
 
 /* Human-readable name of a status code (static string). */
 const char *tv_status_string(int32_t status);

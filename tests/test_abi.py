@@ -112,6 +112,20 @@ def test_variant_query_rejects_bad_problems(lib):
     assert tv.tv_verify_variant(prob(dk=96)) == tv.TV_VARIANT_SIMT
 
 
+def test_support_query_matches_forced_launch_checks(lib):
+    # fp32 q/k/v: only SIMT (and AUTO, which falls back to it)
+    f32 = prob(qkv_dtype=tv.TV_F32)
+    assert tv.tv_verify_supports(f32, tv.TV_VARIANT_SIMT) == 1
+    assert tv.tv_verify_supports(f32, tv.TV_VARIANT_AUTO) == 1
+    for v in (tv.TV_VARIANT_TC, tv.TV_VARIANT_TC_STREAM, tv.TV_VARIANT_TC_TILED):
+        assert tv.tv_verify_supports(f32, v) == 0
+        assert verify_rc(f32, variant=v) == tv.TV_ERR_UNSUPPORTED
+    # the large-tree kernels take dk = dv = 128 only
+    assert tv.tv_verify_supports(prob(dk=64, dv=64), tv.TV_VARIANT_TC_TILED) == 0
+    assert tv.tv_verify_supports(prob(dk=12), tv.TV_VARIANT_TC) == -tv.TV_ERR_SHAPE
+    assert tv.tv_verify_supports(prob(), 9) == -tv.TV_ERR_DTYPE
+
+
 def test_empty_batches_are_no_ops(lib):
     assert verify_rc(prob(B=0, total_nodes=0)) == tv.TV_OK
     assert verify_rc(prob(total_nodes=0)) == tv.TV_OK

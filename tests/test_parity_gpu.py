@@ -26,13 +26,13 @@ def _lib():
 
 
 def _tc_supported(batch):
-    """Whether the library takes this shape on the tcgen05 kernel (it reports
-    TV_ERR_UNSUPPORTED for a forced tensor-core run otherwise)."""
+    """Whether the library takes this shape on the one-unit tcgen05 kernel (it
+    reports TV_ERR_UNSUPPORTED for a forced tensor-core run otherwise)."""
     import tree_speculative_verify_tv_gb300 as tv
     p = tv.make_problem(batch.B, batch.H, batch.dk, batch.dv, batch.T, batch.max_nodes,
                         batch.max_depth, tv.TV_DECAY_DIAG if batch.decay == "diag" else 0,
                         tv.TV_BF16 if batch.qkv_dtype == "bf16" else tv.TV_F32, 16, 16, 16)
-    return tv.tv_verify_variant(p) in (tv.TV_VARIANT_TC, tv.TV_VARIANT_TC_STREAM)
+    return tv.tv_verify_supports(p, tv.TV_VARIANT_TC) == 1
 
 
 def _full_check(batch, variant="auto", units=None):

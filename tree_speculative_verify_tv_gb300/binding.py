@@ -28,7 +28,8 @@ TV_VARIANT_TC_TILED = 4
 TV_MAX_NODES, TV_MAX_DEPTH, TV_MAX_DIM = 256, 32, 256
 TV_SERIAL_STATIC_BYTES = 16 << 20
 
-EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_accept_greedy", "tv_commit",
+EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_verify_supports",
+            "tv_accept_greedy", "tv_commit",
             "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_verify_serial",
             "tv_verify_serial_workspace_bytes", "tv_verify_serial_static", "tv_build_tree",
             "tv_accept_stochastic", "tv_tree_attention", "tv_tree_attention_workspace_bytes",
@@ -104,6 +105,8 @@ def load(path: Optional[str] = None):
         L.tv_version.restype = i32
         L.tv_verify_variant.argtypes = [P]
         L.tv_verify_variant.restype = i32
+        L.tv_verify_supports.argtypes = [P, i32]
+        L.tv_verify_supports.restype = i32
         if path is None:
             _lib = L
         return L
@@ -140,6 +143,12 @@ def tv_version() -> int:
 def tv_verify_variant(problem: tv_problem) -> int:
     """Kernel tv_verify would choose (TV_VARIANT_TC / TV_VARIANT_SIMT), or -status."""
     return load().tv_verify_variant(ctypes.byref(problem))
+
+
+def tv_verify_supports(problem: tv_problem, variant: int) -> int:
+    """1 if tv_verify_ex takes `variant` for this problem, 0 if it would report
+    TV_ERR_UNSUPPORTED, or -status for an invalid problem or variant."""
+    return load().tv_verify_supports(ctypes.byref(problem), int(variant))
 
 
 def make_problem(B, H, dk, dv, total_nodes, max_nodes, max_depth, decay, qkv_dtype,

@@ -8,6 +8,12 @@
 
 #include "tv_internal.cuh"
 
+namespace tv {
+// verify_tc_big.cu: whether the staged large-tree kernel takes this problem and is
+// the faster choice (per-channel decay, trees of 64 or more nodes)
+bool verify_tc_staged_preferred(const VerifyArgs &a);
+}  // namespace tv
+
 namespace {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -37,10 +43,12 @@ tv_status check_ptrs(std::initializer_list<const void *> ptrs) {
 }
 
 // The kernel TV_VARIANT_AUTO picks: the one-unit tensor-core kernel where it
-// applies (the streaming kernel only when it is the faster one), the node-tiled
-// tensor-core kernel for trees too large for it, else SIMT.
+// applies (the streaming kernel only when it is the faster one, the staged
+// large-tree kernel for per-channel decay trees of 64 or more nodes), the
+// large-tree tensor-core kernels for trees too large for it, else SIMT.
 int32_t auto_variant(const tv::VerifyArgs &a) {
     if (tv::verify_tc_stream_preferred(a)) return TV_VARIANT_TC_STREAM;
+    if (tv::verify_tc_staged_preferred(a)) return TV_VARIANT_TC_TILED;
     if (tv::verify_tc_supported(a)) return TV_VARIANT_TC;
     if (tv::verify_tc_big_supported(a)) return TV_VARIANT_TC_TILED;
     return TV_VARIANT_SIMT;
@@ -75,6 +83,22 @@ const char *tv_status_string(int32_t s) {
 }
 
 int32_t tv_version(void) { return TV_VERSION; }
+
+int32_t tv_verify_supports(const tv_problem *p, int32_t variant) {
+    tv_status st = check_dims(p);
+    if (st != TV_OK) return -static_cast<int32_t>(st);
+    tv::VerifyArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
+                     p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
+                     nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    switch (variant) {
+        case TV_VARIANT_AUTO:
+        case TV_VARIANT_SIMT: return 1;
+        case TV_VARIANT_TC: return tv::verify_tc_supported(a) ? 1 : 0;
+        case TV_VARIANT_TC_STREAM: return tv::verify_tc_stream_supported(a) ? 1 : 0;
+        case TV_VARIANT_TC_TILED: return tv::verify_tc_big_supported(a) ? 1 : 0;
+        default: return -static_cast<int32_t>(TV_ERR_DTYPE);
+    }
+}
 
 int32_t tv_verify_variant(const tv_problem *p) {
     tv_status st = check_dims(p);

@@ -872,7 +872,8 @@ bool encode_staged_map(CUtensorMap *tm, const void *base, CUtensorMapDataType dt
 }
 
 bool staged_fits(const VerifyArgs &a) {
-    return a.max_nodes <= 256 && StagedLayout(a.max_nodes, a.max_depth).total <= kSmemLimit;
+    return a.max_nodes <= 256 && StagedLayout(a.max_nodes, a.max_depth).total <= kSmemLimit &&
+           encode_fn() != nullptr;
 }
 
 cudaError_t launch_verify_tc_staged(const VerifyArgs &a, cudaStream_t s) {
@@ -903,6 +904,11 @@ bool verify_tc_big_supported(const VerifyArgs &a) {
     return a.qkv_dtype == TV_BF16 && a.dk == kDimG && a.dv == kDimG &&
            a.max_nodes <= kMaxNodes &&
            (staged_fits(a) || BigLayout(a.max_depth).total <= kSmemLimit);
+}
+
+bool verify_tc_staged_preferred(const VerifyArgs &a) {
+    return a.decay == TV_DECAY_DIAG && a.max_nodes >= 64 && verify_tc_big_supported(a) &&
+           staged_fits(a);
 }
 
 cudaError_t launch_verify_tc_big(const VerifyArgs &a, cudaStream_t s) {
