@@ -294,6 +294,44 @@ def test_tiled_tensor_core_malformed_tree():
         assert row_rel_err(res["out"][ss:ee, h], o) <= TOL
 
 
+@pytest.mark.parametrize("decay", ["diag", "scalar"])
+def test_tiled_tensor_core_neighbor_rows_do_not_leak(decay):
+    """The large-tree kernels copy k, g and v rows in boxes of 32 nodes, so a
+    request's boxes run into the next request's rows: non-finite values there must
+    not reach its outputs."""
+    rng = np.random.default_rng(46)
+    b = workloads.random_batch(rng, [5, 40, 17, 70], 2, 128, 128, decay=decay, qkv_dtype="bf16",
+                               depth_cap=8, max_depth=16)
+    s, e = int(b.node_offsets[2]), int(b.node_offsets[3])
+    b.v[s:e] = 0x7F80  # bf16 +inf
+    b.k[s:e] = 0x7FC0  # bf16 NaN
+    b.g[s:e] = np.float32(np.inf)
+    res = run_library(b, variant=4, steps=("verify",))
+    assert res["status"] == 0
+    check_verify(b, res["out"], units=[u for u in range(b.B * b.H) if u // b.H != 2])
+
+
+@pytest.mark.parametrize("md", [21, 22])
+def test_tiled_tensor_core_staged_depth_limit(md):
+    """256-node trees as deep as the staged kernel's shared-memory plan allows (21)
+    and one deeper (the node-tiled kernel), each with a chain to the deepest level."""
+    rng = np.random.default_rng(47 + md)
+    b = workloads.random_batch(rng, [256, 200], 2, 128, 128, decay="diag", qkv_dtype="bf16",
+                               depth_cap=8, max_depth=md)
+    s = int(b.node_offsets[0])
+    par = np.empty(256, np.int32)
+    par[:md] = np.arange(-1, md - 1)
+    par[md:] = rng.integers(-1, md - 1, 256 - md)
+    dep = np.zeros(256, np.int32)
+    for i in range(256):
+        dep[i] = 1 if par[i] < 0 else dep[par[i]] + 1
+    assert dep.max() == md
+    b.parent[s:s + 256], b.depth[s:s + 256] = par, dep
+    res = run_library(b, variant=4, steps=("verify",))
+    assert res["status"] == 0
+    check_verify(b, res["out"])
+
+
 def test_tiled_tensor_core_rejects_other_dims():
     b = workloads.random_batch(np.random.default_rng(45), [4], 1, 64, 64, decay="diag",
                                qkv_dtype="bf16")

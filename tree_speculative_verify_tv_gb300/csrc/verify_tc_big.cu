@@ -355,22 +355,22 @@ __global__ void __launch_bounds__(kThreadsG, 2) verify_tc_big_kernel(const Verif
 //            hi + lo and stored transposed in tensor memory (lane = value channel,
 //            keys along the columns) as the A operand of the H0 term.
 //   phase 0  E = e^g in place, one exponential per node and channel.  In tiles of
-//            64 nodes, each node's e^{G_i} * q_i is the product of its root path's
-//            E rows (shared memory only) and becomes a bf16 hi/lo B operand row
-//            (two tiles in flight); one thread issues D[:, tile] = H0^T (e^{G} * q)
-//            (three products, A from tensor memory).
-//   phase 1  k (n x 128 bf16) lands by TMA where the B tiles were.  The walks:
+//            128 nodes, each node's e^{G_i} * q_i is the product of its root path's
+//            E rows (shared memory only) and becomes a bf16 hi/lo B operand row;
+//            one thread issues D[:, tile] = H0^T (e^{G} * q) (three products, A from
+//            tensor memory) while the next tile's first walks run.
+//   phase 1  k (n x 128 bf16) lands by TMA where the B tile was.  The walks:
 //            w_ij = q_i . (k_j * e^{G_i - G_j}), eight lanes per node and four nodes
-//            per warp, four ancestors per round with one transposed reduction.
+//            per warp (nodes bucketed by depth), four ancestors per round with one
+//            transposed reduction.
 //   phase 2  v lands by TMA (128-byte swizzled, MN-major: node rows of 64 channels)
 //            where E was.  Per tile of 64 nodes (two in flight, the second where k
-//            was) the weights are scattered into a
-//            dense bf16 hi/lo K-major B operand W[i][j] (zero off the root paths)
-//            and one thread issues D[:, tile] += V^T W^T (K = ancestors j < the
-//            tile's end).  The epilogue copies D from tensor memory to the rows
-//            of out.
+//            was) the weights are scattered into a dense bf16 hi/lo K-major B
+//            operand W[i][j] (zero off the root paths) and one thread issues
+//            D[:, tile] += V^T W^T (K = ancestors j < the tile's end).  The
+//            epilogue copies D from tensor memory to the rows of out.
 // Shared memory at 256 nodes and depth 16: 128 KB (E, then v + a W tile), 64 KB
-// (B tiles, then k, then a W tile), 16 KB w, 8 KB root paths, parents and depths.
+// (the B tile, then k, then a W tile), 16 KB w, 8 KB root paths, parents and depths.
 // ============================================================================
 
 constexpr int kThreadsS = 512;
@@ -610,18 +610,19 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         return max(x, __shfl_xor_sync(0xffffffffu, x, 16));
     };
 
-    // ---- phase 0: H0 term in tiles of 64 nodes, B operands double-buffered where k
-    // goes later: per node the product of its root path's E rows times q, split into
-    // bf16 hi/lo rows; D[:, tile] = A_hi B_hi + A_lo B_hi + A_hi B_lo (A from tensor
-    // memory)
-    const int ntile0 = (n + kTile2 - 1) / kTile2;
+    // ---- phase 0: H0 term in tiles of 128 nodes (two 64-node rounds of walks each),
+    // the B operand where k goes later: per node the product of its root path's E
+    // rows times q, split into bf16 hi/lo rows; D[:, tile] = A_hi B_hi + A_lo B_hi +
+    // A_hi B_lo (A from tensor memory)
+    const int nround0 = (n + kTile2 - 1) / kTile2;
+    const int ntile0 = (n + 2 * kTile2 - 1) / (2 * kTile2);
     {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            if (!run || t >= ntile0) break;
-            const int il = 4 * warp + grp, i = t * kTile2 + il;
+        for (int r = 0; r < 4; ++r) {
+            if (!run || r >= nround0) break;
+            const int il = 4 * warp + grp, i = r * kTile2 + il;
             float qf[16], f[16];
-            unpack_q(q0[t], qf);
+            unpack_q(q0[r], qf);
             const int di = i < n ? sDep[i] : 0;
             const int dmax = group_max(di);
             const int16_t *anc = sAnc + (i < n ? i : 0) * md;
@@ -648,41 +649,44 @@ __global__ void __launch_bounds__(kThreadsS, 1)
             uint32_t hi[8], lo[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) split_pair(qf[2 * e] * f[2 * e], qf[2 * e + 1] * f[2 * e + 1], hi[e], lo[e]);
-            if (t >= 2) {  // tile t - 2's MMAs still read this buffer
-                run = wait_all(kBarMma0 + (t & 1), ((t - 2) >> 1) & 1);
+            if (r == 2) {  // tile 0's MMAs still read the operand
+                run = wait_all(kBarMma0, 0);
                 if (!run) break;
             }
-            uint8_t *Bt = R2 + (t & 1) * 32768;
+            const int row = (r & 1) * kTile2 + il;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const uint32_t o = swz_offset(il, 32 * u + 4 * l8, kTile2 * 128);
-                *reinterpret_cast<uint2 *>(Bt + o) = make_uint2(hi[2 * u], hi[2 * u + 1]);
-                *reinterpret_cast<uint2 *>(Bt + 16384 + o) = make_uint2(lo[2 * u], lo[2 * u + 1]);
+                const uint32_t o = swz_offset(row, 32 * u + 4 * l8, 2 * kTile2 * 128);
+                *reinterpret_cast<uint2 *>(R2 + o) = make_uint2(hi[2 * u], hi[2 * u + 1]);
+                *reinterpret_cast<uint2 *>(R2 + 32768 + o) = make_uint2(lo[2 * u], lo[2 * u + 1]);
             }
+            if ((r & 1) == 0 && r + 1 < nround0) continue;  // the tile's second round follows
+            // rows of a tile's missing second round are stale: their columns (nodes
+            // past n) are never stored
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
             ptx::tc_fence_after_sync();
             if (tid == 0) {
                 // descriptors step by adding 16-byte units to the start-address field
-                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTile2);
-                const uint64_t bh = ptx::desc_kmajor_sw128(ptx::smem_addr(Bt), 1024);
-                const uint64_t bl = bh + (16384 >> 4);
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 2 * kTile2);
+                const uint64_t bh = ptx::desc_kmajor_sw128(ptx::smem_addr(R2), 1024);
+                const uint64_t bl = bh + (32768 >> 4);
 #pragma unroll 1
                 for (int p = 0; p < 3; ++p)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)  // 16-key steps
-                        ptx::mma_bf16_ts(tmem + t * kTile2, tmem + kA0 + (p == 1 ? 64 : 0) + kk * 8,
+                        ptx::mma_bf16_ts(tmem + (r >> 1) * 2 * kTile2, tmem + kA0 + (p == 1 ? 64 : 0) + kk * 8,
                                          (p == 2 ? bl : bh) +
-                                             (((kk / 4) * (kTile2 * 128) + (kk % 4) * 32) >> 4),
+                                             (((kk / 4) * (2 * kTile2 * 128) + (kk % 4) * 32) >> 4),
                                          idesc, (p > 0 || kk > 0) ? 1u : 0u);
-                ptx::mma_commit(bar(kBarMma0 + (t & 1)));
+                ptx::mma_commit(bar(kBarMma0 + (r >> 1)));
             }
         }
     }
-    if (run && ntile0 > 0) run = wait_all(kBarMma0 + ((ntile0 - 1) & 1), ((ntile0 - 1) >> 1) & 1);
+    if (run && ntile0 > 0) run = wait_all(kBarMma0 + (ntile0 - 1), 0);
 
-    // ---- phase 1: k rows where the B tiles were; the walks (the first round's q
+    // ---- phase 1: k rows where the B tile was; the walks (the first round's q
     // rows requested while k lands, the others one round ahead)
     auto walk_node = [&](int pos) { return pos < n ? static_cast<int>(sOrd[pos]) : n; };
     uint2 qn[4];
