@@ -348,12 +348,13 @@ __global__ void __launch_bounds__(kThreadsG, 2) verify_tc_big_kernel(const Verif
 // Staged variant: the whole request's rows in shared memory, both terms on the
 // tensor cores.
 //
-// One CTA = one (request, head), 512 threads, one CTA per SM.  The same closed
-// form, reorganised so that no ancestor row is fetched through the caches more
-// than once per request:
-//   start    g (n x 128 fp32) and H0 are requested by TMA; H0 is split into bf16
-//            hi + lo and stored transposed in tensor memory (lane = value channel,
-//            keys along the columns) as the A operand of the H0 term.
+// Persistent: one CTA of 512 threads per SM takes the (request, head) units
+// blockIdx.x, + gridDim.x, ... in turn.  The same closed form, reorganised so that
+// no ancestor row is fetched through the caches more than once per unit:
+//   start    g (n x 128 fp32) and H0 are requested by TMA while the previous unit
+//            finishes; H0 is split into bf16 hi + lo and stored transposed in
+//            tensor memory (lane = value channel, keys along the columns) as the A
+//            operand of the H0 term.
 //   phase 0  E = e^g in place, one exponential per node and channel.  In tiles of
 //            128 nodes, each node's e^{G_i} * q_i is the product of its root path's
 //            E rows (shared memory only) and becomes a bf16 hi/lo B operand row;
@@ -364,13 +365,15 @@ __global__ void __launch_bounds__(kThreadsG, 2) verify_tc_big_kernel(const Verif
 //            per warp (nodes bucketed by depth), four ancestors per round with one
 //            transposed reduction.
 //   phase 2  v lands by TMA (128-byte swizzled, MN-major: node rows of 64 channels)
-//            where E was.  Per tile of 64 nodes (two in flight, the second where k
-//            was) the weights are scattered into a dense bf16 hi/lo K-major B
-//            operand W[i][j] (zero off the root paths) and one thread issues
-//            D[:, tile] += V^T W^T (K = ancestors j < the tile's end).  The
-//            epilogue copies D from tensor memory to the rows of out.
-// Shared memory at 256 nodes and depth 16: 128 KB (E, then v + a W tile), 64 KB
-// (the B tile, then k, then a W tile), 16 KB w, 8 KB root paths, parents and depths.
+//            where E was, then the next unit's H0 (into k's place) and q rows.
+//            Per tile of 64 nodes the weights are scattered into a dense bf16
+//            hi/lo K-major B operand W[i][j] (zero off the root paths) and one
+//            thread issues D[:, tile] += V^T W^T (K = ancestors j < the tile's
+//            end); while a tile's MMAs run, the previous tile's columns of D go
+//            from tensor memory to the rows of out.  Once the last MMAs are done
+//            the next unit's g is requested where E was.
+// Shared memory at 256 nodes and depth 16: 128 KB (E, then v + the W tile), 64 KB
+// (H0, the B tile, then k), 16 KB w, 8 KB root paths, parents and depths.
 // ============================================================================
 
 constexpr int kThreadsS = 512;
@@ -426,8 +429,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     int *sFlag = reinterpret_cast<int *>(smem + L.misc_off + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int unit = blockIdx.x, b = unit / H, h = unit % H;
-    enum { kBarG = 0, kBarH0, kBarK, kBarV, kBarMma0, kBarMma1, kBarMma2, kBarMma3, kBars };
+    const int nunits = a.B * a.H;
+    enum { kBarG = 0, kBarH0, kBarK, kBarV, kBarMma0, kBarMma1, kBarMma2, kBars };
     auto bar = [&](int i) { return ptx::smem_addr(&bars[i]); };
     constexpr uint32_t ncols = 512;  // D: columns 0..255; H0^T hi/lo: kA0 .. kA0 + 127
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
@@ -435,7 +438,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     if (tid == 0) {
         for (int i = 0; i < kBars; ++i) ptx::mbar_init(bar(i), 1);
         ptx::fence_mbar_init();
-        *sFlag = 0;
         if (DIAG) ptx::prefetch_tensormap(&tm_g);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
@@ -449,152 +451,61 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *sTmem;
 
-    ptx::grid_dependency_wait();  // inputs may be written by the previous kernel
-    int off = 0, n = 0;
-    const bool range_ok = request_range(a.node_offsets, b, a.T, a.max_nodes, off, n);
-    if (!range_ok && tid == 0 && h == 0) report(a.status, TV_ERR_TREE);
-    const bool have_nodes = range_ok && n > 0;
-    const int nbox = (n + kBoxRows - 1) / kBoxRows;
-    // copies in flight, as seen by thread 0 (each barrier completes at most once)
+    // Every barrier completes once per use; its count of completions consumed so
+    // far (the same in every thread) gives the parity of the next one.  The copies
+    // in flight are tracked by thread 0 for the bounded waits at the end.
+    uint32_t nG = 0, nH0 = 0, nK = 0, nV = 0, nM0 = 0, nM1 = 0, nM2 = 0;
     bool pend_g = false, pend_h0 = false, pend_k = false, pend_v = false;
-    if (tid == 0 && have_nodes) {
-        // H0 (64 KB) where the phase-0 operand tiles go later
-        const float *src = a.H0 + (size_t)unit * kDimG * kDimG;
+    // thread 0 waits on a barrier, everyone learns the outcome
+    auto wait_all = [&](int i, uint32_t &count) {
+        bool ok = true;
+        if (tid == 0) ok = ptx::mbar_wait(bar(i), count & 1u, kWaitLimit);
+        ok = __syncthreads_and(ok);
+        if (ok) ++count;
+        else if (tid == 0) report(a.status, TV_ERR_TIMEOUT);
+        return ok;
+    };
+
+    struct Unit {
+        int b, h, off, n;
+        bool ok;
+    };
+    auto unit_at = [&](int u) {
+        Unit x;
+        x.b = u / H;
+        x.h = u % H;
+        x.ok = request_range(a.node_offsets, x.b, a.T, a.max_nodes, x.off, x.n);
+        return x;
+    };
+    // a unit's H0 (64 KB, where the phase-0 operand goes later) and g rows, by thread 0
+    auto issue_h0 = [&](int u) {
+        const float *src = a.H0 + (size_t)u * kDimG * kDimG;
         ptx::mbar_arrive_expect_tx(bar(kBarH0), kABytes);
         for (int c = 0; c < 4; ++c)
             ptx::bulk_g2s(ptx::smem_addr(R2) + c * kChunkG, src + c * kChunkRows * kDimG, kChunkG,
                           bar(kBarH0));
         pend_h0 = true;
-        if (DIAG) {
-            ptx::mbar_arrive_expect_tx(bar(kBarG), nbox * kBoxRows * kDimG * 4);
-            for (int r = 0; r < nbox; ++r)
-                ptx::tma_load_3d(ptx::smem_addr(R1) + r * kBoxRows * kDimG * 4, &tm_g, 0, h,
-                                 off + r * kBoxRows, bar(kBarG));
-            pend_g = true;
-        }
-    }
-    ptx::grid_launch_dependents();
+    };
+    auto issue_g = [&](const Unit &x) {
+        const int nb = (x.n + kBoxRows - 1) / kBoxRows;
+        ptx::mbar_arrive_expect_tx(bar(kBarG), nb * kBoxRows * kDimG * 4);
+        for (int r = 0; r < nb; ++r)
+            ptx::tma_load_3d(ptx::smem_addr(R1) + r * kBoxRows * kDimG * 4, &tm_g, 0, x.h,
+                             x.off + r * kBoxRows, bar(kBarG));
+        pend_g = true;
+    };
 
-    // The q rows of this warp's phase-0 nodes, read while the tree is checked and
-    // g and H0 land.  Walks use eight lanes per node, four nodes per warp (node
-    // 4 * warp + group of each 64-node round); lane l of a group holds channels
-    // 32 t + 4 l + m (t, m < 4), so that a group's loads of one row cover whole
-    // 128-byte lines.
+    // Walks use eight lanes per node, four nodes per warp (node 4 * warp + group of
+    // each 64-node round); lane l of a group holds channels 32 t + 4 l + m (t, m < 4),
+    // so that a group's loads of one row cover whole 128-byte lines.
     const int grp = lane >> 3, l8 = lane & 7;
-    auto qrow = [&](int i, uint2 (&r)[4]) {
+    auto qrow = [&](const Unit &x, int i, uint2 (&r)[4]) {
 #pragma unroll
         for (int t = 0; t < 4; ++t)
-            r[t] = i < n ? *reinterpret_cast<const uint2 *>(
-                               q + ((size_t)(off + i) * H + h) * kDimG + 32 * t + 4 * l8)
-                         : make_uint2(0u, 0u);
+            r[t] = i < x.n ? *reinterpret_cast<const uint2 *>(
+                                 q + ((size_t)(x.off + i) * H + x.h) * kDimG + 32 * t + 4 * l8)
+                           : make_uint2(0u, 0u);
     };
-    uint2 q0[4][4];  // phase-0 rounds (n <= 256: at most four)
-    if (have_nodes)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) qrow(t * kTile2 + 4 * warp + grp, q0[t]);
-
-    // ---- the tree: parents precede children, depth = depth(parent) + 1 <= max_depth;
-    // then every node's root path (node first), and for scalar decay E = e^g
-    if (have_nodes)
-        for (int i = tid; i < n; i += kThreadsS) {
-            const int p = a.parent[off + i];
-            const int d = a.depth[off + i];
-            const bool ok = p >= -1 && p < i && d >= 1 && d <= md;
-            sPar[i] = static_cast<int16_t>(ok ? p : -1);
-            sDep[i] = static_cast<int16_t>(ok ? d : 1);
-            if (!ok) *sFlag = 1;
-            if (!DIAG) sE[i] = expf(a.g[(size_t)(off + i) * H + h]);
-        }
-    __syncthreads();
-    if (have_nodes && *sFlag == 0)
-        for (int i = tid; i < n; i += kThreadsS) {
-            const int p = sPar[i];
-            if (sDep[i] != (p < 0 ? 1 : sDep[p] + 1)) *sFlag = 1;
-        }
-    __syncthreads();
-    const bool tree_ok = *sFlag == 0;
-    if (have_nodes && tree_ok)
-        for (int i = tid; i < n; i += kThreadsS) {
-            int j = i;
-            const int di = sDep[i];
-            for (int d = 0; d < di; ++d) {
-                sAnc[i * md + d] = static_cast<int16_t>(j);
-                j = sPar[j];
-            }
-        }
-    if (have_nodes && !tree_ok) {
-        for (int e = tid; e < n * kDimG; e += kThreadsS)
-            a.out[((size_t)(off + e / kDimG) * H + h) * kDimG + e % kDimG] = 0.f;
-        if (tid == 0 && h == 0) report(a.status, TV_ERR_TREE);
-    }
-    bool run = have_nodes && tree_ok;
-
-    // the walks' order: nodes bucketed by depth (a warp's four walks then take
-    // similar numbers of steps, and siblings read the same ancestor rows together)
-    if (run) {
-        if (tid <= md) sCnt[tid] = 0;
-        __syncthreads();
-        int slot = 0;
-        if (tid < n) slot = atomicAdd(&sCnt[sDep[tid]], 1);
-        __syncthreads();
-        if (tid == 0)
-            for (int d = 0, acc = 0; d <= md; ++d) {
-                const int c = sCnt[d];
-                sCnt[d] = acc;
-                acc += c;
-            }
-        __syncthreads();
-        if (tid < n) sOrd[sCnt[sDep[tid]] + slot] = static_cast<int16_t>(tid);
-    }
-
-    // thread 0 waits on a barrier, everyone learns the outcome
-    auto wait_all = [&](int i, uint32_t parity) {
-        bool ok = true;
-        if (tid == 0) ok = ptx::mbar_wait(bar(i), parity, kWaitLimit);
-        ok = __syncthreads_and(ok);
-        if (!ok && tid == 0) report(a.status, TV_ERR_TIMEOUT);
-        return ok;
-    };
-
-    // ---- H0^T as the A operand of the H0 term, in tensor memory: lane = value
-    // channel c, two keys per 32-bit column (the even key in the low half), hi in
-    // columns kA0 .. kA0 + 63 and lo in the next 64.  Each warp writes its lane
-    // quadrant's channels for 32 keys, from H0's rows in shared memory.
-    if (run) {
-        run = wait_all(kBarH0, 0);
-        if (tid == 0 && run) pend_h0 = false;
-    }
-    if (run) {
-        const int qd = warp & 3, cb = warp >> 2;
-        const float *h0 = reinterpret_cast<const float *>(R2) + (32 * cb) * kDimG + 32 * qd + lane;
-        float x0[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x0[e] = h0[e * kDimG];
-        uint32_t hi[2][8], lo[2][8];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) split_pair(x0[2 * e], x0[2 * e + 1], hi[e / 8][e % 8], lo[e / 8][e % 8]);
-        const uint32_t ta = tmem + (static_cast<uint32_t>(32 * qd) << 16) + kA0 + 16 * cb;
-        ptx::tmem_st_x8(ta, hi[0]);
-        ptx::tmem_st_x8(ta + 8, hi[1]);
-        ptx::tmem_st_x8(ta + 64, lo[0]);
-        ptx::tmem_st_x8(ta + 72, lo[1]);
-        ptx::tmem_wait_st();
-    }
-
-    // ---- phase 0: E = e^g in place
-    if (run && DIAG) {
-        run = wait_all(kBarG, 0);
-        if (tid == 0 && run) pend_g = false;
-        if (run)
-            for (int e = tid; e < n * (kDimG / 4); e += kThreadsS) {
-                float4 *p = reinterpret_cast<float4 *>(sE) + e;
-                float4 x = *p;
-                x.x = __expf(x.x); x.y = __expf(x.y); x.z = __expf(x.z); x.w = __expf(x.w);
-                *p = x;
-            }
-    }
-    __syncthreads();  // E is complete
-
     auto unpack_q = [&](const uint2 (&r)[4], float (&x)[16]) {
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -610,13 +521,138 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         return max(x, __shfl_xor_sync(0xffffffffu, x, 16));
     };
 
-    // ---- phase 0: H0 term in tiles of 128 nodes (two 64-node rounds of walks each),
-    // the B operand where k goes later: per node the product of its root path's E
-    // rows times q, split into bf16 hi/lo rows; D[:, tile] = A_hi B_hi + A_lo B_hi +
-    // A_hi B_lo (A from tensor memory)
-    const int nround0 = (n + kTile2 - 1) / kTile2;
-    const int ntile0 = (n + 2 * kTile2 - 1) / (2 * kTile2);
-    {
+    ptx::grid_dependency_wait();  // inputs may be written by the previous kernel
+    ptx::grid_launch_dependents();
+
+    // The CTA takes units blockIdx.x, + gridDim.x, ...  A unit's H0, g and phase-0 q
+    // rows are requested while the previous unit finishes (for the first one, here).
+    int u = blockIdx.x;
+    Unit cur = unit_at(u < nunits ? u : 0);
+    uint2 q0[4][4];  // phase-0 rounds (n <= 256: at most four)
+    if (u < nunits && cur.ok && cur.n > 0) {
+        if (tid == 0) {
+            issue_h0(u);
+            if (DIAG) issue_g(cur);
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) qrow(cur, t * kTile2 + 4 * warp + grp, q0[t]);
+    }
+    bool alive = true;  // false after a timed-out wait: the CTA stops
+    for (; alive && u < nunits; u += gridDim.x) {
+        const int h = cur.h, off = cur.off, n = cur.n;
+        const bool have_nodes = cur.ok && n > 0;
+        if (!cur.ok && tid == 0 && h == 0) report(a.status, TV_ERR_TREE);
+        const int nbox = (n + kBoxRows - 1) / kBoxRows;
+        const int un = u + gridDim.x;
+        const Unit nxt = unit_at(un < nunits ? un : 0);
+        const bool have_next = un < nunits && nxt.ok && nxt.n > 0;
+
+        // ---- the tree: parents precede children, depth = depth(parent) + 1 <=
+        // max_depth; then every node's root path (node first), and for scalar decay
+        // E = e^g
+        if (tid == 0) *sFlag = 0;
+        __syncthreads();
+        if (have_nodes)
+            for (int i = tid; i < n; i += kThreadsS) {
+                const int p = a.parent[off + i];
+                const int d = a.depth[off + i];
+                const bool ok = p >= -1 && p < i && d >= 1 && d <= md;
+                sPar[i] = static_cast<int16_t>(ok ? p : -1);
+                sDep[i] = static_cast<int16_t>(ok ? d : 1);
+                if (!ok) *sFlag = 1;
+                if (!DIAG) sE[i] = expf(a.g[(size_t)(off + i) * H + h]);
+            }
+        __syncthreads();
+        if (have_nodes && *sFlag == 0)
+            for (int i = tid; i < n; i += kThreadsS) {
+                const int p = sPar[i];
+                if (sDep[i] != (p < 0 ? 1 : sDep[p] + 1)) *sFlag = 1;
+            }
+        __syncthreads();
+        const bool tree_ok = *sFlag == 0;
+        if (have_nodes && tree_ok)
+            for (int i = tid; i < n; i += kThreadsS) {
+                int j = i;
+                const int di = sDep[i];
+                for (int d = 0; d < di; ++d) {
+                    sAnc[i * md + d] = static_cast<int16_t>(j);
+                    j = sPar[j];
+                }
+            }
+        if (have_nodes && !tree_ok) {
+            for (int e = tid; e < n * kDimG; e += kThreadsS)
+                a.out[((size_t)(off + e / kDimG) * H + h) * kDimG + e % kDimG] = 0.f;
+            if (tid == 0 && h == 0) report(a.status, TV_ERR_TREE);
+        }
+        bool run = have_nodes && tree_ok;
+
+        // the walks' order: nodes bucketed by depth (a warp's four walks then take
+        // similar numbers of steps, and siblings read the same ancestor rows together)
+        if (run) {
+            if (tid <= md) sCnt[tid] = 0;
+            __syncthreads();
+            int slot = 0;
+            if (tid < n) slot = atomicAdd(&sCnt[sDep[tid]], 1);
+            __syncthreads();
+            if (tid == 0)
+                for (int d = 0, acc = 0; d <= md; ++d) {
+                    const int c = sCnt[d];
+                    sCnt[d] = acc;
+                    acc += c;
+                }
+            __syncthreads();
+            if (tid < n) sOrd[sCnt[sDep[tid]] + slot] = static_cast<int16_t>(tid);
+        }
+
+        // ---- H0^T as the A operand of the H0 term, in tensor memory: lane = value
+        // channel c, two keys per 32-bit column (the even key in the low half), hi in
+        // columns kA0 .. kA0 + 63 and lo in the next 64.  Each warp writes its lane
+        // quadrant's channels for 32 keys, from H0's rows in shared memory.  (H0 and g
+        // were requested for every unit with nodes, so they are consumed even when
+        // its tree is malformed.)
+        if (have_nodes) {
+            alive = wait_all(kBarH0, nH0);
+            if (tid == 0 && alive) pend_h0 = false;
+            run = run && alive;
+        }
+        if (run) {
+            const int qd = warp & 3, cb = warp >> 2;
+            const float *h0 = reinterpret_cast<const float *>(R2) + (32 * cb) * kDimG + 32 * qd + lane;
+            float x0[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x0[e] = h0[e * kDimG];
+            uint32_t hi[2][8], lo[2][8];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) split_pair(x0[2 * e], x0[2 * e + 1], hi[e / 8][e % 8], lo[e / 8][e % 8]);
+            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * qd) << 16) + kA0 + 16 * cb;
+            ptx::tmem_st_x8(ta, hi[0]);
+            ptx::tmem_st_x8(ta + 8, hi[1]);
+            ptx::tmem_st_x8(ta + 64, lo[0]);
+            ptx::tmem_st_x8(ta + 72, lo[1]);
+            ptx::tmem_wait_st();
+        }
+
+        // ---- phase 0: E = e^g in place
+        if (have_nodes && DIAG && alive) {
+            alive = wait_all(kBarG, nG);
+            if (tid == 0 && alive) pend_g = false;
+            run = run && alive;
+            if (run)
+                for (int e = tid; e < n * (kDimG / 4); e += kThreadsS) {
+                    float4 *p = reinterpret_cast<float4 *>(sE) + e;
+                    float4 x = *p;
+                    x.x = __expf(x.x); x.y = __expf(x.y); x.z = __expf(x.z); x.w = __expf(x.w);
+                    *p = x;
+                }
+        }
+        __syncthreads();  // E is complete; H0 has been read out of R2
+
+        // ---- phase 0: H0 term in tiles of 128 nodes (two 64-node rounds of walks
+        // each), the B operand where H0 was: per node the product of its root path's
+        // E rows times q, split into bf16 hi/lo rows; D[:, tile] = A_hi B_hi +
+        // A_lo B_hi + A_hi B_lo (A from tensor memory)
+        const int nround0 = (n + kTile2 - 1) / kTile2;
+        const int ntile0 = (n + 2 * kTile2 - 1) / (2 * kTile2);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             if (!run || r >= nround0) break;
@@ -635,9 +671,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
                         const int j = anc[d0 + p];
                         if (DIAG) {
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const float4 e = *reinterpret_cast<const float4 *>(sE + j * kDimG + 32 * u + 4 * l8);
-                                f[4 * u] *= e.x; f[4 * u + 1] *= e.y; f[4 * u + 2] *= e.z; f[4 * u + 3] *= e.w;
+                            for (int c = 0; c < 4; ++c) {
+                                const float4 e = *reinterpret_cast<const float4 *>(sE + j * kDimG + 32 * c + 4 * l8);
+                                f[4 * c] *= e.x; f[4 * c + 1] *= e.y; f[4 * c + 2] *= e.z; f[4 * c + 3] *= e.w;
                             }
                         } else {
                             const float e = sE[j];
@@ -650,15 +686,16 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) split_pair(qf[2 * e] * f[2 * e], qf[2 * e + 1] * f[2 * e + 1], hi[e], lo[e]);
             if (r == 2) {  // tile 0's MMAs still read the operand
-                run = wait_all(kBarMma0, 0);
+                alive = wait_all(kBarMma0, nM0);
+                run = run && alive;
                 if (!run) break;
             }
             const int row = (r & 1) * kTile2 + il;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t o = swz_offset(row, 32 * u + 4 * l8, 2 * kTile2 * 128);
-                *reinterpret_cast<uint2 *>(R2 + o) = make_uint2(hi[2 * u], hi[2 * u + 1]);
-                *reinterpret_cast<uint2 *>(R2 + 32768 + o) = make_uint2(lo[2 * u], lo[2 * u + 1]);
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t o = swz_offset(row, 32 * c + 4 * l8, 2 * kTile2 * 128);
+                *reinterpret_cast<uint2 *>(R2 + o) = make_uint2(hi[2 * c], hi[2 * c + 1]);
+                *reinterpret_cast<uint2 *>(R2 + 32768 + o) = make_uint2(lo[2 * c], lo[2 * c + 1]);
             }
             if ((r & 1) == 0 && r + 1 < nround0) continue;  // the tile's second round follows
             // rows of a tile's missing second round are stale: their columns (nodes
@@ -683,180 +720,207 @@ __global__ void __launch_bounds__(kThreadsS, 1)
                 ptx::mma_commit(bar(kBarMma0 + (r >> 1)));
             }
         }
-    }
-    if (run && ntile0 > 0) run = wait_all(kBarMma0 + (ntile0 - 1), 0);
-
-    // ---- phase 1: k rows where the B tile was; the walks (the first round's q
-    // rows requested while k lands, the others one round ahead)
-    auto walk_node = [&](int pos) { return pos < n ? static_cast<int>(sOrd[pos]) : n; };
-    uint2 qn[4];
-    if (run) qrow(walk_node(4 * warp + grp), qn);
-    if (run) {
-        if (tid == 0) {
-            ptx::mbar_arrive_expect_tx(bar(kBarK), nbox * kBoxRows * kDimG * 2);
-            for (int r = 0; r < nbox; ++r)
-                ptx::tma_load_3d(ptx::smem_addr(R2) + r * kBoxRows * kDimG * 2, &tm_k, 0, h,
-                                 off + r * kBoxRows, bar(kBarK));
-            pend_k = true;
+        if (run && ntile0 > 0) {
+            alive = ntile0 == 1 ? wait_all(kBarMma0, nM0) : wait_all(kBarMma1, nM1);
+            run = alive;
         }
-        run = wait_all(kBarK, 0);
-        if (tid == 0 && run) pend_k = false;
-    }
-    if (run) {
-        // four nodes per warp in rounds of 64, in the depth order
-        for (int base = 4 * warp; base < n; base += 4 * kWarpsS) {
-            const int i = walk_node(base + grp);
-            float qf[16];
-            unpack_q(qn, qf);
-            qrow(walk_node(base + grp + 4 * kWarpsS), qn);
-            const int di = i < n ? sDep[i] : 0;
-            const int dmax = group_max(di);
-            const int16_t *anc = sAnc + (i < n ? i : 0) * md;
-            for (int d0 = 0; d0 < dmax; d0 += 4) {
-                // partial dot products of four ancestors (the decay advancing ancestor
-                // by ancestor), then one reduction over the group for all four
-                float part[4];
+
+        // ---- phase 1: k rows where the B operand was; the walks (the first round's
+        // q rows requested while k lands, the others one round ahead)
+        auto walk_node = [&](int pos) { return pos < n ? static_cast<int>(sOrd[pos]) : n; };
+        uint2 qn[4];
+        if (run) qrow(cur, walk_node(4 * warp + grp), qn);
+        if (run) {
+            if (tid == 0) {
+                ptx::mbar_arrive_expect_tx(bar(kBarK), nbox * kBoxRows * kDimG * 2);
+                for (int r = 0; r < nbox; ++r)
+                    ptx::tma_load_3d(ptx::smem_addr(R2) + r * kBoxRows * kDimG * 2, &tm_k, 0, h,
+                                     off + r * kBoxRows, bar(kBarK));
+                pend_k = true;
+            }
+            alive = wait_all(kBarK, nK);
+            if (tid == 0 && alive) pend_k = false;
+            run = alive;
+        }
+        if (run) {
+            // four nodes per warp in rounds of 64, in the depth order
+            for (int base = 4 * warp; base < n; base += 4 * kWarpsS) {
+                const int i = walk_node(base + grp);
+                float qf[16];
+                unpack_q(qn, qf);
+                qrow(cur, walk_node(base + grp + 4 * kWarpsS), qn);
+                const int di = i < n ? sDep[i] : 0;
+                const int dmax = group_max(di);
+                const int16_t *anc = sAnc + (i < n ? i : 0) * md;
+                for (int d0 = 0; d0 < dmax; d0 += 4) {
+                    // partial dot products of four ancestors (the decay advancing
+                    // ancestor by ancestor), then one reduction over the group for all four
+                    float part[4];
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    part[p] = 0.f;
-                    if (d0 + p < di) {
-                        const int j = anc[d0 + p];
-                        const __nv_bfloat16 *kr = sK + j * kDimG + 4 * l8;
-                        const float *er = sE + j * kDimG + 4 * l8;
-                        const float es = DIAG ? 0.f : sE[j];
+                    for (int p = 0; p < 4; ++p) {
+                        part[p] = 0.f;
+                        if (d0 + p < di) {
+                            const int j = anc[d0 + p];
+                            const __nv_bfloat16 *kr = sK + j * kDimG + 4 * l8;
+                            const float *er = sE + j * kDimG + 4 * l8;
+                            const float es = DIAG ? 0.f : sE[j];
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const uint2 kraw = *reinterpret_cast<const uint2 *>(kr + 32 * t);
-                            const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kraw);
-                            part[p] += qf[4 * t] * __low2float(k2[0]) + qf[4 * t + 1] * __high2float(k2[0]) +
-                                       qf[4 * t + 2] * __low2float(k2[1]) + qf[4 * t + 3] * __high2float(k2[1]);
-                            if (DIAG) {
-                                const float4 e = *reinterpret_cast<const float4 *>(er + 32 * t);
-                                qf[4 * t] *= e.x; qf[4 * t + 1] *= e.y;
-                                qf[4 * t + 2] *= e.z; qf[4 * t + 3] *= e.w;
-                            } else {
+                            for (int t = 0; t < 4; ++t) {
+                                const uint2 kraw = *reinterpret_cast<const uint2 *>(kr + 32 * t);
+                                const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kraw);
+                                part[p] += qf[4 * t] * __low2float(k2[0]) + qf[4 * t + 1] * __high2float(k2[0]) +
+                                           qf[4 * t + 2] * __low2float(k2[1]) + qf[4 * t + 3] * __high2float(k2[1]);
+                                if (DIAG) {
+                                    const float4 e = *reinterpret_cast<const float4 *>(er + 32 * t);
+                                    qf[4 * t] *= e.x; qf[4 * t + 1] *= e.y;
+                                    qf[4 * t + 2] *= e.z; qf[4 * t + 3] *= e.w;
+                                } else {
 #pragma unroll
-                                for (int m = 0; m < 4; ++m) qf[4 * t + m] *= es;
+                                    for (int m = 0; m < 4; ++m) qf[4 * t + m] *= es;
+                                }
                             }
                         }
                     }
+                    // lanes with bit 2 clear keep ancestors 0,1 and the others 2,3;
+                    // then bit 1 picks one of the two; bit 0 completes the sum
+                    const bool b2 = l8 & 4, b1 = l8 & 2;
+                    float x0 = b2 ? part[2] : part[0], x1 = b2 ? part[3] : part[1];
+                    const float y0 = b2 ? part[0] : part[2], y1 = b2 ? part[1] : part[3];
+                    x0 += __shfl_xor_sync(0xffffffffu, y0, 4);
+                    x1 += __shfl_xor_sync(0xffffffffu, y1, 4);
+                    float z = b1 ? x1 : x0;
+                    z += __shfl_xor_sync(0xffffffffu, b1 ? x0 : x1, 2);
+                    z += __shfl_xor_sync(0xffffffffu, z, 1);
+                    const int which = (b2 ? 2 : 0) + (b1 ? 1 : 0);  // ancestor d0 + which
+                    if ((l8 & 1) == 0 && d0 + which < di) sW[i * md + d0 + which] = z;
                 }
-                // lanes with bit 2 clear keep ancestors 0,1 and the others 2,3; then
-                // bit 1 picks one of the two; bit 0 completes the sum
-                const bool b2 = l8 & 4, b1 = l8 & 2;
-                float x0 = b2 ? part[2] : part[0], x1 = b2 ? part[3] : part[1];
-                const float y0 = b2 ? part[0] : part[2], y1 = b2 ? part[1] : part[3];
-                x0 += __shfl_xor_sync(0xffffffffu, y0, 4);
-                x1 += __shfl_xor_sync(0xffffffffu, y1, 4);
-                float z = b1 ? x1 : x0;
-                z += __shfl_xor_sync(0xffffffffu, b1 ? x0 : x1, 2);
-                z += __shfl_xor_sync(0xffffffffu, z, 1);
-                const int which = (b2 ? 2 : 0) + (b1 ? 1 : 0);  // ancestor d0 + which
-                if ((l8 & 1) == 0 && d0 + which < di) sW[i * md + d0 + which] = z;
             }
         }
-    }
-    __syncthreads();  // every walk is done: E, k and w are final
+        __syncthreads();  // every walk is done: E, k and w are final
 
-    // ---- phase 2: v where E was; dense weight tiles of 64 nodes, two in flight
-    // (one where the rest of E was, one where k was); D += V^T W^T
-    const uint32_t slab_v = static_cast<uint32_t>(npad) * 128;  // one 64-channel block of v
-    constexpr uint32_t wslab = kTileW * 128;                     // 64 rows x 64 keys
-    const uint32_t w_half = static_cast<uint32_t>(npad / 64) * wslab;  // hi (or lo) of a tile
-    if (run && tid == 0) {
-        ptx::mbar_arrive_expect_tx(bar(kBarV), 2 * nbox * kBoxRows * 128);
-        for (int s = 0; s < 2; ++s)
-            for (int r = 0; r < nbox; ++r)
-                ptx::tma_load_3d(ptx::smem_addr(R1) + s * slab_v + r * kBoxRows * 128, &tm_v, 64 * s,
-                                 h, off + r * kBoxRows, bar(kBarV));
-        pend_v = true;
-    }
-    const int ntile2 = (n + kTileW - 1) / kTileW;
-    const int n16 = (n + 15) & ~15;
-    for (int t = 0; run && t < ntile2; ++t) {
-        const int kt = min(n16, (t + 1) * kTileW);  // keys j < kt can be ancestors
-        const int nslab = (kt + 63) / 64;
-        uint8_t *Wt = (t & 1) ? R2 : R1 + 2 * slab_v;
-        if (t >= 2) {  // tile t - 2's MMAs still read this buffer
-            run = wait_all(kBarMma2 + (t & 1), ((t - 2) >> 1) & 1);
-            if (!run) break;
+        // ---- phase 2: v where E was; dense weight tiles of 64 nodes in the rest of
+        // E's space; D += V^T W^T
+        const uint32_t slab_v = static_cast<uint32_t>(npad) * 128;  // one 64-channel block of v
+        constexpr uint32_t wslab = kTileW * 128;                     // 64 rows x 64 keys
+        const uint32_t w_half = static_cast<uint32_t>(npad / 64) * wslab;  // hi (or lo) of a tile
+        uint8_t *Wt = R1 + 2 * slab_v;
+        if (run && tid == 0) {
+            ptx::mbar_arrive_expect_tx(bar(kBarV), 2 * nbox * kBoxRows * 128);
+            for (int s = 0; s < 2; ++s)
+                for (int r = 0; r < nbox; ++r)
+                    ptx::tma_load_3d(ptx::smem_addr(R1) + s * slab_v + r * kBoxRows * 128, &tm_v,
+                                     64 * s, h, off + r * kBoxRows, bar(kBarV));
+            pend_v = true;
         }
-        for (int e = tid; e < nslab * (wslab / 16); e += kThreadsS) {  // 16-byte pieces
-            *reinterpret_cast<uint4 *>(Wt + e * 16) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4 *>(Wt + w_half + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+        // R2 (k) is free until the end of the unit: the next unit's H0, after v; and
+        // the next unit's phase-0 q rows
+        if (alive && have_next) {
+            if (tid == 0) issue_h0(un);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) qrow(nxt, t * kTile2 + 4 * warp + grp, q0[t]);
         }
-        __syncthreads();
-        for (int e = tid; e < kTileW * md; e += kThreadsS) {
-            const int il = e / md, d = e % md, i = t * kTileW + il;
-            if (i < n && d < sDep[i]) {
-                const float w = sW[i * md + d];
-                const int j = sAnc[i * md + d];
-                const uint32_t bits = __float_as_uint(w);
-                const float whi = __uint_as_float(bits & 0xFFFF0000u);
-                const uint32_t o = swz_offset(il, j, wslab);
-                *reinterpret_cast<uint16_t *>(Wt + o) = static_cast<uint16_t>(bits >> 16);
-                *reinterpret_cast<__nv_bfloat16 *>(Wt + w_half + o) = __float2bfloat16_rn(w - whi);
+        // a finished tile's D columns to the rows of out: lanes = value channels of
+        // the warp's quadrant, 16 columns per warp
+        auto store_tile = [&](int tt) {
+            const int quad = warp & 3, col = tt * kTileW + 16 * (warp >> 2);
+            if (col >= n) return;
+            const int c = 32 * quad + lane;
+            const uint32_t tq = tmem + (static_cast<uint32_t>(32 * quad) << 16) + col;
+            uint32_t r0[8], r1[8];
+            ptx::tmem_ld_x8_nowait(tq, r0);
+            ptx::tmem_ld_x8_nowait(tq + 8, r1);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int i = col + e;
+                if (i < n)
+                    a.out[((size_t)(off + i) * H + h) * kDimG + c] = __uint_as_float(e < 8 ? r0[e] : r1[e - 8]);
             }
-        }
-        if (t == 0) {
-            run = wait_all(kBarV, 0);
-            if (!run) break;
-            if (tid == 0) pend_v = false;
-            // rows n .. n16-1 of v (another request's, or zero past the end) meet
-            // zero weights; clear them so that no non-finite value gets in
-            for (int e = tid; e < (n16 - n) * 2 * 8; e += kThreadsS) {
-                const int row = n + e / 16, s = (e / 8) & 1, piece = e & 7;
-                *reinterpret_cast<uint4 *>(R1 + s * slab_v + row * 128 + piece * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+        };
+        const int ntile2 = (n + kTileW - 1) / kTileW;
+        const int n16 = (n + 15) & ~15;
+        for (int t = 0; run && t < ntile2; ++t) {
+            const int kt = min(n16, (t + 1) * kTileW);  // keys j < kt can be ancestors
+            const int nslab = (kt + 63) / 64;
+            if (t >= 1) {  // tile t - 1's MMAs still read W
+                alive = wait_all(kBarMma2, nM2);
+                run = alive;
+                if (!run) break;
+                ptx::tc_fence_after_sync();
             }
+            for (int e = tid; e < nslab * (wslab / 16); e += kThreadsS) {  // 16-byte pieces
+                *reinterpret_cast<uint4 *>(Wt + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(Wt + w_half + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncthreads();
+            for (int e = tid; e < kTileW * md; e += kThreadsS) {
+                const int il = e / md, d = e % md, i = t * kTileW + il;
+                if (i < n && d < sDep[i]) {
+                    const float w = sW[i * md + d];
+                    const int j = sAnc[i * md + d];
+                    const uint32_t bits = __float_as_uint(w);
+                    const float whi = __uint_as_float(bits & 0xFFFF0000u);
+                    const uint32_t o = swz_offset(il, j, wslab);
+                    *reinterpret_cast<uint16_t *>(Wt + o) = static_cast<uint16_t>(bits >> 16);
+                    *reinterpret_cast<__nv_bfloat16 *>(Wt + w_half + o) = __float2bfloat16_rn(w - whi);
+                }
+            }
+            if (t == 0) {
+                alive = wait_all(kBarV, nV);
+                run = alive;
+                if (!run) break;
+                if (tid == 0) pend_v = false;
+                // rows n .. n16-1 of v (another request's, or zero past the end) meet
+                // zero weights; clear them so that no non-finite value gets in
+                for (int e = tid; e < (n16 - n) * 2 * 8; e += kThreadsS) {
+                    const int row = n + e / 16, s = (e / 8) & 1, piece = e & 7;
+                    *reinterpret_cast<uint4 *>(R1 + s * slab_v + row * 128 + piece * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before_sync();
+            __syncthreads();
+            ptx::tc_fence_after_sync();
+            if (tid == 0) {
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTileW) | (1u << 15);  // A MN-major
+                const uint64_t a0 = ptx::desc_mnmajor_sw128(ptx::smem_addr(R1), slab_v, 1024);
+                const uint64_t wh = ptx::desc_kmajor_sw128(ptx::smem_addr(Wt), 1024), wl = wh + (w_half >> 4);
+#pragma unroll 4
+                for (int kk = 0; kk < kt / 16; ++kk) {
+                    const uint64_t ad = a0 + ((kk * 2048) >> 4);
+                    const uint32_t wo = ((kk / 4) * wslab + (kk % 4) * 32) >> 4;
+                    ptx::mma_bf16(tmem + t * kTileW, ad, wh + wo, idesc, 1u);
+                    ptx::mma_bf16(tmem + t * kTileW, ad, wl + wo, idesc, 1u);
+                }
+                ptx::mma_commit(bar(kBarMma2));
+            }
+            if (t >= 1) store_tile(t - 1);  // while tile t's MMAs run
         }
-        ptx::fence_proxy_async_smem();
+        if (run && ntile2 > 0) {
+            alive = wait_all(kBarMma2, nM2);
+            run = alive;
+        }
+        ptx::tc_fence_after_sync();
+
+        // R1 is free (the tree MMAs are done): the next unit's g, while the last tile
+        // is stored
+        if (alive && have_next && tid == 0 && DIAG) issue_g(nxt);
+        if (run && ntile2 > 0) store_tile(ntile2 - 1);
+        // shared and tensor memory are rewritten by the next unit
         ptx::tc_fence_before_sync();
         __syncthreads();
         ptx::tc_fence_after_sync();
-        if (tid == 0) {
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTileW) | (1u << 15);  // A MN-major
-            const uint64_t a0 = ptx::desc_mnmajor_sw128(ptx::smem_addr(R1), slab_v, 1024);
-            const uint64_t wh = ptx::desc_kmajor_sw128(ptx::smem_addr(Wt), 1024), wl = wh + (w_half >> 4);
-#pragma unroll 4
-            for (int kk = 0; kk < kt / 16; ++kk) {
-                const uint64_t ad = a0 + ((kk * 2048) >> 4);
-                const uint32_t wo = ((kk / 4) * wslab + (kk % 4) * 32) >> 4;
-                ptx::mma_bf16(tmem + t * kTileW, ad, wh + wo, idesc, 1u);
-                ptx::mma_bf16(tmem + t * kTileW, ad, wl + wo, idesc, 1u);
-            }
-            ptx::mma_commit(bar(kBarMma2 + (t & 1)));
-        }
-    }
-    if (run && ntile2 > 0)
-        run = wait_all(kBarMma2 + ((ntile2 - 1) & 1), ((ntile2 - 1) >> 1) & 1);
-    ptx::tc_fence_after_sync();
-
-    // ---- epilogue: lanes = value channels of the warp's quadrant, 64 columns per
-    // warp group; D to the rows of out
-    if (run) {
-        const int quad = warp & 3, cg = warp >> 2;
-        const int c = 32 * quad + lane;
-        const uint32_t tq = tmem + (static_cast<uint32_t>(32 * quad) << 16);
-        for (int col = cg * kTile2; col < n && col < (cg + 1) * kTile2; col += 32) {
-            uint32_t r[32];
-            ptx::tmem_ld_x32_nowait(tq + col, r);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int i = col + e;
-                if (i < n) a.out[((size_t)(off + i) * H + h) * kDimG + c] = __uint_as_float(r[e]);
-            }
-        }
+        cur = nxt;
     }
 
-    // copies still in flight after a failed wait or an early exit: one more bounded
-    // wait each before the CTA (and its shared memory) goes away
+    // copies still in flight after a failed wait: one more bounded wait each before
+    // the CTA (and its shared memory) goes away
     if (tid == 0) {
-        if (pend_g) ptx::mbar_wait(bar(kBarG), 0, kWaitLimit);
-        if (pend_h0) ptx::mbar_wait(bar(kBarH0), 0, kWaitLimit);
-        if (pend_k) ptx::mbar_wait(bar(kBarK), 0, kWaitLimit);
-        if (pend_v) ptx::mbar_wait(bar(kBarV), 0, kWaitLimit);
+        if (pend_g) ptx::mbar_wait(bar(kBarG), nG & 1u, kWaitLimit);
+        if (pend_h0) ptx::mbar_wait(bar(kBarH0), nH0 & 1u, kWaitLimit);
+        if (pend_k) ptx::mbar_wait(bar(kBarK), nK & 1u, kWaitLimit);
+        if (pend_v) ptx::mbar_wait(bar(kBarV), nV & 1u, kWaitLimit);
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -899,7 +963,15 @@ cudaError_t launch_verify_tc_staged(const VerifyArgs &a, cudaStream_t s) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3((unsigned)(a.B * a.H)), dim3(kThreadsS), smem, s, tg, tk, tv_, a);
+    // persistent: one CTA per SM, each taking every gridDim-th (request, head) unit
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long units = (long long)a.B * a.H;
+    const unsigned grid = (unsigned)(units < sms ? units : sms);
+    return launch_pdl(kern, dim3(grid), dim3(kThreadsS), smem, s, tg, tk, tv_, a);
 }
 
 }  // namespace
