@@ -36,18 +36,17 @@ struct WarpBest {
     int i;
 };
 
-// Largest key, then smallest i, over aligned groups of `width` lanes (a power of
-// two; 32 = the whole warp).
-__device__ __forceinline__ WarpBest warp_best(long long k, int i, int width = 32) {
-    for (int o = width >> 1; o > 0; o >>= 1) {
-        const long long ok = __shfl_xor_sync(0xffffffffu, k, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-        if (ok > k || (ok == k && oi < i)) {
-            k = ok;
-            i = oi;
-        }
-    }
-    return {k, i};
+// Largest key, then smallest i, over the lanes in `mask` (every lane of the mask
+// calls with the same mask): three warp reductions, on the key's high word, on its
+// low word among the lanes that tie, and on i among the lanes that tie on both.
+__device__ __forceinline__ WarpBest warp_best(long long k, int i, unsigned mask = 0xffffffffu) {
+    const int hi = static_cast<int>(k >> 32);
+    const unsigned lo = static_cast<unsigned>(k);
+    const int mh = __reduce_max_sync(mask, hi);
+    const unsigned ml = __reduce_max_sync(mask, hi == mh ? lo : 0u);
+    const int mi = __reduce_min_sync(mask, (hi == mh && lo == ml) ? i : 0x7fffffff);
+    return {static_cast<long long>((static_cast<unsigned long long>(static_cast<unsigned>(mh)) << 32) | ml),
+            mi};
 }
 
 __global__ void __launch_bounds__(kWarpsB * 32) build_tree_kernel(BuildArgs a) {
@@ -58,8 +57,6 @@ __global__ void __launch_bounds__(kWarpsB * 32) build_tree_kernel(BuildArgs a) {
     pdl_launch_next();
     if (b >= a.B) return;
     const int C = a.C, cap = a.depth_cap, n = a.n;
-    int cw = 1;  // candidate lanes rounded up to a power of two
-    while (cw < C) cw <<= 1;
     // per warp, in doubles: q [cap][C]; per entry rho (fp64) and score key (int64),
     // best child, depth and taken mask (three 32-bit words, two doubles of room)
     const size_t per_warp = (size_t)cap * C + 4 * (size_t)(n + 1);
@@ -80,8 +77,25 @@ __global__ void __launch_bounds__(kWarpsB * 32) build_tree_kernel(BuildArgs a) {
         const int d = edep[e];
         long long k = -1;
         if (lane < C && !((taken >> lane) & 1u)) k = score_key(erho[e] * sq[d * C + lane]);
-        const WarpBest bb = warp_best(k, lane < C ? lane : 0x7fffffff, cw);
+        const WarpBest bb = warp_best(k, lane < C ? lane : 0x7fffffff);
         if (lane == 0) {
+            escore[e] = bb.k;
+            ebest[e] = bb.i;
+        }
+        __syncwarp();
+    };
+    // the same for entries e0 and (when two) e1 side by side, one per half-warp
+    // (C <= 16), from their rho, depth and taken mask as the caller holds them
+    auto refresh2 = [&](int e0, double rho0, int dep0, uint32_t mask0, int e1, double rho1,
+                        int dep1, bool two) {
+        const int half = lane >> 4, c = lane & 15;
+        const bool act = c < C && (half == 0 || two);
+        const int e = half ? e1 : e0;
+        long long k = -1;
+        if (act && !(((half ? 0u : mask0) >> c) & 1u))
+            k = score_key((half ? rho1 : rho0) * sq[(half ? dep1 : dep0) * C + c]);
+        const WarpBest bb = warp_best(k, act ? c : 0x7fffffff, half ? 0xffff0000u : 0x0000ffffu);
+        if (c == 0 && (half == 0 || two)) {
             escore[e] = bb.k;
             ebest[e] = bb.i;
         }
@@ -100,40 +114,62 @@ __global__ void __launch_bounds__(kWarpsB * 32) build_tree_kernel(BuildArgs a) {
     int32_t *tok_out = a.token + (size_t)b * n;
     double *rho_out = a.rho + (size_t)b * n;
     double total = 0.0;
+    double prev_ratio = 0.0;  // total / C(i), as the previous step computed it
     int count = 0;
+    // entries 0..n in blocks of `per` consecutive entries per lane (per <= 9)
+    const int per = (n + 1 + 31) / 32;
     for (int i = 0; i < n; ++i) {
         long long s = -1;
         int e = 0x7fffffff;
-        for (int k = lane; k <= i; k += 32) {  // entries 0..i exist
-            const long long ks = escore[k];
-            if (ks > s) {  // ascending k in a lane: the first maximum is the lowest
-                s = ks;
-                e = k;
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {  // entries 0..i exist
+            const int k = lane * per + j;
+            if (j < per && k <= i) {
+                const long long ks = escore[k];
+                if (ks > s) {  // ascending k in a lane: the first maximum is the lowest
+                    s = ks;
+                    e = k;
+                }
             }
         }
         const WarpBest best = warp_best(s, e);
         if (best.k < 0) break;  // the frontier is empty
         const int ep = best.i;
-        const double bs = erho[ep] * sq[edep[ep] * C + ebest[ep]];  // the entry's score
-        if (a.cost && i >= 1 && (total + bs) / a.cost[i + 1] < total / a.cost[i]) break;
+        // the entry's score: its key is the bit pattern of the product refresh formed
+        // (a zero of either sign reads back as +0)
+        const double bs = __longlong_as_double(best.k);
+        // the stop rule (sum rho) / C(N) would drop, tested after the frontier update
+        // so that the division overlaps it (on a stop, node i is not counted and its
+        // outputs are overwritten below); total / C(i) is the previous step's
+        // quotient, the same correctly rounded value
+        const double ratio = a.cost ? (total + bs) / a.cost[i + 1] : 0.0;
+        const bool stop = a.cost && i >= 1 && ratio < prev_ratio;
         const int y = ebest[ep];
         const int d = edep[ep] + 1;
+        const double rho_ep = erho[ep];
+        const uint32_t mask_ep = emask[ep] | (1u << y);
         if (lane == 0) {
             par_out[i] = ep - 1;
             tok_out[i] = y;
             rho_out[i] = bs;
-            emask[ep] |= 1u << y;
+            emask[ep] = mask_ep;
             // entry of node i: its children join the frontier below the depth cap
             erho[i + 1] = bs;
             edep[i + 1] = d;
             emask[i + 1] = 0u;
             escore[i + 1] = -1;
         }
-        total += bs;
-        count = i + 1;
         __syncwarp();
-        refresh(ep);
-        if (d < cap) refresh(i + 1);
+        if (C <= 16) {
+            refresh2(ep, rho_ep, d - 1, mask_ep, i + 1, bs, d, d < cap);
+        } else {
+            refresh(ep);
+            if (d < cap) refresh(i + 1);
+        }
+        if (stop) break;
+        total += bs;
+        prev_ratio = ratio;
+        count = i + 1;
     }
     for (int i = count + lane; i < n; i += 32) {
         par_out[i] = -1;
