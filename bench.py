@@ -984,23 +984,26 @@ def run_e2e(args, host_batch, dev, stream, tv, world, fused):
     for s in range(2 * NS):
         step(s)
     torch.cuda.synchronize()
-    # one rotation (NS steps, one per set) as a CUDA graph: fork to the other streams,
-    # the steps with their cross-stream waits, join back
+    # ROT rotations (NS steps each, one per set) as one CUDA graph: fork to the other
+    # streams, the steps with their cross-stream waits, join back.  Replays of a graph
+    # on one stream run one after the other, so the copy pipeline drains only once
+    # per ROT * NS steps.
+    ROT = max(1, min(33, K // NS))
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=streams[0]):
         fork = torch.cuda.Event()
         fork.record(streams[0])
         for st in streams[1:]:
             st.wait_event(fork)
-        for s in range(NS):
+        for s in range(NS * ROT):
             step(s, first=0)
         join_into_first()
     with torch.cuda.stream(streams[0]):
         g.replay()
     torch.cuda.synchronize()
     barrier(world)
-    R = max(1, K // NS)
-    K = R * NS
+    R = max(1, K // (NS * ROT))
+    K = R * NS * ROT
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(streams[0]):
@@ -1021,8 +1024,8 @@ def run_e2e(args, host_batch, dev, stream, tv, world, fused):
             "copies": "one host-to-device copy of the step's inputs and one device-to-host "
                       "copy of its results per step (one staging layout, 256-byte aligned "
                       "fields); three staging sets on three streams, so a step's input "
-                      "copy overlaps the previous step's kernels; a rotation of three "
-                      "steps replays as one CUDA graph"}
+                      "copy overlaps the previous step's kernels and the copies of the "
+                      "other direction; %d steps replay as one CUDA graph" % (NS * ROT)}
 
 
 def profile_folded(args):
