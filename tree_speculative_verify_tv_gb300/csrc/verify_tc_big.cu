@@ -1,5 +1,8 @@
-// verify_tc_big.cu -- tree verification of large trees with the context term on
-// tcgen05 tensor cores, one node tile after another.
+// verify_tc_big.cu -- tree verification of large trees on tcgen05 tensor cores
+// (dk = dv = 128, up to 256 nodes).  Two kernels: the staged kernel (second below)
+// for trees whose k, decay and v rows fit shared memory, and the node-tiled kernel
+// (first) for deeper trees.  The staged kernel also serves per-channel-decay trees
+// of 64 or more nodes, where it beats the one-unit kernel.
 //
 // Tree closed form (Bole summary page, "Core techniques" §1-§2):
 //   o_i = H0^T (e^{G_i} * q_i) + sum_{j in anc*(i)} w_ij v_j,
@@ -8,9 +11,8 @@
 // (per key channel for diagonal decay, one value per node for scalar decay).  Only the
 // per-token factors are read; no per-node state is formed.
 //
-// For dk = dv = 128 and trees whose operands do not fit the single-tile kernel's
-// shared-memory plan (256-node trees).  One CTA = one (request, head), 256 threads,
-// two CTAs per SM at trees of depth <= 16:
+// Node-tiled kernel.  One CTA = one (request, head), 256 threads, two CTAs per SM
+// at trees of depth <= 16:
 //   * H0 (64 KB fp32) streams in as four 32-key chunks and is split once, in place,
 //     into bf16 hi + lo K-major A operands (value channels x keys); they stay in
 //     shared memory for every tile;
