@@ -311,6 +311,28 @@ def test_tiled_tensor_core_neighbor_rows_do_not_leak(decay):
     check_verify(b, res["out"], units=[u for u in range(b.B * b.H) if u // b.H != 2])
 
 
+@pytest.mark.parametrize("decay", ["diag", "scalar"])
+def test_tiled_tensor_core_many_units_with_empty_and_malformed(decay):
+    """The staged kernel runs one CTA per SM over the (request, head) units in turn:
+    512 units, so every CTA takes several, with empty requests and malformed trees
+    between valid ones (units that skip their phases must keep every later unit's
+    copies and barriers in step)."""
+    rng = np.random.default_rng(48 if decay == "diag" else 49)
+    sizes = [int(x) for x in rng.choice([0, 1, 17, 64, 100, 128], 64)]
+    b = workloads.random_batch(rng, sizes, 8, 128, 128, decay=decay, qkv_dtype="bf16",
+                               depth_cap=10, max_depth=12, max_nodes=128)
+    bad = [r for r in range(b.B) if sizes[r] >= 17][::5]
+    for r in bad:  # a parent after its child
+        s = int(b.node_offsets[r])
+        b.parent[s + 3] = 9
+    res = run_library(b, variant=4, steps=("verify",))
+    assert res["status"] == 6  # TV_ERR_TREE
+    for r in bad:
+        s, e = int(b.node_offsets[r]), int(b.node_offsets[r + 1])
+        assert np.all(res["out"][s:e] == 0.0)
+    check_verify(b, res["out"], units=[u for u in range(b.B * b.H) if u // b.H not in bad])
+
+
 @pytest.mark.parametrize("md", [21, 22])
 def test_tiled_tensor_core_staged_depth_limit(md):
     """256-node trees as deep as the staged kernel's shared-memory plan allows (21)
