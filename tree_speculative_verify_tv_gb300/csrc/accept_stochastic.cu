@@ -22,7 +22,10 @@
 // row and no scratch memory.  A pass adds its slice in every CTA, the eight slice
 // sums are exchanged through distributed shared memory, and every CTA adds them in
 // rank order, so all CTAs hold bit-identical sums and take identical decisions (the
-// cluster's control flow stays uniform, which the cluster barriers rely on).
+// cluster's control flow stays uniform, which the cluster barriers rely on).  When a
+// node is entered, each CTA starts asynchronous copies of its slice of the node's p
+// and q rows into shared memory (the passes read them there) and reads its children's
+// test values p(x), q(x) and uniforms in one round trip.
 //
 // Precision: a, b, the tested residual p_k(x) and every comparison are fp64.  The
 // row sums T (and the bonus token's running sums) are formed from per-element terms
@@ -101,22 +104,39 @@ __device__ __forceinline__ double block_sum(DF v, double *red) {
     return t;
 }
 
-// This CTA's part of T = sum_y max(P[y] - a Q[y], 0): elements [y0, y1).
-__device__ __forceinline__ double slice_sum(const float *P, const float *Q, int y0, int y1,
-                                            double a, double *red) {
+// This CTA's part of T = sum_y max(P[y] - a Q[y], 0): elements [y0, y1), read at
+// P[y - base], Q[y - base] (base = 0 for the rows in global memory, y0 for the slice
+// staged in shared memory; the same elements in the same order either way).
+__device__ __forceinline__ double slice_sum(const float *P, const float *Q, int base, int y0,
+                                            int y1, double a, double *red) {
     const float ahi = (float)a, alo = (float)(a - (double)ahi);
     DF acc = {0.f, 0.f};
     for (int y = y0 + threadIdx.x; y < y1; y += kThreadsA)
-        acc = df_add(acc, term(__ldg(P + y), __ldg(Q + y), ahi, alo));
+        acc = df_add(acc, term(P[y - base], Q[y - base], ahi, alo));
     return block_sum(acc, red);
 }
 
-__device__ __forceinline__ double residual_at(const float *P, const float *Q, int x, double a,
-                                              double b) {
-    const double d = (double)P[x] - a * (double)Q[x];
+__device__ __forceinline__ double residual_at(float px, float qx, double a, double b) {
+    const double d = (double)px - a * (double)qx;
     return d > 0.0 ? d / b : 0.0;
 }
 
+// 4-byte asynchronous copy global -> shared (no alignment beyond the element), and
+// the wait for all of this thread's copies.
+__device__ __forceinline__ void cp_async_f32(float *dst, const float *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// STAGED: this CTA's slice of the current node's p and q rows is copied into
+// shared memory as the node is entered, so the passes over it (rejections, bonus)
+// read shared memory; otherwise they read global memory.
+template <bool STAGED>
 __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs a) {
     namespace cg = cooperative_groups;
     __shared__ int s_par[kMaxNodes], s_drf[kMaxNodes], s_path[kMaxDepth];
@@ -124,6 +144,9 @@ __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs 
     __shared__ double s_slot[2];     // this CTA's slice sum of the last two passes
     __shared__ double s_tot;         // this CTA's slice total for the bonus draw
     __shared__ int s_bad, s_idx, s_last;
+    __shared__ float s_px[kMaxNodes], s_qx[kMaxNodes];  // p(x_c), q(x_c) of the tested children
+    __shared__ double s_uc[kMaxNodes];                  // and their uniforms
+    extern __shared__ float s_slice[];                  // STAGED: p slice, then q slice
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int b = blockIdx.x / kCluster, tid = threadIdx.x;
@@ -172,16 +195,45 @@ __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs 
 
     const float *P = a.root_p + (size_t)b * V;
     const float *Q = a.root_q + (size_t)b * V;
+    const int slice = (V + kCluster - 1) / kCluster;  // room per row in s_slice
+    float *sP = s_slice, *sQ = s_slice + slice;
+    // a node is entered: its slice copies start, and its children's test values are
+    // read in one round trip (all threads; the copies are waited for before a pass)
+    auto enter = [&](int node) {
+        if (STAGED)
+            for (int y = y0 + tid; y < y1; y += kThreadsA) {
+                cp_async_f32(sP + (y - y0), P + y);
+                cp_async_f32(sQ + (y - y0), Q + y);
+            }
+        for (int c = node + 1 + tid; c < n; c += kThreadsA)
+            if (s_par[c] == node) {
+                const int x = s_drf[c];
+                s_px[c] = P[x];
+                s_qx[c] = Q[x];
+                s_uc[c] = a.u_accept[off + c];
+            }
+        __syncthreads();
+    };
+    bool slice_ready = !STAGED;
+    auto slice_wait = [&]() {
+        if (!slice_ready) {
+            cp_async_wait_all();
+            __syncthreads();
+            slice_ready = true;
+        }
+    };
+    const float *SP = STAGED ? sP : P, *SQ = STAGED ? sQ : Q;  // what the passes read
+    const int sbase = STAGED ? y0 : 0;
     double ca = 0.0, cb = 1.0;  // residual coefficients at the current node
     int cur = -1, L = 0;
     bool too_deep = false;
+    enter(-1);
     for (;;) {  // every thread of the cluster takes the same branches
         bool found = false;
         for (int c = cur + 1; c < n; ++c) {
             if (s_par[c] != cur) continue;
-            const int x = s_drf[c];
-            const double lhs = a.u_accept[off + c] * (double)Q[x];
-            if (lhs < residual_at(P, Q, x, ca, cb)) {
+            const double lhs = s_uc[c] * (double)s_qx[c];
+            if (lhs < residual_at(s_px[c], s_qx[c], ca, cb)) {
                 if (L >= md) {
                     too_deep = true;
                     break;
@@ -191,14 +243,25 @@ __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs 
                 cur = c;
                 P = a.node_p + (size_t)(off + c) * V;
                 Q = a.node_q + (size_t)(off + c) * V;
+                if (!STAGED) {
+                    SP = P;
+                    SQ = Q;
+                }
                 ca = 0.0;
                 cb = 1.0;
+                // the previous node's copies land and every read of its slice and test
+                // values is done before the child's are requested
+                cp_async_wait_all();
+                __syncthreads();
+                slice_ready = !STAGED;
+                enter(c);
                 found = true;
                 break;
             }
             // rejected: the next residual, unless it sums to zero
             const double na = ca + cb;
-            const double t = cluster_sum(slice_sum(P, Q, y0, y1, na, s_red));
+            slice_wait();
+            const double t = cluster_sum(slice_sum(SP, SQ, sbase, y0, y1, na, s_red));
             if (t > 0.0) {
                 ca = na;
                 cb = t;
@@ -215,8 +278,9 @@ __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs 
         const float ahi = (float)ca, alo = (float)(ca - (double)ahi);
         const int chunk = (y1 - y0 + kThreadsA - 1) / kThreadsA;
         const int x0 = min(y0 + tid * chunk, y1), x1 = min(x0 + chunk, y1);
+        slice_wait();
         DF pacc = {0.f, 0.f};
-        for (int y = x0; y < x1; ++y) pacc = df_add(pacc, term(P[y], Q[y], ahi, alo));
+        for (int y = x0; y < x1; ++y) pacc = df_add(pacc, term(SP[y - sbase], SQ[y - sbase], ahi, alo));
         const int lane = tid & 31, warp = tid >> 5;
         DF incl = pacc;
 #pragma unroll
@@ -254,7 +318,7 @@ __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs 
         if (excl <= target && target < excl + part) {
             double run = excl;
             for (int y = x0; y < x1; ++y) {
-                run += to_double(term(P[y], Q[y], ahi, alo));
+                run += to_double(term(SP[y - sbase], SQ[y - sbase], ahi, alo));
                 if (run > target) {
                     atomicMin(&s_idx, y);
                     break;
@@ -264,7 +328,7 @@ __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs 
         // for a target past the last running sum (rounding): the last index with p > 0
         int last = -1;
         for (int y = x0; y < x1; ++y) {
-            const DF tv = term(P[y], Q[y], ahi, alo);
+            const DF tv = term(SP[y - sbase], SQ[y - sbase], ahi, alo);
             if (tv.hi > 0.f || tv.lo > 0.f) last = y;
         }
         last = __reduce_max_sync(0xffffffffu, last);
@@ -295,16 +359,26 @@ __global__ void __launch_bounds__(kThreadsA) accept_stochastic_kernel(StochArgs 
             }
         }
     }
+    cp_async_wait_all();  // no copy may still be landing when the CTA ends
     cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace
 
 cudaError_t launch_accept_stochastic(const StochArgs &a, cudaStream_t s) {
+    // the node's p and q slices in shared memory when they fit next to the static arrays
+    const size_t slice_bytes = 2 * (size_t)((a.V + kCluster - 1) / kCluster) * sizeof(float);
+    const bool staged = slice_bytes <= 160 * 1024;
+    auto kern = staged ? accept_stochastic_kernel<true> : accept_stochastic_kernel<false>;
+    if (staged) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)slice_bytes);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.B * kCluster);
     cfg.blockDim = dim3(kThreadsA);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = staged ? slice_bytes : 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -315,7 +389,7 @@ cudaError_t launch_accept_stochastic(const StochArgs &a, cudaStream_t s) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, accept_stochastic_kernel, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
