@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kThreadsG, 2) verify_tc_big_kernel(const Verif
 
 constexpr int kThreadsS = 512;
 constexpr int kWarpsS = kThreadsS / 32;
-constexpr int kTile2 = 64;      // nodes per H0-term tile and walk round (MMA N)
+constexpr int kTile2 = 64;      // nodes per walk round (an H0-term tile is two rounds)
 constexpr int kTileW = 64;      // nodes per tree-term tile (MMA N)
 constexpr int kBoxRows = 32;    // node rows per TMA box
 constexpr uint32_t kA0 = 256;   // tensor-memory column of H0^T (hi; lo 64 columns on)
