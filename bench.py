@@ -96,6 +96,8 @@ def parse():
                     help="profiling aid: only run 3 verify launches of this tv_variant on "
                          "--config's workload (config 5 as 2 layers of 32 heads, 512 units), "
                          "then exit")
+    ap.add_argument("--profile-extras", action="store_true",
+                    help="three launches each of tv_build_tree and tv_accept_stochastic (ncu)")
     ap.add_argument("--profile-attention", action="store_true",
                     help="profiling aid: only run 3 tree-attention launches of the attention "
                          "workload, then exit")
@@ -1089,8 +1091,50 @@ def profile_verify(args):
         raise SystemExit("device status %d" % st)
 
 
+def profile_extras(args):
+    """Three launches each of tv_build_tree (the 256-node trees, B=8) and
+    tv_accept_stochastic (config-2 trees, 32000 tokens), for ncu captures."""
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    import workloads
+    tv.build()
+    tv.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    Bt, Ct, cap, nt = 8, 8, 16, 256
+    marg = torch.from_numpy(np.random.default_rng(3).dirichlet(0.2 * np.ones(Ct), size=(Bt, cap))).to(dev)
+    par = torch.empty((Bt, nt), dtype=torch.int32, device=dev)
+    tok = torch.empty((Bt, nt), dtype=torch.int32, device=dev)
+    rho = torch.empty((Bt, nt), dtype=torch.float64, device=dev)
+    cnt = torch.empty(Bt, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        tv.tv_build_tree(Bt, Ct, cap, nt, marg, None, par, tok, rho, cnt, stream)
+    base = workloads.make_config(2, seed=1002)  # the trees of the default bench run
+    vocab = 32000
+    sin = workloads.stochastic_inputs(base, vocab, seed=41)
+    sp = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in sin.items()}
+    sd = tv.DeviceBatch(base, device=dev)
+    sd.status.zero_()
+    slen = torch.empty(base.B, dtype=torch.int32, device=dev)
+    spath = torch.empty((base.B, base.max_depth), dtype=torch.int32, device=dev)
+    sbon = torch.empty(base.B, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        tv.tv_accept_stochastic(base.B, base.T, base.max_nodes, base.max_depth, vocab,
+                                sd.node_offsets, sd.parent, sp["draft"], sp["root_p"], sp["node_p"],
+                                sp["root_q"], sp["node_q"], sp["u_accept"], sp["u_bonus"], slen,
+                                spath, sbon, sd.status, stream)
+    torch.cuda.synchronize()
+    st = int(sd.status[0].item())
+    print(json.dumps({"profile_extras": True, "tree_counts": cnt.tolist(), "status": st}))
+    if st != 0:
+        raise SystemExit("device status %d" % st)
+
+
 def main():
     args = parse()
+    if args.profile_extras:
+        profile_extras(args)
+        return
     if args.profile_verify is not None:
         profile_verify(args)
         return
