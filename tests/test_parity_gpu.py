@@ -107,6 +107,29 @@ def test_config2_seeds(seed, variant):
     _full_check(workloads.config2(seed=seed), variant)
 
 
+def _auto_variant(batch):
+    import tree_speculative_verify_tv_gb300 as tv
+    p = tv.make_problem(batch.B, batch.H, batch.dk, batch.dv, batch.T, batch.max_nodes,
+                        batch.max_depth, tv.TV_DECAY_DIAG if batch.decay == "diag" else 0,
+                        tv.TV_BF16 if batch.qkv_dtype == "bf16" else tv.TV_F32, 16, 16, 16)
+    return tv.tv_verify_variant(p)
+
+
+def test_automatic_kernel_choice():
+    """TV_VARIANT_AUTO: the one-unit kernel for scalar decay and small per-channel
+    trees, the staged large-tree kernel for per-channel trees of 64+ nodes and for
+    trees too large for the one-unit kernels."""
+    import tree_speculative_verify_tv_gb300 as tv
+    assert _auto_variant(workloads.make_config(2)) == tv.TV_VARIANT_TC
+    assert _auto_variant(workloads.make_config(3)) == tv.TV_VARIANT_TC_TILED
+    assert _auto_variant(workloads.make_config(4)) == tv.TV_VARIANT_TC
+    assert _auto_variant(workloads.config5(B=2, layers=1, heads=2)) == tv.TV_VARIANT_TC_TILED
+    small = workloads.random_batch(np.random.default_rng(50), [32, 20], 2, 128, 128, decay="diag",
+                                   qkv_dtype="bf16", depth_cap=8, max_depth=8, max_nodes=32)
+    assert _auto_variant(small) == tv.TV_VARIANT_TC
+    assert _auto_variant(workloads.make_config(1)) == tv.TV_VARIANT_SIMT
+
+
 @pytest.mark.parametrize("variant", ["simt", "auto"])
 def test_config5_reduced(variant):
     _full_check(workloads.config5(B=2, layers=2, heads=4, seed=11), variant)
