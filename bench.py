@@ -898,12 +898,12 @@ def run_e2e(args, host_batch, dev, stream, tv, world, fused):
     in place), so the inputs are the tree, factors and tokens and the results the
     outputs and acceptance; separate pipeline: the state is copied in and H_new out.
 
-    Each step moves one contiguous staging range in and one out.  Three staging sets
-    rotate over three streams, as a decode loop would run them: set s % 3 was last read
-    by the kernels of step s - 2 (as their pending commit), so the input copy of step s
-    waits only for those and overlaps the kernels of step s - 1; the kernels of a step
-    wait for those of the previous step (the state and the pending commit chain
-    through them)."""
+    Each step moves one contiguous staging range in and one out.  Four staging sets
+    rotate over four streams, as a decode loop would run them: set s % 4 was last read
+    by the kernels of step s - 3 (as their pending commit), so the input copy of step s
+    waits only for those and overlaps the kernels of steps s - 2 and s - 1; the kernels
+    of a step wait for those of the previous step (the state and the pending commit
+    chain through them)."""
     import torch
     ins = ["node_offsets", "parent", "depth", "q", "k", "v", "g", "draft", "target",
            "root_argmax"]
@@ -941,7 +941,7 @@ def run_e2e(args, host_batch, dev, stream, tv, world, fused):
                 setattr(obj, n, view)
         return hb, db, h_stage, d_stage
 
-    NS = 3
+    NS = 4
     sets = [staged() for _ in range(NS)]
     if fused:
         for i in range(1, NS):
@@ -960,8 +960,8 @@ def run_e2e(args, host_batch, dev, stream, tv, world, fused):
         hb, db, hs, ds = sets[i]
         st = streams[i]
         with torch.cuda.stream(st):
-            if s - 2 >= first:
-                st.wait_event(kev[(s - 2) % NS])
+            if s - (NS - 1) >= first:
+                st.wait_event(kev[(s - (NS - 1)) % NS])
             ds[:in_end].copy_(hs[:in_end], non_blocking=True)
             if s - 1 >= first:
                 st.wait_event(kev[(s - 1) % NS])
@@ -1025,8 +1025,8 @@ def run_e2e(args, host_batch, dev, stream, tv, world, fused):
             "state": "resident in HBM" if fused else "copied in and out every step",
             "copies": "one host-to-device copy of the step's inputs and one device-to-host "
                       "copy of its results per step (one staging layout, 256-byte aligned "
-                      "fields); three staging sets on three streams, so a step's input "
-                      "copy overlaps the previous step's kernels and the copies of the "
+                      "fields); four staging sets on four streams, so a step's input "
+                      "copy overlaps the previous steps' kernels and the copies of the "
                       "other direction; %d steps replay as one CUDA graph" % (NS * ROT)}
 
 
