@@ -61,7 +61,7 @@ TRAFFIC_SOURCES = {
     "tree_attention": [_CS + f for f in ("tree_attention.cu", "tc_common.cuh", "tc_ptx.cuh",
                                          "tv_internal.cuh")],
 }
-KERNEL_NAMES = {1: "simt", 2: "tcgen05 one unit per CTA", 3: "tcgen05 streaming",
+KERNEL_NAMES = {1: "simt", 2: "tcgen05 one unit per CTA", 3: "tcgen05, all products on tensor cores",
                 4: "tcgen05 node tiles"}
 
 

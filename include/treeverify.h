@@ -84,10 +84,11 @@ typedef enum tv_variant {
     TV_VARIANT_TC = 2,      /* tcgen05 tensor-core kernel, one (request, head) per CTA:
                                bf16 q/k/v, dk in {64,128}, dv in {64,128};
                                TV_ERR_UNSUPPORTED otherwise */
-    TV_VARIANT_TC_STREAM = 3, /* persistent tcgen05 kernel streaming many (request, head)
-                               units per CTA through double-buffered shared memory:
-                               as TV_VARIANT_TC but scalar decay only, and only where two
-                               units' operands fit one CTA's shared memory */
+    TV_VARIANT_TC_FUSED = 3, /* tcgen05 kernel with the context term, the pair scores and
+                               the tree term all on tensor cores, one (request, head) per
+                               CTA: scalar decay, bf16 q/k/v, dk and dv in {64,128},
+                               max_nodes <= 32; TV_ERR_UNSUPPORTED otherwise.  What
+                               TV_VARIANT_AUTO picks where it applies */
     TV_VARIANT_TC_TILED = 4  /* tcgen05 kernels for large trees, one (request, head) per
                                CTA: bf16 q/k/v, dk = dv = 128, trees up to TV_MAX_NODES.
                                Where a request's k, decay and v rows fit shared memory
@@ -96,6 +97,16 @@ typedef enum tv_variant {
                                their ancestors through the caches in node tiles of 64;
                                TV_ERR_UNSUPPORTED otherwise */
 } tv_variant;
+
+/*
+ * Test hook, OR-ed into tv_verify_ex's `variant` together with TV_VARIANT_TC_FUSED
+ * (TV_ERR_UNSUPPORTED with any other variant): the kernel treats its first wait for
+ * a state chunk as expired, so the call takes the library's timeout path -- it
+ * writes TV_ERR_TIMEOUT to dev_status, waits for its copies and products in flight,
+ * frees its tensor memory and returns.  The outputs are then undefined.  For tests
+ * of that failure path; never needed otherwise.
+ */
+#define TV_VARIANT_TEST_EXPIRE_WAIT 0x100
 
 /*
  * Shape and tree of one batch.  The three tree arrays are device memory.
@@ -258,6 +269,16 @@ tv_status tv_build_tree(int32_t B, int32_t C, int32_t depth_cap, int32_t n,
 tv_status tv_verify_serial_static(const tv_problem *p, const float *H0, const void *q,
                                   const void *k, const void *v, const float *g, float *out,
                                   int32_t *dev_status, void *stream);
+
+/*
+ * tv_workspace_bytes -- device workspace tv_verify needs for problem p: always 0.
+ * Every kernel behind tv_verify keeps its transient data (root paths, decay
+ * sums, weights, operand tiles, accumulators) in shared and tensor memory, so
+ * there is no workspace argument.  Kept so that callers written against a
+ * workspace-sizing interface can ask and get the answer.  Returns 0 also for an
+ * invalid problem (tv_verify reports that one).
+ */
+size_t tv_workspace_bytes(const tv_problem *p);
 
 /* tv_verify with an explicit kernel choice (tv_variant). */
 tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, const void *k,

@@ -117,13 +117,49 @@ def test_support_query_matches_forced_launch_checks(lib):
     f32 = prob(qkv_dtype=tv.TV_F32)
     assert tv.tv_verify_supports(f32, tv.TV_VARIANT_SIMT) == 1
     assert tv.tv_verify_supports(f32, tv.TV_VARIANT_AUTO) == 1
-    for v in (tv.TV_VARIANT_TC, tv.TV_VARIANT_TC_STREAM, tv.TV_VARIANT_TC_TILED):
+    for v in (tv.TV_VARIANT_TC, tv.TV_VARIANT_TC_FUSED, tv.TV_VARIANT_TC_TILED):
         assert tv.tv_verify_supports(f32, v) == 0
         assert verify_rc(f32, variant=v) == tv.TV_ERR_UNSUPPORTED
     # the large-tree kernels take dk = dv = 128 only
     assert tv.tv_verify_supports(prob(dk=64, dv=64), tv.TV_VARIANT_TC_TILED) == 0
     assert tv.tv_verify_supports(prob(dk=12), tv.TV_VARIANT_TC) == -tv.TV_ERR_SHAPE
     assert tv.tv_verify_supports(prob(), 9) == -tv.TV_ERR_DTYPE
+
+
+def test_fused_variant_limits(lib):
+    # the fused kernel: scalar decay, bf16, dk and dv in {64, 128}, <= 32 nodes
+    import torch
+    if torch.cuda.is_available():
+        # (the tensor-core kernels need the driver's tensor-map encoder)
+        ok = prob(dk=128, dv=64, max_nodes=16, total_nodes=5)
+        assert tv.tv_verify_supports(ok, tv.TV_VARIANT_TC_FUSED) == 1
+        assert tv.tv_verify_variant(ok) == tv.TV_VARIANT_TC_FUSED
+        assert tv.tv_verify_supports(prob(dk=128, dv=128, max_nodes=32),
+                                     tv.TV_VARIANT_TC_FUSED) == 1
+        # trees of 33..256 nodes keep the one-unit kernel
+        assert tv.tv_verify_variant(prob(dk=128, dv=64, max_nodes=64)) == tv.TV_VARIANT_TC
+    for bad in (prob(dk=128, dv=64, max_nodes=33, total_nodes=5),
+                prob(dk=128, dv=64, decay=tv.TV_DECAY_DIAG),
+                prob(dk=96, dv=64), prob(dk=128, dv=64, qkv_dtype=tv.TV_F32)):
+        assert tv.tv_verify_supports(bad, tv.TV_VARIANT_TC_FUSED) == 0
+        assert verify_rc(bad, variant=tv.TV_VARIANT_TC_FUSED) == tv.TV_ERR_UNSUPPORTED
+
+
+def test_expire_wait_hook_only_with_the_fused_variant(lib):
+    flag = tv.TV_VARIANT_TEST_EXPIRE_WAIT
+    for v in (tv.TV_VARIANT_AUTO, tv.TV_VARIANT_SIMT, tv.TV_VARIANT_TC, tv.TV_VARIANT_TC_TILED):
+        assert verify_rc(prob(dk=128, dv=64), variant=v | flag) == tv.TV_ERR_UNSUPPORTED
+    assert verify_rc(prob(dk=128, dv=64), variant=0x200) == tv.TV_ERR_DTYPE
+    src = open(HEADER).read()
+    m = re.search(r"#define TV_VARIANT_TEST_EXPIRE_WAIT\s+(0x[0-9a-fA-F]+)", src)
+    assert m and int(m.group(1), 16) == flag
+
+
+def test_workspace_bytes_is_zero(lib):
+    # every verify kernel keeps its transient data in shared and tensor memory
+    for p in (prob(), prob(dk=128, dv=64, max_nodes=16), prob(dk=128, dv=128, max_nodes=256),
+              prob(decay=tv.TV_DECAY_DIAG), prob(dk=12)):
+        assert tv.tv_workspace_bytes(p) == 0
 
 
 def test_empty_batches_are_no_ops(lib):

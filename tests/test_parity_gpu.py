@@ -116,11 +116,12 @@ def _auto_variant(batch):
 
 
 def test_automatic_kernel_choice():
-    """TV_VARIANT_AUTO: the one-unit kernel for scalar decay and small per-channel
-    trees, the staged large-tree kernel for per-channel trees of 64+ nodes and for
-    trees too large for the one-unit kernels."""
+    """TV_VARIANT_AUTO: the pipelined kernel for scalar-decay trees of <= 32 nodes,
+    the one-unit kernel for larger scalar-decay trees and small per-channel trees,
+    the staged large-tree kernel for per-channel trees of 64+ nodes and for trees
+    too large for the one-unit kernels."""
     import tree_speculative_verify_tv_gb300 as tv
-    assert _auto_variant(workloads.make_config(2)) == tv.TV_VARIANT_TC
+    assert _auto_variant(workloads.make_config(2)) == tv.TV_VARIANT_TC_FUSED
     assert _auto_variant(workloads.make_config(3)) == tv.TV_VARIANT_TC_TILED
     assert _auto_variant(workloads.make_config(4)) == tv.TV_VARIANT_TC
     assert _auto_variant(workloads.config5(B=2, layers=1, heads=2)) == tv.TV_VARIANT_TC_TILED

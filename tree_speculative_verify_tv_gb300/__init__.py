@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     tv_problem, tv_status_string, tv_verify, tv_verify_variant, tv_verify_supports, tv_version, EXPORTED,
     TV_OK, TV_ERR_NULL, TV_ERR_SHAPE, TV_ERR_DTYPE, TV_ERR_ALIGN, TV_ERR_UNSUPPORTED,
     TV_ERR_TREE, TV_ERR_CUDA, TV_ERR_TIMEOUT, TV_DECAY_SCALAR, TV_DECAY_DIAG, TV_BF16, TV_F32,
-    TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC, TV_VARIANT_TC_STREAM, TV_VARIANT_TC_TILED,
+    TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC, TV_VARIANT_TC_FUSED, TV_VARIANT_TC_TILED,
+    TV_VARIANT_TEST_EXPIRE_WAIT, tv_workspace_bytes,
     TV_MAX_NODES, TV_MAX_DEPTH, TV_MAX_DIM,
 )

@@ -23,12 +23,14 @@ TV_OK, TV_ERR_NULL, TV_ERR_SHAPE, TV_ERR_DTYPE, TV_ERR_ALIGN = 0, 1, 2, 3, 4
 TV_ERR_UNSUPPORTED, TV_ERR_TREE, TV_ERR_CUDA, TV_ERR_TIMEOUT = 5, 6, 7, 8
 TV_DECAY_SCALAR, TV_DECAY_DIAG = 0, 1
 TV_BF16, TV_F32 = 0, 1
-TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC, TV_VARIANT_TC_STREAM = 0, 1, 2, 3
+TV_VARIANT_AUTO, TV_VARIANT_SIMT, TV_VARIANT_TC, TV_VARIANT_TC_FUSED = 0, 1, 2, 3
 TV_VARIANT_TC_TILED = 4
+TV_VARIANT_TEST_EXPIRE_WAIT = 0x100
 TV_MAX_NODES, TV_MAX_DEPTH, TV_MAX_DIM = 256, 32, 256
 TV_SERIAL_STATIC_BYTES = 16 << 20
 
 EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_verify_supports",
+            "tv_workspace_bytes",
             "tv_accept_greedy", "tv_commit",
             "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_verify_serial",
             "tv_verify_serial_workspace_bytes", "tv_verify_serial_static", "tv_build_tree",
@@ -94,6 +96,8 @@ def load(path: Optional[str] = None):
         L.tv_tree_attention_workspace_bytes.restype = ctypes.c_size_t
         L.tv_verify_serial_workspace_bytes.argtypes = [P]
         L.tv_verify_serial_workspace_bytes.restype = ctypes.c_size_t
+        L.tv_workspace_bytes.argtypes = [P]
+        L.tv_workspace_bytes.restype = ctypes.c_size_t
         for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit,
                   L.tv_accept_commit, L.tv_commit_verify, L.tv_accept_greedy_logits,
                   L.tv_verify_serial, L.tv_verify_serial_static, L.tv_build_tree,
@@ -141,7 +145,7 @@ def tv_version() -> int:
 
 
 def tv_verify_variant(problem: tv_problem) -> int:
-    """Kernel tv_verify would choose (TV_VARIANT_TC / TV_VARIANT_SIMT), or -status."""
+    """Kernel tv_verify would choose (a TV_VARIANT_* value), or -status."""
     return load().tv_verify_variant(ctypes.byref(problem))
 
 
@@ -170,6 +174,11 @@ def tv_verify(problem: tv_problem, H0, q, k, v, g, out, dev_status, stream=None,
     rc = load().tv_verify_ex(ctypes.byref(problem), _ptr(H0), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                              _ptr(out), _ptr(dev_status), _stream(stream), int(variant))
     return _check(rc, "tv_verify", check)
+
+
+def tv_workspace_bytes(problem: tv_problem) -> int:
+    """Device workspace tv_verify needs: always 0 (shared and tensor memory only)."""
+    return int(load().tv_workspace_bytes(ctypes.byref(problem)))
 
 
 def tv_verify_serial_workspace_bytes(problem: tv_problem) -> int:

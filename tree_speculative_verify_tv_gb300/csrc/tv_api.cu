@@ -42,12 +42,12 @@ tv_status check_ptrs(std::initializer_list<const void *> ptrs) {
     return TV_OK;
 }
 
-// The kernel TV_VARIANT_AUTO picks: the one-unit tensor-core kernel where it
-// applies (the streaming kernel only when it is the faster one, the staged
-// large-tree kernel for per-channel decay trees of 64 or more nodes), the
+// The kernel TV_VARIANT_AUTO picks: the fused tensor-core kernel for scalar decay
+// trees of up to 32 nodes, the staged large-tree kernel for per-channel decay
+// trees of 64 or more nodes, the one-unit tensor-core kernel where it applies, the
 // large-tree tensor-core kernels for trees too large for it, else SIMT.
 int32_t auto_variant(const tv::VerifyArgs &a) {
-    if (tv::verify_tc_stream_preferred(a)) return TV_VARIANT_TC_STREAM;
+    if (tv::verify_tc_fused_supported(a)) return TV_VARIANT_TC_FUSED;
     if (tv::verify_tc_staged_preferred(a)) return TV_VARIANT_TC_TILED;
     if (tv::verify_tc_supported(a)) return TV_VARIANT_TC;
     if (tv::verify_tc_big_supported(a)) return TV_VARIANT_TC_TILED;
@@ -56,7 +56,7 @@ int32_t auto_variant(const tv::VerifyArgs &a) {
 
 cudaError_t launch_verify_auto(const tv::VerifyArgs &a, cudaStream_t s) {
     switch (auto_variant(a)) {
-        case TV_VARIANT_TC_STREAM: return tv::launch_verify_tc_stream(a, s);
+        case TV_VARIANT_TC_FUSED: return tv::launch_verify_tc_fused(a, s);
         case TV_VARIANT_TC: return tv::launch_verify_tc(a, s);
         case TV_VARIANT_TC_TILED: return tv::launch_verify_tc_big(a, s);
         default: return tv::launch_verify_simt(a, s);
@@ -94,7 +94,7 @@ int32_t tv_verify_supports(const tv_problem *p, int32_t variant) {
         case TV_VARIANT_AUTO:
         case TV_VARIANT_SIMT: return 1;
         case TV_VARIANT_TC: return tv::verify_tc_supported(a) ? 1 : 0;
-        case TV_VARIANT_TC_STREAM: return tv::verify_tc_stream_supported(a) ? 1 : 0;
+        case TV_VARIANT_TC_FUSED: return tv::verify_tc_fused_supported(a) ? 1 : 0;
         case TV_VARIANT_TC_TILED: return tv::verify_tc_big_supported(a) ? 1 : 0;
         default: return -static_cast<int32_t>(TV_ERR_DTYPE);
     }
@@ -109,13 +109,21 @@ int32_t tv_verify_variant(const tv_problem *p) {
     return auto_variant(a);
 }
 
+size_t tv_workspace_bytes(const tv_problem *p) {
+    (void)p;
+    return 0;
+}
+
 tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, const void *k,
                        const void *v, const float *g, float *out, int32_t *dev_status,
                        void *stream, int32_t variant) {
     tv_status st = check_dims(p);
     if (st != TV_OK) return st;
     if (!p->depth && p->total_nodes > 0) return TV_ERR_NULL;
+    const bool expire = (variant & TV_VARIANT_TEST_EXPIRE_WAIT) != 0;
+    variant &= ~TV_VARIANT_TEST_EXPIRE_WAIT;
     if (variant < TV_VARIANT_AUTO || variant > TV_VARIANT_TC_TILED) return TV_ERR_DTYPE;
+    if (expire && variant != TV_VARIANT_TC_FUSED) return TV_ERR_UNSUPPORTED;
     if (!dev_status) return TV_ERR_NULL;
     if (p->B == 0 || p->total_nodes == 0) return TV_OK;
     st = check_ptrs({H0, q, k, v, g, out, p->node_offsets, p->parent, p->depth, dev_status});
@@ -132,9 +140,9 @@ tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, cons
             if (!tv::verify_tc_supported(a)) return TV_ERR_UNSUPPORTED;
             e = tv::launch_verify_tc(a, s);
             break;
-        case TV_VARIANT_TC_STREAM:
-            if (!tv::verify_tc_stream_supported(a)) return TV_ERR_UNSUPPORTED;
-            e = tv::launch_verify_tc_stream(a, s);
+        case TV_VARIANT_TC_FUSED:
+            if (!tv::verify_tc_fused_supported(a)) return TV_ERR_UNSUPPORTED;
+            e = tv::launch_verify_tc_fused(a, s, expire);
             break;
         case TV_VARIANT_TC_TILED:
             if (!tv::verify_tc_big_supported(a)) return TV_ERR_UNSUPPORTED;
@@ -454,6 +462,10 @@ tv_status tv_commit_verify(const tv_problem *p, const tv_pending *pend, float *H
     tv::PendingArgs pa{pend->total_nodes, pend->max_nodes, pend->max_depth, pend->node_offsets,
                        pend->parent, pend->g, pend->k, pend->v, pend->path, pend->accept_len};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->total_nodes > 0 && tv::commit_verify_fused_supported(a, pa)) {
+        cudaError_t e = tv::launch_commit_verify_fused(a, pa, H, s);
+        return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+    }
     if (p->total_nodes > 0 && tv::commit_verify_tc_supported(a, pa)) {
         cudaError_t e = tv::launch_commit_verify_tc(a, pa, H, s);
         return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;

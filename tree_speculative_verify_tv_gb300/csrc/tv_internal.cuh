@@ -110,14 +110,20 @@ bool verify_tc_supported(const VerifyArgs &a);
 // Node-tiled tensor-core kernel for large trees (dk = dv = 128).
 bool verify_tc_big_supported(const VerifyArgs &a);
 cudaError_t launch_verify_tc_big(const VerifyArgs &a, cudaStream_t s);
-// Persistent tensor-core kernel (scalar decay): many units per CTA, double-buffered.
-bool verify_tc_stream_supported(const VerifyArgs &a);
-bool verify_tc_stream_preferred(const VerifyArgs &a);  // what TV_VARIANT_AUTO picks
-cudaError_t launch_verify_tc_stream(const VerifyArgs &a, cudaStream_t s);
+// Scalar-decay kernel with all three products on tensor cores (trees of <= 32
+// nodes), one (request, head) per CTA.  `expire_first_wait` is the test hook of
+// TV_VARIANT_TEST_EXPIRE_WAIT.
+bool verify_tc_fused_supported(const VerifyArgs &a);
+cudaError_t launch_verify_tc_fused(const VerifyArgs &a, cudaStream_t s,
+                                   bool expire_first_wait = false);
 // One-kernel commit + verify (scalar decay, tensor cores); H is read and written.
 bool commit_verify_tc_supported(const VerifyArgs &a, const PendingArgs &p);
 cudaError_t launch_commit_verify_tc(const VerifyArgs &a, const PendingArgs &p, float *H,
                                     cudaStream_t s);
+// The same on the fused kernel (trees of <= 32 nodes).
+bool commit_verify_fused_supported(const VerifyArgs &a, const PendingArgs &p);
+cudaError_t launch_commit_verify_fused(const VerifyArgs &a, const PendingArgs &p, float *H,
+                                       cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs &a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs &a, cudaStream_t s);
 cudaError_t launch_accept_commit(const CommitArgs &a, cudaStream_t s);
