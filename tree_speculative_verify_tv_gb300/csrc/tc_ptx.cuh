@@ -123,6 +123,12 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) from global memory
+// into L2; no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 16-byte asynchronous global -> shared copy (cp.async, L2 only), tracked per
 // thread in commit groups; both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {

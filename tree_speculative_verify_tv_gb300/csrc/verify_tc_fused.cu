@@ -85,6 +85,7 @@ struct FusedParams {
     PendingArgs pend;  // commit + verify only
     float *H_w;        // state rows written back (commit + verify only)
     int tmem_cols;
+    int wave;               // CTAs resident at once (units one wave ahead are prefetched)
     int expire_first_wait;  // test hook: the first wait for a state chunk gives up at once
 };
 
@@ -172,6 +173,11 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
             ptx::bulk_g2s(ptx::smem_addr(sH) + c * kChunkBytes, hsrc + (size_t)c * kChunkVals,
                           kChunkBytes, b_chunk(c));
         }
+    // the state of the unit that starts about one wave later goes to L2 now, so its
+    // CTA finds it there (same bytes, fetched earlier)
+    if (tid == 32 && P.wave > 0 && unit + P.wave < a.B * H)
+        ptx::prefetch_l2((PEND ? P.H_w : a.H0) + (size_t)(unit + P.wave) * dk * DV,
+                         dk * DV * 4);
     ptx::grid_launch_dependents();
 
     if (warp < 4) {
@@ -389,11 +395,37 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
         const int pm = lane < mdp ? pa.path[(size_t)b * mdp + lane] : -1;
         bool pbad = !prange || Lq < 0 || Lq > mdp;
         pbad = pbad || __any_sync(0xffffffffu, lane < Lq && (pm < 0 || pm >= pn));
+        // one round trip: the path's parents and decays, and its factor rows (16-byte
+        // copies into shared memory, scaled once the decays are known)
         int ppar = -2;
         float pg = 0.f;
-        if (!pbad && lane < Lq) {
-            ppar = pa.parent[poff + pm];
-            pg = pa.g[(size_t)(poff + pm) * H + h];
+        const int k8 = dk / 8, v8 = DV / 8;
+        const uint32_t dk16 = ptx::smem_addr(smem + L.pk16_off);
+        const uint32_t dv16 = ptx::smem_addr(smem + L.pv16_off);
+        const __nv_bfloat16 *pk = static_cast<const __nv_bfloat16 *>(pa.k);
+        const __nv_bfloat16 *pv = static_cast<const __nv_bfloat16 *>(pa.v);
+        if (!pbad) {
+            if (lane < Lq) {
+                ppar = pa.parent[poff + pm];
+                pg = pa.g[(size_t)(poff + pm) * H + h];
+            }
+            const int items = Lq * (k8 + v8);
+            for (int base = 0; base < items; base += 32) {
+                const int e = base + lane;
+                const bool isk = e < Lq * k8;
+                const int e2 = isk ? e : e - Lq * k8;
+                const int per = isk ? k8 : v8;
+                const int m = e < items ? e2 / per : 0;
+                const int node = __shfl_sync(0xffffffffu, pm, m);
+                if (e < items) {
+                    const int c8 = (e2 % per) * 8;
+                    const size_t row = (size_t)(poff + node) * H + h;
+                    if (isk)
+                        ptx::cp_async_16(dk16 + (m * dk + c8) * 2, pk + row * dk + c8);
+                    else
+                        ptx::cp_async_16(dv16 + (m * DV + c8) * 2, pv + row * DV + c8);
+                }
+            }
         }
         if (!pbad) {
             const int prev = __shfl_up_sync(0xffffffffu, pm, 1);
@@ -410,12 +442,13 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
             total += y;
         }
         const float scale = expf(suf);
+        ptx::cp_async_wait_all();
+        __syncwarp();
         // factor rows: a_m = e^{G_L - G_{p_m}} k_{p_m} and v_{p_m}, fp32
         float *sPA = reinterpret_cast<float *>(smem + L.pa_off);
         float *sPV = reinterpret_cast<float *>(smem + L.pvv_off);
-        const __nv_bfloat16 *pk = static_cast<const __nv_bfloat16 *>(pa.k);
-        const __nv_bfloat16 *pv = static_cast<const __nv_bfloat16 *>(pa.v);
-        const int k8 = dk / 8, v8 = DV / 8;
+        const __nv_bfloat16 *k16 = reinterpret_cast<const __nv_bfloat16 *>(smem + L.pk16_off);
+        const __nv_bfloat16 *v16 = reinterpret_cast<const __nv_bfloat16 *>(smem + L.pv16_off);
         const int items = Lp * (k8 + v8);
         for (int base = 0; base < items; base += 32) {
             const int e = base + lane;
@@ -424,12 +457,10 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
             const int per = isk ? k8 : v8;
             const int m = e < items ? e2 / per : 0;
             const float sc = __shfl_sync(0xffffffffu, scale, m);
-            const int node = __shfl_sync(0xffffffffu, pm, m);
             if (e < items) {
                 const int c8 = (e2 % per) * 8;
-                const size_t row = (size_t)(poff + node) * H + h;
-                const uint4 raw = *reinterpret_cast<const uint4 *>(isk ? pk + row * dk + c8
-                                                                       : pv + row * DV + c8);
+                const uint4 raw = *reinterpret_cast<const uint4 *>(isk ? k16 + m * dk + c8
+                                                                       : v16 + m * DV + c8);
                 const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
                 float *dst = isk ? sPA + m * dk + c8 : sPV + m * DV + c8;
                 const float f = isk ? sc : 1.f;
@@ -612,6 +643,13 @@ cudaError_t launch_fused_t(const VerifyArgs &a, const PendingArgs *pend, float *
     cudaError_t e = configure_smem_once(kern);
     if (e != cudaSuccess) return e;
     const size_t smem = fused_smem_bytes(a, PEND ? pend->max_depth : 0);
+    int dev = 0, sms = 0, per_sm = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreadsF, smem);
+    if (e != cudaSuccess) return e;
+    P.wave = sms * per_sm;
     return launch_pdl(kern, dim3((unsigned)(a.B * a.H)), dim3(kThreadsF), smem, s, tq, tk, tv_, P);
 }
 
