@@ -136,13 +136,21 @@ def test_config5_reduced(variant):
     _full_check(workloads.config5(B=2, layers=2, heads=4, seed=11), variant)
 
 
-def test_config5_full_size_sampled():
-    """B=8, 36 layers x 32 heads, 256-node trees: every output compared on a sample of
-    (request, head) units the oracle evaluates one by one."""
+def test_config5_full_size_every_unit():
+    """B=8, 36 layers x 32 heads, 256-node trees, the launch the benchmark times: every
+    one of the 9216 (request, head) units compared with the oracle (outputs and
+    committed states), the oracle threaded over all host cores and run in eight
+    slices of units to bound its memory."""
+    import os
     b = workloads.config5()
-    rng = np.random.default_rng(5)
-    units = np.sort(rng.choice(b.B * b.H, 48, replace=False)).astype(np.int32)
-    _full_check(b, "auto", units=units)
+    res = run_library(b, variant=VARIANTS["auto"])
+    assert res["status"] == 0, res["status"]
+    ln, path = check_accept(b, res)
+    threads = os.cpu_count() or 8
+    units = np.arange(b.B * b.H, dtype=np.int32)
+    for part in np.array_split(units, 8):
+        check_verify(b, res["out"], units=part, threads=threads)
+        check_commit(b, res["H_new"], ln, path, units=part, threads=threads)
 
 
 SHAPES = [  # (dk, dv, decay, dtype)

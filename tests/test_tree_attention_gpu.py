@@ -1,10 +1,10 @@
 """GPU parity of tv_tree_attention against the oracle's tree-masked softmax
-attention (fp64).  Tolerance: every (node, head) output row within 8e-3 normwise
-relative error.  The kernel computes scores and sums in fp32 from exact bf16
-inputs and feeds the softmax weights to the weighted sum of values as bf16
-(relative rounding 2^-9 each); the weights' rounding errors are independent, so
-a row's relative error is of order 2^-9 (about 2e-3, measured up to 2.4e-3 in a
-model of that rounding), and 8e-3 = 2^-7 leaves a factor of four."""
+attention (fp64).  Tolerance: the library's output bar, 2e-3 normwise relative
+error per (node, head) output row, measured as for the verify outputs: the
+largest |difference| over the row's d channels divided by the row's largest
+|reference| value.  The kernel forms scores and sums in fp32 from exact bf16
+inputs and feeds the softmax weights to the value sum as a bf16 hi + lo pair
+(|p - hi - lo| <= 2^-16 p), so the weights add no error of the bf16 size."""
 
 import numpy as np
 import pytest
@@ -13,7 +13,7 @@ import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
-TOL = 8e-3
+TOL = 2e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -55,8 +55,8 @@ def reference(batch, a):
 
 
 def row_errors(got, ref):
-    num = np.linalg.norm(got - ref, axis=-1)
-    den = np.linalg.norm(ref, axis=-1)
+    num = np.max(np.abs(got - ref), axis=-1)
+    den = np.maximum(np.max(np.abs(ref), axis=-1), 1e-30)
     return num / den
 
 

@@ -53,11 +53,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // Split two floats into bf16 hi + lo parts: hi keeps the upper 16 bits (exact
 // truncation), so x - hi is exact in fp32 and only lo is rounded (to nearest):
 // |x - hi - lo| <= 2^-16 |x|.  Returns packed pairs (element 0 in the low half).
+// The two remainders are formed by one packed fp32 subtraction (sub.f32x2).
 __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
     const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
-    const float h0 = __uint_as_float(b0 & 0xFFFF0000u), h1 = __uint_as_float(b1 & 0xFFFF0000u);
     hi = __byte_perm(b0, b1, 0x7632);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - h0, x1 - h1);
+    float r0, r1;
+    asm("{\n\t.reg .b64 x, h, d;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 h, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, x, h;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(x0), "f"(x1), "r"(b0 & 0xFFFF0000u), "r"(b1 & 0xFFFF0000u));
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 

@@ -19,12 +19,14 @@
 //   S = Q K^T        tcgen05 kind::f16, M = 128, N = 128 keys, K = d, into one of two
 //                    tensor-memory S/P buffers (S of the next tile is formed while the
 //                    softmax works on this one);
-//   P = 2^(S * scale * log2 e - m) in bf16, written by the softmax threads over the
-//                    first 64 columns of the same buffer (two keys per column);
-//   O += P V         A = P from tensor memory, M = 128, N = d, K = 128 keys, with V
-//                    read as an MN-major operand straight from its TMA tile, and
-//                    l += P 1 (N = 16, an all-ones operand), so the row sums of the bf16
-//                    weights come from the tensor core; O and l stay in tensor memory.
+//   P = 2^(S * scale * log2 e - m) in fp32, split into bf16 hi (upper 16 bits) and
+//                    lo = bf16(P - hi) parts (|P - hi - lo| <= 2^-16 P), written by the
+//                    softmax threads over the same buffer (two keys per column, hi in
+//                    columns 0-63, lo in 64-127);
+//   O += P V         A = P hi, then P lo, from tensor memory, M = 128, N = d, K = 128
+//                    keys, with V read as an MN-major operand straight from its TMA
+//                    tile; O stays in tensor memory.  The row sums l of the fp32
+//                    weights are kept by the softmax threads in registers.
 // The MMA thread issues whichever of the next S and the next P V is ready, so a K tile
 // still in flight never holds back P V, and a buffer takes the next S only after its
 // P V is done.  The reference maximum m of a row is raised only when a tile's maximum
@@ -51,8 +53,7 @@ using tcc::kWaitLimit;
 constexpr int kThreadsAt = 192;
 constexpr uint32_t kSlab = 128 * 128;  // 128 rows x 128 bytes (64 bf16), swizzled
 constexpr float kHeadroom = 8.f;       // log2 units of growth before a rescale
-constexpr uint32_t kTmemCols = 512;    // S buffers at 0 and 128, O at 256, l after O
-constexpr uint32_t kOnesBytes = 1024;  // all-ones bf16 operand giving the row sums of P
+constexpr uint32_t kTmemCols = 512;    // S/P buffers at 0 and 128, O at 256
 
 // Shared memory: Q, a ring of KS K tiles and one of VS V tiles (128 keys each).
 // At d = 128 both rings are 3 deep (224 KB of tiles), at d = 64 both are 6 deep.
@@ -65,8 +66,7 @@ struct AttnLayout {
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kK = kQ + kHalf;           // K tiles [KS]
     static constexpr uint32_t kV = kK + KS * kHalf;      // V tiles [VS]
-    static constexpr uint32_t kOnes = kV + VS * kHalf;
-    static constexpr uint32_t kPar = kOnes + kOnesBytes;  // parent [kMaxNodes] int16
+    static constexpr uint32_t kPar = kV + VS * kHalf;  // parent [kMaxNodes] int16
     static constexpr uint32_t kBar = kPar + kMaxNodes * 2;
     // mbarrier slots: Q landed; K, V tiles landed / free; per tensor-memory S/P
     // buffer: S ready, S read, P written, P V done; every MMA done
@@ -167,12 +167,6 @@ __global__ void __launch_bounds__(kThreadsAt, 1)
         ptx::prefetch_tensormap(&tm_kt);
         ptx::prefetch_tensormap(&tm_vt);
     }
-    {
-        uint4 *ones = reinterpret_cast<uint4 *>(sm + Lay::kOnes);
-        for (int i = tid; i < (int)(kOnesBytes / 16); i += kThreadsAt)
-            ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        ptx::fence_proxy_async_smem();
-    }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(s_tmem), kTmemCols);
         ptx::tmem_relinquish();
@@ -224,7 +218,7 @@ __global__ void __launch_bounds__(kThreadsAt, 1)
     };
     if (empty_rows) write_empty(tid, kThreadsAt);
 
-    const uint32_t sQ = sbase + Lay::kQ, sOnes = sbase + Lay::kOnes;
+    const uint32_t sQ = sbase + Lay::kQ;
     auto sK = [&](int s) { return sbase + Lay::kK + (uint32_t)s * Lay::kHalf; };
     auto sV = [&](int s) { return sbase + Lay::kV + (uint32_t)s * Lay::kHalf; };
     // ring slot of tile j and the parity of its use of that slot
@@ -232,7 +226,7 @@ __global__ void __launch_bounds__(kThreadsAt, 1)
     auto kpar = [](int j) { return (uint32_t)((j / KS) & 1); };
     auto vslot = [](int j) { return j % VS; };
     auto vpar = [](int j) { return (uint32_t)((j / VS) & 1); };
-    constexpr uint32_t kOCol = 256, kLCol = 256 + D;
+    constexpr uint32_t kOCol = 256;
 
     if (!run) {
         // nothing to compute
@@ -280,7 +274,6 @@ __global__ void __launch_bounds__(kThreadsAt, 1)
         if (lane == 0) {
             constexpr uint32_t idS = ptx::idesc_bf16_f32(128, 128);
             constexpr uint32_t idPV = ptx::idesc_bf16_f32_bmn(128, D);
-            constexpr uint32_t idL = ptx::idesc_bf16_f32(128, 16);
             bool ok = wait_phase(bar(kQBar), 0, abort);
             int js = 0, jp = 0;
             long long t_last = clock64();
@@ -309,15 +302,14 @@ __global__ void __launch_bounds__(kThreadsAt, 1)
                     ptx::tc_fence_after_sync();
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        // P: 16 keys = 8 columns of packed bf16 pairs per step
+                        // P: 16 keys = 8 columns of packed bf16 pairs per step, the hi
+                        // part at column 8 kk, the lo part 64 columns further
                         const uint32_t pa = tmem + 128u * s + 8u * kk;
                         const uint64_t bd = ptx::desc_mnmajor_sw128(sV(vs) + kk * 2048u,
                                                                     D == 128 ? kSlab : 0u, 1024);
                         const uint32_t acc = (jp > 0 || kk > 0) ? 1u : 0u;
                         ptx::mma_bf16_ts(tmem + kOCol, pa, bd, idPV, acc);
-                        // all-ones B: any row of the 1 KB buffer will do (8-row step 0)
-                        ptx::mma_bf16_ts(tmem + kLCol, pa,
-                                         ptx::desc_kmajor_sw128(sOnes + (kk & 3) * 32, 0), idL, acc);
+                        ptx::mma_bf16_ts(tmem + kOCol, pa + 64u, bd, idPV, 1u);
                     }
                     ptx::mma_commit(bar(kOBar + s));
                     ptx::mma_commit(bar(kVFree + vs));
@@ -363,6 +355,7 @@ __global__ void __launch_bounds__(kThreadsAt, 1)
         const bool bad = s_flags[0] != 0;
         if (bad && tid == 64 && first_cta) report(a.status, TV_ERR_TREE);
         float m = neg_inf();
+        float lsum = 0.f;  // the row's sum of weights, relative to 2^m
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
             const int s = j & 1;
@@ -446,30 +439,31 @@ __global__ void __launch_bounds__(kThreadsAt, 1)
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                     ptx::tmem_st_x32(tl + kOCol + 32u * c, o);
                 }
-                uint32_t lv[8];
-                ptx::tmem_ld_x8_nowait(tl + kLCol, lv);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 8; ++e) lv[e] = __float_as_uint(__uint_as_float(lv[e]) * alpha);
-                ptx::tmem_st_x8(tl + kLCol, lv);
+                lsum *= alpha;
             }
             if (need) m = t;
 
-            // P over the first 64 columns of this tile's S buffer (S is in registers)
+            // P over this tile's S buffer (S is in registers), split into bf16 hi and lo
+            // parts: hi keeps the upper 16 bits of each fp32 weight, lo = bf16(p - hi),
+            // so p - hi - lo <= 2^-16 p; hi pairs in columns 0-63, lo pairs in 64-127
             if (warp_live) {
                 const float nm = m == neg_inf() ? 0.f : -m;
+                float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t ph[16], pl[16];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const __nv_bfloat162 h2 =
-                            __floats2bfloat162_rn(ex2(fmaf(x[64 * h + 2 * e], sl2, nm)),
-                                                  ex2(fmaf(x[64 * h + 2 * e + 1], sl2, nm)));
-                        pk[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = ex2(fmaf(x[32 * q + 2 * e], sl2, nm));
+                        const float p1 = ex2(fmaf(x[32 * q + 2 * e + 1], sl2, nm));
+                        ls0 += p0;
+                        ls1 += p1;
+                        tcc::split_pair(p0, p1, ph[e], pl[e]);
                     }
-                    ptx::tmem_st_x32(tl + 128u * s + 32u * h, pk);
+                    ptx::tmem_st_x16(tl + 128u * s + 16u * q, ph);
+                    ptx::tmem_st_x16(tl + 128u * s + 64u + 16u * q, pl);
                 }
+                lsum += ls0 + ls1;
             }
             ptx::tmem_wait_st();
             if (vk < 128) {
@@ -496,10 +490,7 @@ __global__ void __launch_bounds__(kThreadsAt, 1)
                                                      ((nt - 1) >> 1) & 1, abort))) {
             ptx::tc_fence_after_sync();
             if (warp_live) {
-                uint32_t lv[8];
-                ptx::tmem_ld_x8_nowait(tl + kLCol, lv);
-                ptx::tmem_wait_ld();
-                const float l = bad ? 0.f : __uint_as_float(lv[0]);
+                const float l = bad ? 0.f : lsum;
                 if (bad) m = neg_inf();  // a malformed tree: zero rows
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 float *dst;
