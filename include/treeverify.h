@@ -258,13 +258,18 @@ tv_status tv_build_tree(int32_t B, int32_t C, int32_t depth_cap, int32_t n,
  *   Problems whose states need more than TV_SERIAL_STATIC_BYTES
  *   (tv_verify_serial_workspace_bytes(p)) are rejected with TV_ERR_UNSUPPORTED
  *   before anything is launched.
- * Set-up: the first call on a device, with that device current, looks up the
- * array's device address there (cudaGetSymbolAddress); make that first call
- * before any stream capture.  Every call on a device shares the one array, and
- * it keeps the last call's contents; the kernel writes every state before it
- * reads it, so nothing has to be cleared between calls.  Calls that overlap on
- * the same GPU (for instance on two streams) race on the array and give wrong
- * results: serialize them.  No device memory is allocated or freed.
+ * Set-up: every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress).  The array's 16 MiB are taken when the CUDA runtime
+ * loads the library's serial-verification code on a device: with lazy module
+ * loading (the CUDA default) that is the first call of tv_verify_serial or
+ * tv_verify_serial_static on that device.  So make that first call before the
+ * process reserves the rest of the device memory for its own pool (else it can
+ * fail with TV_ERR_CUDA, out of memory) and before any stream capture; later calls
+ * take no device memory.  Every call on a device shares the one array, and it
+ * keeps the last call's contents; the kernel writes every state before it reads
+ * it, so nothing has to be cleared between calls.  Calls that overlap on the same
+ * GPU (for instance on two streams) race on the array and give wrong results:
+ * serialize them.  No device memory is allocated or freed by the call itself.
  */
 tv_status tv_verify_serial_static(const tv_problem *p, const float *H0, const void *q,
                                   const void *k, const void *v, const float *g, float *out,

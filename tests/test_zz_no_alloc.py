@@ -54,3 +54,42 @@ def test_static_scratch_matches_workspace_on_two_calls():
         ref, got = _outputs(batch)
         assert np.isfinite(got).all()
         assert row_rel_err(got, ref) <= TOL
+
+
+def test_static_scratch_exactly_full():
+    """A problem whose states fill the array exactly (2 requests x 8 heads x 16 nodes
+    x 128 x 128 fp32 = 16 MiB): the last unit's last node writes the array's last
+    bytes.  One more request is rejected before anything runs."""
+    import tree_speculative_verify_tv_gb300 as tv
+    b = workloads.random_batch(np.random.default_rng(63), [16, 16], 8, 128, 128,
+                               decay="scalar", depth_cap=8, max_depth=8, max_nodes=16)
+    d = tv.DeviceBatch(b)
+    assert tv.tv_verify_serial_workspace_bytes(d.problem()) == tv.TV_SERIAL_STATIC_BYTES
+    ref, got = _outputs(b)
+    assert np.isfinite(got).all()
+    assert row_rel_err(got, ref) <= TOL
+    over = workloads.random_batch(np.random.default_rng(64), [16, 16, 1], 8, 128, 128,
+                                  decay="scalar", depth_cap=8, max_depth=8, max_nodes=16)
+    do = tv.DeviceBatch(over)
+    rc = tv.tv_verify_serial_static(do.problem(), do.H0, do.q, do.k, do.v, do.g, do.out,
+                                    do.status, check=False)
+    assert rc == tv.TV_ERR_UNSUPPORTED
+
+
+def test_static_scratch_takes_no_memory_per_call():
+    """After a first call has loaded the library's code on the device, a call takes no
+    device memory: the free memory the driver reports is the same before and after."""
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    b = workloads.config2(seed=65, B=1)
+    d = tv.DeviceBatch(b)
+    p = d.problem()
+    d.status.zero_()
+    tv.tv_verify_serial_static(p, d.H0, d.q, d.k, d.v, d.g, d.out, d.status)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        tv.tv_verify_serial_static(p, d.H0, d.q, d.k, d.v, d.g, d.out, d.status)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert int(d.status[0]) == 0

@@ -371,8 +371,7 @@ cudaError_t launch_accept_stochastic(const StochArgs &a, cudaStream_t s) {
     const bool staged = slice_bytes <= 160 * 1024;
     auto kern = staged ? accept_stochastic_kernel<true> : accept_stochastic_kernel<false>;
     if (staged) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)slice_bytes);
+        const cudaError_t e = configure_smem_once(kern, false);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};

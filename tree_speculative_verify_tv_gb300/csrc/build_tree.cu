@@ -187,8 +187,7 @@ size_t build_tree_smem_bytes(int C, int depth_cap, int n) {
 
 cudaError_t launch_build_tree(const BuildArgs &a, cudaStream_t s) {
     const size_t smem = build_tree_smem_bytes(a.C, a.depth_cap, a.n);
-    cudaError_t e = cudaFuncSetAttribute(build_tree_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = configure_smem_once(build_tree_kernel, false);
     if (e != cudaSuccess) return e;
     return launch_pdl(build_tree_kernel, dim3((unsigned)((a.B + kWarpsB - 1) / kWarpsB)),
                       dim3(kWarpsB * 32), smem, s, a);

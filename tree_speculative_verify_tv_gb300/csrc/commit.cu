@@ -170,9 +170,7 @@ cudaError_t launch_typed(const CommitArgs &a, cudaStream_t s) {
     const int rpc = rows_per_cta(a.dk, a.dv);
     dim3 grid((unsigned)(a.B * a.H), (unsigned)((a.dk + rpc - 1) / rpc));
     size_t smem = (size_t)a.max_depth * a.dv * sizeof(float);
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        commit_kernel<E, DIAG, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        kMaxDepth * kMaxDim * (int)sizeof(float));
+    const cudaError_t attr = configure_smem_once(commit_kernel<E, DIAG, FUSED>, false);
     if (attr != cudaSuccess) return attr;
     return launch_pdl(commit_kernel<E, DIAG, FUSED>, grid, dim3(kThreads), smem, s, a);
 }

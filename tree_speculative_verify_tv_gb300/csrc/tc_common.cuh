@@ -6,8 +6,6 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
-#include <set>
-#include <utility>
 
 #include "tc_ptx.cuh"
 #include "tv_internal.cuh"
@@ -188,32 +186,6 @@ inline bool encode_rows(CUtensorMap *tm, const void *base, CUtensorMapDataType d
 }
 
 constexpr size_t kSmemLimit = 227 * 1024;
-
-// Raises a kernel's dynamic shared-memory limit to the most a CTA may use, once per
-// (kernel, device) and under a lock.  Launches then pass only their own size, so
-// calls from several host threads never rewrite the attribute under one another.
-// (A device reset by the caller drops the setting; the library is not used across
-// one.)
-template <typename Kern>
-cudaError_t configure_smem_once(Kern kern) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    static std::mutex mu;
-    static std::set<std::pair<const void *, int>> done;
-    std::lock_guard<std::mutex> lock(mu);
-    const auto key = std::make_pair(reinterpret_cast<const void *>(kern), dev);
-    if (done.count(key)) return cudaSuccess;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
-    if (e != cudaSuccess) return e;
-    // without this the driver may configure a smaller shared-memory carveout and fit
-    // fewer CTAs than registers and shared memory allow
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    done.insert(key);
-    return cudaSuccess;
-}
 
 }  // namespace tcc
 }  // namespace tv

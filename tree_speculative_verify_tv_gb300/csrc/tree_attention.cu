@@ -650,8 +650,7 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s) {
         P.ns = fit >= 2 ? fit : 1;
     }
     P.sl2 = a.scale * 1.4426950408889634f;
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        tree_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::kAlloc);
+    const cudaError_t attr = configure_smem_once(tree_attention_kernel<D>, false);
     if (attr != cudaSuccess) return attr;
     const unsigned grid = (unsigned)((size_t)a.B * a.Hkv * P.mts * P.ns);
     cudaError_t e = launch_pdl(tree_attention_kernel<D>, dim3(grid), dim3(kThreadsAt),

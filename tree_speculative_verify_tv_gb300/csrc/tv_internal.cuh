@@ -5,6 +5,10 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "treeverify.h"
 
 namespace tv {
@@ -195,6 +199,40 @@ __device__ __forceinline__ bool load_check_tree(const int32_t *parent, const int
     }
     __syncthreads();
     return *s_flag == 0;
+}
+
+// Raises `kern`'s dynamic shared-memory limit to the most it can use beside its
+// static shared memory (227 KB per CTA in all), once per (kernel, device) and under
+// a lock; with `max_carveout` it also asks for the largest shared-memory carveout.
+// Launches then pass only their own size, so host threads that call the library at
+// the same time never rewrite the attribute under one another, and every device a
+// process drives gets the setting.  (A device reset by the caller drops it; the
+// library is not used across one.)
+template <typename Kern>
+cudaError_t configure_smem_once(Kern kern, bool max_carveout) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(reinterpret_cast<const void *>(kern), dev);
+    if (done.count(key)) return cudaSuccess;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024 - (int)fa.sharedSizeBytes);
+    if (e != cudaSuccess) return e;
+    if (max_carveout) {
+        // without this the driver may configure a smaller shared-memory carveout and
+        // fit fewer CTAs than registers and shared memory allow
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+    }
+    done.insert(key);
+    return cudaSuccess;
 }
 
 // Programmatic dependent launch: wait for the previous kernel in the stream

@@ -14,8 +14,6 @@
 // Per node, each of 256 threads updates its share of the dk x dv state as float4s
 // (dk*dv/1024 float4 each, dv >= 4) and accumulates S_i^T q_i over its rows; the
 // column sums are reduced through shared memory.
-#include <mutex>
-
 #include "tv_internal.cuh"
 
 // Scratch of tv_verify_serial_static: the per-node states of problems that need at
@@ -111,9 +109,7 @@ template <typename E, bool DIAG>
 cudaError_t launch_typed(const VerifyArgs &a, float *ws, cudaStream_t s) {
     const int groups = kThreadsS / (a.dv / 4);
     const size_t smem = ((size_t)3 * a.dk + a.dv + (size_t)groups * a.dv) * sizeof(float);
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        verify_serial_kernel<E, DIAG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)((3 * kMaxDim + kMaxDim + kThreadsS * 4) * sizeof(float)));
+    const cudaError_t attr = configure_smem_once(verify_serial_kernel<E, DIAG>, false);
     if (attr != cudaSuccess) return attr;
     return launch_pdl(verify_serial_kernel<E, DIAG>, dim3((unsigned)(a.B * a.H)),
                       dim3(kThreadsS), smem, s, a, ws);
@@ -127,24 +123,14 @@ size_t verify_serial_workspace_bytes(const VerifyArgs &a) {
 
 namespace {
 
-// Device address of g_serial_states on the current device, looked up once per
-// device with that device current.
+// Device address of g_serial_states on the current device.  It is looked up on
+// every call (cheap once the module is loaded), so the address is never stale, for
+// instance after the caller reset the device.
 cudaError_t static_states(float **ptr) {
-    constexpr int kMaxDevices = 64;
-    static std::mutex mu;
-    static float *addr[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_serial_states);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_serial_states);
-        if (e != cudaSuccess) return e;
-        addr[dev] = static_cast<float *>(p);
-    }
-    *ptr = addr[dev];
+    *ptr = static_cast<float *>(p);
     return cudaSuccess;
 }
 

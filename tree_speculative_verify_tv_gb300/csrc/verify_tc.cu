@@ -973,13 +973,7 @@ size_t tc_smem_bytes(const VerifyArgs &a, int pend_depth = 0) {
 template <typename... KArgs, typename... Args>
 cudaError_t launch_tc_kernel(void (*kern)(KArgs...), const TcParams &P, size_t smem,
                              unsigned grid, cudaStream_t s, Args &&...args) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    // without this the driver may configure a smaller shared-memory carveout and fit
-    // fewer CTAs than registers and shared memory allow
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = configure_smem_once(kern, true);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
@@ -991,11 +985,7 @@ cudaError_t launch_tc_kernel(void (*kern)(KArgs...), const TcParams &P, size_t s
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
         const size_t need = (size_t)smem_sm / (max_ctas + 1) + 1;
-        if (need > smem) {
-            smem = need;
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-        }
+        if (need > smem) smem = need;
     }
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, static_cast<Args &&>(args)...);
 }

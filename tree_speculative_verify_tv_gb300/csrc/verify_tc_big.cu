@@ -960,10 +960,7 @@ cudaError_t launch_verify_tc_staged(const VerifyArgs &a, cudaStream_t s) {
                                               CU_TENSOR_MAP_SWIZZLE_NONE));
     if (!ok) return cudaErrorInvalidValue;
     auto kern = diag ? verify_tc_staged_kernel<true> : verify_tc_staged_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = configure_smem_once(kern, true);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM, each taking every gridDim-th (request, head) unit
     int dev = 0, sms = 0;
@@ -995,10 +992,7 @@ cudaError_t launch_verify_tc_big(const VerifyArgs &a, cudaStream_t s) {
     const size_t smem = BigLayout(a.max_depth).total;
     const bool diag = a.decay == TV_DECAY_DIAG;
     auto kern = diag ? verify_tc_big_kernel<true> : verify_tc_big_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = configure_smem_once(kern, true);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3((unsigned)(a.B * a.H)), dim3(kThreadsG), smem, s, a);
 }

@@ -640,7 +640,7 @@ cudaError_t launch_fused_t(const VerifyArgs &a, const PendingArgs *pend, float *
     P.tmem_cols = tmem_columns(2 * (DV / 64) * NP);
     P.expire_first_wait = expire ? 1 : 0;
     auto kern = verify_tc_fused_kernel<DV, NP, PEND>;
-    cudaError_t e = configure_smem_once(kern);
+    cudaError_t e = configure_smem_once(kern, true);
     if (e != cudaSuccess) return e;
     const size_t smem = fused_smem_bytes(a, PEND ? pend->max_depth : 0);
     int dev = 0, sms = 0, per_sm = 0;
