@@ -55,14 +55,15 @@ WORKLOAD = WORKLOADS[2]
 _CS = "tree_speculative_verify_tv_gb300/csrc/"
 # sources behind each kernel whose DRAM traffic was captured with ncu
 TRAFFIC_SOURCES = {
-    "verify": [_CS + f for f in ("verify_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
-    "commit_verify": [_CS + f for f in ("verify_tc.cu", "tc_common.cuh", "tc_ptx.cuh",
+    "verify": [_CS + f for f in ("verify_tc_fused.cu", "tc_common.cuh", "tc_ptx.cuh",
+                                 "tv_internal.cuh")],
+    "commit_verify": [_CS + f for f in ("verify_tc_fused.cu", "tc_common.cuh", "tc_ptx.cuh",
                                         "tv_internal.cuh")],
     "tree_attention": [_CS + f for f in ("tree_attention.cu", "tc_common.cuh", "tc_ptx.cuh",
                                          "tv_internal.cuh")],
 }
 KERNEL_NAMES = {1: "simt", 2: "tcgen05 one unit per CTA", 3: "tcgen05, all products on tensor cores",
-                4: "tcgen05 node tiles"}
+                4: "tcgen05 large trees (staged or node tiles)"}
 
 
 DEFAULT_STEPS = {1: 40000, 2: 40000, 3: 5000, 4: 400, 5: 40}
@@ -80,6 +81,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--variant", type=int, default=0, help="tv_verify variant (0 auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration block (every configuration's tv_verify "
+                         "at full size)")
     ap.add_argument("--fold", type=int, default=32,
                     help="also time one verify launch over this many config-2 layers folded "
                          "into the head axis (0 = skip)")
@@ -439,6 +443,137 @@ def attention_setup(base, ctx, dev, stream):
     return tree_call, dec_call, cache + side(T), cache + side(B), flops, status
 
 
+# Distributions of the per-node factors (as in the workloads module): q, k, v ~
+# N(0, 1/dk), g per the configuration, H0 ~ N(0, h0 std).  The per-configuration
+# block draws them on the device with a seeded torch generator, so that the 4.8 GB
+# large-tree stack needs no host-side generation; the trees and token arrays come
+# from the workloads module unchanged (values=False).
+G_KIND = {1: "softplus01", 2: "softplus_m1", 3: "logsig16", 4: "softplus_m1", 5: "logsig16"}
+H0_STD = {1: 0.1, 2: 0.05, 3: 0.05, 4: 0.05, 5: 0.05}
+# ncu figures of each configuration's verify kernel (profiles/verify_configs_ncu.txt),
+# valid while the kernel's sources hash to the recorded value
+CONFIG_KERNEL_SOURCES = {
+    3: [_CS + f for f in ("verify_tc_big.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
+    4: [_CS + f for f in ("verify_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
+    5: [_CS + f for f in ("verify_tc_big.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
+}
+
+
+def sources_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        fp = os.path.join(ROOT, p)
+        if os.path.exists(fp):
+            h.update(open(fp, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_config_profile(cfg: int):
+    """Tensor-pipe share and DRAM bytes of config cfg's verify kernel from the
+    committed ncu summary, or None when absent or the sources changed."""
+    fp = os.path.join(ROOT, "profiles", "verify_configs_ncu.txt")
+    if cfg not in CONFIG_KERNEL_SOURCES or not os.path.exists(fp):
+        return None
+    for line in open(fp):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = line.split()
+        if len(f) >= 5 and f[0] == "c%d" % cfg:
+            if f[1] != sources_hash(CONFIG_KERNEL_SOURCES[cfg]):
+                return None
+            return {"tensor_pipe_pct": float(f[2]), "dram_bytes_per_unit": float(f[3]),
+                    "captured_on": f[4]}
+    return None
+
+
+def fill_factors(d, cfg: int, seed: int, dev):
+    """Draw q, k, v, g, H0 of a DeviceBatch on the device (see G_KIND, H0_STD)."""
+    import torch
+    import torch.nn.functional as F
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    T, H, dk, dv, B = max(d.T, 1), d.H, d.dk, d.dv, d.B
+    dt = torch.bfloat16 if d.qkv_dtype == 0 else torch.float32
+    sc = 1.0 / np.sqrt(dk)
+    d.q = (torch.randn((T, H, dk), generator=gen, device=dev) * sc).to(dt)
+    d.k = (torch.randn((T, H, dk), generator=gen, device=dev) * sc).to(dt)
+    d.v = (torch.randn((T, H, dv), generator=gen, device=dev) * sc).to(dt)
+    kind = G_KIND[cfg]
+    if kind == "softplus01":
+        d.g = -F.softplus(torch.randn((T, H), generator=gen, device=dev))
+    elif kind == "softplus_m1":
+        d.g = -F.softplus(torch.randn((T, H), generator=gen, device=dev) * 0.5 - 1.0)
+    else:
+        d.g = F.logsigmoid(torch.randn((T, H, dk), generator=gen, device=dev) + 2.0) / 16.0
+    d.H0 = torch.randn((B, H, dk, dv), generator=gen, device=dev) * H0_STD[cfg]
+
+
+def per_config_block(tv, dev, stream, l2, peak, skip, cfg2_us=None):
+    """tv_verify at every configuration's full size: kernel, algorithmic bytes, launch
+    time (graph replays over input sets rotated past 4x L2), GB/s, fraction of the
+    measured HBM peak, node-heads/s, transient bytes against per-node states, and the
+    tensor-pipe share of the committed ncu capture for configurations 3-5."""
+    import torch
+    import workloads
+    out = {}
+    launches = {1: 400, 2: 400, 3: 100, 4: 20, 5: 5}
+    for cfg in range(1, 6):
+        if cfg in skip:
+            continue
+        hb = workloads.make_config(cfg, seed=1000 + cfg, values=False)
+        vb = verify_bytes(hb)
+        R = 1 if vb >= 4 * l2 else max(2, int(np.ceil(4.0 * l2 / vb)) + 1)
+        if vb < 1 << 20:
+            R = 1  # a few KB: latency only
+        dbs = []
+        for r in range(R):
+            d = tv.DeviceBatch(hb, device=dev)
+            fill_factors(d, cfg, 5000 + 17 * cfg + r, dev)
+            dbs.append(d)
+        variant = dbs[0].variant()
+        K = launches[cfg]
+        with torch.cuda.stream(stream):
+            for d in dbs:
+                d.status.zero_()
+                d.verify(stream=stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(K):
+                dbs[i % R].verify(stream=stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        for d in dbs:
+            if int(d.status[0].item()) != 0:
+                raise SystemExit("device status %d in config %d" % (int(d.status[0].item()), cfg))
+        t = e0.elapsed_time(e1) * 1e-3 / K
+        qk = 2 if hb.qkv_dtype == "bf16" else 4
+        sg = 4 if hb.decay == "scalar" else 4 * hb.dk
+        # the token-level factors that replace per-node states: g, k and v
+        factors = hb.T * hb.H * ((hb.dk + hb.dv) * qk + sg)
+        naive = hb.T * hb.H * hb.dk * hb.dv * 4
+        entry = {"workload": WORKLOADS[cfg], "kernel": KERNEL_NAMES.get(variant, str(variant)),
+                 "bytes_per_launch": int(vb), "launch_us": t * 1e6, "gbs": vb / t / 1e9,
+                 "frac": vb / t / 1e9 / peak, "node_heads_per_s": hb.T * hb.H / t,
+                 "node_heads": hb.T * hb.H, "launches": K, "input_sets": R,
+                 "transient_bytes": {"library_workspace": 0, "factors": int(factors),
+                                     "naive_per_node_states": int(naive),
+                                     "cut_vs_naive": 1.0 - factors / naive}}
+        prof = recorded_config_profile(cfg)
+        if prof is not None:
+            entry["ncu"] = prof
+        out["c%d" % cfg] = entry
+        del g, dbs
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
     import tree_speculative_verify_tv_gb300 as tv
@@ -769,8 +904,8 @@ def run_ours(args, world, rank, local):
                 + 4 * base.B * (3 + base.max_depth) + 4 * base.T)
     cv_launch = t_cv / K
     used_variant = args.variant if args.variant else dbs[0].variant()
-    # the recorded captures are of the tensor-core kernels on the config-2 workload
-    tc2 = cfg == 2 and used_variant == 2
+    # the recorded captures are of the fused tensor-core kernel on the config-2 workload
+    tc2 = cfg == 2 and used_variant == 3
     if fused:
         dom_bytes, dom_t, dom_name = cvb, cv_launch, "tv_commit_verify"
         traffic = recorded_traffic("commit_verify") if tc2 else None
@@ -826,6 +961,30 @@ def run_ours(args, world, rank, local):
                          "units (verify + greedy walk + commit), %.1f s" % (n, upl,
                                                                               base.B * base.H,
                                                                               dt)}
+        v1, upl1, n1, dt1, _ = time_oracle(base, 20, 5.0, 1, fill_budget=True)
+        cpu["one_thread"] = {"value": v1, "unit": UNIT, "cores": 1,
+                             "sample": "%d steps, each on %d units, %.1f s" % (n1, upl1, dt1)}
+
+    # host time of one un-captured call (argument checks, tensor maps, launch)
+    host_call = None
+    configs = None
+    if rank == 0:
+        host_call = {}
+        for name, fn in (("tv_verify", lambda: dbs[0].verify(stream=stream)),
+                         ("tv_commit_verify", lambda: dbs[0].commit_verify(dbs[0], stream=stream))):
+            for _ in range(20):
+                fn()
+            stream.synchronize()
+            NC = 300
+            t0 = time.perf_counter()
+            for _ in range(NC):
+                fn()
+            t1 = time.perf_counter()
+            stream.synchronize()
+            host_call[name] = (t1 - t0) / NC * 1e6
+        host_call["unit"] = "us of host time per call, not captured in a graph"
+        if not args.no_configs:
+            configs = per_config_block(tv, dev, stream, l2, peak, skip=set())
 
     if rank == 0:
         line = {
@@ -871,6 +1030,8 @@ def run_ours(args, world, rank, local):
                 "serial": "tv_verify_serial: node after node, per-node states in a %d MB "
                           "workspace" % (serial_bytes // 2 ** 20)}
                 if t_ser is not None else None),
+            "host_us_per_call": host_call,
+            "per_config": configs,
             "tree_builder": builder,
             "stochastic_accept": stochastic,
             "tree_attention": attention,
@@ -882,8 +1043,9 @@ def run_ours(args, world, rank, local):
                 "step_us_with_it": t_sl / K * 1e6,
                 "step": "tv_commit_verify + tv_accept_greedy_logits"},
             "transient_bytes": {"library_workspace": 0,
+                                # the token-level factors g, k, v kept instead of states
                                 "factors": int(base.T * base.H * (
-                                    (2 * base.dk + base.dv) * (2 if base.qkv_dtype == "bf16" else 4)
+                                    (base.dk + base.dv) * (2 if base.qkv_dtype == "bf16" else 4)
                                     + (4 if base.decay == "scalar" else 4 * base.dk))),
                                 "naive_per_node_states": int(base.T * base.H * base.dk * base.dv
                                                              * 4)},

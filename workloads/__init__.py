@@ -191,8 +191,12 @@ def _normal_scaled(rng, shape, std) -> np.ndarray:
 def assemble(rng, parents: List[np.ndarray], H: int, dk: int, dv: int, *, decay: str,
              qkv_dtype: str, g_kind: str, h0_std: float, draft=None, target=None,
              root_argmax=None, vocab: int = 32, max_depth: Optional[int] = None,
-             max_nodes: Optional[int] = None, name: str = "") -> Batch:
+             max_nodes: Optional[int] = None, name: str = "", values: bool = True) -> Batch:
     """Pack per-request trees and draw the per-node factors.
+
+    values=False skips the factors and the state (q, k, v, g, H0 come back as empty
+    arrays of the right dtype): the trees and tokens only, for a caller that fills
+    the factors itself (the benchmark's timing of large configurations).
 
     g_kind: "softplus01"  g = -softplus(N(0,1))          (scalar decay, c1)
             "softplus_m1" g = -softplus(N(-1, 0.5))      (scalar decay, c2/c4)
@@ -207,6 +211,19 @@ def assemble(rng, parents: List[np.ndarray], H: int, dk: int, dv: int, *, decay:
     parent = np.concatenate(parents).astype(np.int32) if T else np.zeros(0, np.int32)
     depth = (np.concatenate([depths_from_parents(p) for p in parents]).astype(np.int32)
              if T else np.zeros(0, np.int32))
+    if not values:
+        e16 = np.zeros(0, np.uint16 if qkv_dtype == "bf16" else np.float32)
+        return Batch(B=B, H=H, dk=dk, dv=dv, decay=decay, qkv_dtype=qkv_dtype,
+                     node_offsets=offs, parent=parent, depth=depth, q=e16, k=e16, v=e16,
+                     g=np.zeros(0, np.float32), H0=np.zeros(0, np.float32),
+                     draft=np.zeros(T, np.int32) if draft is None else np.asarray(draft, np.int32),
+                     target=np.zeros(T, np.int32) if target is None else np.asarray(target, np.int32),
+                     root_argmax=(np.zeros(B, np.int32) if root_argmax is None
+                                  else np.asarray(root_argmax, np.int32)),
+                     max_nodes=int(max_nodes if max_nodes is not None
+                                   else max(1, int(sizes.max()) if B else 1)),
+                     max_depth=int(max_depth if max_depth is not None
+                                   else (int(depth.max()) if T else 1)), name=name)
     sc = 1.0 / np.sqrt(dk)
     q = _normal_scaled(rng, (T, H, dk), sc)
     k = _normal_scaled(rng, (T, H, dk), sc)
@@ -274,15 +291,16 @@ def _plant_path(rng, parent: np.ndarray, draft: np.ndarray, target: np.ndarray,
     return root_tok
 
 
-def config1(seed: Optional[int] = None) -> Batch:
+def config1(seed: Optional[int] = None, values: bool = True) -> Batch:
     """c1: one request, one head, dk=dv=16, fp32 q/k/v, random recursive 8-node tree."""
     rng = np.random.default_rng(1001 if seed is None else seed)
     par = tree_random_recursive(rng, 8)
     return assemble(rng, [par], 1, 16, 16, decay="scalar", qkv_dtype="f32",
-                    g_kind="softplus01", h0_std=0.1, vocab=32, max_depth=8, name="c1")
+                    g_kind="softplus01", h0_std=0.1, vocab=32, max_depth=8, name="c1",
+                    values=values)
 
 
-def config2(seed: Optional[int] = None, B: int = 16, H: int = 24) -> Batch:
+def config2(seed: Optional[int] = None, B: int = 16, H: int = 24, values: bool = True) -> Batch:
     """c2: Mamba-2-like layer.  B=16, H=24, dk=128, dv=64, bf16, scalar decay.
 
     Fixed top-k tree: 4 children of the context, each continued by a chain of
@@ -307,7 +325,7 @@ def config2(seed: Optional[int] = None, B: int = 16, H: int = 24) -> Batch:
     return assemble(rng, parents, H, 128, 64, decay="scalar", qkv_dtype="bf16",
                     g_kind="softplus_m1", h0_std=0.05, draft=np.concatenate(drafts),
                     target=np.concatenate(targets), root_argmax=np.array(roots), max_depth=4,
-                    name="c2")
+                    name="c2", values=values)
 
 
 def _best_first_requests(rng, B: int, n: int, depth_cap: int, alpha: float, C: int = 8):
@@ -335,19 +353,19 @@ def _best_first_requests(rng, B: int, n: int, depth_cap: int, alpha: float, C: i
     return parents, drafts, targets, roots, rhos
 
 
-def config3(seed: Optional[int] = None, B: int = 32, H: int = 16) -> Batch:
+def config3(seed: Optional[int] = None, B: int = 32, H: int = 16, values: bool = True) -> Batch:
     """c3: GLA-like layer, diagonal decay.  B=32, H=16, dk=dv=128, bf16; best-first
     64-node trees of depth <= 8 from Dirichlet(0.3) marginals over 8 candidates."""
     rng = np.random.default_rng(1003 if seed is None else seed)
     parents, drafts, targets, roots, rhos = _best_first_requests(rng, B, 64, 8, 0.3)
     b = assemble(rng, parents, H, 128, 128, decay="diag", qkv_dtype="bf16", g_kind="logsig16",
                  h0_std=0.05, draft=np.concatenate(drafts), target=np.concatenate(targets),
-                 root_argmax=np.array(roots), max_depth=8, name="c3")
+                 root_argmax=np.array(roots), max_depth=8, name="c3", values=values)
     b.rho_sums = rhos  # type: ignore[attr-defined]
     return b
 
 
-def config4(seed: Optional[int] = None, B: int = 128, H: int = 32) -> Batch:
+def config4(seed: Optional[int] = None, B: int = 128, H: int = 32, values: bool = True) -> Batch:
     """c4: mixed-budget batch.  B=128, H=32, dk=dv=128, bf16, scalar decay; tree
     sizes ~ U{4,8,16,32,64,128}; random parents with depth cap 12."""
     rng = np.random.default_rng(1004 if seed is None else seed)
@@ -355,10 +373,11 @@ def config4(seed: Optional[int] = None, B: int = 128, H: int = 32) -> Batch:
     parents = [tree_random_capped(rng, int(n), 12) for n in sizes]
     return assemble(rng, parents, H, 128, 128, decay="scalar", qkv_dtype="bf16",
                     g_kind="softplus_m1", h0_std=0.05, vocab=32, max_depth=12,
-                    max_nodes=128, name="c4")
+                    max_nodes=128, name="c4", values=values)
 
 
-def config5(seed: Optional[int] = None, B: int = 8, layers: int = 36, heads: int = 32) -> Batch:
+def config5(seed: Optional[int] = None, B: int = 8, layers: int = 36, heads: int = 32,
+            values: bool = True) -> Batch:
     """c5: large-tree stack.  B=8, 36 layers x 32 heads folded into H=1152,
     dk=dv=128, bf16, diagonal decay; best-first 256-node trees of depth <= 16 from
     Dirichlet(0.2) marginals; one planted accepted path per request to a uniform
@@ -381,7 +400,7 @@ def config5(seed: Optional[int] = None, B: int = 8, layers: int = 36, heads: int
     return assemble(rng, parents, layers * heads, 128, 128, decay="diag", qkv_dtype="bf16",
                     g_kind="logsig16", h0_std=0.05, draft=np.concatenate(drafts),
                     target=np.concatenate(targets), root_argmax=np.array(roots),
-                    max_depth=16, name="c5")
+                    max_depth=16, name="c5", values=values)
 
 
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
