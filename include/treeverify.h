@@ -84,11 +84,15 @@ typedef enum tv_variant {
     TV_VARIANT_TC = 2,      /* tcgen05 tensor-core kernel, one (request, head) per CTA:
                                bf16 q/k/v, dk in {64,128}, dv in {64,128};
                                TV_ERR_UNSUPPORTED otherwise */
-    TV_VARIANT_TC_FUSED = 3, /* tcgen05 kernel with the context term, the pair scores and
+    TV_VARIANT_TC_FUSED = 3, /* tcgen05 kernels with the context term, the pair scores and
                                the tree term all on tensor cores, one (request, head) per
-                               CTA: scalar decay, bf16 q/k/v, dk and dv in {64,128},
-                               max_nodes <= 32; TV_ERR_UNSUPPORTED otherwise.  What
-                               TV_VARIANT_AUTO picks where it applies */
+                               CTA, bf16 q/k/v: scalar decay with dk and dv in {64,128}
+                               and max_nodes <= 32, or per-channel decay with dk in
+                               {64,128}, dv = 128 and max_nodes <= 64 (the decay folded
+                               into the factors, e^{G} q and e^{-G} k, where every path
+                               sum |G| <= 69; a unit outside that range takes its pair
+                               weights from a walk of its paths); TV_ERR_UNSUPPORTED
+                               otherwise.  What TV_VARIANT_AUTO picks where it applies */
     TV_VARIANT_TC_TILED = 4  /* tcgen05 kernels for large trees, one (request, head) per
                                CTA: bf16 q/k/v, dk = dv = 128, trees up to TV_MAX_NODES.
                                Where a request's k, decay and v rows fit shared memory

@@ -127,7 +127,8 @@ def test_support_query_matches_forced_launch_checks(lib):
 
 
 def test_fused_variant_limits(lib):
-    # the fused kernel: scalar decay, bf16, dk and dv in {64, 128}, <= 32 nodes
+    # the fused kernels: bf16; scalar decay with dk and dv in {64, 128} and <= 32 nodes,
+    # or per-channel decay with dk in {64, 128}, dv = 128 and <= 64 nodes
     import torch
     if torch.cuda.is_available():
         # (the tensor-core kernels need the driver's tensor-map encoder)
@@ -138,8 +139,13 @@ def test_fused_variant_limits(lib):
                                      tv.TV_VARIANT_TC_FUSED) == 1
         # trees of 33..256 nodes keep the one-unit kernel
         assert tv.tv_verify_variant(prob(dk=128, dv=64, max_nodes=64)) == tv.TV_VARIANT_TC
+        for dk in (64, 128):
+            diag = prob(dk=dk, dv=128, max_nodes=64, decay=tv.TV_DECAY_DIAG)
+            assert tv.tv_verify_supports(diag, tv.TV_VARIANT_TC_FUSED) == 1
+            assert tv.tv_verify_variant(diag) == tv.TV_VARIANT_TC_FUSED
     for bad in (prob(dk=128, dv=64, max_nodes=33, total_nodes=5),
                 prob(dk=128, dv=64, decay=tv.TV_DECAY_DIAG),
+                prob(dk=128, dv=128, max_nodes=65, decay=tv.TV_DECAY_DIAG),
                 prob(dk=96, dv=64), prob(dk=128, dv=64, qkv_dtype=tv.TV_F32)):
         assert tv.tv_verify_supports(bad, tv.TV_VARIANT_TC_FUSED) == 0
         assert verify_rc(bad, variant=tv.TV_VARIANT_TC_FUSED) == tv.TV_ERR_UNSUPPORTED

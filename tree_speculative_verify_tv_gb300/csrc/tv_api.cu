@@ -12,6 +12,10 @@ namespace tv {
 // verify_tc_big.cu: whether the staged large-tree kernel takes this problem and is
 // the faster choice (per-channel decay, trees of 64 or more nodes)
 bool verify_tc_staged_preferred(const VerifyArgs &a);
+// verify_tc_fdiag.cu: the per-channel-decay member of TV_VARIANT_TC_FUSED (dv = 128,
+// trees of up to 64 nodes)
+bool verify_tc_fdiag_supported(const VerifyArgs &a);
+cudaError_t launch_verify_tc_fdiag(const VerifyArgs &a, cudaStream_t s, bool expire_first_wait);
 }  // namespace tv
 
 namespace {
@@ -42,12 +46,24 @@ tv_status check_ptrs(std::initializer_list<const void *> ptrs) {
     return TV_OK;
 }
 
-// The kernel TV_VARIANT_AUTO picks: the fused tensor-core kernel for scalar decay
-// trees of up to 32 nodes, the staged large-tree kernel for per-channel decay
-// trees of 64 or more nodes, the one-unit tensor-core kernel where it applies, the
-// large-tree tensor-core kernels for trees too large for it, else SIMT.
+// TV_VARIANT_TC_FUSED: all products of a unit on tensor cores; scalar decay (trees of
+// up to 32 nodes) or per-channel decay (dv = 128, trees of up to 64 nodes).
+bool fused_supported(const tv::VerifyArgs &a) {
+    return a.decay == TV_DECAY_DIAG ? tv::verify_tc_fdiag_supported(a)
+                                    : tv::verify_tc_fused_supported(a);
+}
+
+cudaError_t launch_fused(const tv::VerifyArgs &a, cudaStream_t s, bool expire) {
+    return a.decay == TV_DECAY_DIAG ? tv::launch_verify_tc_fdiag(a, s, expire)
+                                    : tv::launch_verify_tc_fused(a, s, expire);
+}
+
+// The kernel TV_VARIANT_AUTO picks: the fused tensor-core kernels where they apply,
+// the staged large-tree kernel for per-channel decay trees of 64 or more nodes, the
+// one-unit tensor-core kernel where it applies, the large-tree tensor-core kernels for
+// trees too large for it, else SIMT.
 int32_t auto_variant(const tv::VerifyArgs &a) {
-    if (tv::verify_tc_fused_supported(a)) return TV_VARIANT_TC_FUSED;
+    if (fused_supported(a)) return TV_VARIANT_TC_FUSED;
     if (tv::verify_tc_staged_preferred(a)) return TV_VARIANT_TC_TILED;
     if (tv::verify_tc_supported(a)) return TV_VARIANT_TC;
     if (tv::verify_tc_big_supported(a)) return TV_VARIANT_TC_TILED;
@@ -56,7 +72,7 @@ int32_t auto_variant(const tv::VerifyArgs &a) {
 
 cudaError_t launch_verify_auto(const tv::VerifyArgs &a, cudaStream_t s) {
     switch (auto_variant(a)) {
-        case TV_VARIANT_TC_FUSED: return tv::launch_verify_tc_fused(a, s);
+        case TV_VARIANT_TC_FUSED: return launch_fused(a, s, false);
         case TV_VARIANT_TC: return tv::launch_verify_tc(a, s);
         case TV_VARIANT_TC_TILED: return tv::launch_verify_tc_big(a, s);
         default: return tv::launch_verify_simt(a, s);
@@ -94,7 +110,7 @@ int32_t tv_verify_supports(const tv_problem *p, int32_t variant) {
         case TV_VARIANT_AUTO:
         case TV_VARIANT_SIMT: return 1;
         case TV_VARIANT_TC: return tv::verify_tc_supported(a) ? 1 : 0;
-        case TV_VARIANT_TC_FUSED: return tv::verify_tc_fused_supported(a) ? 1 : 0;
+        case TV_VARIANT_TC_FUSED: return fused_supported(a) ? 1 : 0;
         case TV_VARIANT_TC_TILED: return tv::verify_tc_big_supported(a) ? 1 : 0;
         default: return -static_cast<int32_t>(TV_ERR_DTYPE);
     }
@@ -141,8 +157,8 @@ tv_status tv_verify_ex(const tv_problem *p, const float *H0, const void *q, cons
             e = tv::launch_verify_tc(a, s);
             break;
         case TV_VARIANT_TC_FUSED:
-            if (!tv::verify_tc_fused_supported(a)) return TV_ERR_UNSUPPORTED;
-            e = tv::launch_verify_tc_fused(a, s, expire);
+            if (!fused_supported(a)) return TV_ERR_UNSUPPORTED;
+            e = launch_fused(a, s, expire);
             break;
         case TV_VARIANT_TC_TILED:
             if (!tv::verify_tc_big_supported(a)) return TV_ERR_UNSUPPORTED;
