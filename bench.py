@@ -453,7 +453,7 @@ H0_STD = {1: 0.1, 2: 0.05, 3: 0.05, 4: 0.05, 5: 0.05}
 # ncu figures of each configuration's verify kernel (profiles/verify_configs_ncu.txt),
 # valid while the kernel's sources hash to the recorded value
 CONFIG_KERNEL_SOURCES = {
-    3: [_CS + f for f in ("verify_tc_big.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
+    3: [_CS + f for f in ("verify_tc_fdiag.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
     4: [_CS + f for f in ("verify_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
     5: [_CS + f for f in ("verify_tc_big.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
 }
