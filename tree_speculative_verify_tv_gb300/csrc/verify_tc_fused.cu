@@ -23,7 +23,10 @@
 // at dv = 128) by bulk copy; warps 0-3 rewrite each chunk in place into the tensor
 // core's operand: per 64 channels a block of hi rows and a block of lo rows
 // (128-byte swizzled, MN-major: a row holds one key channel's 64 values), so no
-// transpose is needed.
+// transpose is needed.  For dv = 64 without a pending commit the parts go to tensor
+// memory instead (the A operand of the context product: one thread per lane, lanes
+// 0-63 the hi parts and 64-127 the lo parts of the 64 value channels, packed along the
+// key rows), which saves the in-place barrier and the operand's shared-memory reads.
 //
 // Roles (256 threads):
 //   warps 0-3  chunk copies (thread 0); per chunk: read, apply the pending commit
@@ -113,6 +116,11 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
     constexpr int MG = DV / 64;          // 64-channel groups
     constexpr int R = kChunkVals / DV;   // key rows per chunk: 32 or 16
     constexpr uint32_t kColT = MG * NP;  // tree columns, shared with the scores
+    // dv = 64 without a pending commit: the state's hi / lo parts go to tensor memory (A
+    // operand of the context product; lanes 0-63 hi, 64-127 lo of the 64 value
+    // channels), R / 2 columns a chunk, so a chunk is never rewritten in place
+    constexpr bool kStateTmem = DV == 64 && !PEND;
+    constexpr uint32_t kColA = 2 * MG * NP;
     constexpr int cpr = DV / 8;          // 8-value pieces per state row
     const VerifyArgs &a = P.a;
     extern __shared__ uint8_t smem_raw[];
@@ -209,6 +217,32 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
             }
             named_barrier(1, 128);
             if (*sLate & 2) break;  // the chunk did not land: stop converting
+            if constexpr (kStateTmem) {
+                // thread = tensor-memory lane: value channel 32 (warp & 1) + lane, the hi part
+                // (warps 0-1) or the lo part (warps 2-3) of its R key rows, packed in pairs
+                // along the rows (the A operand layout)
+                const float *cpf = reinterpret_cast<const float *>(sH + c * kChunkBytes) +
+                                   32 * (warp & 1) + lane;
+                uint32_t pk[R / 2];
+#pragma unroll
+                for (int m = 0; m < R / 2; ++m) {
+                    const float x0 = cpf[(2 * m) * DV], x1 = cpf[(2 * m + 1) * DV];
+                    if (warp < 2) {
+                        pk[m] = __byte_perm(__float_as_uint(x0), __float_as_uint(x1), 0x7632);
+                    } else {
+                        uint32_t hi;
+                        split_pair(x0, x1, hi, pk[m]);
+                    }
+                }
+                static_assert(!kStateTmem || R / 2 == 16, "dv = 64: 32 key rows a chunk");
+                ptx::tmem_st_x16(tmem + kColA + c * (R / 2) + (static_cast<uint32_t>(32 * warp) << 16),
+                                 reinterpret_cast<const uint32_t (&)[16]>(pk));
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(b_conv(c));
+                continue;
+            }
             uint8_t *cp = sH + c * kChunkBytes;
             float x[kRows][8];
 #pragma unroll
@@ -514,6 +548,18 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
             if (n == 0) continue;
             const uint32_t qa = ptx::smem_addr(smem + L.q_off);
             const uint32_t ca = ptx::smem_addr(sH) + c * kChunkBytes;
+            if constexpr (kStateTmem) {
+#pragma unroll
+                for (int ks = 0; ks < R / 16; ++ks) {
+                    const int kk = (c * R) / 16 + ks;  // 16-row step of the key channels
+                    const uint64_t bd =
+                        ptx::desc_kmajor_sw128(qa + (kk / 4) * tile_slab + (kk % 4) * 32, 1024);
+                    // A = the hi (lanes 0-63) and lo (64-127) parts in tensor memory
+                    ptx::mma_bf16_ts(tmem, tmem + kColA + c * (R / 2) + ks * 8, bd, idn,
+                                     (c > 0 || ks > 0) ? 1u : 0u);
+                }
+                continue;
+            }
 #pragma unroll
             for (int g = 0; g < MG; ++g)
 #pragma unroll
@@ -637,7 +683,7 @@ cudaError_t launch_fused_t(const VerifyArgs &a, const PendingArgs *pend, float *
     P.a = a;
     P.pend = pend ? *pend : PendingArgs{};
     P.H_w = Hw;
-    P.tmem_cols = tmem_columns(2 * (DV / 64) * NP);
+    P.tmem_cols = tmem_columns(2 * (DV / 64) * NP + (DV == 64 && !PEND ? a.dk / 2 : 0));
     P.expire_first_wait = expire ? 1 : 0;
     auto kern = verify_tc_fused_kernel<DV, NP, PEND>;
     cudaError_t e = configure_smem_once(kern, true);
