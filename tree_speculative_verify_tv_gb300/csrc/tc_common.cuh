@@ -5,6 +5,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -186,6 +187,30 @@ inline bool encode_rows(CUtensorMap *tm, const void *base, CUtensorMapDataType d
 }
 
 constexpr size_t kSmemLimit = 227 * 1024;
+
+// CTAs of `kern` resident on one SM at once: the least of what registers, shared memory
+// (`smem` dynamic bytes) and tensor memory (`tmem_cols` columns of 512) allow.  The
+// runtime's occupancy query knows nothing of tensor memory, and on this part it has
+// reported fewer CTAs than the launch statistics show.
+template <typename Kern>
+cudaError_t resident_ctas(Kern kern, int threads, size_t smem, int tmem_cols, int &per_sm) {
+    int dev = 0, smem_sm = 0, smem_rsv = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+            cudaSuccess)
+        return e;
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;  // allocated per warp
+    const int by_regs = 65536 / (regs_warp * ((threads + 31) / 32));
+    const int by_smem = smem_sm / (int)(smem + fa.sharedSizeBytes + smem_rsv);
+    const int by_tmem = tmem_cols > 0 ? 512 / tmem_cols : 64;
+    per_sm = std::max(1, std::min(std::min(by_regs, by_smem), by_tmem));
+    return cudaSuccess;
+}
 
 }  // namespace tcc
 }  // namespace tv

@@ -59,8 +59,6 @@
 // Every wait is bounded (TV_ERR_TIMEOUT); every copy and product in flight is waited
 // for (bounded) before tensor memory is freed.  Malformed trees zero their rows and set
 // TV_ERR_TREE.
-#include <algorithm>
-
 #include "tc_common.cuh"
 
 namespace tv {
@@ -852,25 +850,12 @@ cudaError_t launch_fdiag_t(const VerifyArgs &a, bool expire, cudaStream_t s) {
     cudaError_t e = configure_smem_once(kern, true);
     if (e != cudaSuccess) return e;
     const size_t smem = DiagLayout(NP, a.dk / kGrpCh).total;
-    // persistent: one CTA per resident slot, each taking every grid-th unit.  The slots
-    // per SM are the least of what registers, shared memory and tensor memory allow (the
-    // runtime's occupancy query knows nothing of tensor memory)
-    int dev = 0, sms = 0, smem_sm = 0, smem_rsv = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
-            cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
-            cudaSuccess)
+    // persistent: one CTA per resident slot, each taking every grid-th unit
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = resident_ctas(kern, kThreadsD, smem, P.tmem_cols, per_sm)) != cudaSuccess)
         return e;
-    cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-    const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;  // allocated per warp
-    const int by_regs = 65536 / (regs_warp * (kThreadsD / 32));
-    const int by_smem = smem_sm / (int)(smem + fa.sharedSizeBytes + smem_rsv);
-    const int by_tmem = 512 / P.tmem_cols;
-    const int per_sm = std::max(1, std::min(std::min(by_regs, by_smem), by_tmem));
     const long long units = (long long)a.B * a.H;
     const long long grid = std::min<long long>(units, (long long)sms * per_sm);
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreadsD), smem, s, tq, tk, tv_, tg, P);

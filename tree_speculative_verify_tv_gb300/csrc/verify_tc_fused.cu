@@ -690,11 +690,10 @@ cudaError_t launch_fused_t(const VerifyArgs &a, const PendingArgs *pend, float *
     if (e != cudaSuccess) return e;
     const size_t smem = fused_smem_bytes(a, PEND ? pend->max_depth : 0);
     int dev = 0, sms = 0, per_sm = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreadsF, smem);
-    if (e != cudaSuccess) return e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = resident_ctas(kern, kThreadsF, smem, P.tmem_cols, per_sm)) != cudaSuccess)
+        return e;
     P.wave = sms * per_sm;
     return launch_pdl(kern, dim3((unsigned)(a.B * a.H)), dim3(kThreadsF), smem, s, tq, tk, tv_, P);
 }
