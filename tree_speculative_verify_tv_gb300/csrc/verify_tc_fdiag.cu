@@ -523,17 +523,19 @@ __global__ void __launch_bounds__(kThreadsD, 2)
             // lane quadrant = warp: value channel c, every node; after all of unit it's
             // products.  Returns false when a wait gave up.
             // (one decision for the four warps: they meet at named barriers)
-            if (tid == 0 && !(!late_now() && ptx::mbar_wait(b_dfull(it), ph(it), kWaitLimit)))
-                atomicOr(sLate, 2);
-            named_barrier(1, kConvWarps * 32);
-            if (*sLate & 2) return false;
+            bool ok = true;
+            if (tid == 0) {
+                ok = !late_now() && ptx::mbar_wait(b_dfull(it), ph(it), kWaitLimit);
+                if (!ok) atomicOr(sLate, 2);
+            }
+            if (!named_barrier_and(1, kConvWarps * 32, ok)) return false;
             ptx::tc_fence_after_sync();
             const int *mt = meta(it);
             const int n = mt[kMN], off = mt[kMOff];
             const int u = unit_of(it), h = u % H;
             if (mt[kMZero])
                 for (int i = 0; i < n; ++i) a.out[((size_t)(off + i) * H + h) * kDvD + c] = 0.f;
-            if (mt[kMRun] && !late_now()) {
+            if (mt[kMRun]) {  // the products are done (verdict above): D holds the outputs
                 constexpr int CW = NP < 32 ? NP : 32;
 #pragma unroll
                 for (int cb = 0; cb < NP; cb += CW) {
@@ -558,10 +560,12 @@ __global__ void __launch_bounds__(kThreadsD, 2)
                 go = false;
                 break;
             }
-            if (tid == 0 && !(!late_now() && ptx::mbar_wait(b_tree(it), ph(it), kWaitLimit)))
-                atomicOr(sLate, 2);
-            named_barrier(1, kConvWarps * 32);
-            if (*sLate & 2) {
+            bool tok = true;
+            if (tid == 0) {
+                tok = !late_now() && ptx::mbar_wait(b_tree(it), ph(it), kWaitLimit);
+                if (!tok) atomicOr(sLate, 2);
+            }
+            if (!named_barrier_and(1, kConvWarps * 32, tok)) {
                 go = false;
                 break;
             }
@@ -569,16 +573,18 @@ __global__ void __launch_bounds__(kThreadsD, 2)
             int q = 0;
             for (; q < nch; ++q) {
                 const int gq = it * nch + q, slot = gq % kRing;
+                bool cok = true;
                 if (tid == 0) {
                     // stop when another role gave up, or when this chunk does not land
-                    const bool ok = !late_now() &&
-                                    ((gq == 0 && P.expire_first_wait)
-                                         ? false  // test hook: treated as expired
-                                         : ptx::mbar_wait(b_slot(slot), (gq / kRing) & 1, kWaitLimit));
-                    if (!ok) atomicOr(sLate, 2);
+                    cok = !late_now() &&
+                          ((gq == 0 && P.expire_first_wait)
+                               ? false  // test hook: treated as expired
+                               : ptx::mbar_wait(b_slot(slot), (gq / kRing) & 1, kWaitLimit));
+                    if (!cok) atomicOr(sLate, 2);
                 }
-                named_barrier(1, kConvWarps * 32);
-                if (*sLate & 2) break;  // the chunk did not land: stop converting
+                // (the verdict travels with the barrier: a flag read after it could already
+                // hold thread 0's verdict on the next chunk)
+                if (!named_barrier_and(1, kConvWarps * 32, cok)) break;  // stop converting
                 const float *cp = reinterpret_cast<const float *>(sH + slot * kChunkBytesD);
                 float x[kChunkRowsD];
 #pragma unroll
@@ -629,10 +635,12 @@ __global__ void __launch_bounds__(kThreadsD, 2)
         // node i = t / kTpn takes pieces kPpt * sub .. of a group's 64 channels
         const int i = t / kTpn, sub = t % kTpn;
         for (int it = 0; it < nu; ++it) {
-            if (t == 0 && !(!late_now() && ptx::mbar_wait(b_tree(it), ph(it), kWaitLimit)))
-                atomicOr(sLate, 4);
-            named_barrier(2, kFT);
-            if (*sLate & 4) break;
+            bool tok = true;
+            if (t == 0) {
+                tok = !late_now() && ptx::mbar_wait(b_tree(it), ph(it), kWaitLimit);
+                if (!tok) atomicOr(sLate, 4);
+            }
+            if (!named_barrier_and(2, kFT, tok)) break;
             int *mt = meta(it);
             bool go = mt[kMRun] != 0;
             const int n = mt[kMN], off = mt[kMOff];
@@ -643,10 +651,12 @@ __global__ void __launch_bounds__(kThreadsD, 2)
             float gmax = 0.f;  // largest |G| seen: the factor range check
             for (int kg = 0; kg < ng && go; ++kg) {
                 uint8_t *fb = sF + kg * kBlock;
-                if (t == 0 && !(!late_now() && ptx::mbar_wait(b_fin(it, kg), ph(it), kWaitLimit)))
-                    atomicOr(sLate, 4);  // another role gave up, or the columns did not land
-                named_barrier(2, kFT);
-                if (*sLate & 4) {
+                bool fok = true;
+                if (t == 0) {
+                    fok = !late_now() && ptx::mbar_wait(b_fin(it, kg), ph(it), kWaitLimit);
+                    if (!fok) atomicOr(sLate, 4);  // another role gave up, or the columns did not land
+                }
+                if (!named_barrier_and(2, kFT, fok)) {
                     if (lane == 0) {  // release the product thread
                         ptx::mbar_arrive(b_facq(it, kg));
                         ptx::mbar_arrive(b_fac(it, kg));
@@ -716,10 +726,12 @@ __global__ void __launch_bounds__(kThreadsD, 2)
             if (!(gmax <= kGLimit)) atomicOr(&mt[kMWalk], 1);
 
             // ---- weights, once the unit's context and score products are done
-            if (t == 0 && !(!late_now() && ptx::mbar_wait(b_sfull(it), ph(it), kWaitLimit)))
-                atomicOr(sLate, 4);
-            named_barrier(2, kFT);
-            go = go && !(*sLate & 4);
+            bool sok = true;
+            if (t == 0) {
+                sok = !late_now() && ptx::mbar_wait(b_sfull(it), ph(it), kWaitLimit);
+                if (!sok) atomicOr(sLate, 4);
+            }
+            go = named_barrier_and(2, kFT, sok) && go;
             const bool walk = go && mt[kMWalk] != 0;
             uint8_t *wS = sF + (ng - 1) * kBlock;  // the last factor block is free now
             // fp32 weights of the walk after the weight tiles

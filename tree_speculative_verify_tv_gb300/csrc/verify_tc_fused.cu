@@ -199,9 +199,14 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
         float alpha = 1.f;
         bool run_chunks = true;
         if constexpr (PEND) {
-            if (tid == 0 && !ptx::mbar_wait(b_pend, 0, kWaitLimit)) atomicOr(sLate, 1);
-            named_barrier(1, 128);
-            run_chunks = *sLate == 0;
+            bool ok = true;
+            if (tid == 0) {
+                ok = *reinterpret_cast<volatile int *>(sLate) == 0 &&
+                     ptx::mbar_wait(b_pend, 0, kWaitLimit);
+                if (!ok) atomicOr(sLate, 1);
+            }
+            // the verdict of thread 0, handed to the four warps by the barrier itself
+            run_chunks = named_barrier_and(1, 128, ok);
             pL = meta[kMetaPL];
             alpha = __int_as_float(meta[kMetaAlpha]);
         }
@@ -209,14 +214,14 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
         const float *pvv = reinterpret_cast<const float *>(smem + L.pvv_off);
         int c = 0;
         for (; c < nch && run_chunks; ++c) {
+            bool ok = true;
             if (tid == 0) {
-                const bool ok = (c == 0 && P.expire_first_wait)
-                                    ? false  // test hook: treated as expired
-                                    : ptx::mbar_wait(b_chunk(c), 0, kWaitLimit);
+                ok = (c == 0 && P.expire_first_wait)
+                         ? false  // test hook: treated as expired
+                         : ptx::mbar_wait(b_chunk(c), 0, kWaitLimit);
                 if (!ok) atomicOr(sLate, 2);
             }
-            named_barrier(1, 128);
-            if (*sLate & 2) break;  // the chunk did not land: stop converting
+            if (!named_barrier_and(1, 128, ok)) break;  // the chunk did not land: stop converting
             if constexpr (kStateTmem) {
                 // thread = tensor-memory lane: value channel 32 (warp & 1) + lane, the hi part
                 // (warps 0-1) or the lo part (warps 2-3) of its R key rows, packed in pairs
