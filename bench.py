@@ -62,7 +62,9 @@ TRAFFIC_SOURCES = {
     "tree_attention": [_CS + f for f in ("tree_attention.cu", "tc_common.cuh", "tc_ptx.cuh",
                                          "tv_internal.cuh")],
 }
-KERNEL_NAMES = {1: "simt", 2: "tcgen05 one unit per CTA", 3: "tcgen05, all products on tensor cores",
+KERNEL_NAMES = {1: "simt", 2: "tcgen05 one unit per CTA",
+                3: "tcgen05 fused (decay in the factors; up to 256-node per-channel trees: "
+                   "context on tensor cores, tree term by fp32 walks)",
                 4: "tcgen05 large trees (staged or node tiles)"}
 
 
@@ -455,7 +457,7 @@ H0_STD = {1: 0.1, 2: 0.05, 3: 0.05, 4: 0.05, 5: 0.05}
 CONFIG_KERNEL_SOURCES = {
     3: [_CS + f for f in ("verify_tc_fdiag.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
     4: [_CS + f for f in ("verify_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
-    5: [_CS + f for f in ("verify_tc_big.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
+    5: [_CS + f for f in ("verify_tc_fwalk.cu", "tc_common.cuh", "tc_ptx.cuh", "tv_internal.cuh")],
 }
 
 

@@ -84,15 +84,20 @@ typedef enum tv_variant {
     TV_VARIANT_TC = 2,      /* tcgen05 tensor-core kernel, one (request, head) per CTA:
                                bf16 q/k/v, dk in {64,128}, dv in {64,128};
                                TV_ERR_UNSUPPORTED otherwise */
-    TV_VARIANT_TC_FUSED = 3, /* tcgen05 kernels with the context term, the pair scores and
-                               the tree term all on tensor cores, one (request, head) per
-                               CTA, bf16 q/k/v: scalar decay with dk and dv in {64,128}
-                               and max_nodes <= 32, or per-channel decay with dk in
-                               {64,128}, dv = 128 and max_nodes <= 64 (the decay folded
-                               into the factors, e^{G} q and e^{-G} k, where every path
-                               sum |G| <= 69; a unit outside that range takes its pair
-                               weights from a walk of its paths); TV_ERR_UNSUPPORTED
-                               otherwise.  What TV_VARIANT_AUTO picks where it applies */
+    TV_VARIANT_TC_FUSED = 3, /* tcgen05 kernels with the decay folded into the factors,
+                               one kernel for a unit's whole path, bf16 q/k/v: scalar
+                               decay with dk and dv in {64,128} and max_nodes <= 32 (the
+                               context term, the pair scores and the tree term all on
+                               tensor cores); per-channel decay with dk in {64,128} and
+                               dv = 128: max_nodes <= 64 with all three on tensor cores,
+                               or max_nodes <= 256 and max_depth <= 16 with the context
+                               term on tensor cores and the pair weights and tree term
+                               by fp32 walks of the root paths.  Per-channel factors are
+                               e^{G} q and e^{-G} k where every path sum |G| <= 69; a
+                               unit outside that range takes its pair weights from a
+                               walk with the decays as running products.
+                               TV_ERR_UNSUPPORTED otherwise.  What TV_VARIANT_AUTO picks
+                               where it applies */
     TV_VARIANT_TC_TILED = 4  /* tcgen05 kernels for large trees, one (request, head) per
                                CTA: bf16 q/k/v, dk = dv = 128, trees up to TV_MAX_NODES.
                                Where a request's k, decay and v rows fit shared memory
@@ -105,7 +110,8 @@ typedef enum tv_variant {
 /*
  * Test hook, OR-ed into tv_verify_ex's `variant` together with TV_VARIANT_TC_FUSED
  * (TV_ERR_UNSUPPORTED with any other variant): the kernel treats its first wait for
- * a state chunk as expired, so the call takes the library's timeout path -- it
+ * an input copy (a state chunk, or the large-tree kernel's first group of rows) as
+ * expired, so the call takes the library's timeout path -- it
  * writes TV_ERR_TIMEOUT to dev_status, waits for its copies and products in flight,
  * frees its tensor memory and returns.  The outputs are then undefined.  For tests
  * of that failure path; never needed otherwise.

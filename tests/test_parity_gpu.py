@@ -117,14 +117,14 @@ def _auto_variant(batch):
 
 def test_automatic_kernel_choice():
     """TV_VARIANT_AUTO: the fused kernels for scalar-decay trees of <= 32 nodes and
-    per-channel trees of <= 64 nodes at dv = 128, the one-unit kernel for larger
-    scalar-decay trees and other small per-channel trees, the staged large-tree
-    kernel for trees too large for those."""
+    per-channel trees at dv = 128 of <= 64 nodes or of <= 256 nodes and depth 16, the
+    one-unit kernel for larger scalar-decay trees and other small per-channel trees,
+    the staged large-tree kernel for trees too large for those."""
     import tree_speculative_verify_tv_gb300 as tv
     assert _auto_variant(workloads.make_config(2)) == tv.TV_VARIANT_TC_FUSED
     assert _auto_variant(workloads.make_config(3)) == tv.TV_VARIANT_TC_FUSED
     assert _auto_variant(workloads.make_config(4)) == tv.TV_VARIANT_TC
-    assert _auto_variant(workloads.config5(B=2, layers=1, heads=2)) == tv.TV_VARIANT_TC_TILED
+    assert _auto_variant(workloads.config5(B=2, layers=1, heads=2)) == tv.TV_VARIANT_TC_FUSED
     small = workloads.random_batch(np.random.default_rng(50), [32, 20], 2, 128, 128, decay="diag",
                                    qkv_dtype="bf16", depth_cap=8, max_depth=8, max_nodes=32)
     assert _auto_variant(small) == tv.TV_VARIANT_TC_FUSED

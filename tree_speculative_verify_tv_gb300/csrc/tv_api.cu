@@ -16,6 +16,10 @@ bool verify_tc_staged_preferred(const VerifyArgs &a);
 // trees of up to 64 nodes)
 bool verify_tc_fdiag_supported(const VerifyArgs &a);
 cudaError_t launch_verify_tc_fdiag(const VerifyArgs &a, cudaStream_t s, bool expire_first_wait);
+// verify_tc_fwalk.cu: its member for larger per-channel-decay trees (dv = 128, up to
+// 256 nodes, depth <= 16): context product on tensor cores, tree term by fp32 walks
+bool verify_tc_fwalk_supported(const VerifyArgs &a);
+cudaError_t launch_verify_tc_fwalk(const VerifyArgs &a, cudaStream_t s, bool expire_first_wait);
 }  // namespace tv
 
 namespace {
@@ -49,13 +53,14 @@ tv_status check_ptrs(std::initializer_list<const void *> ptrs) {
 // TV_VARIANT_TC_FUSED: all products of a unit on tensor cores; scalar decay (trees of
 // up to 32 nodes) or per-channel decay (dv = 128, trees of up to 64 nodes).
 bool fused_supported(const tv::VerifyArgs &a) {
-    return a.decay == TV_DECAY_DIAG ? tv::verify_tc_fdiag_supported(a)
-                                    : tv::verify_tc_fused_supported(a);
+    if (a.decay != TV_DECAY_DIAG) return tv::verify_tc_fused_supported(a);
+    return tv::verify_tc_fdiag_supported(a) || tv::verify_tc_fwalk_supported(a);
 }
 
 cudaError_t launch_fused(const tv::VerifyArgs &a, cudaStream_t s, bool expire) {
-    return a.decay == TV_DECAY_DIAG ? tv::launch_verify_tc_fdiag(a, s, expire)
-                                    : tv::launch_verify_tc_fused(a, s, expire);
+    if (a.decay != TV_DECAY_DIAG) return tv::launch_verify_tc_fused(a, s, expire);
+    return tv::verify_tc_fdiag_supported(a) ? tv::launch_verify_tc_fdiag(a, s, expire)
+                                            : tv::launch_verify_tc_fwalk(a, s, expire);
 }
 
 // The kernel TV_VARIANT_AUTO picks: the fused tensor-core kernels where they apply,

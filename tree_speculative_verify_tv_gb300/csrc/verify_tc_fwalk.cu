@@ -1,0 +1,774 @@
+// verify_tc_fwalk.cu -- per-channel-decay tree verification for trees of up to 256
+// nodes and depth 16, dv = 128: the context product on tcgen05 tensor cores, the tree
+// term by fp32 walks over each node's root path.
+//
+// Tree closed form (Bole summary page, "Core techniques" §1), per-channel decay:
+//   o_i = H0^T (e^{G_i} * q_i) + sum_{j in anc*(i)} w_ij v_j,
+//   w_ij = sum_c q_ic k_jc e^{G_ic - G_jc}
+// with anc*(i) the root path of node i including i and G_i the sum of g over it.  With
+// the scaled factors q~_i = e^{G_i} * q_i and k~_j = e^{-G_j} * k_j the pair decay
+// factors out, w_ij = q~_i . k~_j.
+//
+// Why walks.  A root path holds at most 16 nodes, so of a 256-node tree's 256 x 256
+// pair weights at most 16 per row are used (about 5 in the best-first trees of a
+// large draft budget).  Each weight is then a 128-term fp32 dot product formed on the
+// CUDA cores, and the tree term sum_j w_ij v_j a 16-term fp32 sum per output: no
+// dense score tiles, no bf16 split of the weights, and errors at fp32 rounding.  The
+// context term H0^T q~ is dense (256 x 128 x 128 per unit) and runs on the tensor
+// cores: D[i, c] = sum_k q~[i, k] H0[k, c] with A = q~ (node rows, K-major) and B = the
+// state rows (MN-major), both split into bf16 hi + lo parts, passes hi.hi, hi.lo and
+// lo.hi, fp32 accumulation in tensor memory (two 128-row tiles of 128 columns).
+//
+// Rows.  Each unit's nodes are taken in depth order (row r = the r-th node by depth,
+// then index), so the 32 threads of a warp walk paths of one length.  Two threads own
+// a row, one in warps 0-7 and one in warps 8-15, each taking half of every channel
+// group: its node's path sums and factors over those channels and partial weights (16
+// registers, one per path slot, summed with the other half's once per unit); at the
+// end each forms half of its node's output row (value channels 0-63 or 64-127), read
+// from the row's tensor-memory lane.
+//
+// Copies.  Key channels are taken in groups of 16.  A group's g (fp32 rows of 64 B,
+// 64-byte swizzled), q and k (32 B a row) and 16 state rows arrive by tensor copies into
+// one of three 40 KB staging buffers; after a unit's groups its v arrives the same way
+// (channels 0-63 and 64-127, 128-byte swizzled) in the next two buffers.  The buffers
+// are taken in strict rotation -- a unit's groups, then its two v halves, then the next
+// unit's groups -- so each copy is requested two buffer-uses ahead of its reader and
+// the next unit's first group lands while this unit's outputs are formed.  Per group
+// each thread forms its node's path sums from the staged g rows of its root path, its
+// factors from its own staged q and k columns, writes k~ (fp32 rows, read by the walks
+// of the node's descendants) and the bf16 hi / lo operands of the context product to
+// the products buffer, and after one barrier adds q~_i . k~_j over its path to its
+// weights.  The outputs go out 16 channels at a time through 2 KB of scratch per warp
+// in the products buffer, so that a warp stores whole 64-byte row pieces.  About 171 KB
+// of shared memory: one CTA of 608 threads per SM.
+//
+// Range.  While every |G_ic| <= 69 the scaled factors are finite and normal.  A unit
+// whose path sums leave that range anywhere takes its weights from a second walk with
+// the pair decays as running products of e^{g} along the path; its context product
+// keeps q~, which then underflows only where e^{G_ic} is below fp32's range.
+//
+// Persistent CTAs take every grid-th (request, head) unit.  Roles (608 threads):
+//   warps 0-15  half a tree row each: factors, walks, the unit's outputs
+//   warp 16     tree checks, root-path lists (node indices as bytes) and the depth
+//               order, up to two units ahead (two copies of the tree arrays)
+//   warp 17     tensor memory; one thread issues the context products
+//   warp 18     copies (one thread)
+// Every wait is bounded (TV_ERR_TIMEOUT); copies and products in flight are waited for
+// (bounded) before tensor memory is freed.  Malformed trees zero their rows and set
+// TV_ERR_TREE.
+#include "tc_common.cuh"
+
+namespace tv {
+namespace {
+using namespace tcc;
+
+constexpr int kFacWarpsW = 16;              // warps 0-15: half a tree row per thread
+constexpr int kTreeWarpW = kFacWarpsW;      // warp 8
+constexpr int kMmaWarpW = kFacWarpsW + 1;   // warp 9
+constexpr int kLoadWarpW = kFacWarpsW + 2;  // warp 10
+constexpr int kThreadsW = (kLoadWarpW + 1) * 32;
+constexpr int kFacThreads = kFacWarpsW * 32;  // 512
+constexpr int kRowsW = 256;                   // nodes per tree at most
+constexpr int kSlots = 16;                    // root-path length at most
+constexpr int kDvW = 128;
+constexpr int kGrp = 16;                      // key channels per group
+constexpr int kBoxRows = 32;                  // node rows per copy box
+constexpr int kTmemColsW = 256;               // D: two 128-row tiles x 128 value channels
+constexpr float kLog2eW = 1.4426950408889634f;
+constexpr float kGLimitW = 69.f;
+static_assert(kFacThreads == 2 * kRowsW, "two factor threads per tree row");
+static_assert(kThreadsW == 608, "roles: 16 row warps, tree, product and copy warps");
+
+// staging: three buffers taken in rotation; a group's copies, or half of v
+constexpr int kStages = 3;
+constexpr uint32_t kStageBytes = 40960;
+constexpr uint32_t kSg = 0;        // g: 256 rows x 64 B (16 fp32), chunk x of row j at x ^ ((j / 2) % 4)
+constexpr uint32_t kSq = 16384;    // q: 256 rows x 32 B
+constexpr uint32_t kSk = 24576;    // k: 256 rows x 32 B
+constexpr uint32_t kSh = 32768;    // the group's 16 state rows, 16 x 512 B
+// (v: 256 rows x 128 B of 64 channels, chunk x of row j at x ^ (j % 8))
+// products buffer: a group's k~ rows and context-product operands; after the unit's
+// products, the two halves' partial weights (2 x 256 rows x 64 B), then the output
+// scratch (2 KB per warp)
+constexpr uint32_t kPk = 0;        // k~: 256 rows x 64 B fp32, chunks as g's
+constexpr uint32_t kPqh = 16384;   // q~ hi: two 128-row tiles (K-major, no swizzle)
+constexpr uint32_t kPql = 24576;   // q~ lo
+constexpr uint32_t kPhh = 32768;   // state hi: two 64-channel slabs of 16 rows, MN-major
+constexpr uint32_t kPhl = 36864;   // state lo
+constexpr uint32_t kProdBytes = 40960;
+constexpr uint32_t kQTile = 4096;  // one 128-row tile of q~ hi or lo
+constexpr uint32_t kHSlab = 2048;  // one 64-channel slab of the state rows
+
+// Barriers.  The tree arrays come in two copies (units of even and odd index), so a
+// tree barrier's phase is unit / 2; a staging buffer takes every third use, so its
+// barriers' phase is use / 3; the product barriers alternate strictly between the row
+// threads and the product thread, so their phase is the running group count.
+enum {
+    kWTree = 0,            // [2]: tree arrays of the unit ready
+    kWTfree = 2,           // [2]: tree arrays read (row threads, products, copies: 3)
+    kWStage = 4,           // [3]: a staging use landed
+    kWStageFree = 7,       // [3]: a staging use read
+    kWProd = 10,           // a group's operands written
+    kWProdDone = 11,       // a group's products done
+    kWNumBars = 12
+};
+
+enum { kWN = 0, kWOff, kWRun, kWZero, kWTiles, kWOut, kWMeta = 8 };
+
+// Shared-memory plan, identical on host and device.
+struct WalkLayout {
+    uint32_t s_off, p_off, tree_off, tree_bytes, meta_off, bar_off, misc_off, total;
+    __host__ __device__ WalkLayout() {
+        s_off = 0;
+        p_off = s_off + kStages * kStageBytes;
+        tree_off = p_off + kProdBytes;
+        tree_bytes = kRowsW * 16 + kRowsW + kRowsW + kRowsW * 2;  // paths, order, depths, parents
+        meta_off = tree_off + 2 * tree_bytes;
+        bar_off = align_up(meta_off + 2 * kWMeta * 4, 16);
+        misc_off = bar_off + kWNumBars * 8;
+        total = misc_off + 16 + 2 * 32 * 4 + 1024;  // tmem address, flags, depth counts; alignment
+    }
+};
+
+struct WalkParams {
+    VerifyArgs a;
+    int expire_first_wait;  // test hook: the row threads' first wait for a copy gives up at once
+};
+
+__device__ __forceinline__ float ex2w(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// node index in path slot s (0 = the node itself) of a packed 16-byte path list
+__device__ __forceinline__ int path_node(const uint4 &p, int s) {
+    const uint32_t w = s < 4 ? p.x : s < 8 ? p.y : s < 12 ? p.z : p.w;
+    return static_cast<int>((w >> (8 * (s & 3))) & 0xFFu);
+}
+
+// byte offset of 16-byte chunk x of a 64-byte row j: chunks permuted by row pair (the
+// tensor copy's 64-byte swizzle), so eight rows j of distinct j % 8 fall on distinct banks
+__device__ __forceinline__ uint32_t row64(int j, int x) {
+    return static_cast<uint32_t>(j * 64 + ((x ^ ((j >> 1) & 3)) << 4));
+}
+
+__global__ void __launch_bounds__(kThreadsW, 1)
+    verify_tc_fwalk_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ CUtensorMap tm_g, const WalkParams P) {
+    const VerifyArgs &a = P.a;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int dk = a.dk, H = a.H, ng = dk / kGrp;
+    const int units = a.B * H, G = gridDim.x;
+    const int nu = (units - (int)blockIdx.x + G - 1) / G;  // units of this CTA
+    auto unit_of = [&](int it) { return (int)blockIdx.x + it * G; };
+    const WalkLayout L;
+    uint8_t *sS = smem + L.s_off;
+    uint8_t *sP = smem + L.p_off;
+    auto tree_base = [&](int it) { return smem + L.tree_off + (it & 1) * L.tree_bytes; };
+    auto sPath = [&](int it) { return reinterpret_cast<uint4 *>(tree_base(it)); };
+    auto sOrder = [&](int it) { return tree_base(it) + kRowsW * 16; };
+    auto sDep = [&](int it) { return tree_base(it) + kRowsW * 17; };
+    auto sPar = [&](int it) { return reinterpret_cast<int16_t *>(tree_base(it) + kRowsW * 18); };
+    auto meta = [&](int it) { return reinterpret_cast<int *>(smem + L.meta_off) + (it & 1) * kWMeta; };
+    uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + L.misc_off);
+    int *sLate = reinterpret_cast<int *>(smem + L.misc_off + 4);
+    int *sCnt = reinterpret_cast<int *>(smem + L.misc_off + 16);  // per depth: count, start
+    const uint32_t bar0 = ptx::smem_addr(smem + L.bar_off);
+    auto bar = [&](int idx) { return bar0 + 8u * idx; };
+    const uint32_t b_prod = bar(kWProd), b_pdone = bar(kWProdDone);
+    auto b_tree = [&](int it) { return bar(kWTree + (it & 1)); };
+    auto b_tfree = [&](int it) { return bar(kWTfree + (it & 1)); };
+    auto b_stage = [&](int use) { return bar(kWStage + use % kStages); };
+    auto b_sfree = [&](int use) { return bar(kWStageFree + use % kStages); };
+    auto ph = [](int it) { return static_cast<uint32_t>((it >> 1) & 1); };
+    auto par = [](int use) { return static_cast<uint32_t>(use & 1); };
+    auto uph = [](int use) { return static_cast<uint32_t>((use / kStages) & 1); };
+    auto stage = [&](int use) { return sS + (use % kStages) * kStageBytes; };
+    const uint32_t pA = ptx::smem_addr(sP);
+    auto late_now = [&]() { return *reinterpret_cast<volatile int *>(sLate) != 0; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- prologue that touches no input: barriers, tensor memory
+    if (tid == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+        ptx::prefetch_tensormap(&tm_g);
+        for (int p = 0; p < 2; ++p) {
+            ptx::mbar_init(bar(kWTree + p), 1);
+            ptx::mbar_init(bar(kWTfree + p), 3);
+        }
+        for (int b = 0; b < kStages; ++b) {
+            ptx::mbar_init(bar(kWStage + b), 1);
+            ptx::mbar_init(bar(kWStageFree + b), 1);
+        }
+        ptx::mbar_init(b_prod, 1);
+        ptx::mbar_init(b_pdone, 1);
+        ptx::fence_mbar_init();
+        *sLate = 0;
+    }
+    if (warp == kMmaWarpW) {
+        ptx::tmem_alloc(ptx::smem_addr(sTmem), kTmemColsW);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tD = *sTmem;  // lane = row of a 128-row tile, column = tile * 128 + channel
+
+    ptx::grid_dependency_wait();  // inputs may be written by the previous kernel
+    if (tid == 0) ptx::grid_launch_dependents();
+
+    if (warp == kTreeWarpW) {
+        // ================= trees: checks, root-path lists, depth order
+        for (int it = 0; it < nu; ++it) {
+            bool ok = true;
+            if (it >= 2 && lane == 0)
+                ok = !late_now() && ptx::mbar_wait(b_tfree(it - 2), ph(it - 2), kWaitLimit);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) {
+                if (lane == 0) atomicOr(sLate, 32);
+                break;
+            }
+            const int u = unit_of(it), b = u / H, h = u % H;
+            int off = 0, n = 0;
+            const bool range_ok = request_range(a.node_offsets, b, a.T, a.max_nodes, off, n);
+            if (!range_ok) n = 0;
+            uint4 *path_s = sPath(it);
+            uint8_t *ord_s = sOrder(it), *dep_s = sDep(it);
+            int16_t *par_s = sPar(it);
+            int *mt = meta(it);
+            bool bad = false;
+            int pr[8], dp[8];
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int i = lane + 32 * s;
+                pr[s] = -1;
+                dp[s] = 0;
+                if (i < n) {
+                    pr[s] = a.parent[off + i];
+                    dp[s] = a.depth[off + i];
+                    const bool bi = pr[s] < -1 || pr[s] >= i || dp[s] < 1 || dp[s] > a.max_depth;
+                    bad = bad || bi;
+                    if (bi) pr[s] = -1;  // keeps the lookups below inside the tree
+                    par_s[i] = static_cast<int16_t>(pr[s]);
+                    dep_s[i] = static_cast<uint8_t>(bi ? 0 : dp[s]);
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int i = lane + 32 * s;
+                if (i < n) {
+                    const int want = pr[s] < 0 ? 1 : dep_s[pr[s]] + 1;
+                    bad = bad || dp[s] != want;
+                }
+            }
+            const bool tree_bad = __any_sync(0xffffffffu, bad);
+            const bool run = n > 0 && !tree_bad;
+            if (run) {
+                // root-path lists: the node, its parent, ... up to its root (depth entries)
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s) {
+                    const int i = lane + 32 * s;
+                    if (i < n) {
+                        uint32_t w4[4] = {0u, 0u, 0u, 0u};
+                        int j = i;
+#pragma unroll
+                        for (int sl = 0; sl < kSlots; ++sl) {
+                            if (j >= 0) {
+                                w4[sl >> 2] |= static_cast<uint32_t>(j) << (8 * (sl & 3));
+                                j = par_s[j];
+                            }
+                        }
+                        path_s[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+                // depth order: rank within a depth by node index, then per-depth starts
+                if (lane <= kSlots) sCnt[lane] = 0;
+                __syncwarp();
+                int rk[8];
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const int i = lane + 32 * s;
+                    const int d = i < n ? dp[s] : 0;
+                    const uint32_t m = __match_any_sync(0xffffffffu, d);
+                    const int base = d > 0 ? sCnt[d] : 0;
+                    rk[s] = base + __popc(m & ((1u << lane) - 1u));
+                    __syncwarp();
+                    if (d > 0 && lane == __ffs(m) - 1) sCnt[d] = base + __popc(m);
+                    __syncwarp();
+                }
+                const int cnt = (lane >= 1 && lane <= kSlots) ? sCnt[lane] : 0;
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                __syncwarp();
+                if (lane <= kSlots) sCnt[32 + lane] = incl - cnt;
+                __syncwarp();
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const int i = lane + 32 * s;
+                    if (i < n) ord_s[sCnt[32 + dp[s]] + rk[s]] = static_cast<uint8_t>(i);
+                }
+            }
+            if (lane == 0) {
+                if (!range_ok && h == 0) report(a.status, TV_ERR_TREE);
+                if (n > 0 && tree_bad && h == 0) report(a.status, TV_ERR_TREE);
+                mt[kWN] = n;
+                mt[kWOff] = off;
+                mt[kWRun] = run ? 1 : 0;
+                mt[kWZero] = (n > 0 && tree_bad) ? 1 : 0;
+                mt[kWTiles] = (n + 127) / 128;
+                mt[kWOut] = 0;
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(b_tree(it));
+        }
+    } else if (warp == kLoadWarpW) {
+        if (lane == 0) {
+            // ================= copies (one thread): staging uses in rotation -- a unit's
+            // groups, then its two v halves; each use waits for the use three before it
+            int U = 0;  // staging uses issued
+            bool ok = true;
+            auto wait_ok = [&](uint32_t b, uint32_t parity) {
+                if (late_now()) return false;
+                if (!ptx::mbar_wait(b, parity, kWaitLimit)) atomicOr(sLate, 64);
+                return !late_now();
+            };
+            auto take = [&]() {  // the buffer of use U is free
+                return U < kStages || wait_ok(b_sfree(U - kStages), uph(U - kStages));
+            };
+            for (int it = 0; it < nu && ok; ++it) {
+                if (!wait_ok(b_tree(it), ph(it))) break;
+                const int *mt = meta(it);
+                const int n = mt[kWN], off = mt[kWOff], run = mt[kWRun];
+                ptx::mbar_arrive(b_tfree(it));
+                if (!run) continue;
+                const int u = unit_of(it), h = u % H;
+                const int rows = (n + kBoxRows - 1) / kBoxRows * kBoxRows;
+                for (int g = 0; g < ng + 2 && ok; ++g, ++U) {
+                    if (!take()) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = ptx::smem_addr(stage(U));
+                    if (g < ng) {
+                        ptx::mbar_arrive_expect_tx(b_stage(U), rows * (64 + 32 + 32) + kGrp * kDvW * 4);
+                        for (int r = 0; r < rows; r += kBoxRows) {
+                            ptx::tma_load_3d(dst + kSg + r * 64, &tm_g, g * kGrp, h, off + r, b_stage(U));
+                            ptx::tma_load_3d(dst + kSq + r * 32, &tm_q, g * kGrp, h, off + r, b_stage(U));
+                            ptx::tma_load_3d(dst + kSk + r * 32, &tm_k, g * kGrp, h, off + r, b_stage(U));
+                        }
+                        ptx::bulk_g2s(dst + kSh, a.H0 + ((size_t)u * dk + g * kGrp) * kDvW,
+                                      kGrp * kDvW * 4, b_stage(U));
+                    } else {  // v channels 0-63, then 64-127
+                        ptx::mbar_arrive_expect_tx(b_stage(U), rows * 128);
+                        for (int r = 0; r < rows; r += kBoxRows)
+                            ptx::tma_load_3d(dst + r * 128, &tm_v, (g - ng) * 64, h, off + r, b_stage(U));
+                    }
+                }
+            }
+            // every copy requested lands before the CTA's memory can go away (a buffer's
+            // uses are issued one at a time, so only the last of each can be pending)
+            bool drained = true;
+            for (int k = 1; k <= kStages && k <= U; ++k)
+                drained = ptx::mbar_wait(b_stage(U - k), uph(U - k), kWaitLimit) && drained;
+            if (!drained) atomicOr(sLate, 128);
+        }
+    } else if (warp == kMmaWarpW) {
+        if (lane == 0) {
+            // ================= context products (one thread)
+            int pu = 0;
+            auto wait_ok = [&](uint32_t b, uint32_t parity) {
+                if (late_now()) return false;
+                if (!ptx::mbar_wait(b, parity, kWaitLimit)) atomicOr(sLate, 16);
+                return !late_now();
+            };
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32_bmn(128, 128);
+            const uint64_t bh = ptx::desc_mnmajor_sw128(pA + kPhh, kHSlab, 1024);
+            const uint64_t bl = ptx::desc_mnmajor_sw128(pA + kPhl, kHSlab, 1024);
+            bool ok = true;
+            for (int it = 0; it < nu && ok; ++it) {
+                if (!wait_ok(b_tree(it), ph(it))) break;
+                const int *mt = meta(it);
+                const int run = mt[kWRun], tiles = mt[kWTiles];
+                ptx::mbar_arrive(b_tfree(it));
+                if (!run) continue;
+                for (int g = 0; g < ng; ++g) {
+                    if (!wait_ok(b_prod, par(pu))) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    for (int t = 0; t < tiles; ++t) {
+                        const uint32_t d = tD + t * 128;
+                        const uint64_t ah = ptx::desc_kmajor_noswizzle(pA + kPqh + t * kQTile, 128, 256);
+                        const uint64_t al = ptx::desc_kmajor_noswizzle(pA + kPql + t * kQTile, 128, 256);
+                        ptx::mma_bf16(d, ah, bh, idesc, g > 0 ? 1u : 0u);
+                        ptx::mma_bf16(d, ah, bl, idesc, 1u);
+                        ptx::mma_bf16(d, al, bh, idesc, 1u);
+                    }
+                    ptx::mma_commit(b_pdone);
+                    ++pu;
+                }
+            }
+            // the products complete before tensor memory is freed
+            if (pu > 0 && !ptx::mbar_wait(b_pdone, par(pu - 1), kWaitLimit)) atomicOr(sLate, 128);
+        }
+    } else {
+        // ================= tree rows (warps 0-15): row r = (warp % 8) * 32 + lane of the
+        // depth order; half hf = warp / 8 takes 8 of every group's 16 key channels (16-byte
+        // chunks 2 hf, 2 hf + 1 of a 64-byte g or k~ row) and value channels 64 hf ..
+        const int ft = tid;                         // 0 .. 511
+        // groups: row r = ft / 2, half hf = ft % 2 (the two halves of a row in adjacent
+        // lanes, so that a warp's 16-byte loads of ancestor rows touch 4 rows, 2 chunks
+        // each, per 8 lanes); outputs: row re = (warp % 8) * 32 + lane (its tensor-memory
+        // lane), value-channel half he = warp / 8
+        const int hf = ft & 1, r = ft >> 1;
+        const int he = warp >> 3, re = (warp & 7) * 32 + lane;
+        const int qd = warp & 3, tile = (warp >> 2) & 1;  // tensor-memory lane quadrant, D tile
+        const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(a.q);
+        const __nv_bfloat16 *kgl = static_cast<const __nv_bfloat16 *>(a.k);
+        int pu = 0, U = 0;  // groups handed to the product thread, staging uses read
+        bool first = true;
+        // thread 0 waits (for b, then b2, where given); the barrier hands its verdict to all
+        // 512 threads at once (a flag read after the barrier could already carry the
+        // verdict of thread 0's next wait)
+        auto sync_wait = [&](uint32_t b, uint32_t parity, bool expire, uint32_t b2 = 0u,
+                             uint32_t parity2 = 0u) {
+            bool ok = true;
+            if (ft == 0) {
+                ok = !late_now() && !expire && (b == 0u || ptx::mbar_wait(b, parity, kWaitLimit));
+                if (ok && b2 != 0u) ok = ptx::mbar_wait(b2, parity2, kWaitLimit);
+                if (!ok) atomicOr(sLate, 4);
+            }
+            return named_barrier_and(1, kFacThreads, ok);
+        };
+        for (int it = 0; it < nu; ++it) {
+            if (!sync_wait(b_tree(it), ph(it), false)) break;
+            int *mt = meta(it);
+            const int n = mt[kWN], off = mt[kWOff], run = mt[kWRun];
+            const int u = unit_of(it), h = u % H;
+            if (!run) {
+                if (mt[kWZero] && r < n) {
+                    float4 *o = reinterpret_cast<float4 *>(a.out + ((size_t)(off + r) * H + h) * kDvW + 64 * hf);
+#pragma unroll 4
+                    for (int x = 0; x < 16; ++x) o[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                named_barrier(1, kFacThreads);
+                if (ft == 0) ptx::mbar_arrive(b_tfree(it));
+                continue;
+            }
+            const bool active = r < n;
+            const int i = active ? sOrder(it)[r] : 0;
+            const int d = active ? sDep(it)[i] : 0;
+            const uint4 path = active ? sPath(it)[i] : make_uint4(0u, 0u, 0u, 0u);
+            float w[kSlots];
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) w[s] = 0.f;
+            float gmax = 0.f;
+            // path sums of this half's 8 channels of a group over the root path (staged g
+            // rows); run for group g + 1 together with group g's walk, so that the two
+            // shared-memory-bound loops overlap
+            auto path_sums = [&](const uint8_t *sb, float (&Gs)[8]) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) Gs[e] = 0.f;
+                if (!active) return;
+#pragma unroll
+                for (int s = 0; s < kSlots; ++s) {
+                    if (s < d) {
+                        const int j = path_node(path, s);
+#pragma unroll
+                        for (int x = 0; x < 2; ++x) {
+                            const float4 gv = *reinterpret_cast<const float4 *>(sb + kSg + row64(j, 2 * hf + x));
+                            Gs[4 * x] += gv.x; Gs[4 * x + 1] += gv.y;
+                            Gs[4 * x + 2] += gv.z; Gs[4 * x + 3] += gv.w;
+                        }
+                    }
+                }
+            };
+            // partial weights: w_s += this half of q~_i . k~_j (k~ rows of the group in the
+            // products buffer)
+            auto walk = [&](const float (&qt)[8]) {
+                if (!active) return;
+#pragma unroll
+                for (int s = 0; s < kSlots; ++s) {
+                    if (s < d) {
+                        const int j = path_node(path, s);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int x = 0; x < 2; ++x) {
+                            const float4 kv = *reinterpret_cast<const float4 *>(sP + kPk + row64(j, 2 * hf + x));
+                            acc = fmaf(qt[4 * x], kv.x, acc);
+                            acc = fmaf(qt[4 * x + 1], kv.y, acc);
+                            acc = fmaf(qt[4 * x + 2], kv.z, acc);
+                            acc = fmaf(qt[4 * x + 3], kv.w, acc);
+                        }
+                        w[s] += acc;
+                    }
+                }
+            };
+            float Gs[8], qt[8];
+            // the first group's copies have landed
+            bool go = sync_wait(b_stage(U), uph(U), first && P.expire_first_wait);
+            first = false;
+            if (go) path_sums(stage(U), Gs);
+            for (int g = 0; g < ng && go; ++g, ++U) {
+                // the previous group's walks are done (this barrier) and its products too:
+                // the products buffer is free
+                if (!sync_wait(pu > 0 ? b_pdone : 0u, pu > 0 ? par(pu - 1) : 0u, false)) {
+                    go = false;
+                    break;
+                }
+                const uint8_t *sb = stage(U);
+                if (active) {
+                    // own q and k columns (bf16, 16 bytes each), factors 4 channels at a time
+                    const uint4 qh = *reinterpret_cast<const uint4 *>(sb + kSq + i * 32 + 16 * hf);
+                    const uint4 kh = *reinterpret_cast<const uint4 *>(sb + kSk + i * 32 + 16 * hf);
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const uint32_t qa = x == 0 ? qh.x : qh.z, qb = x == 0 ? qh.y : qh.w;
+                        const uint32_t ka = x == 0 ? kh.x : kh.z, kb = x == 0 ? kh.y : kh.w;
+                        const float qv[4] = {bf16lo(qa), bf16hi(qa), bf16lo(qb), bf16hi(qb)};
+                        const float kv[4] = {bf16lo(ka), bf16hi(ka), bf16lo(kb), bf16hi(kb)};
+                        float kt[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float Gc = Gs[4 * x + e];
+                            gmax = fmaxf(gmax, fabsf(Gc));
+                            const float l2 = Gc * kLog2eW;
+                            qt[4 * x + e] = qv[e] * ex2w(l2);
+                            kt[e] = kv[e] * ex2w(-l2);
+                        }
+                        *reinterpret_cast<float4 *>(sP + kPk + row64(i, 2 * hf + x)) =
+                            make_float4(kt[0], kt[1], kt[2], kt[3]);
+                    }
+                    // q~ hi / lo: row r of tile r / 128, 8-row x 16-byte core matrices; this
+                    // half's 8 channels are the K-chunk hf
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) split_pair(qt[2 * m], qt[2 * m + 1], hi[m], lo[m]);
+                    const int rr = r & 127;
+                    const uint32_t qo = (r >> 7) * kQTile + (rr >> 3) * 256 + (rr & 7) * 16 + 128 * hf;
+                    *reinterpret_cast<uint4 *>(sP + kPqh + qo) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(sP + kPql + qo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qt[e] = 0.f;
+                }
+                {
+                    // the group's 16 state rows -> hi / lo, MN-major with 128-byte swizzle:
+                    // row k of slab c / 64 at k * 128, 16-byte chunk (c % 64) / 8 XOR k % 8;
+                    // thread ft takes 4 channels: row ft / 32, channels 4 (ft % 32) ..
+                    const int kr = ft >> 5, c4 = ft & 31;
+                    const float4 x0 = *reinterpret_cast<const float4 *>(sb + kSh + kr * 512 + c4 * 16);
+                    uint32_t hi[2], lo[2];
+                    split_pair(x0.x, x0.y, hi[0], lo[0]);
+                    split_pair(x0.z, x0.w, hi[1], lo[1]);
+                    const uint32_t ho = (c4 >> 4) * kHSlab + kr * 128 + ((((c4 & 15) >> 1) ^ (kr & 7)) << 4) + (c4 & 1) * 8;
+                    *reinterpret_cast<uint2 *>(sP + kPhh + ho) = make_uint2(hi[0], hi[1]);
+                    *reinterpret_cast<uint2 *>(sP + kPhl + ho) = make_uint2(lo[0], lo[1]);
+                }
+                ptx::fence_proxy_async_smem();
+                // staging read, operands and k~ rows written; the next group's copies have
+                // landed
+                const bool more = g + 1 < ng;
+                if (!sync_wait(more ? b_stage(U + 1) : 0u, more ? uph(U + 1) : 0u, false)) {
+                    go = false;
+                    break;
+                }
+                if (ft == 0) {
+                    ptx::mbar_arrive(b_prod);
+                    ptx::mbar_arrive(b_sfree(U));
+                }
+                ++pu;
+                // this group's walk and the next group's path sums
+                float qw[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qw[e] = qt[e];
+                if (more) path_sums(stage(U + 1), Gs);
+                walk(qw);
+            }
+            if (!go) break;
+            // path sums out of range anywhere in the unit: weights by the walk over global
+            // memory (pair decays as running products of e^{g} along the path; a cold path,
+            // kept compact; each half takes its own channels)
+            if (!(gmax <= kGLimitW)) atomicOr(&mt[kWOut], 1);
+            // every walk has read the k~ rows; D is full once the last group's products are
+            if (!sync_wait(b_pdone, par(pu - 1), false)) break;
+            if (mt[kWOut] != 0 && active) {
+                const size_t row_i = ((size_t)(off + i) * H + h) * dk;
+#pragma unroll
+                for (int s = 0; s < kSlots; ++s) w[s] = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < dk; ++c) {
+                    if (((c >> 3) & 1) != hf) continue;  // this half's 8 of each 16 channels
+                    const float qv = __bfloat162float(qg[row_i + c]);
+                    float fr = 1.f;
+#pragma unroll
+                    for (int s = 0; s < kSlots; ++s) {
+                        if (s < d) {
+                            const size_t rj = ((size_t)(off + path_node(path, s)) * H + h) * dk + c;
+                            w[s] += qv * __bfloat162float(kgl[rj]) * fr;
+                            fr *= expf(a.g[rj]);
+                        }
+                    }
+                }
+            }
+            // the two halves' partial weights meet in the products buffer (free now); the
+            // output thread of row re adds them, the low-channel half's first
+            {
+                float4 *mine = reinterpret_cast<float4 *>(sP + (hf * 256 + r) * 64);
+#pragma unroll
+                for (int x = 0; x < 4; ++x) mine[x] = make_float4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                named_barrier(1, kFacThreads);
+                const float4 *p0 = reinterpret_cast<const float4 *>(sP + re * 64);
+                const float4 *p1 = reinterpret_cast<const float4 *>(sP + (256 + re) * 64);
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const float4 lo4 = p0[x], hi4 = p1[x];
+                    w[4 * x] = lo4.x + hi4.x; w[4 * x + 1] = lo4.y + hi4.y;
+                    w[4 * x + 2] = lo4.z + hi4.z; w[4 * x + 3] = lo4.w + hi4.w;
+                }
+                named_barrier(1, kFacThreads);  // read before the scratch reuses the space
+            }
+            // the output row's node and root path
+            const bool eact = re < n;
+            const int ie = eact ? sOrder(it)[re] : 0;
+            const int de = eact ? sDep(it)[ie] : 0;
+            const uint4 pathe = eact ? sPath(it)[ie] : make_uint4(0u, 0u, 0u, 0u);
+            ptx::tc_fence_after_sync();
+            // outputs: D[re, 64 he + :] + sum_s w_s v_{path s}, 16 channels at a time from
+            // this half's v (staging use uv + hf).  Each piece goes through the warp's
+            // scratch in the products buffer (row = lane, 64 B, chunks permuted by row pair)
+            // and leaves as 64-byte row pieces, 8 rows per store instruction.
+            uint8_t *scr = sP + warp * 2048;
+            const int uv = U;  // v channels 0-63: use uv, 64-127: use uv + 1
+            if (!sync_wait(b_stage(uv), uph(uv), false, b_stage(uv + 1), uph(uv + 1))) break;
+            const uint8_t *vb = stage(uv + he);
+#pragma unroll 1
+            for (int m4 = 0; m4 < 4; ++m4) {
+                const int m = 4 * he + m4;   // 16-channel piece of the row
+                const int c0 = (2 * m) & 7;  // first 16-byte chunk of the piece in a v row
+                uint32_t dv[16];
+                ptx::tmem_ld_x16_nowait(tD + (static_cast<uint32_t>(32 * qd) << 16) + tile * 128 + 16 * m, dv);
+                ptx::tmem_wait_ld();
+                float acc[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[e] = __uint_as_float(dv[e]);
+                if (eact) {
+#pragma unroll
+                    for (int s = 0; s < kSlots; ++s) {
+                        if (s < de) {
+                            const int j = path_node(pathe, s);
+                            const float ws = w[s];
+#pragma unroll
+                            for (int x = 0; x < 2; ++x) {
+                                const uint4 raw = *reinterpret_cast<const uint4 *>(vb + j * 128 + (((c0 + x) ^ (j & 7)) << 4));
+                                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    acc[8 * x + 2 * e] = fmaf(ws, bf16lo(wv[e]), acc[8 * x + 2 * e]);
+                                    acc[8 * x + 2 * e + 1] = fmaf(ws, bf16hi(wv[e]), acc[8 * x + 2 * e + 1]);
+                                }
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    *reinterpret_cast<float4 *>(scr + row64(lane, x)) =
+                        make_float4(acc[4 * x], acc[4 * x + 1], acc[4 * x + 2], acc[4 * x + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = 8 * k + (lane >> 2), x = lane & 3;
+                    const float4 val = *reinterpret_cast<const float4 *>(scr + row64(row, x));
+                    const int node = __shfl_sync(0xffffffffu, ie, row);
+                    if (32 * (warp & 7) + row < n)
+                        *reinterpret_cast<float4 *>(a.out + ((size_t)(off + node) * H + h) * kDvW + 16 * m + 4 * x) = val;
+                }
+                __syncwarp();
+            }
+            ptx::tc_fence_before_sync();
+            named_barrier(1, kFacThreads);  // D, v, the scratch and the unit's tree arrays read
+            if (ft == 0) {
+                ptx::mbar_arrive(b_sfree(uv));
+                ptx::mbar_arrive(b_sfree(uv + 1));
+                ptx::mbar_arrive(b_tfree(it));
+            }
+            U += 2;
+        }
+    }
+
+    // ================= all roles done: report, free tensor memory
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (tid == 0 && *sLate) report(a.status, TV_ERR_TIMEOUT);
+    if (warp == kMmaWarpW) ptx::tmem_dealloc(tD, kTmemColsW);
+}
+
+// node rows of `width` elements per (node, head): dims (width, H, T), boxes of
+// `box_w` elements x one head x kBoxRows nodes
+bool encode_node_rows(CUtensorMap *tm, const void *base, CUtensorMapDataType dt, int esize, int width,
+                      int H, int T, int box_w, CUtensorMapSwizzle swz) {
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * esize, (cuuint64_t)width * esize * H};
+    const cuuint32_t box[3] = {(cuuint32_t)box_w, 1, (cuuint32_t)kBoxRows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode_fn()(tm, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool verify_tc_fwalk_supported(const VerifyArgs &a) {
+    return a.decay == TV_DECAY_DIAG && a.qkv_dtype == TV_BF16 && (a.dk == 64 || a.dk == 128) &&
+           a.dv == kDvW && a.max_nodes >= 1 && a.max_nodes <= kRowsW && a.max_depth >= 1 &&
+           a.max_depth <= kSlots && encode_fn() != nullptr && WalkLayout().total <= kSmemLimit;
+}
+
+cudaError_t launch_verify_tc_fwalk(const VerifyArgs &a, cudaStream_t s, bool expire_first_wait) {
+    if (!verify_tc_fwalk_supported(a)) return cudaErrorNotSupported;
+    const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tq, tk, tv_, tg;
+    // q, k: 16-channel rows; g: 16 fp32 channels, 64-byte swizzle; v: 64-channel
+    // 128-byte-swizzled rows
+    if (!(encode_node_rows(&tq, a.q, BF, 2, a.dk, a.H, a.T, kGrp, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+          encode_node_rows(&tk, a.k, BF, 2, a.dk, a.H, a.T, kGrp, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+          encode_node_rows(&tv_, a.v, BF, 2, kDvW, a.H, a.T, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+          encode_node_rows(&tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dk, a.H, a.T, kGrp,
+                           CU_TENSOR_MAP_SWIZZLE_64B)))
+        return cudaErrorInvalidValue;
+    WalkParams P;
+    P.a = a;
+    P.expire_first_wait = expire_first_wait ? 1 : 0;
+    auto kern = verify_tc_fwalk_kernel;
+    cudaError_t e = configure_smem_once(kern, true);
+    if (e != cudaSuccess) return e;
+    const size_t smem = WalkLayout().total;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = resident_ctas(kern, kThreadsW, smem, kTmemColsW, per_sm)) != cudaSuccess)
+        return e;
+    const long long units = (long long)a.B * a.H;
+    const long long grid = std::min<long long>(units, (long long)sms * per_sm);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreadsW), smem, s, tq, tk, tv_, tg, P);
+}
+
+}  // namespace tv
