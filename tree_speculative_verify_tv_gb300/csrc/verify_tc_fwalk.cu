@@ -5,50 +5,43 @@
 // Tree closed form (Bole summary page, "Core techniques" §1), per-channel decay:
 //   o_i = H0^T (e^{G_i} * q_i) + sum_{j in anc*(i)} w_ij v_j,
 //   w_ij = sum_c q_ic k_jc e^{G_ic - G_jc}
-// with anc*(i) the root path of node i including i and G_i the sum of g over it.  With
-// the scaled factors q~_i = e^{G_i} * q_i and k~_j = e^{-G_j} * k_j the pair decay
-// factors out, w_ij = q~_i . k~_j.
+// with anc*(i) the root path of node i including i and G_i the sum of g over it.  On a
+// root path i = a_0, a_1 = parent(i), ..., the pair decay of a_s is the sum of g over
+// a_0 .. a_{s-1}, so one walk up the path, keeping that running sum P, gives every pair
+// weight w_{i a_s} = sum_c q_ic k_{a_s c} e^{P_c} and, at the root, G_i = P.
 //
 // Why walks.  A root path holds at most 16 nodes, so of a 256-node tree's 256 x 256
 // pair weights at most 16 per row are used (about 5 in the best-first trees of a
-// large draft budget).  Each weight is then a 128-term fp32 dot product formed on the
-// CUDA cores, and the tree term sum_j w_ij v_j a 16-term fp32 sum per output: no
-// dense score tiles, no bf16 split of the weights, and errors at fp32 rounding.  The
-// context term H0^T q~ is dense (256 x 128 x 128 per unit) and runs on the tensor
-// cores: D[i, c] = sum_k q~[i, k] H0[k, c] with A = q~ (node rows, K-major) and B = the
-// state rows (MN-major), both split into bf16 hi + lo parts, passes hi.hi, hi.lo and
-// lo.hi, fp32 accumulation in tensor memory (two 128-row tiles of 128 columns).
+// large draft budget).  Each weight is a 128-term fp32 sum formed on the CUDA cores and
+// the tree term sum_j w_ij v_j a 16-term fp32 sum per output: no dense score tiles, no
+// bf16 split of the weights, no decay factored out of a pair (so no range limit on the
+// path sums), errors at fp32 rounding.  The context term H0^T (e^{G} * q) is dense (256
+// x 128 x 128 per unit) and runs on the tensor cores: D[i, c] = sum_k q~[i, k] H0[k, c]
+// with q~ = e^{G} * q, A = q~ (node rows, K-major) and B = the state rows (MN-major),
+// both split into bf16 hi + lo parts, passes hi.hi, hi.lo and lo.hi, fp32 accumulation
+// in tensor memory (two 128-row tiles of 128 columns).
 //
 // Rows.  Each unit's nodes are taken in depth order (row r = the r-th node by depth,
-// then index), so the 32 threads of a warp walk paths of one length.  Two threads own
-// a row, one in warps 0-7 and one in warps 8-15, each taking half of every channel
-// group: its node's path sums and factors over those channels and partial weights (16
-// registers, one per path slot, summed with the other half's once per unit); at the
-// end each forms half of its node's output row (value channels 0-63 or 64-127), read
-// from the row's tensor-memory lane.
+// then index).  During the channel groups two adjacent lanes own a row, each taking 8 of
+// every 16-channel group: the walk up its node's path over those channels, the partial
+// pair weights (16 registers, one per path slot, summed with the neighbour lane's once
+// per unit) and the q~ operand.  For the outputs a thread owns the row of its
+// tensor-memory lane and half of the value channels.
 //
-// Copies.  Key channels are taken in groups of 16.  A group's g (fp32 rows of 64 B,
-// 64-byte swizzled), q and k (32 B a row) and 16 state rows arrive by tensor copies into
-// one of three 40 KB staging buffers; after a unit's groups its v arrives the same way
-// (channels 0-63 and 64-127, 128-byte swizzled) in the next two buffers.  The buffers
-// are taken in strict rotation -- a unit's groups, then its two v halves, then the next
-// unit's groups -- so each copy is requested two buffer-uses ahead of its reader and
-// the next unit's first group lands while this unit's outputs are formed.  Per group
-// each thread forms its node's path sums from the staged g rows of its root path, its
-// factors from its own staged q and k columns, writes k~ (fp32 rows, read by the walks
-// of the node's descendants) and the bf16 hi / lo operands of the context product to
-// the products buffer, and after one barrier adds q~_i . k~_j over its path to its
-// weights.  The outputs go out 16 channels at a time through 2 KB of scratch per warp
-// in the products buffer, so that a warp stores whole 64-byte row pieces.  About 171 KB
-// of shared memory: one CTA of 608 threads per SM.
-//
-// Range.  While every |G_ic| <= 69 the scaled factors are finite and normal.  A unit
-// whose path sums leave that range anywhere takes its weights from a second walk with
-// the pair decays as running products of e^{g} along the path; its context product
-// keeps q~, which then underflows only where e^{G_ic} is below fp32's range.
+// Copies.  A group's g (fp32 rows of 64 B, 64-byte swizzled), q and k (32 B a row) and
+// 16 state rows arrive by tensor copies into one of three 40 KB staging buffers; after a
+// unit's groups its v arrives the same way (channels 0-63 and 64-127, 128-byte swizzled)
+// in the next two buffers.  The buffers are taken in strict rotation -- a unit's groups,
+// then its two v halves, then the next unit's groups -- so each copy is requested two
+// uses ahead of its readers.  A group's walk needs nothing from other threads, so the
+// row warps run through the groups without meeting: each warp hands its part of the
+// operands to the product thread and releases the staging buffer by mbarrier arrivals,
+// and the operands alternate between two buffers.  The outputs go out 16 channels at a
+// time through 2 KB of scratch per warp, so that a warp stores whole 64-byte row pieces.
+// About 179 KB of shared memory: one CTA of 608 threads per SM.
 //
 // Persistent CTAs take every grid-th (request, head) unit.  Roles (608 threads):
-//   warps 0-15  half a tree row each: factors, walks, the unit's outputs
+//   warps 0-15  rows: walks and operands (per group), outputs (per unit)
 //   warp 16     tree checks, root-path lists (node indices as bytes) and the depth
 //               order, up to two units ahead (two copies of the tree arrays)
 //   warp 17     tensor memory; one thread issues the context products
@@ -75,7 +68,6 @@ constexpr int kGrp = 16;                      // key channels per group
 constexpr int kBoxRows = 32;                  // node rows per copy box
 constexpr int kTmemColsW = 256;               // D: two 128-row tiles x 128 value channels
 constexpr float kLog2eW = 1.4426950408889634f;
-constexpr float kGLimitW = 69.f;
 static_assert(kFacThreads == 2 * kRowsW, "two factor threads per tree row");
 static_assert(kThreadsW == 608, "roles: 16 row warps, tree, product and copy warps");
 
@@ -87,30 +79,31 @@ constexpr uint32_t kSq = 16384;    // q: 256 rows x 32 B
 constexpr uint32_t kSk = 24576;    // k: 256 rows x 32 B
 constexpr uint32_t kSh = 32768;    // the group's 16 state rows, 16 x 512 B
 // (v: 256 rows x 128 B of 64 channels, chunk x of row j at x ^ (j % 8))
-// products buffer: a group's k~ rows and context-product operands; after the unit's
-// products, the two halves' partial weights (2 x 256 rows x 64 B), then the output
-// scratch (2 KB per warp)
-constexpr uint32_t kPk = 0;        // k~: 256 rows x 64 B fp32, chunks as g's
-constexpr uint32_t kPqh = 16384;   // q~ hi: two 128-row tiles (K-major, no swizzle)
-constexpr uint32_t kPql = 24576;   // q~ lo
-constexpr uint32_t kPhh = 32768;   // state hi: two 64-channel slabs of 16 rows, MN-major
-constexpr uint32_t kPhl = 36864;   // state lo
-constexpr uint32_t kProdBytes = 40960;
+// operand buffers (two, alternating by group): the context product's operands; after a
+// unit's products both hold the rows' weights (256 x 64 B) and the output scratch
+constexpr uint32_t kPqh = 0;       // q~ hi: two 128-row tiles (K-major, no swizzle)
+constexpr uint32_t kPql = 8192;    // q~ lo
+constexpr uint32_t kPhh = 16384;   // state hi: two 64-channel slabs of 16 rows, MN-major
+constexpr uint32_t kPhl = 20480;   // state lo
+constexpr uint32_t kPBuf = 24576;  // one operand buffer
+constexpr uint32_t kProdBytes = 2 * kPBuf;
+constexpr uint32_t kScratch = 16384;  // output scratch after the weights, 2 KB per row warp
 constexpr uint32_t kQTile = 4096;  // one 128-row tile of q~ hi or lo
 constexpr uint32_t kHSlab = 2048;  // one 64-channel slab of the state rows
 
 // Barriers.  The tree arrays come in two copies (units of even and odd index), so a
 // tree barrier's phase is unit / 2; a staging buffer takes every third use, so its
-// barriers' phase is use / 3; the product barriers alternate strictly between the row
-// threads and the product thread, so their phase is the running group count.
+// barriers' phase is use / 3; an operand buffer every second group, so its barriers'
+// phase is group / 2.  A row warp arrives on a buffer's barrier once per use, and can
+// reach the buffer's next use only after all sixteen have arrived.
 enum {
     kWTree = 0,            // [2]: tree arrays of the unit ready
     kWTfree = 2,           // [2]: tree arrays read (row threads, products, copies: 3)
     kWStage = 4,           // [3]: a staging use landed
-    kWStageFree = 7,       // [3]: a staging use read
-    kWProd = 10,           // a group's operands written
-    kWProdDone = 11,       // a group's products done
-    kWNumBars = 12
+    kWStageFree = 7,       // [3]: a staging use read (one arrival per row warp)
+    kWProd = 10,           // [2]: a group's operands written (one arrival per row warp)
+    kWProdDone = 12,       // [2]: a group's products done
+    kWNumBars = 14
 };
 
 enum { kWN = 0, kWOff, kWRun, kWZero, kWTiles, kWOut, kWMeta = 8 };
@@ -132,7 +125,7 @@ struct WalkLayout {
 
 struct WalkParams {
     VerifyArgs a;
-    int expire_first_wait;  // test hook: the row threads' first wait for a copy gives up at once
+    int expire_first_wait;  // test hook: each row warp's first wait for a copy gives up at once
 };
 
 __device__ __forceinline__ float ex2w(float x) {
@@ -183,13 +176,14 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     int *sCnt = reinterpret_cast<int *>(smem + L.misc_off + 16);  // per depth: count, start
     const uint32_t bar0 = ptx::smem_addr(smem + L.bar_off);
     auto bar = [&](int idx) { return bar0 + 8u * idx; };
-    const uint32_t b_prod = bar(kWProd), b_pdone = bar(kWProdDone);
+    auto b_prod = [&](int grp) { return bar(kWProd + (grp & 1)); };
+    auto b_pdone = [&](int grp) { return bar(kWProdDone + (grp & 1)); };
+    auto gph = [](int grp) { return static_cast<uint32_t>((grp >> 1) & 1); };  // operand phase
     auto b_tree = [&](int it) { return bar(kWTree + (it & 1)); };
     auto b_tfree = [&](int it) { return bar(kWTfree + (it & 1)); };
     auto b_stage = [&](int use) { return bar(kWStage + use % kStages); };
     auto b_sfree = [&](int use) { return bar(kWStageFree + use % kStages); };
     auto ph = [](int it) { return static_cast<uint32_t>((it >> 1) & 1); };
-    auto par = [](int use) { return static_cast<uint32_t>(use & 1); };
     auto uph = [](int use) { return static_cast<uint32_t>((use / kStages) & 1); };
     auto stage = [&](int use) { return sS + (use % kStages) * kStageBytes; };
     const uint32_t pA = ptx::smem_addr(sP);
@@ -209,10 +203,12 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         }
         for (int b = 0; b < kStages; ++b) {
             ptx::mbar_init(bar(kWStage + b), 1);
-            ptx::mbar_init(bar(kWStageFree + b), 1);
+            ptx::mbar_init(bar(kWStageFree + b), kFacWarpsW);
         }
-        ptx::mbar_init(b_prod, 1);
-        ptx::mbar_init(b_pdone, 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar(kWProd + b), kFacWarpsW);
+            ptx::mbar_init(bar(kWProdDone + b), 1);
+        }
         ptx::fence_mbar_init();
         *sLate = 0;
     }
@@ -398,8 +394,6 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 return !late_now();
             };
             constexpr uint32_t idesc = ptx::idesc_bf16_f32_bmn(128, 128);
-            const uint64_t bh = ptx::desc_mnmajor_sw128(pA + kPhh, kHSlab, 1024);
-            const uint64_t bl = ptx::desc_mnmajor_sw128(pA + kPhl, kHSlab, 1024);
             bool ok = true;
             for (int it = 0; it < nu && ok; ++it) {
                 if (!wait_ok(b_tree(it), ph(it))) break;
@@ -408,57 +402,63 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 ptx::mbar_arrive(b_tfree(it));
                 if (!run) continue;
                 for (int g = 0; g < ng; ++g) {
-                    if (!wait_ok(b_prod, par(pu))) {
+                    if (!wait_ok(b_prod(pu), gph(pu))) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after_sync();
+                    const uint32_t pb = pA + (pu & 1) * kPBuf;
+                    const uint64_t bh = ptx::desc_mnmajor_sw128(pb + kPhh, kHSlab, 1024);
+                    const uint64_t bl = ptx::desc_mnmajor_sw128(pb + kPhl, kHSlab, 1024);
                     for (int t = 0; t < tiles; ++t) {
                         const uint32_t d = tD + t * 128;
-                        const uint64_t ah = ptx::desc_kmajor_noswizzle(pA + kPqh + t * kQTile, 128, 256);
-                        const uint64_t al = ptx::desc_kmajor_noswizzle(pA + kPql + t * kQTile, 128, 256);
+                        const uint64_t ah = ptx::desc_kmajor_noswizzle(pb + kPqh + t * kQTile, 128, 256);
+                        const uint64_t al = ptx::desc_kmajor_noswizzle(pb + kPql + t * kQTile, 128, 256);
                         ptx::mma_bf16(d, ah, bh, idesc, g > 0 ? 1u : 0u);
                         ptx::mma_bf16(d, ah, bl, idesc, 1u);
                         ptx::mma_bf16(d, al, bh, idesc, 1u);
                     }
-                    ptx::mma_commit(b_pdone);
+                    ptx::mma_commit(b_pdone(pu));
                     ++pu;
                 }
             }
-            // the products complete before tensor memory is freed
-            if (pu > 0 && !ptx::mbar_wait(b_pdone, par(pu - 1), kWaitLimit)) atomicOr(sLate, 128);
+            // the products complete before tensor memory is freed (commits complete in order)
+            if (pu > 0 && !ptx::mbar_wait(b_pdone(pu - 1), gph(pu - 1), kWaitLimit)) atomicOr(sLate, 128);
         }
     } else {
-        // ================= tree rows (warps 0-15): row r = (warp % 8) * 32 + lane of the
-        // depth order; half hf = warp / 8 takes 8 of every group's 16 key channels (16-byte
-        // chunks 2 hf, 2 hf + 1 of a 64-byte g or k~ row) and value channels 64 hf ..
-        const int ft = tid;                         // 0 .. 511
-        // groups: row r = ft / 2, half hf = ft % 2 (the two halves of a row in adjacent
-        // lanes, so that a warp's 16-byte loads of ancestor rows touch 4 rows, 2 chunks
-        // each, per 8 lanes); outputs: row re = (warp % 8) * 32 + lane (its tensor-memory
-        // lane), value-channel half he = warp / 8
+        // ================= rows (warps 0-15).  Groups: row r = ft / 2, half hf = ft % 2 of
+        // every 16-channel group (8 channels: 16-byte chunks 2 hf, 2 hf + 1 of a 64-byte g
+        // row, bytes 16 hf .. of a 32-byte q or k row).  Outputs: row re = (warp % 8) * 32 +
+        // lane, its tensor-memory lane, and value channels 64 he .., he = warp / 8.
+        const int ft = tid;
         const int hf = ft & 1, r = ft >> 1;
         const int he = warp >> 3, re = (warp & 7) * 32 + lane;
         const int qd = warp & 3, tile = (warp >> 2) & 1;  // tensor-memory lane quadrant, D tile
-        const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(a.q);
-        const __nv_bfloat16 *kgl = static_cast<const __nv_bfloat16 *>(a.k);
         int pu = 0, U = 0;  // groups handed to the product thread, staging uses read
         bool first = true;
-        // thread 0 waits (for b, then b2, where given); the barrier hands its verdict to all
-        // 512 threads at once (a flag read after the barrier could already carry the
-        // verdict of thread 0's next wait)
-        auto sync_wait = [&](uint32_t b, uint32_t parity, bool expire, uint32_t b2 = 0u,
+        // the whole role: thread 0 waits (for b, then b2, where given), the barrier hands
+        // the verdict, and-ed with every thread's `mine`, to all 512 threads at once
+        auto sync_wait = [&](uint32_t b, uint32_t parity, bool mine, uint32_t b2 = 0u,
                              uint32_t parity2 = 0u) {
-            bool ok = true;
+            bool ok = mine;
             if (ft == 0) {
-                ok = !late_now() && !expire && (b == 0u || ptx::mbar_wait(b, parity, kWaitLimit));
+                ok = ok && !late_now() && (b == 0u || ptx::mbar_wait(b, parity, kWaitLimit));
                 if (ok && b2 != 0u) ok = ptx::mbar_wait(b2, parity2, kWaitLimit);
                 if (!ok) atomicOr(sLate, 4);
             }
             return named_barrier_and(1, kFacThreads, ok);
         };
+        // one warp: lane 0 waits, the warp learns the verdict
+        auto warp_wait = [&](uint32_t b, uint32_t parity, bool expire) {
+            bool ok = true;
+            if (lane == 0) {
+                ok = !late_now() && !expire && ptx::mbar_wait(b, parity, kWaitLimit);
+                if (!ok) atomicOr(sLate, 8);
+            }
+            return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        };
         for (int it = 0; it < nu; ++it) {
-            if (!sync_wait(b_tree(it), ph(it), false)) break;
+            if (!sync_wait(b_tree(it), ph(it), true)) break;
             int *mt = meta(it);
             const int n = mt[kWN], off = mt[kWOff], run = mt[kWRun];
             const int u = unit_of(it), h = u % H;
@@ -476,98 +476,68 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             const int i = active ? sOrder(it)[r] : 0;
             const int d = active ? sDep(it)[i] : 0;
             const uint4 path = active ? sPath(it)[i] : make_uint4(0u, 0u, 0u, 0u);
+            const int dmax = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(d));
             float w[kSlots];
 #pragma unroll
             for (int s = 0; s < kSlots; ++s) w[s] = 0.f;
-            float gmax = 0.f;
-            // path sums of this half's 8 channels of a group over the root path (staged g
-            // rows); run for group g + 1 together with group g's walk, so that the two
-            // shared-memory-bound loops overlap
-            auto path_sums = [&](const uint8_t *sb, float (&Gs)[8]) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) Gs[e] = 0.f;
-                if (!active) return;
-#pragma unroll
-                for (int s = 0; s < kSlots; ++s) {
-                    if (s < d) {
-                        const int j = path_node(path, s);
-#pragma unroll
-                        for (int x = 0; x < 2; ++x) {
-                            const float4 gv = *reinterpret_cast<const float4 *>(sb + kSg + row64(j, 2 * hf + x));
-                            Gs[4 * x] += gv.x; Gs[4 * x + 1] += gv.y;
-                            Gs[4 * x + 2] += gv.z; Gs[4 * x + 3] += gv.w;
-                        }
-                    }
-                }
-            };
-            // partial weights: w_s += this half of q~_i . k~_j (k~ rows of the group in the
-            // products buffer)
-            auto walk = [&](const float (&qt)[8]) {
-                if (!active) return;
-#pragma unroll
-                for (int s = 0; s < kSlots; ++s) {
-                    if (s < d) {
-                        const int j = path_node(path, s);
-                        float acc = 0.f;
-#pragma unroll
-                        for (int x = 0; x < 2; ++x) {
-                            const float4 kv = *reinterpret_cast<const float4 *>(sP + kPk + row64(j, 2 * hf + x));
-                            acc = fmaf(qt[4 * x], kv.x, acc);
-                            acc = fmaf(qt[4 * x + 1], kv.y, acc);
-                            acc = fmaf(qt[4 * x + 2], kv.z, acc);
-                            acc = fmaf(qt[4 * x + 3], kv.w, acc);
-                        }
-                        w[s] += acc;
-                    }
-                }
-            };
-            float Gs[8], qt[8];
-            // the first group's copies have landed
-            bool go = sync_wait(b_stage(U), uph(U), first && P.expire_first_wait);
-            first = false;
-            if (go) path_sums(stage(U), Gs);
-            for (int g = 0; g < ng && go; ++g, ++U) {
-                // the previous group's walks are done (this barrier) and its products too:
-                // the products buffer is free
-                if (!sync_wait(pu > 0 ? b_pdone : 0u, pu > 0 ? par(pu - 1) : 0u, false)) {
-                    go = false;
-                    break;
-                }
+            bool ok = true;  // the same in every lane of the warp
+            for (int g = 0; g < ng; ++g, ++U, ++pu) {
+                // the group's copies have landed, and the operand buffer's previous products
+                // (group pu - 2) are done
+                if (ok) ok = warp_wait(b_stage(U), uph(U), first && P.expire_first_wait);
+                first = false;
+                if (ok && pu >= 2) ok = warp_wait(b_pdone(pu - 2), gph(pu - 2), false);
+                if (!ok) continue;
                 const uint8_t *sb = stage(U);
+                uint8_t *pb = sP + (pu & 1) * kPBuf;
+                float qt[8];
                 if (active) {
-                    // own q and k columns (bf16, 16 bytes each), factors 4 channels at a time
+                    // the walk up the root path: at slot s the running sum P of g over the
+                    // slots below it is the pair decay of the slot's node, in base 2
                     const uint4 qh = *reinterpret_cast<const uint4 *>(sb + kSq + i * 32 + 16 * hf);
-                    const uint4 kh = *reinterpret_cast<const uint4 *>(sb + kSk + i * 32 + 16 * hf);
+                    const uint32_t qw[4] = {qh.x, qh.y, qh.z, qh.w};
+                    float qv[8], P2[8];
 #pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        const uint32_t qa = x == 0 ? qh.x : qh.z, qb = x == 0 ? qh.y : qh.w;
-                        const uint32_t ka = x == 0 ? kh.x : kh.z, kb = x == 0 ? kh.y : kh.w;
-                        const float qv[4] = {bf16lo(qa), bf16hi(qa), bf16lo(qb), bf16hi(qb)};
-                        const float kv[4] = {bf16lo(ka), bf16hi(ka), bf16lo(kb), bf16hi(kb)};
-                        float kt[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float Gc = Gs[4 * x + e];
-                            gmax = fmaxf(gmax, fabsf(Gc));
-                            const float l2 = Gc * kLog2eW;
-                            qt[4 * x + e] = qv[e] * ex2w(l2);
-                            kt[e] = kv[e] * ex2w(-l2);
-                        }
-                        *reinterpret_cast<float4 *>(sP + kPk + row64(i, 2 * hf + x)) =
-                            make_float4(kt[0], kt[1], kt[2], kt[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        qv[2 * e] = bf16lo(qw[e]);
+                        qv[2 * e + 1] = bf16hi(qw[e]);
                     }
-                    // q~ hi / lo: row r of tile r / 128, 8-row x 16-byte core matrices; this
-                    // half's 8 channels are the K-chunk hf
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) P2[e] = 0.f;
+#pragma unroll
+                    for (int s = 0; s < kSlots; ++s) {
+                        if (s >= dmax) break;
+                        if (s < d) {
+                            const int j = path_node(path, s);
+                            const uint32_t o = row64(j, 2 * hf);
+                            const float4 g0 = *reinterpret_cast<const float4 *>(sb + kSg + o);
+                            const float4 g1 = *reinterpret_cast<const float4 *>(sb + kSg + (o ^ 16u));
+                            const uint4 kr = *reinterpret_cast<const uint4 *>(sb + kSk + j * 32 + 16 * hf);
+                            const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+                            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                            float acc = 0.f;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                acc = fmaf(qv[2 * e] * bf16lo(kw[e]), ex2w(P2[2 * e]), acc);
+                                acc = fmaf(qv[2 * e + 1] * bf16hi(kw[e]), ex2w(P2[2 * e + 1]), acc);
+                            }
+                            w[s] += acc;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) P2[e] = fmaf(gv[e], kLog2eW, P2[e]);
+                        }
+                    }
+                    // at the root P = G_i: the context product's q~ = e^{G_i} q_i, hi / lo in
+                    // row r of tile r / 128 (8-row x 16-byte core matrices; this half's 8
+                    // channels are the K-chunk hf)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qt[e] = qv[e] * ex2w(P2[e]);
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int m = 0; m < 4; ++m) split_pair(qt[2 * m], qt[2 * m + 1], hi[m], lo[m]);
                     const int rr = r & 127;
                     const uint32_t qo = (r >> 7) * kQTile + (rr >> 3) * 256 + (rr & 7) * 16 + 128 * hf;
-                    *reinterpret_cast<uint4 *>(sP + kPqh + qo) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4 *>(sP + kPql + qo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) qt[e] = 0.f;
+                    *reinterpret_cast<uint4 *>(pb + kPqh + qo) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(pb + kPql + qo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
                 {
                     // the group's 16 state rows -> hi / lo, MN-major with 128-byte swizzle:
@@ -579,85 +549,51 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                     split_pair(x0.x, x0.y, hi[0], lo[0]);
                     split_pair(x0.z, x0.w, hi[1], lo[1]);
                     const uint32_t ho = (c4 >> 4) * kHSlab + kr * 128 + ((((c4 & 15) >> 1) ^ (kr & 7)) << 4) + (c4 & 1) * 8;
-                    *reinterpret_cast<uint2 *>(sP + kPhh + ho) = make_uint2(hi[0], hi[1]);
-                    *reinterpret_cast<uint2 *>(sP + kPhl + ho) = make_uint2(lo[0], lo[1]);
+                    *reinterpret_cast<uint2 *>(pb + kPhh + ho) = make_uint2(hi[0], hi[1]);
+                    *reinterpret_cast<uint2 *>(pb + kPhl + ho) = make_uint2(lo[0], lo[1]);
                 }
+                // this warp's operands are written and its reads of the staging buffer done
                 ptx::fence_proxy_async_smem();
-                // staging read, operands and k~ rows written; the next group's copies have
-                // landed
-                const bool more = g + 1 < ng;
-                if (!sync_wait(more ? b_stage(U + 1) : 0u, more ? uph(U + 1) : 0u, false)) {
-                    go = false;
-                    break;
-                }
-                if (ft == 0) {
-                    ptx::mbar_arrive(b_prod);
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(b_prod(pu));
                     ptx::mbar_arrive(b_sfree(U));
                 }
-                ++pu;
-                // this group's walk and the next group's path sums
-                float qw[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) qw[e] = qt[e];
-                if (more) path_sums(stage(U + 1), Gs);
-                walk(qw);
             }
-            if (!go) break;
-            // path sums out of range anywhere in the unit: weights by the walk over global
-            // memory (pair decays as running products of e^{g} along the path; a cold path,
-            // kept compact; each half takes its own channels)
-            if (!(gmax <= kGLimitW)) atomicOr(&mt[kWOut], 1);
-            // every walk has read the k~ rows; D is full once the last group's products are
-            if (!sync_wait(b_pdone, par(pu - 1), false)) break;
-            if (mt[kWOut] != 0 && active) {
-                const size_t row_i = ((size_t)(off + i) * H + h) * dk;
+            // the two halves of a row sit in adjacent lanes: full weights in both
 #pragma unroll
-                for (int s = 0; s < kSlots; ++s) w[s] = 0.f;
-#pragma unroll 1
-                for (int c = 0; c < dk; ++c) {
-                    if (((c >> 3) & 1) != hf) continue;  // this half's 8 of each 16 channels
-                    const float qv = __bfloat162float(qg[row_i + c]);
-                    float fr = 1.f;
+            for (int s = 0; s < kSlots; ++s) w[s] += __shfl_xor_sync(0xffffffffu, w[s], 1);
+            // every warp through its groups (a warp that gave up makes all stop here); D is
+            // full once the last group's products are done, and v has landed
+            const int uv = U;  // v channels 0-63: use uv, 64-127: use uv + 1
+            if (!sync_wait(b_pdone(pu - 1), gph(pu - 1), ok, b_stage(uv), uph(uv))) break;
+            if (!sync_wait(b_stage(uv + 1), uph(uv + 1), true)) break;
+            // the rows' weights to the output threads, through the operand buffers (free now)
+            if (hf == 0) {
+                float4 *wr = reinterpret_cast<float4 *>(sP + r * 64);
 #pragma unroll
-                    for (int s = 0; s < kSlots; ++s) {
-                        if (s < d) {
-                            const size_t rj = ((size_t)(off + path_node(path, s)) * H + h) * dk + c;
-                            w[s] += qv * __bfloat162float(kgl[rj]) * fr;
-                            fr *= expf(a.g[rj]);
-                        }
-                    }
-                }
+                for (int x = 0; x < 4; ++x) wr[x] = make_float4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
             }
-            // the two halves' partial weights meet in the products buffer (free now); the
-            // output thread of row re adds them, the low-channel half's first
+            named_barrier(1, kFacThreads);
             {
-                float4 *mine = reinterpret_cast<float4 *>(sP + (hf * 256 + r) * 64);
-#pragma unroll
-                for (int x = 0; x < 4; ++x) mine[x] = make_float4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
-                named_barrier(1, kFacThreads);
-                const float4 *p0 = reinterpret_cast<const float4 *>(sP + re * 64);
-                const float4 *p1 = reinterpret_cast<const float4 *>(sP + (256 + re) * 64);
+                const float4 *wr = reinterpret_cast<const float4 *>(sP + re * 64);
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
-                    const float4 lo4 = p0[x], hi4 = p1[x];
-                    w[4 * x] = lo4.x + hi4.x; w[4 * x + 1] = lo4.y + hi4.y;
-                    w[4 * x + 2] = lo4.z + hi4.z; w[4 * x + 3] = lo4.w + hi4.w;
+                    const float4 v4 = wr[x];
+                    w[4 * x] = v4.x; w[4 * x + 1] = v4.y; w[4 * x + 2] = v4.z; w[4 * x + 3] = v4.w;
                 }
-                named_barrier(1, kFacThreads);  // read before the scratch reuses the space
             }
-            // the output row's node and root path
             const bool eact = re < n;
             const int ie = eact ? sOrder(it)[re] : 0;
             const int de = eact ? sDep(it)[ie] : 0;
             const uint4 pathe = eact ? sPath(it)[ie] : make_uint4(0u, 0u, 0u, 0u);
+            const int dmaxe = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(de));
             ptx::tc_fence_after_sync();
             // outputs: D[re, 64 he + :] + sum_s w_s v_{path s}, 16 channels at a time from
-            // this half's v (staging use uv + hf).  Each piece goes through the warp's
-            // scratch in the products buffer (row = lane, 64 B, chunks permuted by row pair)
-            // and leaves as 64-byte row pieces, 8 rows per store instruction.
-            uint8_t *scr = sP + warp * 2048;
-            const int uv = U;  // v channels 0-63: use uv, 64-127: use uv + 1
-            if (!sync_wait(b_stage(uv), uph(uv), false, b_stage(uv + 1), uph(uv + 1))) break;
+            // this half's v.  Each piece goes through the warp's scratch (row = lane, 64 B,
+            // chunks permuted by row pair) and leaves as 64-byte row pieces, 8 rows per store
+            // instruction.
+            uint8_t *scr = sP + kScratch + warp * 2048;
             const uint8_t *vb = stage(uv + he);
 #pragma unroll 1
             for (int m4 = 0; m4 < 4; ++m4) {
@@ -672,6 +608,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 if (eact) {
 #pragma unroll
                     for (int s = 0; s < kSlots; ++s) {
+                        if (s >= dmaxe) break;
                         if (s < de) {
                             const int j = path_node(pathe, s);
                             const float ws = w[s];
@@ -704,12 +641,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 __syncwarp();
             }
             ptx::tc_fence_before_sync();
-            named_barrier(1, kFacThreads);  // D, v, the scratch and the unit's tree arrays read
-            if (ft == 0) {
+            __syncwarp();
+            if (lane == 0) {  // this warp's reads of v done
                 ptx::mbar_arrive(b_sfree(uv));
                 ptx::mbar_arrive(b_sfree(uv + 1));
-                ptx::mbar_arrive(b_tfree(it));
             }
+            named_barrier(1, kFacThreads);  // D, the weights, the scratch and the tree arrays read
+            if (ft == 0) ptx::mbar_arrive(b_tfree(it));
             U += 2;
         }
     }
