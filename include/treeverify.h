@@ -92,10 +92,11 @@ typedef enum tv_variant {
                                dv = 128: max_nodes <= 64 with all three on tensor cores,
                                or max_nodes <= 256 and max_depth <= 16 with the context
                                term on tensor cores and the pair weights and tree term
-                               by fp32 walks of the root paths.  Per-channel factors are
-                               e^{G} q and e^{-G} k where every path sum |G| <= 69; a
-                               unit outside that range takes its pair weights from a
-                               walk with the decays as running products.
+                               by fp32 walks up the root paths (the pair decays summed
+                               along the walk).  The 64-node kernel's factors are e^{G} q
+                               and e^{-G} k where every path sum |G| <= 69; a unit
+                               outside that range takes its pair weights from a walk
+                               with the decays as running products.
                                TV_ERR_UNSUPPORTED otherwise.  What TV_VARIANT_AUTO picks
                                where it applies */
     TV_VARIANT_TC_TILED = 4  /* tcgen05 kernels for large trees, one (request, head) per
