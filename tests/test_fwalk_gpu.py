@@ -4,10 +4,11 @@ against the state rows hi/lo) and the tree term by fp32 walks of each node's roo
 path.  Cases: the large-tree stack at reduced size (every unit against the fp64
 oracle) and against the staged large-tree kernel, ragged trees of 0-256 nodes (one
 and two 128-row tiles) at dk = 64 and 128, chains of depth 16 and stars of 256
-roots, path sums outside the factors' range (the walk over global memory), growing
-decay, non-finite rows next to a request (copy boxes of 32 nodes), malformed trees
-and depth errors among many units per persistent CTA, canaries around the outputs,
-and the timeout path (TV_VARIANT_TEST_EXPIRE_WAIT)."""
+roots, path sums far below -69 (e^{G} under the fp32 range: the walk sums each
+pair's decay, so no factor leaves the range), growing decay, non-finite rows next to
+a request (copy boxes of 32 nodes), malformed trees and depth errors among many units
+per persistent CTA, canaries around the outputs, and the timeout path
+(TV_VARIANT_TEST_EXPIRE_WAIT)."""
 import numpy as np
 import pytest
 
@@ -93,8 +94,10 @@ def test_fwalk_chains_of_16_and_stars_of_256():
     check_verify(b, out, threads=16)
 
 
-def test_fwalk_path_sums_out_of_range_take_the_walk():
-    """Requests whose path sums leave +-69 in some channel next to requests in range."""
+def test_fwalk_path_sums_far_below_the_fp32_range():
+    """Requests whose path sums fall to -150 or -360 in some channels next to requests
+    with moderate decay: pair decays are summed along the walk, so the outputs stay
+    exact where a factor e^{-G} would overflow."""
     rng = np.random.default_rng(13)
     b = _diag(rng, [140, 256, 17, 200, 33, 5], 4, 128, depth_cap=10, max_depth=16)
     g = b.g.reshape(b.T, b.H, b.dk)
