@@ -80,7 +80,8 @@ constexpr uint32_t kSk = 24576;    // k: 256 rows x 32 B
 constexpr uint32_t kSh = 32768;    // the group's 16 state rows, 16 x 512 B
 // (v: 256 rows x 128 B of 64 channels, chunk x of row j at x ^ (j % 8))
 // operand buffers (two, alternating by group): the context product's operands; after a
-// unit's products both hold the rows' weights (256 x 64 B) and the output scratch
+// unit's products both hold the rows' weights (16 slots x 256 rows, fp32, slot-major) and
+// the output scratch
 constexpr uint32_t kPqh = 0;       // q~ hi: two 128-row tiles (K-major, no swizzle)
 constexpr uint32_t kPql = 8192;    // q~ lo
 constexpr uint32_t kPhh = 16384;   // state hi: two 64-channel slabs of 16 rows, MN-major
@@ -136,6 +137,7 @@ __device__ __forceinline__ float ex2w(float x) {
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float2 bf16pair(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
 
 // node index in path slot s (0 = the node itself) of a packed 16-byte path list
 __device__ __forceinline__ int path_node(const uint4 &p, int s) {
@@ -448,11 +450,16 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             }
             return named_barrier_and(1, kFacThreads, ok);
         };
-        // one warp: lane 0 waits, the warp learns the verdict
-        auto warp_wait = [&](uint32_t b, uint32_t parity, bool expire) {
+        // one warp: lane 0 waits for b (then b2, where given), the warp learns the
+        // verdict.  The phases are usually complete already: one test each first.
+        auto warp_wait = [&](uint32_t b, uint32_t parity, uint32_t b2, uint32_t parity2, bool expire) {
             bool ok = true;
             if (lane == 0) {
-                ok = !late_now() && !expire && ptx::mbar_wait(b, parity, kWaitLimit);
+                ok = !expire && (ptx::mbar_test_wait(b, parity) ||
+                                 (!late_now() && ptx::mbar_wait(b, parity, kWaitLimit)));
+                if (ok && b2 != 0u)
+                    ok = ptx::mbar_test_wait(b2, parity2) ||
+                         (!late_now() && ptx::mbar_wait(b2, parity2, kWaitLimit));
                 if (!ok) atomicOr(sLate, 8);
             }
             return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -484,9 +491,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             for (int g = 0; g < ng; ++g, ++U, ++pu) {
                 // the group's copies have landed, and the operand buffer's previous products
                 // (group pu - 2) are done
-                if (ok) ok = warp_wait(b_stage(U), uph(U), first && P.expire_first_wait);
+                if (ok)
+                    ok = warp_wait(b_stage(U), uph(U), pu >= 2 ? b_pdone(pu - 2) : 0u, gph(pu - 2),
+                                   first && P.expire_first_wait);
                 first = false;
-                if (ok && pu >= 2) ok = warp_wait(b_pdone(pu - 2), gph(pu - 2), false);
                 if (!ok) continue;
                 const uint8_t *sb = stage(U);
                 uint8_t *pb = sP + (pu & 1) * kPBuf;
@@ -568,21 +576,14 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             const int uv = U;  // v channels 0-63: use uv, 64-127: use uv + 1
             if (!sync_wait(b_pdone(pu - 1), gph(pu - 1), ok, b_stage(uv), uph(uv))) break;
             if (!sync_wait(b_stage(uv + 1), uph(uv + 1), true)) break;
-            // the rows' weights to the output threads, through the operand buffers (free now)
+            // the rows' weights to the output threads, through the operand buffers (free
+            // now): slot s of row r at sW[s * 256 + r], read by the output threads slot by slot
+            float *sW = reinterpret_cast<float *>(sP);
             if (hf == 0) {
-                float4 *wr = reinterpret_cast<float4 *>(sP + r * 64);
 #pragma unroll
-                for (int x = 0; x < 4; ++x) wr[x] = make_float4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                for (int s = 0; s < kSlots; ++s) sW[s * kRowsW + r] = w[s];
             }
             named_barrier(1, kFacThreads);
-            {
-                const float4 *wr = reinterpret_cast<const float4 *>(sP + re * 64);
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const float4 v4 = wr[x];
-                    w[4 * x] = v4.x; w[4 * x + 1] = v4.y; w[4 * x + 2] = v4.z; w[4 * x + 3] = v4.w;
-                }
-            }
             const bool eact = re < n;
             const int ie = eact ? sOrder(it)[re] : 0;
             const int de = eact ? sDep(it)[ie] : 0;
@@ -602,25 +603,25 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 uint32_t dv[16];
                 ptx::tmem_ld_x16_nowait(tD + (static_cast<uint32_t>(32 * qd) << 16) + tile * 128 + 16 * m, dv);
                 ptx::tmem_wait_ld();
-                float acc[16];
+                float2 acc[8];  // channel pairs (2e, 2e + 1) of the piece
 #pragma unroll
-                for (int e = 0; e < 16; ++e) acc[e] = __uint_as_float(dv[e]);
+                for (int e = 0; e < 8; ++e)
+                    acc[e] = make_float2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1]));
                 if (eact) {
 #pragma unroll
                     for (int s = 0; s < kSlots; ++s) {
                         if (s >= dmaxe) break;
                         if (s < de) {
                             const int j = path_node(pathe, s);
-                            const float ws = w[s];
+                            const float wsv = sW[s * kRowsW + re];
+                            const float2 ws = make_float2(wsv, wsv);
 #pragma unroll
                             for (int x = 0; x < 2; ++x) {
                                 const uint4 raw = *reinterpret_cast<const uint4 *>(vb + j * 128 + (((c0 + x) ^ (j & 7)) << 4));
-                                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    acc[8 * x + 2 * e] = fmaf(ws, bf16lo(wv[e]), acc[8 * x + 2 * e]);
-                                    acc[8 * x + 2 * e + 1] = fmaf(ws, bf16hi(wv[e]), acc[8 * x + 2 * e + 1]);
-                                }
+                                acc[4 * x] = __ffma2_rn(ws, bf16pair(raw.x), acc[4 * x]);
+                                acc[4 * x + 1] = __ffma2_rn(ws, bf16pair(raw.y), acc[4 * x + 1]);
+                                acc[4 * x + 2] = __ffma2_rn(ws, bf16pair(raw.z), acc[4 * x + 2]);
+                                acc[4 * x + 3] = __ffma2_rn(ws, bf16pair(raw.w), acc[4 * x + 3]);
                             }
                         }
                     }
@@ -628,7 +629,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
 #pragma unroll
                 for (int x = 0; x < 4; ++x)
                     *reinterpret_cast<float4 *>(scr + row64(lane, x)) =
-                        make_float4(acc[4 * x], acc[4 * x + 1], acc[4 * x + 2], acc[4 * x + 3]);
+                        make_float4(acc[2 * x].x, acc[2 * x].y, acc[2 * x + 1].x, acc[2 * x + 1].y);
                 __syncwarp();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
