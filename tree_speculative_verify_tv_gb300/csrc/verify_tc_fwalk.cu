@@ -36,9 +36,13 @@
 // uses ahead of its readers.  A group's walk needs nothing from other threads, so the
 // row warps run through the groups without meeting: each warp hands its part of the
 // operands to the product thread and releases the staging buffer by mbarrier arrivals,
-// and the operands alternate between two buffers.  The outputs go out 16 channels at a
-// time through 2 KB of scratch per warp, so that a warp stores whole 64-byte row pieces.
-// About 179 KB of shared memory: one CTA of 608 threads per SM.
+// and the operands alternate between two buffers.  A wait tests its phase once before
+// the bounded loop: the phase has usually completed, and under the walks' shared-memory
+// traffic each test costs a few hundred cycles.  The rows' weights reach the output
+// threads slot-major (one slot of 32 consecutive rows per load), the tree term is summed
+// in packed fp32 pairs, and the outputs go out 16 channels at a time through 2 KB of
+// scratch per warp, so that a warp stores whole 64-byte row pieces.  About 180 KB of
+// shared memory: one CTA of 608 threads per SM.
 //
 // Persistent CTAs take every grid-th (request, head) unit.  Roles (608 threads):
 //   warps 0-15  rows: walks and operands (per group), outputs (per unit)
