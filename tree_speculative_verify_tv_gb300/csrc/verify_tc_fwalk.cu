@@ -60,9 +60,9 @@ namespace {
 using namespace tcc;
 
 constexpr int kFacWarpsW = 16;              // warps 0-15: half a tree row per thread
-constexpr int kTreeWarpW = kFacWarpsW;      // warp 8
-constexpr int kMmaWarpW = kFacWarpsW + 1;   // warp 9
-constexpr int kLoadWarpW = kFacWarpsW + 2;  // warp 10
+constexpr int kTreeWarpW = kFacWarpsW;      // warp 16
+constexpr int kMmaWarpW = kFacWarpsW + 1;   // warp 17
+constexpr int kLoadWarpW = kFacWarpsW + 2;  // warp 18
 constexpr int kThreadsW = (kLoadWarpW + 1) * 32;
 constexpr int kFacThreads = kFacWarpsW * 32;  // 512
 constexpr int kRowsW = 256;                   // nodes per tree at most
