@@ -3,10 +3,13 @@ Mamba-2-like workload (B=16 requests, H=24 heads, dk=128, dv=64, 16-node top-4
 draft trees, bf16 q/k/v, fp32 states, scalar decay).  One step verifies the
 tree, runs the greedy acceptance walk and commits the accepted path:
 
-  --pipeline fused (default): tv_commit_verify (the previous step's accepted
-      paths applied to the state in place, then the tree verified against it)
-      + tv_accept_greedy.  In steady state every step does one commit, one
-      verification and one walk; the state stays resident and is streamed once.
+  --pipeline one (default): tv_accept_commit_verify, one launch: the greedy walk
+      of the previous tree, the commit of its path to the state in place, and the
+      verification of the current tree against the committed state.  Every step
+      does one walk, one commit and one verification; the state stays resident and
+      is streamed once.
+  --pipeline fused: tv_commit_verify (the previous step's accepted paths applied
+      to the state in place, then the tree verified against it) + tv_accept_greedy.
   --pipeline separate: tv_verify + tv_accept_commit (walk and commit in one
       launch), the state streamed by both kernels.
 
@@ -56,9 +59,12 @@ _CS = "tree_speculative_verify_tv_gb300/csrc/"
 # sources behind each kernel whose DRAM traffic was captured with ncu
 TRAFFIC_SOURCES = {
     "verify": [_CS + f for f in ("verify_tc_fused.cu", "tc_common.cuh", "tc_ptx.cuh",
-                                 "tv_internal.cuh")],
+                                 "tv_internal.cuh", "greedy_walk.cuh")],
     "commit_verify": [_CS + f for f in ("verify_tc_fused.cu", "tc_common.cuh", "tc_ptx.cuh",
-                                        "tv_internal.cuh")],
+                                        "tv_internal.cuh", "greedy_walk.cuh")],
+    "accept_commit_verify": [_CS + f for f in ("verify_tc_fused.cu", "tc_common.cuh",
+                                               "tc_ptx.cuh", "tv_internal.cuh",
+                                               "greedy_walk.cuh")],
     "tree_attention": [_CS + f for f in ("tree_attention.cu", "tc_common.cuh", "tc_ptx.cuh",
                                          "tv_internal.cuh")],
 }
@@ -92,9 +98,10 @@ def parse():
     ap.add_argument("--profile-folded", type=int, default=None, metavar="VARIANT",
                     help="profiling aid: only run 3 verify launches of this tv_variant over "
                          "--fold config-2 layers folded into the head axis, then exit")
-    ap.add_argument("--pipeline", default="fused", choices=["fused", "separate"],
-                    help="step as tv_commit_verify + tv_accept_greedy (fused) or as "
-                         "tv_verify + tv_accept_commit (separate)")
+    ap.add_argument("--pipeline", default="one", choices=["one", "fused", "separate"],
+                    help="step as tv_accept_commit_verify (one), as tv_commit_verify + "
+                         "tv_accept_greedy (fused) or as tv_verify + tv_accept_commit "
+                         "(separate)")
     ap.add_argument("--attention-ctx", type=int, default=4096,
                     help="shared-prefix positions per request for the tree-attention line "
                          "(0 = skip it)")
@@ -149,6 +156,13 @@ def commit_verify_bytes(b, lens) -> int:
     L = int(np.sum(lens))
     return (verify_bytes(b) + written + L * b.H * (b.dk * qk + b.dv * qk + g) + 4 * L
             + 4 * (b.B + 1) + 4 * b.B + 4 * b.B * b.max_depth)
+
+
+def accept_commit_verify_bytes(b, lens) -> int:
+    """Algorithmic HBM bytes of one tv_accept_commit_verify launch: those of
+    tv_commit_verify, plus the previous tree's parents, draft and target tokens and
+    root tokens the walk reads and the bonus tokens it writes."""
+    return commit_verify_bytes(b, lens) + 12 * b.T + 4 * b.B + 4 * b.B
 
 
 def commit_bytes(b, lens) -> int:
@@ -623,7 +637,14 @@ def run_ours(args, world, rank, local):
                                    d.parent, d.draft, rl, nl, root_am, tgt_am, d.accept_len,
                                    d.path, d.bonus, d.status, stream)
 
-    fused = args.pipeline == "fused"
+    mode = args.pipeline
+    fused = mode in ("one", "fused")  # the state stays resident and is updated in place
+
+    def step_one(d):
+        # one pass of the hot path in one launch: the greedy walk of the previous tree
+        # (this set's own, in the rotation), the commit of the paths it finds to the
+        # resident state, and the verification of this set's tree
+        d.accept_commit_verify(d, stream=stream)
 
     def step_fused(d):
         # one pass of the hot path: the commit of this set's previous accepted paths
@@ -637,7 +658,7 @@ def run_ours(args, world, rank, local):
         d.verify(stream=stream, variant=args.variant)
         d.accept_commit(stream=stream)
 
-    step = step_fused if fused else step_separate
+    step = {"one": step_one, "fused": step_fused, "separate": step_separate}[mode]
 
     with torch.cuda.stream(stream):
         for d in dbs:
@@ -666,6 +687,10 @@ def run_ours(args, world, rank, local):
                 return lambda d=d: step(d)
             if kind == "step_separate":
                 return lambda d=d: step_separate(d)
+            if kind == "step_fused":
+                return lambda d=d: step_fused(d)
+            if kind == "step_one":
+                return lambda d=d: step_one(d)
             if kind == "commit_verify":
                 return lambda d=d: d.commit_verify(d, stream=stream)
             if kind == "verify":
@@ -727,7 +752,11 @@ def run_ours(args, world, rank, local):
     t_al, _, _ = timed("accept_logits", K)
     t_ser = timed("serial", max(1, K // 8))[0] * 8 if serial_ws is not None else None
     t_sl, _, _ = timed("step_logits", K)
-    t_sep = timed("step_separate", K)[0] if fused else t_step
+    t_modes = {mode: t_step}
+    for m in ("one", "fused", "separate"):
+        if m not in t_modes:
+            t_modes[m] = timed("step_" + m, K)[0]
+    t_sep = t_modes["separate"]
     sampler.stop()
     for d in dbs:
         st = int(d.status[0].item())
@@ -740,7 +769,7 @@ def run_ours(args, world, rank, local):
     ms_per_step = t_step_max / K * 1e3
 
     # ---------------- end to end through the binding with pinned host buffers
-    e2e = run_e2e(args, sets[0], dev, stream, tv, world, fused)
+    e2e = run_e2e(args, sets[0], dev, stream, tv, world, mode)
 
     # ---------------- one verify launch over `fold` layers folded into the head axis
     folded = {}
@@ -908,7 +937,12 @@ def run_ours(args, world, rank, local):
     used_variant = args.variant if args.variant else dbs[0].variant()
     # the recorded captures are of the fused tensor-core kernel on the config-2 workload
     tc2 = cfg == 2 and used_variant == 3
-    if fused:
+    if mode == "one":
+        # the step is the one launch
+        dom_bytes, dom_t = accept_commit_verify_bytes(base, lens), t_step / K
+        dom_name = "tv_accept_commit_verify"
+        traffic = recorded_traffic("accept_commit_verify") if tc2 else None
+    elif fused:
         dom_bytes, dom_t, dom_name = cvb, cv_launch, "tv_commit_verify"
         traffic = recorded_traffic("commit_verify") if tc2 else None
     else:
@@ -973,7 +1007,9 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         host_call = {}
         for name, fn in (("tv_verify", lambda: dbs[0].verify(stream=stream)),
-                         ("tv_commit_verify", lambda: dbs[0].commit_verify(dbs[0], stream=stream))):
+                         ("tv_commit_verify", lambda: dbs[0].commit_verify(dbs[0], stream=stream)),
+                         ("tv_accept_commit_verify",
+                          lambda: dbs[0].accept_commit_verify(dbs[0], stream=stream))):
             for _ in range(20):
                 fn()
             stream.synchronize()
@@ -997,9 +1033,13 @@ def run_ours(args, world, rank, local):
                        "dv": base.dv, "max_nodes": base.max_nodes,
                        "node_heads_per_step": node_heads,
                        "verify_kernel": KERNEL_NAMES.get(used_variant, str(used_variant)),
-                       "pipeline": ("tv_commit_verify + tv_accept_greedy; state resident in "
-                                    "HBM, updated in place" if fused else
-                                    "tv_verify + tv_accept_commit"),
+                       "pipeline": {"one": "tv_accept_commit_verify (one launch: the previous "
+                                           "tree's greedy walk, its commit, this tree's "
+                                           "verification); state resident in HBM, updated "
+                                           "in place",
+                                    "fused": "tv_commit_verify + tv_accept_greedy; state "
+                                             "resident in HBM, updated in place",
+                                    "separate": "tv_verify + tv_accept_commit"}[mode],
                        "inputs": "bf16 q/k/v, fp32 g/H0/out/H_new",
                        "l2": "inputs larger than L2: %d input sets rotated, %.0f MB touched per "
                              "cycle vs %.0f MB L2" % (R, R * per_set / 1e6, l2 / 1e6),
@@ -1009,16 +1049,16 @@ def run_ours(args, world, rank, local):
             "same_bytes_read_reduction": same_bytes,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * K,
+            "gpu_launches": (1 if mode == "one" else 2) * K,
             "clocks": clocks,
             "kernels_us": {"verify": t_verify / K * 1e6, "accept_commit": t_acom / K * 1e6,
                            "commit_verify": t_cv / K * 1e6,
                            "accept (separate call)": t_accept / K * 1e6,
                            "commit (separate call)": t_commit / K * 1e6},
-            "step_kernels": (["tv_commit_verify", "tv_accept_greedy"] if fused
-                             else ["tv_verify", "tv_accept_commit"]),
-            "step_us": {"fused": t_step / K * 1e6 if fused else None,
-                        "separate": t_sep / K * 1e6},
+            "step_kernels": {"one": ["tv_accept_commit_verify"],
+                             "fused": ["tv_commit_verify", "tv_accept_greedy"],
+                             "separate": ["tv_verify", "tv_accept_commit"]}[mode],
+            "step_us": {m: t / K * 1e6 for m, t in t_modes.items()},
             "verify_only": {"value": node_heads / v_launch, "unit": UNIT,
                             "gbs": vb / v_launch / 1e9, "bytes_per_launch": vb,
                             "frac": vb / v_launch / 1e9 / peak,
@@ -1055,12 +1095,14 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, host_batch, dev, stream, tv, world, fused):
+def run_e2e(args, host_batch, dev, stream, tv, world, mode):
     """The step through the binding with host buffers: pinned host -> device copies
     of the step's inputs, the calls, device -> pinned host copies of its results.
-    Fused pipeline: the state is resident on the device (tv_commit_verify updates it
-    in place), so the inputs are the tree, factors and tokens and the results the
-    outputs and acceptance; separate pipeline: the state is copied in and H_new out.
+    One-launch and fused pipelines: the state is resident on the device (the commit
+    updates it in place), so the inputs are the tree, factors and tokens and the
+    results the outputs and acceptance; separate pipeline: the state is copied in and
+    H_new out.  In the one-launch pipeline a step's acceptance results are the walk
+    of the previous step's tree, written to the step's own result buffers.
 
     Each step moves one contiguous staging range in and one out.  Four staging sets
     rotate over four streams, as a decode loop would run them: set s % 4 was last read
@@ -1069,6 +1111,7 @@ def run_e2e(args, host_batch, dev, stream, tv, world, fused):
     of a step wait for those of the previous step (the state and the pending commit
     chain through them)."""
     import torch
+    fused = mode in ("one", "fused")
     ins = ["node_offsets", "parent", "depth", "q", "k", "v", "g", "draft", "target",
            "root_argmax"]
     outs = ["out", "accept_len", "path", "bonus"]
@@ -1129,7 +1172,9 @@ def run_e2e(args, host_batch, dev, stream, tv, world, fused):
             ds[:in_end].copy_(hs[:in_end], non_blocking=True)
             if s - 1 >= first:
                 st.wait_event(kev[(s - 1) % NS])
-            if fused:
+            if mode == "one":
+                db.accept_commit_verify(sets[(s - 1) % NS][1], stream=st)
+            elif fused:
                 db.commit_verify(sets[(s - 1) % NS][1], stream=st)
                 db.accept(stream=st)
             else:

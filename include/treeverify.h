@@ -445,6 +445,34 @@ tv_status tv_commit_verify(const tv_problem *p, const tv_pending *pend, float *H
                            int32_t *dev_status, void *stream);
 
 /*
+ * tv_accept_commit_verify -- one step of the loop in one launch: the greedy walk of
+ * the previous step's tree (LLM Primer VI ch. 9 §9.1), the commit of the path it
+ * finds (Bole summary page, "Core techniques" §2) and the verification of the
+ * current tree against the committed state (§1).
+ * Same results as tv_accept_greedy on the previous tree followed by
+ * tv_commit_verify with the paths it wrote.  For tv_commit_verify's one-kernel shapes
+ * every block of a request runs the walk itself on shared memory (the head-0 block
+ * writes its results), so the commit does not wait for a separate acceptance launch;
+ * other shapes run the walk and then tv_commit_verify.
+ *
+ *   p, H, q, k, v, g, out   the current step, as in tv_commit_verify
+ *   prev         the previous step's tree and factors, as in tv_pending; its path and
+ *                accept_len fields are not read
+ *   draft_tokens, target_argmax [T'], root_argmax [B]   the previous tree's tokens,
+ *                as in tv_accept_greedy
+ *   accept_len [B], path [B][prev->max_depth], bonus [B]   outputs, as written by
+ *                tv_accept_greedy
+ * Device-detected errors: those of tv_accept_greedy on the previous tree (that
+ * request then commits nothing) and of tv_verify on the current one.
+ */
+tv_status tv_accept_commit_verify(const tv_problem *p, const tv_pending *prev,
+                                  const int32_t *draft_tokens, const int32_t *target_argmax,
+                                  const int32_t *root_argmax, int32_t *accept_len, int32_t *path,
+                                  int32_t *bonus, float *H, const void *q, const void *k,
+                                  const void *v, const float *g, float *out, int32_t *dev_status,
+                                  void *stream);
+
+/*
  * tv_tree_attention -- softmax attention of one attention layer over every
  * request's draft tree, the attention layers' share of the verification pass of a
  * hybrid model.  LLM Primer VI ch. 9: the target runs one forward pass over the

@@ -128,7 +128,8 @@ def test_support_query_matches_forced_launch_checks(lib):
 
 def test_fused_variant_limits(lib):
     # the fused kernels: bf16; scalar decay with dk and dv in {64, 128} and <= 32 nodes,
-    # or per-channel decay with dk in {64, 128}, dv = 128 and <= 64 nodes
+    # or per-channel decay with dk in {64, 128}, dv = 128 and <= 64 nodes, or <= 256
+    # nodes of depth <= 16
     import torch
     if torch.cuda.is_available():
         # (the tensor-core kernels need the driver's tensor-map encoder)
@@ -145,7 +146,7 @@ def test_fused_variant_limits(lib):
             assert tv.tv_verify_variant(diag) == tv.TV_VARIANT_TC_FUSED
     for bad in (prob(dk=128, dv=64, max_nodes=33, total_nodes=5),
                 prob(dk=128, dv=64, decay=tv.TV_DECAY_DIAG),
-                prob(dk=128, dv=128, max_nodes=65, decay=tv.TV_DECAY_DIAG),
+                prob(dk=128, dv=128, max_nodes=65, max_depth=17, decay=tv.TV_DECAY_DIAG),
                 prob(dk=96, dv=64), prob(dk=128, dv=64, qkv_dtype=tv.TV_F32)):
         assert tv.tv_verify_supports(bad, tv.TV_VARIANT_TC_FUSED) == 0
         assert verify_rc(bad, variant=tv.TV_VARIANT_TC_FUSED) == tv.TV_ERR_UNSUPPORTED
@@ -381,3 +382,22 @@ def test_build_tree_rejects_bad_arguments(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         tv.load(str(tmp_path / "missing.so"))
+
+
+def test_accept_commit_verify_rejects_bad_arguments(lib):
+    def rc(p=None, pe="default", **kw):
+        a = dict(dr=P[13], tg=P[14], root=P[15], ln=P[11], path=P[10], bonus=P[12], H=P[3],
+                 q=P[4], k=P[5], v=P[6], g=P[7], out=P[8], st=P[9])
+        a.update(kw)
+        pe = pend() if pe == "default" else pe
+        return tv.tv_accept_commit_verify(p or prob(), pe, a["dr"], a["tg"], a["root"], a["ln"],
+                                          a["path"], a["bonus"], a["H"], a["q"], a["k"], a["v"],
+                                          a["g"], a["out"], a["st"], stream=0, check=False)
+    assert rc(prob(dk=12)) == tv.TV_ERR_SHAPE
+    assert rc(pe=None) == tv.TV_ERR_NULL
+    assert rc(dr=None) == tv.TV_ERR_NULL
+    assert rc(bonus=None) == tv.TV_ERR_NULL
+    assert rc(pe=pend(max_depth=40)) == tv.TV_ERR_UNSUPPORTED
+    assert rc(pe=pend(total_nodes=100)) == tv.TV_ERR_SHAPE
+    assert rc(path=P[10] + 4) == tv.TV_ERR_ALIGN
+    assert rc(prob(B=0, total_nodes=0), pe=pend(total_nodes=0)) == tv.TV_OK

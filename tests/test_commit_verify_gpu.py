@@ -215,3 +215,87 @@ def test_commit_verify_malformed_pending_path(defect):
         assert mat_rel_err(Hd[u // prev.H, u % prev.H].astype(np.float64),
                            H[u // prev.H, u % prev.H]) <= TOL
     check_verify(dataclasses.replace(cur, H0=H), dc.out[:cur.T].cpu().numpy().astype(np.float64))
+
+
+def _acv_and_separate(prev, cur):
+    """tv_accept_commit_verify, and the same step as tv_accept_greedy then
+    tv_commit_verify, on copies of the same inputs: (batch holding the walk's results,
+    current batch) for each."""
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    runs = []
+    for fused in (True, False):
+        dp, dc = tv.DeviceBatch(prev), tv.DeviceBatch(cur)
+        dc.H0.copy_(dp.H0)
+        dc.status.zero_()
+        dp.status.zero_()
+        for d in (dp, dc):
+            d.accept_len.fill_(-7)
+            d.path.fill_(-7)
+            d.bonus.fill_(-7)
+        dc.out.fill_(float("nan"))
+        if fused:
+            dc.accept_commit_verify(dp)  # the walk's results land in dc's result buffers
+            acc = dc
+        else:
+            dp.accept()
+            dc.commit_verify(dp)
+            acc = dp
+        torch.cuda.synchronize()
+        runs.append((acc, dc))
+    return runs
+
+
+@pytest.mark.parametrize("c", [2, 4])
+def test_accept_commit_verify_equals_accept_then_commit_verify(c):
+    """Config 2 takes the one-kernel path (the walk runs in every block), config 4 the
+    walk kernel and then tv_commit_verify: both bit-identical to the two calls."""
+    import torch
+    prev, cur = workloads.make_config(c, 51), workloads.make_config(c, 52)
+    (fp, fc), (sp, sc) = _acv_and_separate(prev, cur)
+    assert int(fc.status[0]) == 0 and int(sc.status[0]) == 0 and int(sp.status[0]) == 0
+    B = prev.B
+    assert torch.equal(fp.accept_len[:B], sp.accept_len[:B])
+    assert torch.equal(fp.path[:B], sp.path[:B])
+    assert torch.equal(fp.bonus[:B], sp.bonus[:B])
+    assert torch.equal(fc.H0, sc.H0)
+    assert torch.equal(fc.out[:cur.T], sc.out[:cur.T])
+
+
+def test_accept_commit_verify_against_the_oracle():
+    prev, cur = _pair(workloads.config2)
+    H_ref, cur_ref, ln, path = _oracle_two_steps(prev, cur)
+    (fp, fc), _ = _acv_and_separate(prev, cur)
+    assert int(fc.status[0]) == 0
+    assert np.array_equal(fp.accept_len[:prev.B].cpu().numpy(), ln)
+    assert np.array_equal(fp.path[:prev.B].cpu().numpy(), path)
+    Hd = fc.H0.cpu().numpy().astype(np.float64)
+    worst = max(mat_rel_err(Hd[b, h], H_ref[b, h]) for b in range(prev.B) for h in range(prev.H))
+    assert worst <= TOL, "state rel err %.3e" % worst
+    check_verify(cur_ref, fc.out[:cur.T].cpu().numpy().astype(np.float64))
+
+
+def test_accept_commit_verify_malformed_previous_tree():
+    """A previous tree with a parent after its child: TV_ERR_TREE, that request gets
+    accept_len 0, path -1, bonus -1 and no commit; the other requests are exact."""
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    prev, cur = workloads.config2(seed=61, B=3, H=2), workloads.config2(seed=62, B=3, H=2)
+    s = int(prev.node_offsets[1])
+    prev.parent[s + 2] = 7
+    dp, dc = tv.DeviceBatch(prev), tv.DeviceBatch(cur)
+    dc.H0.copy_(dp.H0)
+    dc.status.zero_()
+    dc.accept_commit_verify(dp)
+    torch.cuda.synchronize()
+    assert int(dc.status[0]) == tv.TV_ERR_TREE
+    assert int(dc.accept_len[1]) == 0 and int(dc.bonus[1]) == -1
+    assert torch.all(dc.path[1] == -1)
+    assert torch.equal(dc.H0[1], dp.H0[1])
+    # the other requests: as the separate calls on an intact copy of their trees
+    good = workloads.config2(seed=61, B=3, H=2)
+    H_ref, cur_ref, ln, path = _oracle_two_steps(good, cur, units=[0, 1, 4, 5])
+    for b in (0, 2):
+        assert int(dc.accept_len[b]) == ln[b]
+        for h in range(prev.H):
+            assert mat_rel_err(dc.H0[b, h].cpu().numpy().astype(np.float64), H_ref[b, h]) <= TOL

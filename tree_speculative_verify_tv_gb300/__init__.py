@@ -16,6 +16,8 @@ include/treeverify.h; this package is the ctypes binding):
   (a baseline for the closed form)
 * ``tv_commit_verify`` the previous step's commit applied to the state in place,
   then ``tv_verify`` against it (one launch for the tensor-core shapes)
+* ``tv_accept_commit_verify`` the previous tree's greedy walk, its commit and the
+  verification of the current tree (one launch for the same shapes)
 
 ``build()`` compiles the CUDA sources in-tree for sm_103a.
 """
@@ -23,6 +25,7 @@ from ._build import build, LIB
 from .binding import (  # noqa: F401
     DeviceBatch, TVError, load, make_pending, make_problem, status_string, tv_accept_commit,
     tv_accept_greedy, tv_accept_greedy_logits, tv_commit, tv_commit_verify, tv_pending,
+    tv_accept_commit_verify,
     tv_verify_serial, tv_verify_serial_workspace_bytes, tv_verify_serial_static, tv_build_tree,
     tv_accept_stochastic, tv_tree_attention, tv_tree_attention_workspace_bytes,
     TV_SERIAL_STATIC_BYTES,

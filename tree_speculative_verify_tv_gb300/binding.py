@@ -32,7 +32,8 @@ TV_SERIAL_STATIC_BYTES = 16 << 20
 EXPORTED = ("tv_verify", "tv_verify_ex", "tv_verify_variant", "tv_verify_supports",
             "tv_workspace_bytes",
             "tv_accept_greedy", "tv_commit",
-            "tv_accept_commit", "tv_commit_verify", "tv_accept_greedy_logits", "tv_verify_serial",
+            "tv_accept_commit", "tv_commit_verify", "tv_accept_commit_verify",
+            "tv_accept_greedy_logits", "tv_verify_serial",
             "tv_verify_serial_workspace_bytes", "tv_verify_serial_static", "tv_build_tree",
             "tv_accept_stochastic", "tv_tree_attention", "tv_tree_attention_workspace_bytes",
             "tv_status_string", "tv_version")
@@ -85,6 +86,7 @@ def load(path: Optional[str] = None):
         L.tv_accept_commit.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.tv_commit_verify.argtypes = [P, ctypes.POINTER(tv_pending), vp, vp, vp, vp, vp, vp, vp,
                                        vp]
+        L.tv_accept_commit_verify.argtypes = [P, ctypes.POINTER(tv_pending)] + [vp] * 14
         L.tv_accept_greedy_logits.argtypes = [i32, i32, i32, i32, i32] + [vp] * 12
         L.tv_verify_serial.argtypes = [P] + [vp] * 7 + [ctypes.c_size_t, vp, vp]
         L.tv_verify_serial_static.argtypes = [P] + [vp] * 8
@@ -99,7 +101,8 @@ def load(path: Optional[str] = None):
         L.tv_workspace_bytes.argtypes = [P]
         L.tv_workspace_bytes.restype = ctypes.c_size_t
         for f in (L.tv_verify, L.tv_verify_ex, L.tv_accept_greedy, L.tv_commit,
-                  L.tv_accept_commit, L.tv_commit_verify, L.tv_accept_greedy_logits,
+                  L.tv_accept_commit, L.tv_commit_verify, L.tv_accept_commit_verify,
+                  L.tv_accept_greedy_logits,
                   L.tv_verify_serial, L.tv_verify_serial_static, L.tv_build_tree,
                   L.tv_accept_stochastic, L.tv_tree_attention):
             f.restype = ctypes.c_int32
@@ -293,6 +296,18 @@ def tv_commit_verify(problem: tv_problem, pending: Optional[tv_pending], H, q, k
     return _check(rc, "tv_commit_verify", check)
 
 
+def tv_accept_commit_verify(problem: tv_problem, prev: Optional[tv_pending], draft_tokens,
+                            target_argmax, root_argmax, accept_len, path, bonus, H, q, k, v, g,
+                            out, dev_status, stream=None, check: bool = True) -> int:
+    pp = ctypes.byref(prev) if prev is not None else None
+    rc = load().tv_accept_commit_verify(ctypes.byref(problem), pp,
+                                        _ptr(draft_tokens), _ptr(target_argmax),
+                                        _ptr(root_argmax), _ptr(accept_len), _ptr(path),
+                                        _ptr(bonus), _ptr(H), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(out), _ptr(dev_status), _stream(stream))
+    return _check(rc, "tv_accept_commit_verify", check)
+
+
 # ---------------------------------------------------------------- device batches
 
 
@@ -387,6 +402,16 @@ class DeviceBatch:
         pend = pending.pending() if pending is not None else None
         return tv_commit_verify(self.problem(), pend, self.H0, self.q, self.k, self.v, self.g,
                                 self.out, self.status, stream, check)
+
+    def accept_commit_verify(self, prev: "DeviceBatch", stream=None, check=True):
+        """One step of the loop: the greedy walk of `prev`'s tree, the commit of the paths
+        it finds to this batch's state H0 in place, and the verification of this batch's
+        tree, in one call.  The walk's results (of `prev`'s tree) go to this batch's
+        accept_len, path and bonus, the step's own result buffers."""
+        return tv_accept_commit_verify(self.problem(), prev.pending(), prev.draft, prev.target,
+                                       prev.root_argmax, self.accept_len, self.path, self.bonus,
+                                       self.H0, self.q, self.k, self.v, self.g, self.out,
+                                       self.status, stream, check)
 
     def commit(self, stream=None, in_place=False, check=True):
         dst = self.H0 if in_place else self.H_new

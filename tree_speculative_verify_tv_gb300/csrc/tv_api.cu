@@ -20,6 +20,11 @@ cudaError_t launch_verify_tc_fdiag(const VerifyArgs &a, cudaStream_t s, bool exp
 // 256 nodes, depth <= 16): context product on tensor cores, tree term by fp32 walks
 bool verify_tc_fwalk_supported(const VerifyArgs &a);
 cudaError_t launch_verify_tc_fwalk(const VerifyArgs &a, cudaStream_t s, bool expire_first_wait);
+// verify_tc_fused.cu: commit + verify with the pending path found by the greedy walk of
+// p's tree in the same kernel (its results written to acc's len, path and bonus)
+bool accept_commit_verify_fused_supported(const VerifyArgs &a, const PendingArgs &p);
+cudaError_t launch_accept_commit_verify_fused(const VerifyArgs &a, const PendingArgs &p,
+                                              const AcceptArgs &acc, float *H, cudaStream_t s);
 }  // namespace tv
 
 namespace {
@@ -501,6 +506,61 @@ tv_status tv_commit_verify(const tv_problem *p, const tv_pending *pend, float *H
     if (p->total_nodes == 0) return TV_OK;
     e = launch_verify_auto(a, s);
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+
+tv_status tv_accept_commit_verify(const tv_problem *p, const tv_pending *prev,
+                                  const int32_t *draft_tokens, const int32_t *target_argmax,
+                                  const int32_t *root_argmax, int32_t *accept_len, int32_t *path,
+                                  int32_t *bonus, float *H, const void *q, const void *k,
+                                  const void *v, const float *g, float *out, int32_t *dev_status,
+                                  void *stream) {
+    tv_status st = check_dims(p);
+    if (st != TV_OK) return st;
+    if (!prev || !dev_status || !H || !prev->node_offsets || !root_argmax || !accept_len ||
+        !path || !bonus)
+        return TV_ERR_NULL;
+    if (!p->depth && p->total_nodes > 0) return TV_ERR_NULL;
+    if (prev->total_nodes < 0 || prev->max_nodes < 1 || prev->max_depth < 1) return TV_ERR_SHAPE;
+    if (prev->max_nodes > TV_MAX_NODES || prev->max_depth > TV_MAX_DEPTH)
+        return TV_ERR_UNSUPPORTED;
+    if ((int64_t)prev->total_nodes > (int64_t)p->B * prev->max_nodes) return TV_ERR_SHAPE;
+    if (prev->total_nodes > 0 &&
+        (!prev->parent || !prev->g || !prev->k || !prev->v || !draft_tokens || !target_argmax))
+        return TV_ERR_NULL;
+    if (p->total_nodes > 0 && (!q || !k || !v || !g || !out)) return TV_ERR_NULL;
+    if (p->B == 0) return TV_OK;
+    st = check_ptrs({H, dev_status, p->node_offsets, prev->node_offsets, root_argmax, accept_len,
+                     path, bonus});
+    if (st != TV_OK) return st;
+    if (prev->total_nodes > 0) {
+        st = check_ptrs({prev->parent, prev->g, prev->k, prev->v, draft_tokens, target_argmax});
+        if (st != TV_OK) return st;
+    }
+    if (p->total_nodes > 0) {
+        st = check_ptrs({q, k, v, g, out, p->parent, p->depth});
+        if (st != TV_OK) return st;
+    }
+    tv::VerifyArgs a{p->B, p->H, p->dk, p->dv, p->total_nodes, p->max_nodes, p->max_depth,
+                     p->decay, p->qkv_dtype, p->node_offsets, p->parent, p->depth,
+                     H, q, k, v, g, out, dev_status};
+    tv::PendingArgs pa{prev->total_nodes, prev->max_nodes, prev->max_depth, prev->node_offsets,
+                       prev->parent, prev->g, prev->k, prev->v, path, accept_len};
+    tv::AcceptArgs acc{p->B, prev->total_nodes, prev->max_nodes, prev->max_depth,
+                       prev->node_offsets, prev->parent, draft_tokens, target_argmax, root_argmax,
+                       accept_len, path, bonus, dev_status};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->total_nodes > 0 && tv::accept_commit_verify_fused_supported(a, pa)) {
+        cudaError_t e = tv::launch_accept_commit_verify_fused(a, pa, acc, H, s);
+        return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+    }
+    // other shapes: the walk, then tv_commit_verify with the paths it wrote
+    cudaError_t e = tv::launch_accept(acc, s);
+    if (e != cudaSuccess) return TV_ERR_CUDA;
+    tv_pending pend = *prev;
+    pend.path = path;
+    pend.accept_len = accept_len;
+    return tv_commit_verify(p, &pend, H, q, k, v, g, out, dev_status, stream);
 }
 
 }  // extern "C"

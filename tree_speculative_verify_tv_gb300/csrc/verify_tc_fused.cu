@@ -43,6 +43,7 @@
 // Every wait is bounded (TV_ERR_TIMEOUT); every copy and product in flight is
 // waited for (bounded) before tensor memory is freed.  Malformed trees zero their
 // rows and set TV_ERR_TREE.
+#include "greedy_walk.cuh"
 #include "tc_common.cuh"
 
 namespace tv {
@@ -59,8 +60,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 // as an M = 128 operand it spans 16 KB from each slab start, all inside the plan.
 struct FusedLayout {
     uint32_t q_off, k_off, v_off, whi_off, wlo_off, eg_off, meta_off, pk16_off, pv16_off,
-        pa_off, pvv_off, bar_off, misc_off, h_off, total;
-    __host__ __device__ FusedLayout(int dk, int dv, int np, int pd) {
+        pa_off, pvv_off, bar_off, misc_off, acc_off, accf_off, h_off, total;
+    // pd: the pending path's depth bound (commit + verify); an: the previous tree's node
+    // bound when its greedy walk runs here (accept + commit + verify), else 0
+    __host__ __device__ FusedLayout(int dk, int dv, int np, int pd, int an = 0) {
         const uint32_t tile = (dk / 64) * np * 128;
         q_off = 0;
         k_off = align_up(q_off + tile, 1024);
@@ -75,7 +78,11 @@ struct FusedLayout {
         pvv_off = pa_off + pd * dk * 4;
         bar_off = align_up(pvv_off + pd * dv * 4, 16);
         misc_off = bar_off + (kMaxChunksF * 2 + 8) * 8;
-        h_off = align_up(misc_off + 16, 1024);
+        // accept mode: the walk's parent, draft and target rows and path, then every
+        // node's k and v rows (bf16), prefetched while the walk runs
+        acc_off = align_up(misc_off + 16, 16);
+        accf_off = acc_off + align_up((3 * an + kMaxDepth) * 4, 16);
+        h_off = align_up(accf_off + an * (dk + dv) * 2, 1024);
         total = h_off + dk * dv * 4 + 1024;  // + slack for 1024-byte base alignment
     }
 };
@@ -87,6 +94,11 @@ struct FusedParams {
     VerifyArgs a;
     PendingArgs pend;  // commit + verify only
     float *H_w;        // state rows written back (commit + verify only)
+    // accept + commit + verify: the pending path is the greedy walk of the previous tree
+    // (pend's tree), which the head-0 block of each request also writes out
+    int acc;
+    const int32_t *acc_draft, *acc_target, *acc_root;
+    int32_t *acc_len, *acc_path, *acc_bonus;
     int tmem_cols;
     int wave;               // CTAs resident at once (units one wave ahead are prefetched)
     int expire_first_wait;  // test hook: the first wait for a state chunk gives up at once
@@ -128,7 +140,7 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int dk = a.dk, H = a.H;
     const int pd = PEND ? P.pend.max_depth : 0;
-    const FusedLayout L(dk, DV, NP, pd);
+    const FusedLayout L(dk, DV, NP, pd, PEND && P.acc ? P.pend.max_nodes : 0);
     const int nch = dk / R;  // chunks
     const uint32_t tile_slab = NP * 128;
     int *meta = reinterpret_cast<int *>(smem + L.meta_off);
@@ -430,20 +442,69 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
         const int mdp = pa.max_depth;
         int poff = 0, pn = 0;
         const bool prange = request_range(pa.node_offsets, b, pa.T, pa.max_nodes, poff, pn);
-        const int Lq = pa.len[b];
-        const int pm = lane < mdp ? pa.path[(size_t)b * mdp + lane] : -1;
-        bool pbad = !prange || Lq < 0 || Lq > mdp;
-        pbad = pbad || __any_sync(0xffffffffu, lane < Lq && (pm < 0 || pm >= pn));
-        // one round trip: the path's parents and decays, and its factor rows (16-byte
-        // copies into shared memory, scaled once the decays are known)
-        int ppar = -2;
-        float pg = 0.f;
+        int Lq, pm;
+        bool pbad;
         const int k8 = dk / 8, v8 = DV / 8;
-        const uint32_t dk16 = ptx::smem_addr(smem + L.pk16_off);
-        const uint32_t dv16 = ptx::smem_addr(smem + L.pv16_off);
         const __nv_bfloat16 *pk = static_cast<const __nv_bfloat16 *>(pa.k);
         const __nv_bfloat16 *pv = static_cast<const __nv_bfloat16 *>(pa.v);
-        if (!pbad) {
+        float gl = 0.f;  // accept mode: lane i holds node i's decay
+        if (P.acc) {
+            // every node's factor rows and decay, requested now so that they arrive with
+            // the tree arrays below: the path's rows are then in shared memory once the
+            // walk has found it (the previous tree has at most 32 nodes here)
+            const int nacc = prange ? pn : 0;
+            const uint32_t fk = ptx::smem_addr(smem + L.accf_off);
+            const uint32_t fv = fk + pa.max_nodes * dk * 2;
+            for (int e = lane; e < nacc * (k8 + v8); e += 32) {
+                const bool isk = e < nacc * k8;
+                const int e2 = isk ? e : e - nacc * k8;
+                const int per = isk ? k8 : v8;
+                const int node = e2 / per, c8 = (e2 % per) * 8;
+                const size_t row = (size_t)(poff + node) * H + h;
+                if (isk)
+                    ptx::cp_async_16(fk + (node * dk + c8) * 2, pk + row * dk + c8);
+                else
+                    ptx::cp_async_16(fv + (node * DV + c8) * 2, pv + row * DV + c8);
+            }
+            if (lane < nacc) gl = pa.g[(size_t)(poff + lane) * H + h];
+            // the greedy walk of the previous tree (LLM Primer VI ch. 9 §9.1) finds the
+            // path; every block of the request runs it, the head-0 block writes it out
+            int *wpar = reinterpret_cast<int *>(smem + L.acc_off);
+            int *wdrf = wpar + pa.max_nodes, *wtgt = wdrf + pa.max_nodes;
+            int *wpath = wtgt + pa.max_nodes;
+            int32_t bonus = -1;
+            const int Lw = prange ? warp_greedy_walk(pa.parent, P.acc_draft, P.acc_target, poff, pn,
+                                                     mdp, P.acc_root[b], wpar, wdrf, wtgt, wpath,
+                                                     &bonus)
+                                  : -1;
+            __syncwarp();
+            if (h == 0) {
+                for (int m = lane; m < mdp; m += 32) P.acc_path[(size_t)b * mdp + m] = m < Lw ? wpath[m] : -1;
+                if (lane == 0) {
+                    P.acc_len[b] = Lw < 0 ? 0 : Lw;
+                    P.acc_bonus[b] = Lw < 0 ? -1 : bonus;
+                }
+            }
+            Lq = Lw < 0 ? 0 : Lw;
+            pm = lane < Lq ? wpath[lane] : -1;
+            pbad = Lw < 0;
+        } else {
+            Lq = pa.len[b];
+            pm = lane < mdp ? pa.path[(size_t)b * mdp + lane] : -1;
+            pbad = !prange || Lq < 0 || Lq > mdp;
+            pbad = pbad || __any_sync(0xffffffffu, lane < Lq && (pm < 0 || pm >= pn));
+        }
+        // one round trip: the path's parents and decays, and its factor rows (16-byte
+        // copies into shared memory, scaled once the decays are known).  In accept mode
+        // they are already requested, and the walk's path is a root path by construction.
+        int ppar = -2;
+        float pg = 0.f;
+        const uint32_t dk16 = ptx::smem_addr(smem + L.pk16_off);
+        const uint32_t dv16 = ptx::smem_addr(smem + L.pv16_off);
+        if (P.acc) {
+            const float gp = __shfl_sync(0xffffffffu, gl, lane < Lq ? pm & 31 : 0);
+            if (lane < Lq) pg = gp;
+        } else if (!pbad) {
             if (lane < Lq) {
                 ppar = pa.parent[poff + pm];
                 pg = pa.g[(size_t)(poff + pm) * H + h];
@@ -466,7 +527,7 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
                 }
             }
         }
-        if (!pbad) {
+        if (!pbad && !P.acc) {
             const int prev = __shfl_up_sync(0xffffffffu, pm, 1);
             pbad = __any_sync(0xffffffffu, lane < Lq && ppar != (lane == 0 ? -1 : prev));
         }
@@ -486,8 +547,12 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
         // factor rows: a_m = e^{G_L - G_{p_m}} k_{p_m} and v_{p_m}, fp32
         float *sPA = reinterpret_cast<float *>(smem + L.pa_off);
         float *sPV = reinterpret_cast<float *>(smem + L.pvv_off);
-        const __nv_bfloat16 *k16 = reinterpret_cast<const __nv_bfloat16 *>(smem + L.pk16_off);
-        const __nv_bfloat16 *v16 = reinterpret_cast<const __nv_bfloat16 *>(smem + L.pv16_off);
+        // the staged rows: by path slot, or in accept mode by node
+        const __nv_bfloat16 *k16 = reinterpret_cast<const __nv_bfloat16 *>(
+            smem + (P.acc ? L.accf_off : L.pk16_off));
+        const __nv_bfloat16 *v16 =
+            P.acc ? k16 + pa.max_nodes * dk
+                  : reinterpret_cast<const __nv_bfloat16 *>(smem + L.pv16_off);
         const int items = Lp * (k8 + v8);
         for (int base = 0; base < items; base += 32) {
             const int e = base + lane;
@@ -496,10 +561,11 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
             const int per = isk ? k8 : v8;
             const int m = e < items ? e2 / per : 0;
             const float sc = __shfl_sync(0xffffffffu, scale, m);
+            const int srow = P.acc ? __shfl_sync(0xffffffffu, pm, m) : m;
             if (e < items) {
                 const int c8 = (e2 % per) * 8;
-                const uint4 raw = *reinterpret_cast<const uint4 *>(isk ? k16 + m * dk + c8
-                                                                       : v16 + m * DV + c8);
+                const uint4 raw = *reinterpret_cast<const uint4 *>(isk ? k16 + srow * dk + c8
+                                                                       : v16 + srow * DV + c8);
                 const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
                 float *dst = isk ? sPA + m * dk + c8 : sPV + m * DV + c8;
                 const float f = isk ? sc : 1.f;
@@ -664,9 +730,9 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
 
 // ---------------------------------------------------------------- host side
 
-size_t fused_smem_bytes(const VerifyArgs &a, int pd) {
+size_t fused_smem_bytes(const VerifyArgs &a, int pd, int an = 0) {
     const int np = a.max_nodes > 16 ? 32 : 16;
-    return FusedLayout(a.dk, a.dv, np, pd).total;
+    return FusedLayout(a.dk, a.dv, np, pd, an).total;
 }
 
 bool fused_shape_ok(const VerifyArgs &a) {
@@ -676,7 +742,7 @@ bool fused_shape_ok(const VerifyArgs &a) {
 
 template <int DV, int NP, bool PEND>
 cudaError_t launch_fused_t(const VerifyArgs &a, const PendingArgs *pend, float *Hw, bool expire,
-                           cudaStream_t s) {
+                           cudaStream_t s, const AcceptArgs *acc) {
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tq, tk, tv_;
     // q and k: K-major operand tiles; v: MN-major blocks of 64 channels
@@ -688,12 +754,20 @@ cudaError_t launch_fused_t(const VerifyArgs &a, const PendingArgs *pend, float *
     P.a = a;
     P.pend = pend ? *pend : PendingArgs{};
     P.H_w = Hw;
+    P.acc = acc != nullptr;
+    P.acc_draft = acc ? acc->draft : nullptr;
+    P.acc_target = acc ? acc->target : nullptr;
+    P.acc_root = acc ? acc->root : nullptr;
+    P.acc_len = acc ? acc->len : nullptr;
+    P.acc_path = acc ? acc->path : nullptr;
+    P.acc_bonus = acc ? acc->bonus : nullptr;
     P.tmem_cols = tmem_columns(2 * (DV / 64) * NP + (DV == 64 && !PEND ? a.dk / 2 : 0));
     P.expire_first_wait = expire ? 1 : 0;
     auto kern = verify_tc_fused_kernel<DV, NP, PEND>;
     cudaError_t e = configure_smem_once(kern, true);
     if (e != cudaSuccess) return e;
-    const size_t smem = fused_smem_bytes(a, PEND ? pend->max_depth : 0);
+    const size_t smem = fused_smem_bytes(a, PEND ? pend->max_depth : 0,
+                                         PEND && acc ? pend->max_nodes : 0);
     int dev = 0, sms = 0, per_sm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
@@ -705,13 +779,13 @@ cudaError_t launch_fused_t(const VerifyArgs &a, const PendingArgs *pend, float *
 
 template <bool PEND>
 cudaError_t launch_fused(const VerifyArgs &a, const PendingArgs *pend, float *Hw, bool expire,
-                         cudaStream_t s) {
+                         cudaStream_t s, const AcceptArgs *acc = nullptr) {
     const bool np16 = a.max_nodes <= 16;
     if (a.dv == 64)
-        return np16 ? launch_fused_t<64, 16, PEND>(a, pend, Hw, expire, s)
-                    : launch_fused_t<64, 32, PEND>(a, pend, Hw, expire, s);
-    return np16 ? launch_fused_t<128, 16, PEND>(a, pend, Hw, expire, s)
-                : launch_fused_t<128, 32, PEND>(a, pend, Hw, expire, s);
+        return np16 ? launch_fused_t<64, 16, PEND>(a, pend, Hw, expire, s, acc)
+                    : launch_fused_t<64, 32, PEND>(a, pend, Hw, expire, s, acc);
+    return np16 ? launch_fused_t<128, 16, PEND>(a, pend, Hw, expire, s, acc)
+                : launch_fused_t<128, 32, PEND>(a, pend, Hw, expire, s, acc);
 }
 
 }  // namespace
@@ -733,6 +807,18 @@ cudaError_t launch_commit_verify_fused(const VerifyArgs &a, const PendingArgs &p
                                        cudaStream_t s) {
     if (!commit_verify_fused_supported(a, p)) return cudaErrorNotSupported;
     return launch_fused<true>(a, &p, H, false, s);
+}
+
+bool accept_commit_verify_fused_supported(const VerifyArgs &a, const PendingArgs &p) {
+    // the previous tree's nodes' factor rows are staged whole (one per lane's decay)
+    return fused_shape_ok(a) && p.max_nodes <= 32 &&
+           fused_smem_bytes(a, p.max_depth, p.max_nodes) <= kSmemLimit;
+}
+
+cudaError_t launch_accept_commit_verify_fused(const VerifyArgs &a, const PendingArgs &p,
+                                              const AcceptArgs &acc, float *H, cudaStream_t s) {
+    if (!accept_commit_verify_fused_supported(a, p)) return cudaErrorNotSupported;
+    return launch_fused<true>(a, &p, H, false, s, &acc);
 }
 
 }  // namespace tv
