@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
     auto b_conv = [&](int c) { return bar_base + 8u * (kMaxChunksF + c); };
     const uint32_t b_qkv = bar_base + 8u * (2 * kMaxChunksF);
     const uint32_t b_sfull = b_qkv + 8, b_wready = b_qkv + 16, b_dfull = b_qkv + 24,
-                   b_pend = b_qkv + 32, b_final = b_qkv + 40;
+                   b_pend = b_qkv + 32, b_final = b_qkv + 40, b_issue = b_qkv + 48;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x, b = unit / H, h = unit % H;
@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
         ptx::mbar_init(b_dfull, 1);
         ptx::mbar_init(b_pend, 1);
         ptx::mbar_init(b_final, 1);
+        ptx::mbar_init(b_issue, 1);
         ptx::fence_mbar_init();
         *sLate = 0;
     }
@@ -187,12 +188,16 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
 
     ptx::grid_dependency_wait();  // inputs may be written by the previous kernel
     const float *hsrc = (PEND ? P.H_w : a.H0) + (size_t)unit * dk * DV;
-    if (tid == 0)
+    auto copy_state = [&]() {
         for (int c = 0; c < nch; ++c) {
             ptx::mbar_arrive_expect_tx(b_chunk(c), kChunkBytes);
             ptx::bulk_g2s(ptx::smem_addr(sH) + c * kChunkBytes, hsrc + (size_t)c * kChunkVals,
                           kChunkBytes, b_chunk(c));
         }
+    };
+    // with a pending commit the state is copied once the pending path's loads are out
+    // (below), so that they do not queue behind every block's state
+    if (!PEND && tid == 0) copy_state();
     // the state of the unit that starts about one wave later goes to L2 now, so its
     // CTA finds it there (same bytes, fetched earlier)
     if (tid == 32 && P.wave > 0 && unit + P.wave < a.B * H)
@@ -213,6 +218,9 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
         if constexpr (PEND) {
             bool ok = true;
             if (tid == 0) {
+                // the state copies follow the pending path's loads (issued by warp 5)
+                if (!ptx::mbar_wait(b_issue, 0, kWaitLimit)) atomicOr(sLate, 1);
+                copy_state();
                 ok = *reinterpret_cast<volatile int *>(sLate) == 0 &&
                      ptx::mbar_wait(b_pend, 0, kWaitLimit);
                 if (!ok) atomicOr(sLate, 1);
@@ -468,15 +476,32 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
             }
             if (lane < nacc) gl = pa.g[(size_t)(poff + lane) * H + h];
             // the greedy walk of the previous tree (LLM Primer VI ch. 9 §9.1) finds the
-            // path; every block of the request runs it, the head-0 block writes it out
+            // path; every block of the request runs it, the head-0 block writes it out.
+            // Lane i loads node i's parent and tokens; then the state copies may start.
+            int wp = -1, wd = 0, wt = 0;
+            if (lane < nacc) {
+                wp = pa.parent[poff + lane];
+                wd = P.acc_draft[poff + lane];
+                wt = P.acc_target[poff + lane];
+            }
+            const int32_t root = P.acc_root[b];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(b_issue);
             int *wpar = reinterpret_cast<int *>(smem + L.acc_off);
             int *wdrf = wpar + pa.max_nodes, *wtgt = wdrf + pa.max_nodes;
             int *wpath = wtgt + pa.max_nodes;
+            if (lane < nacc) {
+                wpar[lane] = wp;
+                wdrf[lane] = wd;
+                wtgt[lane] = wt;
+            }
+            const bool wbad = __any_sync(0xffffffffu, lane < nacc && (wp < -1 || wp >= lane));
+            __syncwarp();
             int32_t bonus = -1;
-            const int Lw = prange ? warp_greedy_walk(pa.parent, P.acc_draft, P.acc_target, poff, pn,
-                                                     mdp, P.acc_root[b], wpar, wdrf, wtgt, wpath,
-                                                     &bonus)
-                                  : -1;
+            const int Lw = (prange && !wbad)
+                               ? warp_greedy_walk_shared(wpar, wdrf, wtgt, nacc, mdp, root, wpath,
+                                                         &bonus)
+                               : -1;
             __syncwarp();
             if (h == 0) {
                 for (int m = lane; m < mdp; m += 32) P.acc_path[(size_t)b * mdp + m] = m < Lw ? wpath[m] : -1;
@@ -526,6 +551,10 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
                         ptx::cp_async_16(dv16 + (m * DV + c8) * 2, pv + row * DV + c8);
                 }
             }
+        }
+        if (!P.acc) {
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(b_issue);  // the path's loads are out
         }
         if (!pbad && !P.acc) {
             const int prev = __shfl_up_sync(0xffffffffu, pm, 1);
