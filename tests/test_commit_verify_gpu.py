@@ -299,3 +299,36 @@ def test_accept_commit_verify_malformed_previous_tree():
         assert int(dc.accept_len[b]) == ln[b]
         for h in range(prev.H):
             assert mat_rel_err(dc.H0[b, h].cpu().numpy().astype(np.float64), H_ref[b, h]) <= TOL
+
+
+@pytest.mark.parametrize("call", ["commit_verify", "accept_commit_verify"])
+def test_write_back_of_a_state_only_16_byte_aligned(call):
+    """The committed rows go back with 256-bit stores where the state is 32-byte
+    aligned and with 128-bit stores where it is only 16-byte aligned: both give the
+    same bits."""
+    import torch
+    import tree_speculative_verify_tv_gb300 as tv
+    prev, cur = workloads.make_config(2, 61), workloads.make_config(2, 62)
+    res = []
+    for shift in (0, 4):
+        dp, dc = tv.DeviceBatch(prev), tv.DeviceBatch(cur)
+        buf = torch.empty(dc.H0.numel() + 8, dtype=torch.float32, device="cuda")
+        H = buf[shift:shift + dc.H0.numel()].view_as(dc.H0)
+        assert (H.data_ptr() % 32 == 0) == (shift == 0) and H.data_ptr() % 16 == 0
+        H.copy_(dp.H0)
+        dc.H0 = H
+        dc.status.zero_()
+        dp.status.zero_()
+        if call == "commit_verify":
+            dp.accept()
+            dc.commit_verify(dp)
+            ln = dp.accept_len
+        else:
+            dc.accept_commit_verify(dp)
+            ln = dc.accept_len
+        torch.cuda.synchronize()
+        assert int(dc.status[0]) == 0
+        assert int(ln[:prev.B].max()) > 0  # some rows are written back
+        res.append((dc.H0.clone(), dc.out[:cur.T].clone()))
+    assert torch.equal(res[0][0], res[1][0])
+    assert torch.equal(res[0][1], res[1][1])

@@ -30,8 +30,9 @@
 //
 // Roles (256 threads):
 //   warps 0-3  chunk copies (thread 0); per chunk: read, apply the pending commit
-//              (tv_commit_verify: H <- e^{G_L} H + sum_m a_m v_m^T, rows written
-//              back to HBM), barrier, write the hi / lo blocks
+//              (tv_commit_verify: H <- e^{G_L} H + sum_m a_m v_m^T), barrier, write
+//              the hi / lo blocks, hand the chunk to the products, then write the
+//              updated rows back to HBM (256-bit stores where the state allows)
 //   warp 4     offsets, q/k/v tile copies, tree checks, path sums G (pointer
 //              doubling over the warp, lane = node), ancestor masks, e^{G_i}; the
 //              weights from D_S into the weight tiles (its tensor-memory quadrant
@@ -94,6 +95,7 @@ struct FusedParams {
     VerifyArgs a;
     PendingArgs pend;  // commit + verify only
     float *H_w;        // state rows written back (commit + verify only)
+    int wb32;          // H_w is 32-byte aligned: the write-back uses 256-bit stores
     // accept + commit + verify: the pending path is the greedy walk of the previous tree
     // (pend's tree), which the head-0 block of each request also writes out
     int acc;
@@ -103,6 +105,13 @@ struct FusedParams {
     int wave;               // CTAs resident at once (units one wave ahead are prefetched)
     int expire_first_wait;  // test hook: the first wait for a state chunk gives up at once
 };
+
+// 8 floats to a 32-byte aligned global address in one 256-bit store
+__device__ __forceinline__ void st_global_v8(float *p, const float (&x)[8]) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(x[0]),
+                 "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7])
+                 : "memory");
+}
 
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
@@ -279,7 +288,8 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
                 x[t][4] = v1.x; x[t][5] = v1.y; x[t][6] = v1.z; x[t][7] = v1.w;
             }
             if (PEND && pL > 0) {
-                // the pending rank-pL update on these rows, written back to the state
+                // the pending rank-pL update on these rows (written back to the state
+                // once the chunk is handed to the products)
 #pragma unroll
                 for (int t = 0; t < kRows; ++t)
 #pragma unroll
@@ -294,13 +304,6 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
 #pragma unroll
                         for (int e = 0; e < 8; ++e) x[t][e] += am * vm[e];
                     }
-                }
-                float *Hw = P.H_w + ((size_t)unit * dk + c * R) * DV + pc * 8;
-#pragma unroll
-                for (int t = 0; t < kRows; ++t) {
-                    float4 *dst = reinterpret_cast<float4 *>(Hw + (r0 + rstep * t) * DV);
-                    dst[0] = make_float4(x[t][0], x[t][1], x[t][2], x[t][3]);
-                    dst[1] = make_float4(x[t][4], x[t][5], x[t][6], x[t][7]);
                 }
             }
             named_barrier(1, 128);  // the whole chunk is read before it is rewritten
@@ -317,6 +320,21 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(b_conv(c));
+            if (PEND && pL > 0) {
+                // a thread's 8 values of a row fill one 32-byte sector: one 256-bit store
+                // where the state is 32-byte aligned, else two 128-bit stores
+                float *Hw = P.H_w + ((size_t)unit * dk + c * R) * DV + pc * 8;
+#pragma unroll
+                for (int t = 0; t < kRows; ++t) {
+                    float *dst = Hw + (r0 + rstep * t) * DV;
+                    if (P.wb32) {
+                        st_global_v8(dst, x[t]);
+                    } else {
+                        reinterpret_cast<float4 *>(dst)[0] = make_float4(x[t][0], x[t][1], x[t][2], x[t][3]);
+                        reinterpret_cast<float4 *>(dst)[1] = make_float4(x[t][4], x[t][5], x[t][6], x[t][7]);
+                    }
+                }
+            }
         }
         // after a failed wait the remaining chunks are released unconverted, so the
         // product thread does not wait on them (the outputs are not written then)
@@ -783,6 +801,7 @@ cudaError_t launch_fused_t(const VerifyArgs &a, const PendingArgs *pend, float *
     P.a = a;
     P.pend = pend ? *pend : PendingArgs{};
     P.H_w = Hw;
+    P.wb32 = (reinterpret_cast<uintptr_t>(Hw) & 31u) == 0 ? 1 : 0;
     P.acc = acc != nullptr;
     P.acc_draft = acc ? acc->draft : nullptr;
     P.acc_target = acc ? acc->target : nullptr;
