@@ -29,10 +29,11 @@
 // key rows), which saves the in-place barrier and the operand's shared-memory reads.
 //
 // Roles (256 threads):
-//   warps 0-3  chunk copies (thread 0); per chunk: read, apply the pending commit
-//              (tv_commit_verify: H <- e^{G_L} H + sum_m a_m v_m^T), barrier, write
-//              the hi / lo blocks, hand the chunk to the products, then write the
-//              updated rows back to HBM (256-bit stores where the state allows)
+//   warps 0-3  chunk copies (thread 0); per chunk (per pair of chunks with a pending
+//              commit): read, apply the pending commit (tv_commit_verify: H <-
+//              e^{G_L} H + sum_m a_m v_m^T), barrier, write the hi / lo blocks, hand
+//              the chunks to the products, then write the updated rows back to HBM
+//              (256-bit stores where the state allows)
 //   warp 4     offsets, q/k/v tile copies, tree checks, path sums G (pointer
 //              doubling over the warp, lane = node), ancestor masks, e^{G_i}; the
 //              weights from D_S into the weight tiles (its tensor-memory quadrant
@@ -242,12 +243,14 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
         const float *pa = reinterpret_cast<const float *>(smem + L.pa_off);
         const float *pvv = reinterpret_cast<const float *>(smem + L.pvv_off);
         int c = 0;
-        for (; c < nch && run_chunks; ++c) {
+        constexpr int CPI = (PEND && !kStateTmem) ? 2 : 1;  // chunks per step
+        for (; c < nch && run_chunks; c += CPI) {
             bool ok = true;
             if (tid == 0) {
                 ok = (c == 0 && P.expire_first_wait)
                          ? false  // test hook: treated as expired
                          : ptx::mbar_wait(b_chunk(c), 0, kWaitLimit);
+                if (CPI == 2 && ok) ok = ptx::mbar_wait(b_chunk(c + 1), 0, kWaitLimit);
                 if (!ok) atomicOr(sLate, 2);
             }
             if (!named_barrier_and(1, 128, ok)) break;  // the chunk did not land: stop converting
@@ -277,61 +280,76 @@ __global__ void __launch_bounds__(kThreadsF, PEND ? 3 : 4)
                 if (lane == 0) ptx::mbar_arrive(b_conv(c));
                 continue;
             }
-            uint8_t *cp = sH + c * kChunkBytes;
-            float x[kRows][8];
+            float x[CPI][kRows][8];
 #pragma unroll
-            for (int t = 0; t < kRows; ++t) {
-                const float4 *src =
-                    reinterpret_cast<const float4 *>(cp + ((r0 + rstep * t) * DV + pc * 8) * 4);
-                const float4 v0 = src[0], v1 = src[1];
-                x[t][0] = v0.x; x[t][1] = v0.y; x[t][2] = v0.z; x[t][3] = v0.w;
-                x[t][4] = v1.x; x[t][5] = v1.y; x[t][6] = v1.z; x[t][7] = v1.w;
-            }
+            for (int cc = 0; cc < CPI; ++cc)
+#pragma unroll
+                for (int t = 0; t < kRows; ++t) {
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        sH + (c + cc) * kChunkBytes + ((r0 + rstep * t) * DV + pc * 8) * 4);
+                    const float4 v0 = src[0], v1 = src[1];
+                    x[cc][t][0] = v0.x; x[cc][t][1] = v0.y; x[cc][t][2] = v0.z; x[cc][t][3] = v0.w;
+                    x[cc][t][4] = v1.x; x[cc][t][5] = v1.y; x[cc][t][6] = v1.z; x[cc][t][7] = v1.w;
+                }
             if (PEND && pL > 0) {
                 // the pending rank-pL update on these rows (written back to the state
-                // once the chunk is handed to the products)
+                // once the chunks are handed to the products)
 #pragma unroll
-                for (int t = 0; t < kRows; ++t)
+                for (int cc = 0; cc < CPI; ++cc)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[t][e] *= alpha;
+                    for (int t = 0; t < kRows; ++t)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[cc][t][e] *= alpha;
                 for (int m = 0; m < pL; ++m) {
                     const float4 va = *reinterpret_cast<const float4 *>(pvv + m * DV + pc * 8);
                     const float4 vb = *reinterpret_cast<const float4 *>(pvv + m * DV + pc * 8 + 4);
                     const float vm[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
-                    for (int t = 0; t < kRows; ++t) {
-                        const float am = pa[m * dk + c * R + r0 + rstep * t];
+                    for (int cc = 0; cc < CPI; ++cc)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[t][e] += am * vm[e];
-                    }
+                        for (int t = 0; t < kRows; ++t) {
+                            const float am = pa[m * dk + (c + cc) * R + r0 + rstep * t];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) x[cc][t][e] += am * vm[e];
+                        }
                 }
             }
             named_barrier(1, 128);  // the whole chunk is read before it is rewritten
 #pragma unroll
-            for (int t = 0; t < kRows; ++t) {
-                const int r = r0 + rstep * t;
-                uint32_t hi[4], lo[4];
+            for (int cc = 0; cc < CPI; ++cc)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) split_pair(x[t][2 * e], x[t][2 * e + 1], hi[e], lo[e]);
-                uint8_t *blk = cp + g * (2 * R * 128) + r * 128 + ((cg ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(blk) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(blk + R * 128) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
+                for (int t = 0; t < kRows; ++t) {
+                    const int r = r0 + rstep * t;
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        split_pair(x[cc][t][2 * e], x[cc][t][2 * e + 1], hi[e], lo[e]);
+                    uint8_t *blk = sH + (c + cc) * kChunkBytes + g * (2 * R * 128) + r * 128 +
+                                   ((cg ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(blk) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(blk + R * 128) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
             ptx::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(b_conv(c));
+            if (lane == 0)
+                for (int cc = 0; cc < CPI; ++cc) ptx::mbar_arrive(b_conv(c + cc));
             if (PEND && pL > 0) {
                 // a thread's 8 values of a row fill one 32-byte sector: one 256-bit store
                 // where the state is 32-byte aligned, else two 128-bit stores
-                float *Hw = P.H_w + ((size_t)unit * dk + c * R) * DV + pc * 8;
 #pragma unroll
-                for (int t = 0; t < kRows; ++t) {
-                    float *dst = Hw + (r0 + rstep * t) * DV;
-                    if (P.wb32) {
-                        st_global_v8(dst, x[t]);
-                    } else {
-                        reinterpret_cast<float4 *>(dst)[0] = make_float4(x[t][0], x[t][1], x[t][2], x[t][3]);
-                        reinterpret_cast<float4 *>(dst)[1] = make_float4(x[t][4], x[t][5], x[t][6], x[t][7]);
+                for (int cc = 0; cc < CPI; ++cc) {
+                    float *Hw = P.H_w + ((size_t)unit * dk + (c + cc) * R) * DV + pc * 8;
+#pragma unroll
+                    for (int t = 0; t < kRows; ++t) {
+                        float *dst = Hw + (r0 + rstep * t) * DV;
+                        if (P.wb32) {
+                            st_global_v8(dst, x[cc][t]);
+                        } else {
+                            reinterpret_cast<float4 *>(dst)[0] =
+                                make_float4(x[cc][t][0], x[cc][t][1], x[cc][t][2], x[cc][t][3]);
+                            reinterpret_cast<float4 *>(dst)[1] =
+                                make_float4(x[cc][t][4], x[cc][t][5], x[cc][t][6], x[cc][t][7]);
+                        }
                     }
                 }
             }
