@@ -262,6 +262,26 @@ def test_accept_commit_verify_equals_accept_then_commit_verify(c):
     assert torch.equal(fc.out[:cur.T], sc.out[:cur.T])
 
 
+def test_accept_commit_verify_ragged_trees():
+    """Trees of different sizes, so that a request's previous tree does not start at
+    b * max_nodes (its arrays are requested again at the actual range): the one-launch
+    step still equals tv_accept_greedy then tv_commit_verify bit for bit."""
+    import torch
+    rng = np.random.default_rng(91)
+    kw = dict(decay="scalar", qkv_dtype="bf16", depth_cap=8, vocab=3, max_depth=8)
+    prev = workloads.random_batch(rng, [5, 16, 9, 32, 1, 12, 20, 3], 4, 128, 64, **kw)
+    cur = workloads.random_batch(rng, [7, 32, 2, 11, 16, 4, 30, 9], 4, 128, 64, **kw)
+    (fp, fc), (sp, sc) = _acv_and_separate(prev, cur)
+    assert int(fc.status[0]) == 0 and int(sc.status[0]) == 0 and int(sp.status[0]) == 0
+    B = prev.B
+    assert int(sp.accept_len[:B].max()) > 0
+    assert torch.equal(fp.accept_len[:B], sp.accept_len[:B])
+    assert torch.equal(fp.path[:B], sp.path[:B])
+    assert torch.equal(fp.bonus[:B], sp.bonus[:B])
+    assert torch.equal(fc.H0, sc.H0)
+    assert torch.equal(fc.out[:cur.T], sc.out[:cur.T])
+
+
 def test_accept_commit_verify_against_the_oracle():
     prev, cur = _pair(workloads.config2)
     H_ref, cur_ref, ln, path = _oracle_two_steps(prev, cur)
