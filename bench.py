@@ -770,6 +770,11 @@ def run_ours(args, world, rank, local):
 
     # ---------------- end to end through the binding with pinned host buffers
     e2e = run_e2e(args, sets[0], dev, stream, tv, world, mode)
+    if mode in ("one", "fused"):
+        # the same with the layer's outputs read back every step as well
+        wo = run_e2e(args, sets[0], dev, stream, tv, world, mode, read_outputs=True)
+        e2e["with_outputs_read_back"] = {k: wo[k] for k in ("value", "unit", "h2d_bytes_per_step",
+                                                             "d2h_bytes_per_step", "ms_per_step")}
 
     # ---------------- one verify launch over `fold` layers folded into the head axis
     folded = {}
@@ -1095,13 +1100,15 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, host_batch, dev, stream, tv, world, mode):
+def run_e2e(args, host_batch, dev, stream, tv, world, mode, read_outputs=False):
     """The step through the binding with host buffers: pinned host -> device copies
     of the step's inputs, the calls, device -> pinned host copies of its results.
     One-launch and fused pipelines: the state is resident on the device (the commit
-    updates it in place), so the inputs are the tree, factors and tokens and the
-    results the outputs and acceptance; separate pipeline: the state is copied in and
-    H_new out.  In the one-launch pipeline a step's acceptance results are the walk
+    updates it in place), so the inputs are the tree, factors and tokens, and the
+    results the host needs are the acceptance (lengths, paths, bonus tokens) and the
+    status; the layer's outputs stay in HBM for the next layer unless `read_outputs`
+    asks for them too.  Separate pipeline: the state is copied in and H_new and the
+    outputs out.  In the one-launch pipeline a step's acceptance results are the walk
     of the previous step's tree, written to the step's own result buffers.
 
     Each step moves one contiguous staging range in and one out.  Four staging sets
@@ -1118,10 +1125,13 @@ def run_e2e(args, host_batch, dev, stream, tv, world, mode):
     if not fused:
         ins.append("H0")
         outs.append("H_new")
+    elif not read_outputs:
+        outs = ["accept_len", "path", "bonus"]
     # one staging layout on both sides: the step's inputs, the status word and the
-    # results; the batch's tensors become views into it.  The status travels both
-    # ways, so an error in any step stays set and is caught after the timed region.
-    names = ins + ["status"] + outs
+    # results (then the outputs, where they are not read back); the batch's tensors
+    # become views into it.  The status travels both ways, so an error in any step
+    # stays set and is caught after the timed region.
+    names = ins + ["status"] + outs + ([] if "out" in outs else ["out"])
     probe = tv.DeviceBatch(host_batch, device=dev)
     offs, pos = {}, 0
     for n in names:
@@ -1132,6 +1142,7 @@ def run_e2e(args, host_batch, dev, stream, tv, world, mode):
     total = (pos + 255) // 256 * 256
     in_end = offs["status"] + probe.status.numel() * probe.status.element_size()
     out_begin = offs["status"]
+    out_end = total if "out" in outs else offs["out"]
     del probe
 
     def staged():
@@ -1156,7 +1167,7 @@ def run_e2e(args, host_batch, dev, stream, tv, world, mode):
     streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(NS - 1)]
     kev = [torch.cuda.Event() for _ in range(NS)]  # kernels of the step that last used a set
     h2d = in_end
-    d2h = total - out_begin
+    d2h = out_end - out_begin
     # about 2 GB of host<->device traffic at most (at least 3 steps)
     K = max(NS, min(args.e2e_steps, max(3, int(2e9 / max(h2d + d2h, 1)))))
 
@@ -1181,7 +1192,7 @@ def run_e2e(args, host_batch, dev, stream, tv, world, mode):
                 db.verify(stream=st, variant=args.variant)
                 db.accept_commit(stream=st)
             kev[i].record(st)
-            hs[out_begin:].copy_(ds[out_begin:], non_blocking=True)
+            hs[out_begin:out_end].copy_(ds[out_begin:out_end], non_blocking=True)
 
     def join_into_first():
         for st in streams[1:]:
@@ -1232,6 +1243,7 @@ def run_e2e(args, host_batch, dev, stream, tv, world, mode):
     return {"value": nh / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": dt / K * 1e3,
             "state": "resident in HBM" if fused else "copied in and out every step",
+            "results_read": "+".join(["status"] + outs),
             "copies": "one host-to-device copy of the step's inputs and one device-to-host "
                       "copy of its results per step (one staging layout, 256-byte aligned "
                       "fields); four staging sets on four streams, so a step's input "
